@@ -1,0 +1,106 @@
+"""CPU fp64 oracle for the attention forward pass.
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by ``__graft_entry__.smoke``
+and by the bench's CPU-baseline and reference legs.  The CUDA product path
+never imports, links or runs anything here, and nothing here touches the
+CUDA path.
+
+``attention_rows`` / ``attention`` wrap ``oracle.c`` (the three passes of
+"Safe Softmax and the Three Passes" in "The Details of Flash Attention",
+fp64); ``tiled_model`` holds a second, tile-by-tile restatement of the online
+recurrence used only to pin the intermediate numbers of the worked example.
+Row chunks run on host threads (ctypes releases the GIL during the C call).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with the host C compiler."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            f = lib.oracle_attention_rows
+            f.restype = ctypes.c_int
+            f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 4 + [
+                ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def attention_rows(q, k, v, scale, causal, rows, threads=None):
+    """Exact O rows and LSE for the given row ids (bh * N + i), in float64.
+
+    q, k, v: float32 arrays shaped [B, H, N, d], holding the exact input values.
+    Returns (o[len(rows), d], lse[len(rows)]).
+    """
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    k = np.ascontiguousarray(k, dtype=np.float32)
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    if q.ndim != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must be [B, H, N, d] arrays of one shape")
+    B, H, N, d = q.shape
+    rows = np.ascontiguousarray(rows, dtype=np.int64).ravel()
+    o = np.empty((rows.size, d), dtype=np.float64)
+    lse = np.empty(rows.size, dtype=np.float64)
+    if rows.size == 0:
+        return o, lse
+    lib = _load()
+    threads = threads or default_threads()
+    nchunks = min(rows.size, max(1, threads * 4))
+    bounds = np.linspace(0, rows.size, nchunks + 1).astype(np.int64)
+
+    def run(c):
+        lo, hi = int(bounds[c]), int(bounds[c + 1])
+        if hi <= lo:
+            return 0
+        work = np.empty(N, dtype=np.float64)
+        return lib.oracle_attention_rows(
+            q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, N, d,
+            float(scale), int(bool(causal)), rows[lo:].ctypes.data, hi - lo,
+            o[lo:].ctypes.data, lse[lo:].ctypes.data, work.ctypes.data)
+
+    if threads == 1 or nchunks == 1:
+        codes = [run(c) for c in range(nchunks)]
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            codes = list(ex.map(run, range(nchunks)))
+    bad = [c for c in codes if c != 0]
+    if bad:
+        raise RuntimeError(f"oracle_attention_rows failed with code {bad[0]}")
+    return o, lse
+
+
+def attention(q, k, v, scale, causal=False, threads=None):
+    """Exact O [B, H, N, d] and LSE [B, H, N] for every row, in float64."""
+    B, H, N, d = np.shape(q)
+    rows = np.arange(B * H * N, dtype=np.int64)
+    o, lse = attention_rows(q, k, v, scale, causal, rows, threads)
+    return o.reshape(B, H, N, d), lse.reshape(B, H, N)

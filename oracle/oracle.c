@@ -1,0 +1,82 @@
+/*
+ * CPU oracle for the exact attention forward pass  O = softmax(Q K^T * scale) V.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The tests, the package's smoke check and the
+ * bench's CPU-baseline leg call it; the CUDA product path never does, and
+ * this file shares no code, header or constant with it.
+ *
+ * Plain, slow and meant to be checked by eye.  Everything is computed in
+ * double precision from float32 inputs (which hold the exact bf16 or fp32
+ * values the GPU sees).  For one query row it follows the three loops of
+ * "Safe Softmax and the Three Passes" in "The Details of Flash Attention"
+ * (ggluo.github.io), with the scores x_j of the section "The Attention
+ * Computation":
+ *
+ *   x_j  = scale * sum_t Q[i,t] K[j,t]              for every key j in range
+ *   pass 1: m   = max_j x_j
+ *   pass 2: d_T = sum_j exp(x_j - m)
+ *   pass 3: O[i,:] = sum_j exp(x_j - m) / d_T * V[j,:]
+ *
+ * and the per-row log-sum-exp  LSE_i = m + ln d_T, the natural log of
+ * sum_j exp(x_j).  Keys in range are all N keys, or j <= i under the causal
+ * mask (keys after the query are set to -inf before the softmax, as the
+ * masked_fill in "PyTorch Implementation" of the rohit.vision post
+ * "Transformer Attention: A Mathematical Deep Dive" does).  The scores of
+ * one row are kept in a work buffer of N doubles between the passes; no
+ * N x N matrix is ever formed.
+ *
+ * Layout: Q, K, V are contiguous [B, H, N, d] row-major float32.  A "row id"
+ * is bh * N + i with bh = b * H + h.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+
+/* Returns 0 on success, 1 on a bad argument, 2 when a row has no key in
+ * range (cannot happen for N >= 1: the causal row i always sees key 0). */
+int oracle_attention_rows(const float *q, const float *k, const float *v,
+                          int64_t B, int64_t H, int64_t N, int64_t d,
+                          double scale, int causal,
+                          const int64_t *rows, int64_t nrows,
+                          double *o, double *lse, double *work)
+{
+    if (!q || !k || !v || !rows || !o || !work) return 1;
+    if (B < 1 || H < 1 || N < 1 || d < 1 || nrows < 0) return 1;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t id = rows[r];
+        if (id < 0 || id >= B * H * N) return 1;
+        int64_t bh = id / N;
+        int64_t i = id % N;
+        const float *qi = q + (bh * N + i) * d;
+        const float *kh = k + bh * N * d;
+        const float *vh = v + bh * N * d;
+        int64_t nkeys = causal ? i + 1 : N;
+        if (nkeys < 1) return 2;
+
+        /* scores x_j */
+        for (int64_t j = 0; j < nkeys; ++j) {
+            double dot = 0.0;
+            for (int64_t t = 0; t < d; ++t)
+                dot += (double)qi[t] * (double)kh[j * d + t];
+            work[j] = scale * dot;
+        }
+        /* pass 1: the row maximum m */
+        double m = -INFINITY;
+        for (int64_t j = 0; j < nkeys; ++j)
+            if (work[j] > m) m = work[j];
+        /* pass 2: the denominator d_T */
+        double dT = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j)
+            dT += exp(work[j] - m);
+        /* pass 3: the weighted sum of the value rows */
+        double *oi = o + r * d;
+        for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            double w = exp(work[j] - m) / dT;
+            for (int64_t t = 0; t < d; ++t)
+                oi[t] += w * (double)vh[j * d + t];
+        }
+        if (lse) lse[r] = m + log(dT);
+    }
+    return 0;
+}
