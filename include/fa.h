@@ -1,0 +1,111 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact attention forward pass.
+ *
+ * The operation is the one every page on the subject defines:
+ *
+ *     O = softmax(Q K^T * scale) V,   softmax taken row by row over the keys,
+ *
+ * ("Deep Learning - Flash Attention", "Refresher - Softmax of a Matrix
+ * Normalizes Each Row"; "The Details of Flash Attention", "The Attention
+ * Computation"), computed tile by tile with the online-softmax recurrence
+ * (running row maximum m, running denominator l, rescale factor
+ * alpha = exp(m_old - m_new)) of "The Details of Flash Attention", "Online
+ * Softmax" and "Tiling the Loop", so that the N x N score matrix never
+ * reaches global memory.  The result is exact up to floating-point rounding
+ * ("FlashAttention", ai360xpert.com, "Show Me the Code").
+ *
+ * Conventions shared by every entry point:
+ *   - Q, K, V and O are contiguous row-major [B, H, N, d] tensors (batch,
+ *     head, sequence, head dimension), the (B, nhead, N, nd) shape of "The
+ *     Details of Flash Attention", "The Attention Computation".  Batch and
+ *     head are independent problems.
+ *   - LSE is a contiguous [B, H, N] float32 tensor:
+ *     LSE[b,h,i] = ln sum_j exp(scale * q_i . k_j), i.e. m_i + ln l_i in
+ *     natural-log units of the scaled scores -- the per-row softmax
+ *     statistics that "FlashAttention" (ai360xpert.com, "Recomputation in
+ *     the backward pass") keeps instead of the weights.
+ *   - causal != 0 masks key j > query i (the mask of "PyTorch
+ *     Implementation" in "Transformer Attention: A Mathematical Deep Dive");
+ *     key tiles that lie wholly above the diagonal are skipped.
+ *   - The caller owns every buffer.  The library allocates no device memory
+ *     and keeps no per-call state; it caches one function-pointer lookup.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Argument errors are reported before anything is
+ *     launched; launch errors are reported on return; a device-side timeout
+ *     (a pipeline wait that gave up) is reported by fa_check_device_error.
+ *   - There is no CPU fallback: a shape or dtype no kernel covers returns
+ *     FA_ERR_UNSUPPORTED.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,   /* NULL/misaligned pointer, bad size, non-finite scale */
+    FA_ERR_UNSUPPORTED = 2,   /* valid arguments that no kernel here covers */
+    FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (text in fa_last_error) */
+    FA_ERR_TIMEOUT = 4        /* a device pipeline wait gave up (see fa_check_device_error) */
+} fa_status;
+
+typedef enum fa_dtype {
+    FA_BF16 = 0,              /* bfloat16 storage */
+    FA_FP32 = 1               /* float32 storage */
+} fa_dtype;
+
+/* fa_forward_ex flags */
+#define FA_FLAG_GENERAL_PATH 0x1u  /* run the general-d CUDA-core kernel even where
+                                      the tensor-core kernel applies */
+
+/*
+ * fa_forward -- O (and LSE) of one attention forward pass.
+ *
+ *   q, k, v   device pointers, [B, H, N, d] elements of `in_dtype`.
+ *   o         device pointer, [B, H, N, d] elements of `o_dtype`; written.
+ *   lse       device pointer to [B, H, N] float32, or NULL to skip it.
+ *   B, H, N   >= 1; B * H * N < 2^31.   d: 1 <= d <= 1024.
+ *   scale     finite; pass 1/sqrt(d) for the usual 1/sqrt(d_k) scaling.
+ *   causal    0 or non-zero (mask key j > query i).
+ *   in_dtype, o_dtype   fa_dtype values.
+ *   stream    cudaStream_t to enqueue on.
+ *
+ * Pointers must be aligned to their element size; the tensor-core kernel is
+ * used when in_dtype = FA_BF16, d is 64 or 128 and q, k, v, o are 16-byte
+ * aligned, the general-d kernel otherwise.  Outputs are undefined if the
+ * call does not return FA_OK.  O must not overlap Q, K, V or LSE.
+ */
+fa_status fa_forward(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+                     int in_dtype, int o_dtype, void *stream);
+
+/* fa_forward with FA_FLAG_* bits in `flags` (0 = fa_forward). */
+fa_status fa_forward_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                        int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+                        int in_dtype, int o_dtype, void *stream, uint32_t flags);
+
+/*
+ * fa_check_device_error -- synchronise `stream`, then read and clear the
+ * device-side error word the kernels set when a bounded pipeline wait gives
+ * up.  Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if the stream itself
+ * reports an error.
+ */
+fa_status fa_check_device_error(void *stream);
+
+/* Text of the last failure on the calling host thread ("" if none).  The
+ * pointer stays valid until the next fa_* call on that thread. */
+const char *fa_last_error(void);
+
+/* Library version string, e.g. "0.1.0 sm_103a". */
+const char *fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */

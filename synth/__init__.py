@@ -29,6 +29,8 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -41,7 +43,7 @@ _S31 = np.uint64(31)
 _S11 = np.uint64(11)
 _ONE = np.uint64(1)
 
-CHUNK = 1 << 22
+CHUNK = 1 << 20
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -95,16 +97,23 @@ def tensor(stream: int, shape, dtype: str, mult: float = 1.0) -> np.ndarray:
     applied after rounding and must then be a power of two so that the
     product stays exact.
     """
+    if dtype not in ("bf16", "fp32"):
+        raise ValueError(f"unknown dtype {dtype!r}")
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.float32)
-    for lo in range(0, n, CHUNK):
+
+    def fill(lo):
         hi = min(n, lo + CHUNK)
         x = normal(stream, hi - lo, lo).astype(np.float32)
-        if dtype == "bf16":
-            x = round_to_bf16(x)
-        elif dtype != "fp32":
-            raise ValueError(f"unknown dtype {dtype!r}")
-        out[lo:hi] = x
+        out[lo:hi] = round_to_bf16(x) if dtype == "bf16" else x
+
+    starts = range(0, n, CHUNK)
+    if len(starts) > 1:
+        # numpy releases the GIL inside these array operations
+        with ThreadPoolExecutor(max_workers=min(len(starts), os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, starts))
+    elif n:
+        fill(0)
     if mult != 1.0:
         m, e = math.frexp(mult)
         if m != 0.5:

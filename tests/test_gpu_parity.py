@@ -1,0 +1,151 @@
+"""GPU parity: the CUDA kernels (through the C ABI) against the CPU fp64 oracle.
+
+Small shapes are compared element by element on every output; the five
+workload shapes at full size are compared on sampled rows (every head's
+first and last rows and tile edges, plus a seeded draw) against the full
+key range.  Both kernels are covered: the tensor-core kernel (bf16, d of 64
+or 128) through the default dispatch and the general-d kernel through
+FA_FLAG_GENERAL_PATH.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import tiled_online_softmax_attn_gb300 as fa
+from parity import compare, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+TORCH_DT = {"bf16": torch.bfloat16, "fp32": torch.float32}
+PATHS = {"auto": 0, "general": fa.FA_FLAG_GENERAL_PATH}
+
+
+def to_dev(x, dtype):
+    return torch.from_numpy(np.ascontiguousarray(x)).to("cuda").to(TORCH_DT[dtype])
+
+
+def run(q, k, v, dtype, scale, causal, o_dtype=None, flags=0):
+    qd, kd, vd = (to_dev(x, dtype) for x in (q, k, v))
+    o, lse = fa.fa_forward(qd, kd, vd, scale=scale, causal=causal,
+                           o_dtype=TORCH_DT[o_dtype or dtype], flags=flags)
+    torch.cuda.synchronize()
+    assert fa.check_device_error() == fa.FA_OK, fa.last_error()
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def full_check(w, path, o_dtype=None):
+    q, k, v = w.inputs()
+    o, lse = run(q, k, v, w.dtype, w.scale, w.causal, o_dtype, PATHS[path])
+    o_ref, lse_ref = oracle.attention(q, k, v, w.scale, w.causal)
+    return compare(o, lse, o_ref, lse_ref, w.dtype, o_dtype or w.dtype)
+
+
+SMALL = [
+    # (B, H, N, d, dtype, causal): several tiles plus ragged tails
+    (1, 2, 256, 64, "bf16", False),
+    (1, 2, 256, 64, "bf16", True),
+    (2, 3, 200, 64, "bf16", True),
+    (1, 2, 77, 128, "bf16", False),
+    (2, 1, 129, 128, "bf16", False),
+    (1, 2, 300, 128, "bf16", True),
+    (1, 1, 513, 64, "bf16", True),
+    (1, 1, 640, 128, "bf16", False),
+    (1, 1, 1, 64, "bf16", False),
+    (1, 1, 1, 128, "bf16", True),
+    (3, 2, 96, 128, "fp32", False),
+]
+
+
+@pytest.mark.parametrize("path", ["auto", "general"])
+@pytest.mark.parametrize("B,H,N,d,dtype,causal", SMALL)
+def test_small_shapes_full(B, H, N, d, dtype, causal, path):
+    w = synth.Workload("t", B, H, N, d, dtype, causal, seed=1000 + N + d)
+    full_check(w, path)
+
+
+@pytest.mark.parametrize("d", [1, 3, 16, 40, 100, 200, 257])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_general_head_dims(d, dtype, causal):
+    w = synth.Workload("t", 1, 2, 150, d, dtype, causal, seed=2000 + d)
+    full_check(w, "general")
+
+
+@pytest.mark.parametrize("path", ["auto", "general"])
+@pytest.mark.parametrize("o_dtype", ["bf16", "fp32"])
+def test_tiny_workload(path, o_dtype):
+    full_check(synth.WORKLOADS["tiny"], path, o_dtype)
+
+
+def test_large_d_fp32_workload():
+    stats = full_check(synth.WORKLOADS["large_d"], "auto")
+    assert stats["o_max"] <= 2e-4
+
+
+def _sampled(w, o_dtype=None, flags=0, nrows=384):
+    q, k, v = w.inputs()
+    o, lse = run(q, k, v, w.dtype, w.scale, w.causal, o_dtype, flags)
+    rows = sample_rows(w.B, w.H, w.N, nrows, seed=w.seed)
+    o_ref, lse_ref = oracle.attention_rows(q, k, v, w.scale, w.causal, rows)
+    return compare(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref,
+                   w.dtype, o_dtype or w.dtype)
+
+
+@pytest.mark.parametrize("name", ["multihead", "causal", "peaked"])
+def test_full_size_workloads_sampled(name):
+    _sampled(synth.WORKLOADS[name])
+
+
+def test_peaked_workload_fp32_output():
+    """With fp32 O the plain bounds hold without the bf16 rounding floor."""
+    _sampled(synth.WORKLOADS["peaked"], o_dtype="fp32")
+
+
+def test_repeat_runs_are_bitwise_identical():
+    w = synth.WORKLOADS["tiny"].scaled(N=333, causal=True)
+    q, k, v = w.inputs()
+    a = run(q, k, v, w.dtype, w.scale, w.causal)
+    b = run(q, k, v, w.dtype, w.scale, w.causal)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_side_stream_and_no_lse():
+    w = synth.WORKLOADS["tiny"]
+    q, k, v = (to_dev(x, "bf16") for x in w.inputs())
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o, lse = fa.fa_forward(q, k, v, return_lse=False, stream=s)
+    s.synchronize()
+    assert lse is None
+    o_ref, _ = oracle.attention(*w.inputs(), w.scale, False)
+    compare(o.float().cpu().numpy(), None, o_ref, None, "bf16", "bf16")
+
+
+def test_uniform_scores_give_mean_of_values_on_gpu():
+    """Q = 0: every causal row i is the mean of v_0..v_i (closed form)."""
+    N, d = 300, 128
+    v = synth.tensor(77, (1, 1, N, d), "bf16")
+    q = np.zeros_like(v)
+    k = synth.tensor(78, (1, 1, N, d), "bf16")
+    for flags in PATHS.values():
+        o, lse = run(q, k, v, "bf16", 0.1, True, "fp32", flags)
+        ref = np.cumsum(v[0, 0].astype(np.float64), axis=0) / np.arange(1, N + 1)[:, None]
+        assert np.abs(o[0, 0] - ref).max() < 1e-3
+        assert np.abs(lse[0, 0] - np.log(np.arange(1, N + 1))).max() < 1e-4
+
+
+def test_invalid_arguments_are_rejected_before_launch():
+    q = torch.zeros((1, 1, 8, 64), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    st = fa.forward_raw(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), None,
+                        1, 1, 8, 64, float("nan"), 0, fa.FA_BF16, fa.FA_BF16)
+    assert st == fa.FA_ERR_INVALID_ARG
+    st = fa.forward_raw(q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), None,
+                        1, 1, 8, 64, 1.0, 0, fa.FA_BF16, fa.FA_BF16)
+    assert st == fa.FA_ERR_INVALID_ARG and "overlap" in fa.last_error()
+    st = fa.forward_raw(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), None,
+                        1, 1, 8, 2048, 1.0, 0, fa.FA_BF16, fa.FA_BF16)
+    assert st == fa.FA_ERR_UNSUPPORTED

@@ -1,0 +1,9 @@
+"""GB300 (sm_103a) exact attention forward, O = softmax(Q K^T * scale) V.
+
+The work runs in hand-written CUDA kernels behind the C ABI of
+``include/fa.h`` (``libfa_gb300.so``); this package is its thin Python
+binding.  Build the library with ``tiled_online_softmax_attn_gb300.build.build()``.
+"""
+from ._binding import (FA_BF16, FA_ERR_CUDA, FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT,  # noqa: F401
+                       FA_ERR_UNSUPPORTED, FA_FLAG_GENERAL_PATH, FA_FP32, FA_OK, FAError,
+                       check_device_error, fa_forward, forward_raw, last_error, load, version)

@@ -1,0 +1,139 @@
+"""ctypes binding of the C ABI in include/fa.h.
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+kernels of libfa_gb300.so.  There is no fallback -- if the library is
+missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
+                4: "FA_ERR_TIMEOUT"}
+
+FA_BF16 = 0
+FA_FP32 = 1
+FA_FLAG_GENERAL_PATH = 0x1
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa_gb300.so")
+
+# name -> (restype, argtypes) for every function include/fa.h declares
+_I64 = ctypes.c_int64
+_P = ctypes.c_void_p
+SIGNATURES = {
+    "fa_forward": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
+                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]),
+    "fa_forward_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, ctypes.c_uint32]),
+    "fa_check_device_error": (ctypes.c_int, [_P]),
+    "fa_last_error": (ctypes.c_char_p, []),
+    "fa_version": (ctypes.c_char_p, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def load(path: str | None = None):
+    """Load libfa_gb300.so (built by ``build()``) and bind its symbols."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise FileNotFoundError(
+                f"{p} is missing: build the CUDA library first (__graft_entry__.build())")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def last_error() -> str:
+    return load().fa_last_error().decode()
+
+
+def version() -> str:
+    return load().fa_version().decode()
+
+
+def check(status: int) -> None:
+    if status != FA_OK:
+        raise FAError(status, last_error())
+
+
+def forward_raw(q, k, v, o, lse, B, H, N, d, scale, causal, in_dtype, o_dtype, stream=0, flags=0) -> int:
+    """Direct call with integer pointers; returns the fa_status."""
+    lib = load()
+    return lib.fa_forward_ex(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), in_dtype,
+                             o_dtype, stream, flags)
+
+
+def check_device_error(stream=0) -> int:
+    return load().fa_check_device_error(stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t == torch.bfloat16:
+        return FA_BF16
+    if t == torch.float32:
+        return FA_FP32
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def fa_forward(q, k, v, o=None, lse=None, scale=None, causal=False, o_dtype=None,
+               return_lse=True, stream=None, flags=0):
+    """O = softmax(q k^T * scale) v on [B, H, N, d] CUDA tensors.
+
+    Returns (o, lse); ``lse`` is None when ``return_lse`` is False and no
+    buffer was passed.  ``o``/``lse`` may be given to write into existing
+    buffers.  ``scale`` defaults to 1/sqrt(d).  The call is asynchronous on
+    ``stream`` (default: torch's current stream).
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor [B, H, N, d]")
+    if q.shape != k.shape or q.shape != v.shape or q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError("q, k, v must share shape and dtype")
+    B, H, N, d = q.shape
+    in_code = _dtype_code(q.dtype)
+    if o is None:
+        o = torch.empty(q.shape, dtype=o_dtype or q.dtype, device=q.device)
+    elif not o.is_contiguous() or o.shape != q.shape:
+        raise ValueError("o must be contiguous with q's shape")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or lse.shape != (B, H, N)):
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    st = forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                     lse.data_ptr() if lse is not None else None, B, H, N, d, float(scale),
+                     causal, in_code, _dtype_code(o.dtype), stream, flags)
+    check(st)
+    return o, lse
