@@ -1,19 +1,550 @@
-// Tensor-core attention forward (tcgen05 + TMA) -- placeholder until the
-// kernel lands: reports itself unsupported so the general path runs.
+// Tensor-core attention forward for sm_103a: TMA -> shared memory ->
+// tcgen05.mma into tensor memory, warp-specialised online softmax.
+//
+// Algorithm: the tiled online-softmax forward of "Deep Learning - Flash
+// Attention" ("An Example", steps 4-7) and "FlashAttention" (ai360xpert.com,
+// "Tiling and online softmax"), in the unnormalised form -- O and l are
+// multiplied by alpha = 2^(m_old - m_new) when a key tile raises the running
+// row maximum, P = 2^(S * scale * log2 e - m_new) feeds O += P V, and O is
+// divided by l once after the last key tile.  Scores live in log2 units so
+// each weight is one FFMA and one ex2.
+//
+// One CTA owns two 128-row query tiles (Q0, Q1) of one (batch, head) and
+// streams that head's K/V tiles (128 keys) through a shared-memory ring:
+//
+//   warp 8  (TMA)      loads Q0, Q1 once and K_j, V_j into the K and V rings
+//                      (full/empty mbarrier pairs per slot);
+//   warp 9  (MMA)      allocates tensor memory and, from one thread, issues
+//                      S_t = Q_t K_j^T (SS form) and O_t += P_t V_j (A operand
+//                      read from tensor memory), alternating the two tiles so
+//                      the tensor core works on one tile while the other
+//                      tile's softmax runs;
+//   warps 0-3 / 4-7    softmax for Q0 / Q1: one query row per thread (a warp
+//                      reads its 32 tensor-memory lanes), row max, weights,
+//                      row sum, bf16 P written back over S, the alpha rescale
+//                      of O in tensor memory, and the epilogue (O / l, LSE).
+//
+// Tensor memory (512 columns x 128 lanes x 32 bit):
+//   [  0,128) S0 / P0   [128,256) S1 / P1   [256, 256+D) O0   [256+D, 256+2D) O1
+// P_t (bf16, two per column) overwrites the first 64 columns of S_t; the
+// next S_t MMA is issued after the P_t V MMA, and MMAs from one thread run
+// in issue order.
+//
+// Every mbarrier wait is bounded (a caller-given limit in ns).  A wait that
+// gives up sets the device error word and a CTA-wide abort flag; every role
+// then leaves its loop, the MMA thread waits for its issued MMAs, the TMA
+// thread for its issued loads, and tensor memory is freed before exit.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <cmath>
 #include <cstdint>
+#include <mutex>
+
 #include "fa_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace fa {
 
 __device__ uint32_t g_tc_error_word;
 
-bool tc_supported(const Problem &) { return false; }
+namespace {
 
-cudaError_t launch_tc(const Problem &, cudaStream_t, uint32_t, const char **detail)
+using namespace ptx;
+
+constexpr int BM = 128;           // query rows per tile (tensor-memory lanes)
+constexpr int BN = 128;           // keys per tile
+constexpr int NUM_THREADS = 320;  // 10 warps
+constexpr int TMA_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr uint32_t TMEM_COLS = 512;
+
+// error word bits
+constexpr uint32_t ERR_WAIT_TMA = 1u;       // producer gave up waiting for a free slot
+constexpr uint32_t ERR_WAIT_MMA = 2u;       // MMA thread gave up waiting for data or P
+constexpr uint32_t ERR_WAIT_SOFTMAX = 4u;   // softmax gave up waiting for S or O
+constexpr uint32_t ERR_DRAIN = 8u;          // teardown could not confirm in-flight work
+
+template <int D>
+struct Cfg {
+    static constexpr int CHUNKS = D / 64;                  // 128-byte swizzle chunks per row
+    static constexpr uint32_t TILE_BYTES = BM * D * 2;     // one 128 x D bf16 tile
+    static constexpr int KS = (D == 128) ? 2 : 3;          // K ring slots
+    static constexpr int VS = (D == 128) ? 2 : 3;          // V ring slots
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_K = 2 * TILE_BYTES;
+    static constexpr uint32_t OFF_V = OFF_K + KS * TILE_BYTES;
+    static constexpr uint32_t SMEM_TILES = OFF_V + VS * TILE_BYTES;
+    static constexpr uint32_t SMEM_BYTES = SMEM_TILES + 1024;  // + alignment slack
+    static constexpr uint32_t COL_O = 256;                 // O0 at 256, O1 at 256 + D
+};
+
+struct Params {
+    int N;             // sequence length
+    int BH;            // batch * heads
+    int n_qblocks;     // CTAs per head (256 query rows each)
+    int n_kv;          // key tiles per head
+    float scale_log2;  // scale * log2(e), > 0
+    int causal;
+    int skip_load;     // fault injection: never issue the K load of this tile (-1 = off)
+    uint64_t wait_limit_ns;
+    void *o;
+    float *lse;
+    int o_fp32;
+};
+
+struct __align__(8) Barriers {
+    uint64_t q_full[2];
+    uint64_t k_full[3], k_empty[3];
+    uint64_t v_full[3], v_empty[3];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_full[2];
+    uint64_t drain;
+};
+
+__device__ __forceinline__ void raise_error(uint32_t bit, volatile int *abort_flag)
 {
-    *detail = "tensor-core kernel not built";
-    return cudaErrorNotSupported;
+    atomicOr(&g_tc_error_word, bit);
+    *abort_flag = 1;
+}
+
+// A bounded wait that also returns early once another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int *abort_flag)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((spin & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void store_o_row(void *o, int o_fp32, size_t row_elem, const float *vals,
+                                            int col0, int ncols)
+{
+    if (o_fp32) {
+        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(o) + row_elem + col0);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+            if (4 * x < ncols) dst[x] = make_float4(vals[4 * x], vals[4 * x + 1], vals[4 * x + 2], vals[4 * x + 3]);
+        }
+    } else {
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o) + row_elem + col0);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            uint4 w;
+            w.x = pack_bf16x2(vals[8 * x + 0], vals[8 * x + 1]);
+            w.y = pack_bf16x2(vals[8 * x + 2], vals[8 * x + 3]);
+            w.z = pack_bf16x2(vals[8 * x + 4], vals[8 * x + 5]);
+            w.w = pack_bf16x2(vals[8 * x + 6], vals[8 * x + 7]);
+            dst[x] = w;
+        }
+    }
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+             const __grid_constant__ CUtensorMap tm_v, const Params prm)
+{
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ Barriers bars;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ volatile int abort_flag;
+
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s_base = smem_addr(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- work item: (query block of 256 rows, head)
+    int qb, bh;
+    if (CAUSAL) {  // longest query blocks first
+        qb = prm.n_qblocks - 1 - (int)(blockIdx.x / prm.BH);
+        bh = (int)(blockIdx.x % prm.BH);
+    } else {       // CTAs of one head run together and share its K/V in L2
+        qb = (int)(blockIdx.x % prm.n_qblocks);
+        bh = (int)(blockIdx.x / prm.n_qblocks);
+    }
+    const int N = prm.N;
+    const int qrow0 = qb * 2 * BM;  // first row of Q0; Q1 starts BM later
+    // key tiles each query tile needs: all, or up to its diagonal under the mask
+    const int n0 = CAUSAL ? min(prm.n_kv, 2 * qb + 1) : prm.n_kv;
+    const int n1 = CAUSAL ? min(prm.n_kv, 2 * qb + 2) : prm.n_kv;
+
+    // ---- setup
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_addr(&bars.q_full[0]), 1);
+        mbar_init(smem_addr(&bars.q_full[1]), 1);
+        for (int s = 0; s < 3; ++s) {
+            mbar_init(smem_addr(&bars.k_full[s]), 1);
+            mbar_init(smem_addr(&bars.k_empty[s]), 1);
+            mbar_init(smem_addr(&bars.v_full[s]), 1);
+            mbar_init(smem_addr(&bars.v_empty[s]), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_addr(&bars.s_full[t]), 1);
+            mbar_init(smem_addr(&bars.p_full[t]), 128);
+            mbar_init(smem_addr(&bars.o_full[t]), 1);
+        }
+        mbar_init(smem_addr(&bars.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == MMA_WARP) {
+        tmem_alloc(smem_addr(&tmem_base_s), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    const uint64_t limit = prm.wait_limit_ns;
+
+    if (warp == TMA_WARP) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            const uint64_t pol_q = policy_evict_first();
+            const uint64_t pol_kv = policy_evict_last();
+            int k_issued = 0, v_issued = 0;  // tiles whose loads were issued
+            bool ok = true;
+            auto load_q = [&](int t) {
+                const uint32_t bar = smem_addr(&bars.q_full[t]);
+                mbar_arrive_expect_tx(bar, C::TILE_BYTES);
+                for (int c = 0; c < C::CHUNKS; ++c)
+                    tma_load_3d(s_base + C::OFF_Q + t * C::TILE_BYTES + c * (BM * 128), &tm_q, bar, c * 64,
+                                qrow0 + t * BM, bh, pol_q);
+            };
+            auto load_kv = [&](bool is_k, int j) -> bool {
+                const int S = is_k ? C::KS : C::VS;
+                const int slot = j % S;
+                const uint32_t n_use = (uint32_t)(j / S);
+                const uint32_t empty = smem_addr(is_k ? &bars.k_empty[slot] : &bars.v_empty[slot]);
+                const uint32_t full = smem_addr(is_k ? &bars.k_full[slot] : &bars.v_full[slot]);
+                if (!wait_or_abort(empty, (n_use & 1u) ^ 1u, limit, &abort_flag)) return false;
+                if (is_k && j == prm.skip_load) return true;  // fault injection: never arrives
+                mbar_arrive_expect_tx(full, C::TILE_BYTES);
+                const uint32_t dst = s_base + (is_k ? C::OFF_K : C::OFF_V) + slot * C::TILE_BYTES;
+                for (int c = 0; c < C::CHUNKS; ++c)
+                    tma_load_3d(dst + c * (BN * 128), is_k ? &tm_k : &tm_v, full, c * 64, j * BN, bh, pol_kv);
+                return true;
+            };
+            load_q(0);
+            ok = load_kv(true, 0);
+            if (ok) { k_issued = 1; load_q(1); }
+            if (ok) { ok = load_kv(false, 0); if (ok) v_issued = 1; }
+            for (int j = 1; ok && j < n1; ++j) {
+                ok = load_kv(true, j);
+                if (ok) { k_issued = j + 1; ok = load_kv(false, j); }
+                if (ok) v_issued = j + 1;
+            }
+            if (!ok) {
+                if (!abort_flag) raise_error(ERR_WAIT_TMA, &abort_flag);
+            }
+            // Before the CTA exits, every load issued must have landed.
+            auto drain = [&](bool is_k, int issued) {
+                const int S = is_k ? C::KS : C::VS;
+                for (int j = max(0, issued - S); j < issued; ++j) {
+                    if (is_k && j == prm.skip_load) continue;
+                    const uint32_t full = smem_addr(is_k ? &bars.k_full[j % S] : &bars.v_full[j % S]);
+                    if (!mbar_wait_bounded(full, (uint32_t)((j / S) & 1), limit)) atomicOr(&g_tc_error_word, ERR_DRAIN);
+                }
+            };
+            if (abort_flag) {
+                drain(true, k_issued);
+                drain(false, v_issued);
+                for (int t = 0; t < 2; ++t)
+                    if (!mbar_wait_bounded(smem_addr(&bars.q_full[t]), 0, limit)) atomicOr(&g_tc_error_word, ERR_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
+            const uint32_t idesc_o = idesc_bf16_f32(BM, D, 0, 1);
+            const uint32_t sQ = s_base + C::OFF_Q, sK = s_base + C::OFF_K, sV = s_base + C::OFF_V;
+            bool ok = true;
+            bool issued_any = false;
+            auto wait = [&](uint64_t *b, uint32_t parity) -> bool {
+                if (!ok) return false;
+                if (!wait_or_abort(smem_addr(b), parity, limit, &abort_flag)) {
+                    ok = false;
+                    if (!abort_flag) raise_error(ERR_WAIT_MMA, &abort_flag);
+                    return false;
+                }
+                return true;
+            };
+            // S_t = Q_t K_j^T   (M = 128 rows, N = 128 keys, K = D in steps of 16)
+            auto mma_s = [&](int t, int j) {
+                const uint32_t q = sQ + t * C::TILE_BYTES, k = sK + (j % C::KS) * C::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+                    mma_ss(tmem + t * 128, sdesc_sw128(q + off, 16, 1024), sdesc_sw128(k + off, 16, 1024),
+                           idesc_s, kk > 0 ? 1u : 0u);
+                }
+                issued_any = true;
+            };
+            // O_t += P_t V_j   (M = 128 rows, N = D, K = 128 keys in steps of 16)
+            auto mma_o = [&](int t, int j) {
+                const uint32_t v = sV + (j % C::VS) * C::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(tmem + C::COL_O + t * D, tmem + t * 128 + kk * 8,
+                           sdesc_sw128(v + kk * (16 * 128), BN * 128, 1024), idesc_o,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                issued_any = true;
+            };
+            if (wait(&bars.q_full[0], 0) && wait(&bars.k_full[0], 0)) {
+                tc_fence_after();
+                mma_s(0, 0);
+                mma_commit(smem_addr(&bars.s_full[0]));
+            }
+            if (wait(&bars.q_full[1], 0)) {
+                tc_fence_after();
+                mma_s(1, 0);
+                mma_commit(smem_addr(&bars.s_full[1]));
+                mma_commit(smem_addr(&bars.k_empty[0]));
+            }
+            for (int j = 1; ok && j < n1; ++j) {
+                if (!wait(&bars.k_full[j % C::KS], (uint32_t)((j / C::KS) & 1))) break;
+                if (!wait(&bars.v_full[(j - 1) % C::VS], (uint32_t)(((j - 1) / C::VS) & 1))) break;
+                // tile 0
+                if (j <= n0) {
+                    if (!wait(&bars.p_full[0], (uint32_t)((j - 1) & 1))) break;
+                    tc_fence_after();
+                    mma_o(0, j - 1);
+                    if (j < n0) {
+                        mma_s(0, j);
+                        mma_commit(smem_addr(&bars.s_full[0]));
+                    } else {
+                        mma_commit(smem_addr(&bars.o_full[0]));
+                    }
+                }
+                // tile 1
+                if (!wait(&bars.p_full[1], (uint32_t)((j - 1) & 1))) break;
+                tc_fence_after();
+                mma_o(1, j - 1);
+                mma_s(1, j);
+                mma_commit(smem_addr(&bars.s_full[1]));
+                mma_commit(smem_addr(&bars.k_empty[j % C::KS]));
+                mma_commit(smem_addr(&bars.v_empty[(j - 1) % C::VS]));
+            }
+            if (ok) {
+                const int last = n1 - 1;
+                if (wait(&bars.v_full[last % C::VS], (uint32_t)((last / C::VS) & 1))) {
+                    if (n0 == n1 && wait(&bars.p_full[0], (uint32_t)(last & 1))) {
+                        tc_fence_after();
+                        mma_o(0, last);
+                        mma_commit(smem_addr(&bars.o_full[0]));
+                    }
+                    if (wait(&bars.p_full[1], (uint32_t)(last & 1))) {
+                        tc_fence_after();
+                        mma_o(1, last);
+                        mma_commit(smem_addr(&bars.o_full[1]));
+                    }
+                }
+            }
+            if (!ok && issued_any) {
+                // every MMA issued so far must finish before tensor memory is freed
+                mma_commit(smem_addr(&bars.drain));
+                if (!mbar_wait_bounded(smem_addr(&bars.drain), 0, limit)) atomicOr(&g_tc_error_word, ERR_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================================================================ softmax + epilogue
+        const int t = warp >> 2;          // query tile 0 or 1
+        const int quarter = warp & 3;     // tensor-memory lanes 32*quarter ...
+        const int r = quarter * 32 + lane;
+        const int grow = qrow0 + t * BM + r;  // global query row of this thread
+        const int n_t = t == 0 ? n0 : n1;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t tS = lane_base + t * 128;
+        const uint32_t tO = lane_base + C::COL_O + t * D;
+        const float sl = prm.scale_log2;
+        float m = -INFINITY;  // running maximum, log2 units
+        float l = 0.f;        // running denominator
+        bool ok = true;
+        for (int j = 0; j < n_t; ++j) {
+            if (!wait_or_abort(smem_addr(&bars.s_full[t]), (uint32_t)(j & 1), limit, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float s[BN];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(tS + c * 32, raw);
+#pragma unroll
+                for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(raw[x]);
+            }
+            const int kv0 = j * BN;
+            int lim = N - kv0;                          // keys >= N are padding
+            if (CAUSAL) lim = min(lim, grow - kv0 + 1);  // keys after this query
+            if (lim < BN) {
+#pragma unroll
+                for (int c = 0; c < BN; ++c)
+                    if (c >= lim) s[c] = -INFINITY;
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+            const float m_new = fmaxf(m, mx * sl);
+            const float base = (m_new == -INFINITY) ? 0.f : m_new;
+            const float alpha = ex2(m - base);  // 0 on the first tile
+            float rs = 0.f;
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const float p0 = ex2(fmaf(s[c * 32 + 2 * x], sl, -base));
+                    const float p1 = ex2(fmaf(s[c * 32 + 2 * x + 1], sl, -base));
+                    rs += p0 + p1;
+                    pk[x] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(tS + c * 16, pk);
+            }
+            l = l * alpha + rs;
+            // O_t already holds every earlier P V product: the commit that
+            // signalled this S tile covers all MMAs issued before it.
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(tO + c * 32, raw);
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) raw[x] = __float_as_uint(__uint_as_float(raw[x]) * alpha);
+                    tmem_st32(tO + c * 32, raw);
+                }
+            }
+            m = m_new;
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_addr(&bars.p_full[t]));
+        }
+        // ---- epilogue: O / l, LSE
+        if (ok && wait_or_abort(smem_addr(&bars.o_full[t]), 0, limit, &abort_flag)) {
+            tc_fence_after();
+            const float inv_l = 1.f / l;
+            const size_t row_elem = ((size_t)bh * N + (size_t)grow) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(tO + c * 32, raw);
+                float vals[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) vals[x] = __uint_as_float(raw[x]) * inv_l;
+                if (grow < N) store_o_row<D>(prm.o, prm.o_fp32, row_elem, vals, c * 32, 32);
+            }
+            if (prm.lse && grow < N) prm.lse[(size_t)bh * N + grow] = (m + log2f(l)) * 0.69314718055994530942f;
+        } else if (!abort_flag) {
+            raise_error(ERR_WAIT_SOFTMAX, &abort_flag);
+        } else {
+            atomicOr(&g_tc_error_word, ERR_WAIT_SOFTMAX);
+        }
+    }
+
+    // ---- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [BH, N, d] bf16 viewed as a 3-D tensor (d innermost); box = 64 columns
+// (128 bytes, the swizzle width) x 128 rows x 1 head.  Rows past N of a head
+// read as zeros.
+bool make_map(CUtensorMap *map, const void *ptr, int64_t BH, int64_t N, int64_t d)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)(N * d * 2)};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, const char **detail)
+{
+    using Cf = Cfg<D>;
+    CUtensorMap mq, mk, mv;
+    const int64_t BH = p.B * p.H;
+    if (!make_map(&mq, p.q, BH, p.N, D) || !make_map(&mk, p.k, BH, p.N, D) || !make_map(&mv, p.v, BH, p.N, D)) {
+        *detail = "cuTensorMapEncodeTiled failed or is unavailable";
+        return cudaErrorInvalidValue;
+    }
+    Params prm;
+    prm.N = (int)p.N;
+    prm.BH = (int)BH;
+    prm.n_qblocks = (int)((p.N + 2 * BM - 1) / (2 * BM));
+    prm.n_kv = (int)((p.N + BN - 1) / BN);
+    prm.scale_log2 = p.scale * 1.4426950408889634f;
+    prm.causal = CAUSAL;
+    prm.skip_load = -1;
+    prm.wait_limit_ns = 2000000000ull;  // 2 s: far above any legitimate wait
+    prm.o = p.o;
+    prm.lse = p.lse;
+    prm.o_fp32 = p.o_dtype == 1;
+    (void)flags;
+    auto kern = fa_tc_kernel<D, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = (int64_t)prm.n_qblocks * BH;
+    kern<<<(unsigned)grid, NUM_THREADS, Cf::SMEM_BYTES, stream>>>(mq, mk, mv, prm);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(const Problem &p)
+{
+    if (p.in_dtype != 0 || !(p.d == 64 || p.d == 128) || !(p.scale > 0.f)) return false;
+    auto al16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
+    return al16(p.q) && al16(p.k) && al16(p.v) && al16(p.o);
+}
+
+cudaError_t launch_tc(const Problem &p, cudaStream_t stream, uint32_t flags, const char **detail)
+{
+    if (p.d == 128) return p.causal ? launch_typed<128, true>(p, stream, flags, detail)
+                                    : launch_typed<128, false>(p, stream, flags, detail);
+    return p.causal ? launch_typed<64, true>(p, stream, flags, detail) : launch_typed<64, false>(p, stream, flags, detail);
 }
 
 cudaError_t tc_take_error_word(uint32_t *word, cudaStream_t stream)
