@@ -1,0 +1,368 @@
+"""Benchmark of the attention forward pass on GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload multihead|causal|peaked|tiny|large_d]
+
+One step = one forward pass (fa_forward, one kernel launch) over the whole
+workload.  Default workload: B=4, H=32, N=4096, d=128, bf16, non-causal --
+the multi-head shape the throughput target is quoted on.  Inputs are the
+seeded synthetic tensors of ``synth`` (i.i.d. N(0,1), rounded to bf16),
+resident in HBM before timing.  Q, K and V (403 MB) are larger than L2
+(129 MB), so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  ``value`` is TFLOP/s = 4*B*H*N^2*d / time
+(halved under a causal mask) summed over ranks; ``e2e`` is the same metric
+through fa_forward_host with pinned host buffers, the copies inside the
+timed region; ``roofline`` relates the kernel to the measured bf16 tensor
+peak; ``cpu_baseline`` times the CPU oracle on a bounded row sample.
+
+``--impl reference`` times that oracle (the plain CPU definition) as the
+reference arm on the same workload, a bounded row sample per step.
+Under torchrun (N > 1) every rank runs the whole workload on its own GPU
+(independent replicas: the forward pass has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (4·B·H·N²·d/time) and % of GB300 BF16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {"tc": "tiled_online_softmax_attn_gb300/csrc/fa_tc.cu",
+                  "general": "tiled_online_softmax_attn_gb300/csrc/fa_general.cu"}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_desc(w):
+    return (f"{w.name}: B={w.B} H={w.H} N={w.N} d={w.d} {w.dtype}"
+            f"{' causal' if w.causal else ''}{' QK x%g' % w.qk_mult if w.qk_mult != 1 else ''}")
+
+
+def source_digest(path):
+    with open(os.path.join(ROOT, path), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (matching digest) for this workload."""
+    path = os.path.join(ROOT, "profiles", f"ncu_{kernel_key}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_d = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    m_t = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
+    if not m_d or not m_t or m_d.group(1) != source_digest(KERNEL_SOURCES[kernel_key]):
+        return None
+    return float(m_t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = open(os.devnull, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                clk, mxc, pw = float(f[1]), float(f[2]), float(f[3])
+            except ValueError:
+                continue
+            mx = mxc
+            if pw > 200.0:   # samples under load
+                sm.append(clk)
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples_under_load": len(sm), "samples": len(self.lines)}
+
+
+def oracle_rows_rate(w, q, k, v, seconds, seed=0):
+    """Times the CPU oracle on a seeded row sample sized for about `seconds`;
+    returns (TFLOP/s, rows, threads, elapsed)."""
+    import oracle
+    threads = oracle.default_threads()
+    rng = np.random.default_rng(seed)
+    total = w.B * w.H * w.N
+    calib = rng.integers(0, total, size=max(threads, 8))
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.scale, w.causal, calib, threads)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    nrows = int(max(threads, min(total, len(calib) * seconds / dt)))
+    rows = rng.integers(0, total, size=nrows)
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.scale, w.causal, rows, threads)
+    el = time.perf_counter() - t0
+    i = rows % w.N
+    keys = (i + 1) if w.causal else np.full(nrows, w.N)
+    flops = float(4.0 * w.d * keys.sum())
+    return flops / el / 1e12, nrows, threads, el
+
+
+def reference_arm(args, w, q, k, v, rank, world):
+    """The oracle (plain fp64 CPU definition) timed as the reference arm."""
+    if rank != 0:
+        return
+    per_step = max(0.5, min(10.0, 90.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_rows_rate(w, q, k, v, per_step, seed=1)
+    rates, rows_total, el_total, threads = [], 0, 0.0, 1
+    for s in range(args.steps):
+        r, nrows, threads, el = oracle_rows_rate(w, q, k, v, per_step, seed=100 + s)
+        rates.append(r)
+        rows_total += nrows
+        el_total += el
+    value = statistics.mean(rates)
+    step_flops_full = w.flops
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_flops_full / (value * 1e12) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": workload_desc(w), "B": w.B, "H": w.H, "N": w.N,
+                                         "d": w.d, "causal": w.causal, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_total} seeded query rows (full key range each) over "
+                                   f"{args.steps} steps, {el_total:.1f} s; ms_per_step extrapolates "
+                                   f"to the whole workload"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def measure_e2e(args, w, fa, torch, dev, stream, q_h, k_h, v_h, q, o, lse, tdt, dist, world):
+    """The workload end to end through fa_forward_host: host-to-device copy of
+    Q, K, V from pinned host memory, the kernels, and the copy of O and LSE
+    back, every step inside the timed region."""
+    o_h = torch.empty(w.shape, dtype=tdt).pin_memory()
+    lse_h = torch.empty(w.shape[:3], dtype=torch.float32).pin_memory()
+    ws_bytes = fa.host_workspace_size(w.B, w.H, w.N, w.d, q.dtype, q.dtype)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        fa.forward_host(q_h, k_h, v_h, o_h, lse_h, ws, scale=w.scale, causal=w.causal, stream=stream)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = o.numel() * o.element_size() + lse.numel() * 4
+    # the host-buffer result must be the device result
+    if not torch.equal(o_h, o.cpu()) or not torch.equal(lse_h, lse.cpu()):
+        raise RuntimeError("host-buffer path disagrees with the device path")
+    return {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "fa_forward_host (pinned host buffers, wall clock per synchronous call)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="multihead", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--batch", type=int, help="override B of the workload (smaller profiling cases)")
+    ap.add_argument("--heads", type=int, help="override H of the workload")
+    ap.add_argument("--e2e-steps", type=int, default=20, help="0 skips the end-to-end measurement")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = synth.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.scaled(B=args.batch)
+    if args.heads:
+        w = w.scaled(H=args.heads)
+
+    if args.impl == "reference":
+        if rank == 0:
+            q, k, v = w.inputs()
+            reference_arm(args, w, q, k, v, rank, world)
+        return
+
+    import torch
+    import tiled_online_softmax_attn_gb300 as fa
+    from tiled_online_softmax_attn_gb300 import build as fa_build
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    fa_build.build()
+    fa.load()
+
+    q_np, k_np, v_np = w.inputs()
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    q_h, k_h, v_h = (torch.from_numpy(x).to(tdt).pin_memory() for x in (q_np, k_np, v_np))
+    q, k, v = (x.to(dev) for x in (q_h, k_h, v_h))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.shape[:3], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches = {"n": 0}
+
+    def step():
+        fa.fa_forward(q, k, v, o=o, lse=lse, scale=w.scale, causal=w.causal, stream=stream)
+        launches["n"] += 1
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.check_device_error(stream.cuda_stream) != fa.FA_OK:
+        raise RuntimeError(fa.last_error())
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches["n"] = 0
+    with ClockSampler(local_rank) as clocks:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    ms_total = e0.elapsed_time(e1)
+    timed_launches = launches["n"]
+    if fa.check_device_error(stream.cuda_stream) != fa.FA_OK:
+        raise RuntimeError(fa.last_error())
+    if dist:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * w.flops / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end: host buffers through fa_forward_host, copies inside the timed region
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = measure_e2e(args, w, fa, torch, dev, stream, q_h, k_h, v_h, q, o, lse, tdt, dist, world)
+    line_e2e = e2e
+
+    peaks, peak_kind = load_peaks()
+    kernel_key = "tc" if (w.dtype == "bf16" and w.d in (64, 128)) else "general"
+    if kernel_key == "tc":
+        peak = float(peaks["bf16_tflops"])
+        achieved = w.flops / (ms_step * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak}
+    else:
+        peak = float(peaks["hbm_gbs"])
+        achieved = w.bytes / (ms_step * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak}
+    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json, burst)" if peak_kind == "measured" else "fallback"
+    roof["traffic"] = profiled_traffic(kernel_key, w.name)
+    roof["algorithmic_bytes"] = w.bytes
+    roof["algorithmic_flops"] = w.flops
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "seed": w.seed, "parallelism": "replicas",
+                   "l2": "no flush: Q, K, V (%.0f MB) exceed L2 (129 MB)" % (3 * q.numel() * q.element_size() / 1e6)},
+        "pct_bf16_peak": 100.0 * (w.flops / (ms_step * 1e-3) / 1e12) / float(peaks["bf16_tflops"]),
+        "pct_bf16_peak_sustained": 100.0 * (w.flops / (ms_step * 1e-3) / 1e12) / float(peaks["bf16_tflops_sustained"]),
+        "roofline": roof,
+        "e2e": line_e2e,
+        "gpu_launches": timed_launches,
+        "kernel": kernel_key,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, nrows, threads, el = oracle_rows_rate(w, q_np, k_np, v_np, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{nrows} seeded query rows of the workload, full key range "
+                                          f"each, {el:.1f} s on {threads} host threads"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

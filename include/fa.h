@@ -90,6 +90,37 @@ fa_status fa_forward_ex(const void *q, const void *k, const void *v, void *o, fl
                         int in_dtype, int o_dtype, void *stream, uint32_t flags);
 
 /*
+ * fa_host_workspace_size -- bytes of device workspace fa_forward_host needs
+ * for this problem (device copies of Q, K, V, O and LSE, 256-byte aligned
+ * each).  Returns 0 for arguments fa_forward would reject.
+ */
+size_t fa_host_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int o_dtype);
+
+/*
+ * fa_forward_host -- the same forward pass on HOST buffers, end to end.
+ *
+ *   q_h, k_h, v_h  host pointers, [B, H, N, d] elements of `in_dtype`
+ *                  (page-locked memory lets the copies overlap the kernels).
+ *   o_h            host pointer, [B, H, N, d] elements of `o_dtype`; written.
+ *   lse_h          host pointer to [B, H, N] float32, or NULL.
+ *   workspace      device pointer, >= fa_host_workspace_size(...) bytes,
+ *                  256-byte aligned, owned by the caller; its contents on
+ *                  return are unspecified.
+ *   the rest       as fa_forward.
+ *
+ * The heads are split into up to 8 chunks; chunk c's host-to-device copy
+ * (on `stream`), its kernel and its device-to-host copy (on two streams the
+ * library creates once per device) form a pipeline, so copies in both
+ * directions overlap the compute of other chunks.  The call is synchronous:
+ * it returns once o_h and lse_h hold the result, or with the first error
+ * (a device-side timeout included).
+ */
+fa_status fa_forward_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, float *lse_h,
+                          int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+                          int in_dtype, int o_dtype, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/*
  * fa_check_device_error -- synchronise `stream`, then read and clear the
  * device-side error word the kernels set when a bounded pipeline wait gives
  * up.  Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if the stream itself

@@ -149,3 +149,33 @@ def test_invalid_arguments_are_rejected_before_launch():
     st = fa.forward_raw(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), None,
                         1, 1, 8, 2048, 1.0, 0, fa.FA_BF16, fa.FA_BF16)
     assert st == fa.FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("B,H,N,d,dtype,causal", [(2, 5, 300, 128, "bf16", True), (2, 8, 1024, 128, "bf16", True),
+                                                  (1, 3, 200, 64, "bf16", False),
+                                                  (1, 2, 100, 40, "fp32", False)])
+def test_host_buffer_entry_point_matches_device_path(B, H, N, d, dtype, causal):
+    """fa_forward_host (pinned host buffers, pipelined chunks of heads) gives
+    the same bits as fa_forward on device buffers, and both match the oracle."""
+    w = synth.Workload("t", B, H, N, d, dtype, causal, seed=3000 + N)
+    q, k, v = w.inputs()
+    tdt = TORCH_DT[dtype]
+    qh, kh, vh = (torch.from_numpy(x).to(tdt).pin_memory() for x in (q, k, v))
+    oh = torch.empty(w.shape, dtype=tdt).pin_memory()
+    lh = torch.empty(w.shape[:3], dtype=torch.float32).pin_memory()
+    ws = torch.empty(fa.host_workspace_size(B, H, N, d, tdt, tdt), dtype=torch.uint8, device="cuda")
+    for _ in range(2):   # repeated calls reuse the cached streams and events
+        fa.forward_host(qh, kh, vh, oh, lh, ws, scale=w.scale, causal=causal)
+    od, ld = fa.fa_forward(qh.cuda(), kh.cuda(), vh.cuda(), scale=w.scale, causal=causal)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, od.cpu()) and torch.equal(lh, ld.cpu())
+    o_ref, l_ref = oracle.attention(q, k, v, w.scale, causal)
+    compare(oh.float().numpy(), lh.numpy(), o_ref, l_ref, dtype, dtype)
+
+
+def test_host_buffer_entry_point_rejects_small_workspace():
+    x = torch.zeros((1, 1, 8, 64), dtype=torch.bfloat16)
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.FAError) as e:
+        fa.forward_host(x, x, x, torch.empty_like(x), None, ws)
+    assert e.value.status == fa.FA_ERR_INVALID_ARG

@@ -33,6 +33,9 @@ SIGNATURES = {
                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]),
     "fa_forward_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, ctypes.c_uint32]),
+    "fa_host_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int]),
+    "fa_forward_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
+                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "fa_check_device_error": (ctypes.c_int, [_P]),
     "fa_last_error": (ctypes.c_char_p, []),
     "fa_version": (ctypes.c_char_p, []),
@@ -135,5 +138,41 @@ def fa_forward(q, k, v, o=None, lse=None, scale=None, causal=False, o_dtype=None
     st = forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                      lse.data_ptr() if lse is not None else None, B, H, N, d, float(scale),
                      causal, in_code, _dtype_code(o.dtype), stream, flags)
+    check(st)
+    return o, lse
+
+
+def host_workspace_size(B, H, N, d, in_dtype, o_dtype) -> int:
+    """Device workspace bytes fa_forward_host needs (dtypes: torch dtypes or FA_* codes)."""
+    ic = in_dtype if isinstance(in_dtype, int) else _dtype_code(in_dtype)
+    oc = o_dtype if isinstance(o_dtype, int) else _dtype_code(o_dtype)
+    return int(load().fa_host_workspace_size(B, H, N, d, ic, oc))
+
+
+def forward_host(q, k, v, o, lse, workspace, scale=None, causal=False, stream=None):
+    """fa_forward_host on CPU tensors (pinned for overlap); ``workspace`` is a
+    CUDA uint8 tensor of at least host_workspace_size bytes.  Synchronous."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        if t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D host tensor")
+    if q.shape != k.shape or q.shape != v.shape or q.shape != o.shape:
+        raise ValueError("q, k, v, o must share one shape")
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    if lse is not None and (lse.is_cuda or lse.dtype != torch.float32 or lse.shape != (B, H, N)):
+        raise ValueError("lse must be a float32 [B, H, N] host tensor")
+    st = load().fa_forward_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                lse.data_ptr() if lse is not None else None, B, H, N, d,
+                                float(scale), int(bool(causal)), _dtype_code(q.dtype),
+                                _dtype_code(o.dtype), workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(), stream)
     check(st)
     return o, lse

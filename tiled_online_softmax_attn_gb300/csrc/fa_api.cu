@@ -2,10 +2,12 @@
 // launch, status codes and the thread-local error text.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "../../include/fa.h"
@@ -68,6 +70,63 @@ fa_status validate(const fa::Problem &p)
     return FA_OK;
 }
 
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Device-side copies of the tensors inside an fa_forward_host workspace.
+struct HostLayout {
+    size_t q, k, v, o, lse, total;
+};
+
+HostLayout host_layout(const fa::Problem &p)
+{
+    const size_t n = (size_t)(p.B * p.H * p.N * p.d);
+    const size_t in_b = align256(n * dtype_size(p.in_dtype));
+    const size_t o_b = align256(n * dtype_size(p.o_dtype));
+    const size_t l_b = align256((size_t)(p.B * p.H * p.N) * 4);
+    HostLayout L;
+    L.q = 0;
+    L.k = in_b;
+    L.v = 2 * in_b;
+    L.o = 3 * in_b;
+    L.lse = 3 * in_b + o_b;
+    L.total = 3 * in_b + o_b + l_b;
+    return L;
+}
+
+// Streams and events the host-buffer pipeline uses, created once per device.
+constexpr int MAX_DEVICES = 64;
+constexpr int MAX_CHUNKS = 8;
+struct PipelineRes {
+    bool ready = false;
+    cudaStream_t compute = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, copied[MAX_CHUNKS] = {}, computed[MAX_CHUNKS] = {};
+};
+PipelineRes g_pipes[MAX_DEVICES];
+std::mutex g_pipes_mu;
+
+cudaError_t pipeline_res(PipelineRes **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> g(g_pipes_mu);
+    PipelineRes &r = g_pipes[dev];
+    if (!r.ready) {
+        const unsigned fl = cudaStreamNonBlocking;
+        if ((e = cudaStreamCreateWithFlags(&r.compute, fl)) != cudaSuccess) return e;
+        if ((e = cudaStreamCreateWithFlags(&r.d2h, fl)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&r.start, cudaEventDisableTiming)) != cudaSuccess) return e;
+        for (int c = 0; c < MAX_CHUNKS; ++c) {
+            if ((e = cudaEventCreateWithFlags(&r.copied[c], cudaEventDisableTiming)) != cudaSuccess) return e;
+            if ((e = cudaEventCreateWithFlags(&r.computed[c], cudaEventDisableTiming)) != cudaSuccess) return e;
+        }
+        r.ready = true;
+    }
+    *out = &r;
+    return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -101,6 +160,92 @@ fa_status fa_forward(const void *q, const void *k, const void *v, void *o, float
                      void *stream)
 {
     return fa_forward_ex(q, k, v, o, lse, B, H, N, d, scale, causal, in_dtype, o_dtype, stream, 0u);
+}
+
+size_t fa_host_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int o_dtype)
+{
+    fa::Problem p{reinterpret_cast<const void *>(256), reinterpret_cast<const void *>(256),
+                  reinterpret_cast<const void *>(256), reinterpret_cast<void *>(256), nullptr,
+                  B, H, N, d, 1.0f, 0, in_dtype, o_dtype};
+    std::string saved = g_last_error;
+    // validate() also rejects the aliasing of these placeholder pointers, so
+    // check the size and dtype rules alone
+    bool ok = (in_dtype == FA_BF16 || in_dtype == FA_FP32) && (o_dtype == FA_BF16 || o_dtype == FA_FP32) &&
+              B >= 1 && H >= 1 && N >= 1 && d >= 1 && d <= 1024 && B <= INT32_MAX && H <= INT32_MAX &&
+              N <= INT32_MAX && B * H <= (int64_t)INT32_MAX / N;
+    g_last_error = saved;
+    return ok ? host_layout(p).total : 0;
+}
+
+fa_status fa_forward_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, float *lse_h,
+                          int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+                          int in_dtype, int o_dtype, void *workspace, size_t workspace_bytes,
+                          void *stream)
+{
+    g_last_error.clear();
+    if (!q_h || !k_h || !v_h || !o_h) return fail(FA_ERR_INVALID_ARG, "q_h, k_h, v_h and o_h must be non-NULL");
+    if (!workspace || !aligned(workspace, 256)) return fail(FA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
+    const size_t need = fa_host_workspace_size(B, H, N, d, in_dtype, o_dtype);
+    if (need == 0) {
+        // reuse fa_forward's messages for bad sizes and dtypes
+        fa::Problem p{q_h, k_h, v_h, o_h, lse_h, B, H, N, d, scale, causal != 0, in_dtype, o_dtype};
+        fa_status st = validate(p);
+        return st != FA_OK ? st : fail(FA_ERR_INVALID_ARG, "bad problem size");
+    }
+    if (workspace_bytes < need)
+        return fail(FA_ERR_INVALID_ARG, "workspace of %zu bytes is below the %zu bytes needed", workspace_bytes, need);
+    if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    fa::Problem full{q_h, k_h, v_h, o_h, lse_h, B, H, N, d, scale, causal != 0, in_dtype, o_dtype};
+    const HostLayout L = host_layout(full);
+    PipelineRes *res = nullptr;
+    cudaError_t e = pipeline_res(&res);
+    if (e != cudaSuccess) return cuda_fail(e, "creating the copy pipeline");
+    cudaStream_t s_in = static_cast<cudaStream_t>(stream);
+
+    const int64_t BH = B * H;
+    const size_t ei = dtype_size(in_dtype), eo = dtype_size(o_dtype);
+    const size_t head_elems = (size_t)(N * d);
+    const size_t in_bytes_total = 3 * (size_t)BH * head_elems * ei;
+    int chunks = (int)std::min<int64_t>({(int64_t)MAX_CHUNKS, BH, (int64_t)(in_bytes_total >> 22) + 1});
+    chunks = std::max(chunks, 1);
+
+    // the internal streams start after earlier work on the caller's stream
+    if ((e = cudaEventRecord(res->start, s_in)) != cudaSuccess) return cuda_fail(e, "event record");
+    if ((e = cudaStreamWaitEvent(res->compute, res->start, 0)) != cudaSuccess) return cuda_fail(e, "stream wait");
+    if ((e = cudaStreamWaitEvent(res->d2h, res->start, 0)) != cudaSuccess) return cuda_fail(e, "stream wait");
+
+    for (int c = 0; c < chunks; ++c) {
+        const int64_t h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks, nh = h1 - h0;
+        if (nh == 0) continue;
+        const size_t off_in = (size_t)h0 * head_elems * ei, n_in = (size_t)nh * head_elems * ei;
+        const size_t off_o = (size_t)h0 * head_elems * eo, n_o = (size_t)nh * head_elems * eo;
+        const size_t off_l = (size_t)h0 * N * 4, n_l = (size_t)nh * N * 4;
+        const uint8_t *qh = static_cast<const uint8_t *>(q_h), *kh = static_cast<const uint8_t *>(k_h),
+                      *vh = static_cast<const uint8_t *>(v_h);
+        if ((e = cudaMemcpyAsync(ws + L.q + off_in, qh + off_in, n_in, cudaMemcpyHostToDevice, s_in)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(ws + L.k + off_in, kh + off_in, n_in, cudaMemcpyHostToDevice, s_in)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(ws + L.v + off_in, vh + off_in, n_in, cudaMemcpyHostToDevice, s_in)) != cudaSuccess ||
+            (e = cudaEventRecord(res->copied[c], s_in)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(res->compute, res->copied[c], 0)) != cudaSuccess)
+            return cuda_fail(e, "host-to-device copy");
+        fa_status st = fa_forward(ws + L.q + off_in, ws + L.k + off_in, ws + L.v + off_in, ws + L.o + off_o,
+                                  lse_h ? reinterpret_cast<float *>(ws + L.lse + off_l) : nullptr,
+                                  1, nh, N, d, scale, causal, in_dtype, o_dtype, res->compute);
+        if (st != FA_OK) return st;
+        if ((e = cudaEventRecord(res->computed[c], res->compute)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(res->d2h, res->computed[c], 0)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(static_cast<uint8_t *>(o_h) + off_o, ws + L.o + off_o, n_o,
+                                 cudaMemcpyDeviceToHost, res->d2h)) != cudaSuccess)
+            return cuda_fail(e, "device-to-host copy");
+        if (lse_h && (e = cudaMemcpyAsync(reinterpret_cast<uint8_t *>(lse_h) + off_l, ws + L.lse + off_l, n_l,
+                                          cudaMemcpyDeviceToHost, res->d2h)) != cudaSuccess)
+            return cuda_fail(e, "device-to-host copy");
+    }
+    if ((e = cudaStreamSynchronize(res->d2h)) != cudaSuccess) return cuda_fail(e, "synchronize");
+    if ((e = cudaStreamSynchronize(res->compute)) != cudaSuccess) return cuda_fail(e, "synchronize");
+    return fa_check_device_error(stream);
 }
 
 fa_status fa_check_device_error(void *stream)
