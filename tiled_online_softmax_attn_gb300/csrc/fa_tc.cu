@@ -60,6 +60,7 @@ constexpr int NUM_THREADS = 320;  // 10 warps
 constexpr int TMA_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr uint32_t TMEM_COLS = 512;
+constexpr float RESCALE_LOG2 = 8.0f;  // lazy-rescale threshold, log2 units
 
 // error word bits
 constexpr uint32_t ERR_WAIT_TMA = 1u;       // producer gave up waiting for a free slot
@@ -124,6 +125,22 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
             if (globaltimer_ns() - t0 > limit_ns) return false;
         }
     }
+}
+
+// Maximum of 128 scores: eight independent chains of three-input maxima,
+// then a short combine (depth 11 instead of a 127-long dependency chain).
+__device__ __forceinline__ float row_max_128(const float (&s)[128])
+{
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = max3f(s[16 * i], s[16 * i + 1], s[16 * i + 2]);
+#pragma unroll
+    for (int k = 3; k < 15; k += 2)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = max3f(a[i], s[16 * i + k], s[16 * i + k + 1]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = fmaxf(a[i], s[16 * i + 15]);
+    return max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
 }
 
 template <int D>
@@ -377,7 +394,8 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const uint32_t tO = lane_base + C::COL_O + t * D;
         const float sl = prm.scale_log2;
         float m = -INFINITY;  // running maximum, log2 units
-        float l = 0.f;        // running denominator
+        float l = 0.f;        // running denominator (exact weights): LSE
+        float lq = 0.f;       // running denominator of the bf16 weights: O / lq
         bool ok = true;
         for (int j = 0; j < n_t; ++j) {
             if (!wait_or_abort(smem_addr(&bars.s_full[t]), (uint32_t)(j & 1), limit, &abort_flag)) {
@@ -386,12 +404,11 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
             tc_fence_after();
             float s[BN];
+            {
+                uint32_t raw[BN];
+                tmem_ld128(tS, raw);
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t raw[32];
-                tmem_ld32(tS + c * 32, raw);
-#pragma unroll
-                for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(raw[x]);
+                for (int x = 0; x < BN; ++x) s[x] = __uint_as_float(raw[x]);
             }
             const int kv0 = j * BN;
             int lim = N - kv0;                          // keys >= N are padding
@@ -401,39 +418,59 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 for (int c = 0; c < BN; ++c)
                     if (c >= lim) s[c] = -INFINITY;
             }
-            float mx = s[0];
-#pragma unroll
-            for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
-            const float m_new = fmaxf(m, mx * sl);
-            const float base = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = ex2(m - base);  // 0 on the first tile
-            float rs = 0.f;
+            const float m_tile = row_max_128(s) * sl;
+            // Lazy rescaling: the reference maximum m moves only when the tile's
+            // maximum exceeds it by more than RESCALE_LOG2 (weights then stay
+            // below 2^RESCALE_LOG2).  Softmax is invariant to the shift, so O / l
+            // and m + log2 l are unchanged; alpha is 1 on most tiles.
+            float alpha = 1.f;
+            if (m_tile > m + RESCALE_LOG2) {
+                alpha = ex2(m - m_tile);  // 0 on the first tile (m = -inf)
+                m = m_tile;
+            }
+            const float base = (m == -INFINITY) ? 0.f : m;  // a row with no key yet
+            const uint64_t sl2 = f2_pack(sl, sl), nb2 = f2_pack(-base, -base);
+            uint64_t rs2[2] = {0ull, 0ull}, rq2[2] = {0ull, 0ull};
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
-                    const float p0 = ex2(fmaf(s[c * 32 + 2 * x], sl, -base));
-                    const float p1 = ex2(fmaf(s[c * 32 + 2 * x + 1], sl, -base));
-                    rs += p0 + p1;
+                    float a0, a1;
+                    f2_unpack(f2_fma(f2_pack(s[c * 32 + 2 * x], s[c * 32 + 2 * x + 1]), sl2, nb2), a0, a1);
+                    const float p0 = ex2(a0), p1 = ex2(a1);
                     pk[x] = pack_bf16x2(p0, p1);
+                    rs2[x & 1] = f2_add(rs2[x & 1], f2_pack(p0, p1));
+                    // lq sums the bf16 weights the P V product uses, so O's
+                    // numerator and denominator see the same rounding
+                    rq2[x & 1] = f2_add(rq2[x & 1], f2_pack(__uint_as_float(pk[x] << 16),
+                                                            __uint_as_float(pk[x] & 0xFFFF0000u)));
                 }
                 tmem_st16(tS + c * 16, pk);
             }
-            l = l * alpha + rs;
+            float r0, r1, q0, q1;
+            f2_unpack(f2_add(rs2[0], rs2[1]), r0, r1);
+            f2_unpack(f2_add(rq2[0], rq2[1]), q0, q1);
+            l = l * alpha + (r0 + r1);
+            lq = lq * alpha + (q0 + q1);
             // O_t already holds every earlier P V product: the commit that
             // signalled this S tile covers all MMAs issued before it.
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t raw[32];
                     tmem_ld32(tO + c * 32, raw);
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) raw[x] = __float_as_uint(__uint_as_float(raw[x]) * alpha);
+                    for (int x = 0; x < 16; ++x) {
+                        float o0, o1;
+                        f2_unpack(f2_mul(f2_pack(__uint_as_float(raw[2 * x]), __uint_as_float(raw[2 * x + 1])), a2), o0, o1);
+                        raw[2 * x] = __float_as_uint(o0);
+                        raw[2 * x + 1] = __float_as_uint(o1);
+                    }
                     tmem_st32(tO + c * 32, raw);
                 }
             }
-            m = m_new;
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_addr(&bars.p_full[t]));
@@ -441,7 +478,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         // ---- epilogue: O / l, LSE
         if (ok && wait_or_abort(smem_addr(&bars.o_full[t]), 0, limit, &abort_flag)) {
             tc_fence_after();
-            const float inv_l = 1.f / l;
+            const float inv_l = 1.f / lq;
             const size_t row_elem = ((size_t)bh * N + (size_t)grow) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
