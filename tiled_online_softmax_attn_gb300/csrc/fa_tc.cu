@@ -395,7 +395,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const float sl = prm.scale_log2;
         float m = -INFINITY;  // running maximum, log2 units
         float l = 0.f;        // running denominator (exact weights): LSE
-        float lq = 0.f;       // running denominator of the bf16 weights: O / lq
+        float dq = 0.f;       // bf16 rounding of each tile's largest weight: O / (l + dq)
         bool ok = true;
         for (int j = 0; j < n_t; ++j) {
             if (!wait_or_abort(smem_addr(&bars.s_full[t]), (uint32_t)(j & 1), limit, &abort_flag)) {
@@ -418,7 +418,8 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 for (int c = 0; c < BN; ++c)
                     if (c >= lim) s[c] = -INFINITY;
             }
-            const float m_tile = row_max_128(s) * sl;
+            const float mx = row_max_128(s);
+            const float m_tile = mx * sl;
             // Lazy rescaling: the reference maximum m moves only when the tile's
             // maximum exceeds it by more than RESCALE_LOG2 (weights then stay
             // below 2^RESCALE_LOG2).  Softmax is invariant to the shift, so O / l
@@ -430,7 +431,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
             const float base = (m == -INFINITY) ? 0.f : m;  // a row with no key yet
             const uint64_t sl2 = f2_pack(sl, sl), nb2 = f2_pack(-base, -base);
-            uint64_t rs2[2] = {0ull, 0ull}, rq2[2] = {0ull, 0ull};
+            uint64_t rs2[2] = {0ull, 0ull};
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t pk[16];
@@ -441,18 +442,19 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     const float p0 = ex2(a0), p1 = ex2(a1);
                     pk[x] = pack_bf16x2(p0, p1);
                     rs2[x & 1] = f2_add(rs2[x & 1], f2_pack(p0, p1));
-                    // lq sums the bf16 weights the P V product uses, so O's
-                    // numerator and denominator see the same rounding
-                    rq2[x & 1] = f2_add(rq2[x & 1], f2_pack(__uint_as_float(pk[x] << 16),
-                                                            __uint_as_float(pk[x] & 0xFFFF0000u)));
                 }
                 tmem_st16(tS + c * 16, pk);
             }
-            float r0, r1, q0, q1;
+            float r0, r1;
             f2_unpack(f2_add(rs2[0], rs2[1]), r0, r1);
-            f2_unpack(f2_add(rq2[0], rq2[1]), q0, q1);
             l = l * alpha + (r0 + r1);
-            lq = lq * alpha + (q0 + q1);
+            // The P V product sees bf16 weights.  The largest weight of the
+            // tile dominates a peaked row, so the normaliser of O gets that
+            // weight's rounding error added: O's numerator and denominator then
+            // agree on the terms that matter (the same FFMA and ex2 as above,
+            // so p_top is bit-identical to that element's weight).
+            const float p_top = ex2(fmaf(mx, sl, -base));
+            dq = dq * alpha + (__uint_as_float(pack_bf16x2(p_top, 0.f) << 16) - p_top);
             // O_t already holds every earlier P V product: the commit that
             // signalled this S tile covers all MMAs issued before it.
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -478,7 +480,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         // ---- epilogue: O / l, LSE
         if (ok && wait_or_abort(smem_addr(&bars.o_full[t]), 0, limit, &abort_flag)) {
             tc_fence_after();
-            const float inv_l = 1.f / lq;
+            const float inv_l = 1.f / (l + dq);
             const size_t row_elem = ((size_t)bh * N + (size_t)grow) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {

@@ -86,6 +86,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// 3-D tiled prefetch global -> L2 only (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // 3-D tiled store shared -> global (bulk async group).  Coordinates must be
 // non-negative; elements outside the tensor are not written.
 __device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int c0, int c1, int c2)
