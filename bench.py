@@ -147,11 +147,17 @@ def oracle_rows_rate(w, q, k, v, seconds, seed=0):
     threads = oracle.default_threads()
     rng = np.random.default_rng(seed)
     total = w.B * w.H * w.N
-    calib = rng.integers(0, total, size=max(threads, 8))
-    t0 = time.perf_counter()
-    oracle.attention_rows(q, k, v, w.scale, w.causal, calib, threads)
-    dt = max(time.perf_counter() - t0, 1e-6)
-    nrows = int(max(threads, min(total, len(calib) * seconds / dt)))
+    # calibrate on a growing sample until it runs long enough to be representative
+    n_cal = max(threads, 8)
+    while True:
+        calib = rng.integers(0, total, size=n_cal)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, w.scale, w.causal, calib, threads)
+        dt = max(time.perf_counter() - t0, 1e-6)
+        if dt >= min(0.5, seconds / 4) or n_cal >= total:
+            break
+        n_cal = min(total, n_cal * 4)
+    nrows = int(max(threads, min(total, n_cal * seconds / dt)))
     rows = rng.integers(0, total, size=nrows)
     t0 = time.perf_counter()
     oracle.attention_rows(q, k, v, w.scale, w.causal, rows, threads)
