@@ -62,6 +62,13 @@ typedef enum fa_dtype {
 /* fa_forward_ex flags */
 #define FA_FLAG_GENERAL_PATH 0x1u  /* run the general-d CUDA-core kernel even where
                                       the tensor-core kernel applies */
+/* Fault injection for tests of the failure path: the tensor-core kernel's
+ * loader never issues the load of key tile 1, and every pipeline wait gives up
+ * after 20 ms instead of 2 s.  The waits that depend on that tile run out, the
+ * kernel frees its tensor memory and exits, and fa_check_device_error reports
+ * FA_ERR_TIMEOUT; nothing traps, faults or hangs, and the next call works.
+ * Has no effect when N <= 128 or when the general-d kernel runs. */
+#define FA_FLAG_TEST_SKIP_KV_LOAD 0x100u
 
 /*
  * fa_forward -- O (and LSE) of one attention forward pass.

@@ -22,6 +22,7 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3:
 FA_BF16 = 0
 FA_FP32 = 1
 FA_FLAG_GENERAL_PATH = 0x1
+FA_FLAG_TEST_SKIP_KV_LOAD = 0x100
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa_gb300.so")
 

@@ -139,8 +139,8 @@ fa_status fa_forward_ex(const void *q, const void *k, const void *v, void *o, fl
     fa::Problem p{q, k, v, o, lse, B, H, N, d, scale, causal != 0, in_dtype, o_dtype};
     fa_status st = validate(p);
     if (st != FA_OK) return st;
-    if (flags & ~(uint32_t)FA_FLAG_GENERAL_PATH)
-        return fail(FA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~(uint32_t)FA_FLAG_GENERAL_PATH);
+    const uint32_t known = FA_FLAG_GENERAL_PATH | FA_FLAG_TEST_SKIP_KV_LOAD;
+    if (flags & ~known) return fail(FA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~known);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (!(flags & FA_FLAG_GENERAL_PATH) && fa::tc_supported(p)) {

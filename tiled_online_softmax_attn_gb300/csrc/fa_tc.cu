@@ -43,6 +43,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "../../include/fa.h"
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -235,9 +236,10 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             tma_prefetch_desc(&tm_v);
             const uint64_t pol_q = policy_evict_first();
             const uint64_t pol_kv = policy_evict_last();
-            int k_issued = 0, v_issued = 0;  // tiles whose loads were issued
+            int k_issued = 0, v_issued = 0, q_issued = 0;  // tiles whose loads were issued
             bool ok = true;
             auto load_q = [&](int t) {
+                q_issued = t + 1;
                 const uint32_t bar = smem_addr(&bars.q_full[t]);
                 mbar_arrive_expect_tx(bar, C::TILE_BYTES);
                 for (int c = 0; c < C::CHUNKS; ++c)
@@ -282,7 +284,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             if (abort_flag) {
                 drain(true, k_issued);
                 drain(false, v_issued);
-                for (int t = 0; t < 2; ++t)
+                for (int t = 0; t < q_issued; ++t)
                     if (!mbar_wait_bounded(smem_addr(&bars.q_full[t]), 0, limit)) atomicOr(&g_tc_error_word, ERR_DRAIN);
             }
         }
@@ -304,24 +306,31 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 }
                 return true;
             };
+            // Descriptors are built once; a K step only moves the start address
+            // (field bits 0-13 hold address >> 4, and every shared-memory
+            // address here is below 256 KB, so adding offset >> 4 never carries
+            // out of the field).
+            const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024), dq1 = sdesc_sw128(sQ + C::TILE_BYTES, 16, 1024);
+            const uint64_t dk0 = sdesc_sw128(sK, 16, 1024), dv0 = sdesc_sw128(sV, BN * 128, 1024);
+            constexpr uint64_t TILE_STEP = C::TILE_BYTES >> 4;  // one ring slot, in descriptor units
             // S_t = Q_t K_j^T   (M = 128 rows, N = 128 keys, K = D in steps of 16)
             auto mma_s = [&](int t, int j) {
-                const uint32_t q = sQ + t * C::TILE_BYTES, k = sK + (j % C::KS) * C::TILE_BYTES;
+                const uint64_t q = t ? dq1 : dq0, k = dk0 + (uint64_t)(j % C::KS) * TILE_STEP;
+                const uint32_t d_s = tmem + t * 128;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-                    mma_ss(tmem + t * 128, sdesc_sw128(q + off, 16, 1024), sdesc_sw128(k + off, 16, 1024),
-                           idesc_s, kk > 0 ? 1u : 0u);
+                    const uint64_t off = (uint64_t)(((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4);
+                    mma_ss(d_s, q + off, k + off, idesc_s, kk > 0 ? 1u : 0u);
                 }
                 issued_any = true;
             };
             // O_t += P_t V_j   (M = 128 rows, N = D, K = 128 keys in steps of 16)
             auto mma_o = [&](int t, int j) {
-                const uint32_t v = sV + (j % C::VS) * C::TILE_BYTES;
+                const uint64_t v = dv0 + (uint64_t)(j % C::VS) * TILE_STEP;
+                const uint32_t d_o = tmem + C::COL_O + t * D, a_p = tmem + t * 128;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tmem + C::COL_O + t * D, tmem + t * 128 + kk * 8,
-                           sdesc_sw128(v + kk * (16 * 128), BN * 128, 1024), idesc_o,
+                    mma_ts(d_o, a_p + kk * 8, v + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 issued_any = true;
             };
@@ -556,12 +565,13 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     prm.n_kv = (int)((p.N + BN - 1) / BN);
     prm.scale_log2 = p.scale * 1.4426950408889634f;
     prm.causal = CAUSAL;
-    prm.skip_load = -1;
-    prm.wait_limit_ns = 2000000000ull;  // 2 s: far above any legitimate wait
+    const bool inject = (flags & FA_FLAG_TEST_SKIP_KV_LOAD) != 0;
+    prm.skip_load = inject ? 1 : -1;
+    // 2 s is far above any legitimate wait; the fault-injection test uses 20 ms
+    prm.wait_limit_ns = inject ? 20000000ull : 2000000000ull;
     prm.o = p.o;
     prm.lse = p.lse;
     prm.o_fp32 = p.o_dtype == 1;
-    (void)flags;
     auto kern = fa_tc_kernel<D, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM_BYTES);
     if (e != cudaSuccess) return e;
