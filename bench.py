@@ -219,18 +219,31 @@ def measure_e2e(args, w, fa, torch, dev, stream, q_h, k_h, v_h, q, o, lse, tdt, 
         e2e_step()
     torch.cuda.synchronize(dev)
     e2e_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(e2e_ms, dist, dev)
     h2d = 3 * q.numel() * q.element_size()
     d2h = o.numel() * o.element_size() + lse.numel() * 4
     # the host-buffer result must be the device result
     if not torch.equal(o_h, o.cpu()) or not torch.equal(lse_h, lse.cpu()):
         raise RuntimeError("host-buffer path disagrees with the device path")
-    return {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+    return {"value": aggregate_tflops(w.flops, e2e_ms, world), "unit": "TFLOP/s",
             "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "api": "fa_forward_host (pinned host buffers, wall clock per synchronous call)"}
+
+
+def reduce_max(x: float, dist, device=None) -> float:
+    """Maximum of a per-rank float over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(flops_per_rank: float, ms_max: float, world: int) -> float:
+    """Whole-job throughput: every rank runs the full workload (replicas), the
+    job takes as long as its slowest rank."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
 
 
 def main():
@@ -313,12 +326,9 @@ def main():
     timed_launches = launches["n"]
     if fa.check_device_error(stream.cuda_stream) != fa.FA_OK:
         raise RuntimeError(fa.last_error())
-    if dist:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = reduce_max(ms_total, dist, dev)
     ms_step = ms_total / args.steps
-    value = world * w.flops / (ms_step * 1e-3) / 1e12
+    value = aggregate_tflops(w.flops, ms_step, world)
 
     # ---- end to end: host buffers through fa_forward_host, copies inside the timed region
     e2e = None

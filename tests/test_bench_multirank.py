@@ -1,0 +1,67 @@
+"""The bench's multi-rank host logic on CPU (gloo, world size 2).
+
+The forward pass has no exchange step, so N GPUs run independent replicas;
+what needs checking is the host side: the max-over-ranks of the timed region,
+the whole-job aggregate, and that under torchrun only rank 0 prints.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local_ms = 10.0 + 5.0 * rank          # rank 1 is the slow one
+        ms = bench.reduce_max(local_ms, dist)
+        out[rank] = (ms, bench.aggregate_tflops(1e12, ms, world))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_two_gloo_ranks():
+    port = free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
+        got = dict(out)
+    assert got[0] == got[1]
+    ms, tflops = got[0]
+    assert ms == 15.0
+    assert tflops == pytest.approx(2 * 1e12 / 15e-3 / 1e12)
+
+
+def test_single_rank_helpers():
+    assert bench.reduce_max(3.5, None) == 3.5
+    assert bench.aggregate_tflops(2e12, 1.0, 1) == pytest.approx(2000.0)
+
+
+def test_reference_arm_prints_once_under_torchrun():
+    port = free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--workload", "tiny", "--gpus", "2", "--steps", "1", "--warmup", "3"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["unit"] == "TFLOP/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
