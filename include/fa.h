@@ -27,8 +27,10 @@
  *   - causal != 0 masks key j > query i (the mask of "PyTorch
  *     Implementation" in "Transformer Attention: A Mathematical Deep Dive");
  *     key tiles that lie wholly above the diagonal are skipped.
- *   - The caller owns every buffer.  The library allocates no device memory
- *     and keeps no per-call state; it caches one function-pointer lookup.
+ *   - The caller owns every buffer, workspaces included.  The library
+ *     allocates no device memory and keeps no per-call state; it caches one
+ *     driver entry point and, for fa_forward_host, two streams and some
+ *     events per device.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  Argument errors are reported before anything is
  *     launched; launch errors are reported on return; a device-side timeout
@@ -82,9 +84,10 @@ typedef enum fa_dtype {
  *   in_dtype, o_dtype   fa_dtype values.
  *   stream    cudaStream_t to enqueue on.
  *
- * Pointers must be aligned to their element size; the tensor-core kernel is
- * used when in_dtype = FA_BF16, d is 64 or 128 and q, k, v, o are 16-byte
- * aligned, the general-d kernel otherwise.  Outputs are undefined if the
+ * Pointers must be aligned to their element size.  The tensor-core kernel is
+ * used when in_dtype = FA_BF16, d is 64 or 128, scale > 0 and q, k, v, o are
+ * 16-byte aligned; bf16 inputs with d a multiple of 128 in 256..1024 take the
+ * wide-head tensor-core path; everything else the general-d kernel.  Outputs are undefined if the
  * call does not return FA_OK.  O must not overlap Q, K, V or LSE.
  */
 fa_status fa_forward(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -97,9 +100,48 @@ fa_status fa_forward_ex(const void *q, const void *k, const void *v, void *o, fl
                         int in_dtype, int o_dtype, void *stream, uint32_t flags);
 
 /*
+ * fa_workspace_size -- bytes of device workspace that let fa_forward_ws run
+ * this problem on the wide-head tensor-core path at full parallelism: the
+ * bf16 hi/lo copies of fp32 inputs and, when the key range is split across
+ * CTAs, the per-split partial O, m and l that a combine step merges with
+ * the rule of "FlashAttention Engine: Hardware-Aware Exact Attention & SRAM
+ * Tiling" ("Core FlashAttention Mechanics", item 3).  0 means the problem
+ * needs none (the 64/128 tensor-core kernel, or no tensor-core path).
+ */
+size_t fa_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int o_dtype, int causal);
+
+/*
+ * fa_plan -- the kernel path fa_forward_ws would take for this problem with
+ * `workspace_bytes` of workspace (0 = none, as fa_forward): returns the
+ * number of kernel launches one call enqueues (-1 for invalid sizes) and
+ * writes a short description ("tensor-core d=128", "wide-head ...",
+ * "general-d") into desc (may be NULL).  Pointer alignment is assumed.
+ */
+int fa_plan(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int o_dtype, int causal,
+            size_t workspace_bytes, char *desc, size_t desc_len);
+
+/*
+ * fa_forward_ws -- fa_forward with a caller-owned device workspace
+ * (256-byte aligned, contents unspecified on return; must not be used by
+ * anything else until the call's work on `stream` has finished).
+ *
+ * With workspace_bytes >= fa_workspace_size(...) the wide-head path
+ * (fp32 inputs with d % 128 == 0, bf16 inputs with d in {256, 384, ... 1024})
+ * runs on the tensor cores, fp32 operands carried as bf16 hi + lo pairs.
+ * With less (or NULL) it runs with fewer splits, or on the general-d kernel
+ * when fp32 inputs leave no room for their bf16 copies.  fa_forward uses
+ * the wide path only where it needs no workspace (bf16 inputs).
+ */
+fa_status fa_forward_ws(const void *q, const void *k, const void *v, void *o, float *lse,
+                        int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+                        int in_dtype, int o_dtype, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
+/*
  * fa_host_workspace_size -- bytes of device workspace fa_forward_host needs
  * for this problem (device copies of Q, K, V, O and LSE, 256-byte aligned
- * each).  Returns 0 for arguments fa_forward would reject.
+ * each, plus the wide-head path's scratch for one chunk of heads).  Returns 0
+ * for arguments fa_forward would reject.
  */
 size_t fa_host_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int o_dtype);
 

@@ -34,6 +34,11 @@ SIGNATURES = {
                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]),
     "fa_forward_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, ctypes.c_uint32]),
+    "fa_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "fa_plan": (ctypes.c_int, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                               ctypes.c_size_t, ctypes.c_char_p, ctypes.c_size_t]),
+    "fa_forward_ws": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "fa_host_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int]),
     "fa_forward_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, ctypes.c_size_t, _P]),
@@ -105,8 +110,24 @@ def _dtype_code(t) -> int:
     raise TypeError(f"unsupported dtype {t}")
 
 
+def workspace_size(B, H, N, d, in_dtype, o_dtype, causal=False) -> int:
+    """Device workspace bytes fa_forward_ws can use (dtypes: torch dtypes or FA_* codes)."""
+    ic = in_dtype if isinstance(in_dtype, int) else _dtype_code(in_dtype)
+    oc = o_dtype if isinstance(o_dtype, int) else _dtype_code(o_dtype)
+    return int(load().fa_workspace_size(B, H, N, d, ic, oc, int(bool(causal))))
+
+
+def plan(B, H, N, d, in_dtype, o_dtype, causal=False, workspace_bytes=0):
+    """(kernel launches per call, description) of the path fa_forward_ws takes."""
+    ic = in_dtype if isinstance(in_dtype, int) else _dtype_code(in_dtype)
+    oc = o_dtype if isinstance(o_dtype, int) else _dtype_code(o_dtype)
+    buf = ctypes.create_string_buffer(160)
+    n = load().fa_plan(B, H, N, d, ic, oc, int(bool(causal)), workspace_bytes, buf, len(buf))
+    return int(n), buf.value.decode()
+
+
 def fa_forward(q, k, v, o=None, lse=None, scale=None, causal=False, o_dtype=None,
-               return_lse=True, stream=None, flags=0):
+               return_lse=True, stream=None, flags=0, workspace=None):
     """O = softmax(q k^T * scale) v on [B, H, N, d] CUDA tensors.
 
     Returns (o, lse); ``lse`` is None when ``return_lse`` is False and no
@@ -136,9 +157,18 @@ def fa_forward(q, k, v, o=None, lse=None, scale=None, causal=False, o_dtype=None
         stream = torch.cuda.current_stream(q.device).cuda_stream
     elif not isinstance(stream, int):
         stream = stream.cuda_stream
-    st = forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                     lse.data_ptr() if lse is not None else None, B, H, N, d, float(scale),
-                     causal, in_code, _dtype_code(o.dtype), stream, flags)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+            lse.data_ptr() if lse is not None else None, B, H, N, d, float(scale),
+            int(bool(causal)), in_code, _dtype_code(o.dtype))
+    if workspace is not None:
+        if flags:
+            raise ValueError("flags are not available together with a workspace")
+        if not workspace.is_cuda:
+            raise ValueError("workspace must be a CUDA tensor")
+        st = load().fa_forward_ws(*args, workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(), stream)
+    else:
+        st = forward_raw(*args, stream, flags)
     check(st)
     return o, lse
 

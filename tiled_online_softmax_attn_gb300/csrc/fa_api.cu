@@ -72,6 +72,14 @@ fa_status validate(const fa::Problem &p)
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// The size and dtype rules of validate(), without pointers.
+bool size_ok(const fa::Problem &p)
+{
+    return (p.in_dtype == FA_BF16 || p.in_dtype == FA_FP32) && (p.o_dtype == FA_BF16 || p.o_dtype == FA_FP32) &&
+           p.B >= 1 && p.H >= 1 && p.N >= 1 && p.d >= 1 && p.d <= 1024 && p.B <= INT32_MAX && p.H <= INT32_MAX &&
+           p.N <= INT32_MAX && p.B * p.H <= (int64_t)INT32_MAX / p.N;
+}
+
 // Device-side copies of the tensors inside an fa_forward_host workspace.
 struct HostLayout {
     size_t q, k, v, o, lse, total;
@@ -127,9 +135,112 @@ cudaError_t pipeline_res(PipelineRes **out)
     return cudaSuccess;
 }
 
+// Heads per pipelined chunk of fa_forward_host: up to MAX_CHUNKS chunks of
+// at least ~4 MB of input each.
+int host_chunks(const fa::Problem &p)
+{
+    const int64_t BH = p.B * p.H;
+    const size_t in_bytes_total = 3 * (size_t)(BH * p.N * p.d) * dtype_size(p.in_dtype);
+    const int chunks = (int)std::min<int64_t>({(int64_t)MAX_CHUNKS, BH, (int64_t)(in_bytes_total >> 22) + 1});
+    return std::max(chunks, 1);
+}
+
+// Kernel workspace for one chunk of fa_forward_host (the largest chunk).
+size_t chunk_workspace(const fa::Problem &p)
+{
+    const int64_t BH = p.B * p.H;
+    const int chunks = host_chunks(p);
+    fa::Problem c = p;
+    c.B = 1;
+    c.H = (BH + chunks - 1) / chunks;
+    if (fa::tc_supported(c)) return 0;
+    const fa::WidePlan w = fa::wide_plan(c, 1 << 20);
+    return w.ok ? w.workspace_bytes : 0;
+}
+
+// Kernel choice shared by every entry point: the 64/128 tensor-core kernel,
+// then the wide-head tensor-core path (within the workspace given), then the
+// general CUDA-core kernel.
+fa_status dispatch(const fa::Problem &p, void *workspace, size_t workspace_bytes, cudaStream_t s, uint32_t flags)
+{
+    const uint32_t known = FA_FLAG_GENERAL_PATH | FA_FLAG_TEST_SKIP_KV_LOAD;
+    if (flags & ~known) return fail(FA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~known);
+    if (workspace && !aligned(workspace, 256)) return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    cudaError_t e;
+    const char *detail = nullptr;
+    if (!(flags & FA_FLAG_GENERAL_PATH)) {
+        if (fa::tc_supported(p)) {
+            e = fa::launch_tc(p, s, flags, &detail);
+            if (e != cudaSuccess)
+                return detail ? fail(FA_ERR_CUDA, "tensor-core launch: %s", detail) : cuda_fail(e, "tensor-core launch");
+            return FA_OK;
+        }
+        fa::WidePlan w = fa::wide_plan(p, workspace ? 1 << 20 : 1);
+        if (w.ok && workspace && workspace_bytes < w.workspace_bytes) w = fa::wide_plan(p, 1);
+        if (w.ok && (w.workspace_bytes == 0 || (workspace && workspace_bytes >= w.workspace_bytes))) {
+            e = fa::launch_wide(p, w, workspace, s, flags, &detail);
+            if (e != cudaSuccess)
+                return detail ? fail(FA_ERR_CUDA, "wide-head launch: %s", detail) : cuda_fail(e, "wide-head launch");
+            return FA_OK;
+        }
+    }
+    e = fa::launch_general(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "general-d launch");
+    return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t fa_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int o_dtype, int causal)
+{
+    const uintptr_t a = 256;  // placeholder, aligned pointers for planning only
+    fa::Problem p{reinterpret_cast<const void *>(a), reinterpret_cast<const void *>(a), reinterpret_cast<const void *>(a),
+                  reinterpret_cast<void *>(a), nullptr, B, H, N, d, 1.0f, causal != 0, in_dtype, o_dtype};
+    if (!size_ok(p) || fa::tc_supported(p)) return 0;
+    const fa::WidePlan w = fa::wide_plan(p, 1 << 20);
+    return w.ok ? w.workspace_bytes : 0;
+}
+
+int fa_plan(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int o_dtype, int causal,
+            size_t workspace_bytes, char *desc, size_t desc_len)
+{
+    const uintptr_t a = 256;
+    fa::Problem p{reinterpret_cast<const void *>(a), reinterpret_cast<const void *>(a), reinterpret_cast<const void *>(a),
+                  reinterpret_cast<void *>(a), nullptr, B, H, N, d, 1.0f, causal != 0, in_dtype, o_dtype};
+    if (!size_ok(p)) return -1;
+    char buf[160];
+    int launches;
+    if (fa::tc_supported(p)) {
+        launches = 1;
+        snprintf(buf, sizeof(buf), "tensor-core d=%lld", (long long)d);
+    } else {
+        fa::WidePlan w = fa::wide_plan(p, workspace_bytes ? 1 << 20 : 1);
+        if (w.ok && workspace_bytes && workspace_bytes < w.workspace_bytes) w = fa::wide_plan(p, 1);
+        if (w.ok && (w.workspace_bytes == 0 || workspace_bytes >= w.workspace_bytes)) {
+            launches = (w.nprod == 3 ? 3 : 0) + 1 + (w.n_split > 1 ? 1 : 0);
+            snprintf(buf, sizeof(buf), "wide-head %s dv=%d splits=%d", w.nprod == 3 ? "fp32 as bf16 hi+lo" : "bf16",
+                     w.dv, w.n_split);
+        } else {
+            launches = 1;
+            snprintf(buf, sizeof(buf), "general-d");
+        }
+    }
+    if (desc && desc_len) snprintf(desc, desc_len, "%s", buf);
+    return launches;
+}
+
+fa_status fa_forward_ws(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B, int64_t H,
+                        int64_t N, int64_t d, float scale, int causal, int in_dtype, int o_dtype, void *workspace,
+                        size_t workspace_bytes, void *stream)
+{
+    g_last_error.clear();
+    fa::Problem p{q, k, v, o, lse, B, H, N, d, scale, causal != 0, in_dtype, o_dtype};
+    fa_status st = validate(p);
+    if (st != FA_OK) return st;
+    return dispatch(p, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), 0u);
+}
 
 fa_status fa_forward_ex(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                         int64_t H, int64_t N, int64_t d, float scale, int causal, int in_dtype,
@@ -139,20 +250,7 @@ fa_status fa_forward_ex(const void *q, const void *k, const void *v, void *o, fl
     fa::Problem p{q, k, v, o, lse, B, H, N, d, scale, causal != 0, in_dtype, o_dtype};
     fa_status st = validate(p);
     if (st != FA_OK) return st;
-    const uint32_t known = FA_FLAG_GENERAL_PATH | FA_FLAG_TEST_SKIP_KV_LOAD;
-    if (flags & ~known) return fail(FA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~known);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (!(flags & FA_FLAG_GENERAL_PATH) && fa::tc_supported(p)) {
-        const char *detail = nullptr;
-        e = fa::launch_tc(p, s, flags, &detail);
-        if (e != cudaSuccess)
-            return detail ? fail(FA_ERR_CUDA, "tensor-core launch: %s", detail) : cuda_fail(e, "tensor-core launch");
-        return FA_OK;
-    }
-    e = fa::launch_general(p, s);
-    if (e != cudaSuccess) return cuda_fail(e, "general-d launch");
-    return FA_OK;
+    return dispatch(p, nullptr, 0, static_cast<cudaStream_t>(stream), flags);
 }
 
 fa_status fa_forward(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
@@ -167,14 +265,7 @@ size_t fa_host_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d, int in
     fa::Problem p{reinterpret_cast<const void *>(256), reinterpret_cast<const void *>(256),
                   reinterpret_cast<const void *>(256), reinterpret_cast<void *>(256), nullptr,
                   B, H, N, d, 1.0f, 0, in_dtype, o_dtype};
-    std::string saved = g_last_error;
-    // validate() also rejects the aliasing of these placeholder pointers, so
-    // check the size and dtype rules alone
-    bool ok = (in_dtype == FA_BF16 || in_dtype == FA_FP32) && (o_dtype == FA_BF16 || o_dtype == FA_FP32) &&
-              B >= 1 && H >= 1 && N >= 1 && d >= 1 && d <= 1024 && B <= INT32_MAX && H <= INT32_MAX &&
-              N <= INT32_MAX && B * H <= (int64_t)INT32_MAX / N;
-    g_last_error = saved;
-    return ok ? host_layout(p).total : 0;
+    return size_ok(p) ? host_layout(p).total + align256(chunk_workspace(p)) : 0;
 }
 
 fa_status fa_forward_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, float *lse_h,
@@ -207,9 +298,9 @@ fa_status fa_forward_host(const void *q_h, const void *k_h, const void *v_h, voi
     const int64_t BH = B * H;
     const size_t ei = dtype_size(in_dtype), eo = dtype_size(o_dtype);
     const size_t head_elems = (size_t)(N * d);
-    const size_t in_bytes_total = 3 * (size_t)BH * head_elems * ei;
-    int chunks = (int)std::min<int64_t>({(int64_t)MAX_CHUNKS, BH, (int64_t)(in_bytes_total >> 22) + 1});
-    chunks = std::max(chunks, 1);
+    const int chunks = host_chunks(full);
+    uint8_t *kernel_ws = ws + L.total;             // scratch of the wide-head path, shared by the chunks
+    const size_t kernel_ws_bytes = workspace_bytes - L.total;  // (they run in order on one stream)
 
     // the internal streams start after earlier work on the caller's stream
     if ((e = cudaEventRecord(res->start, s_in)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -230,9 +321,10 @@ fa_status fa_forward_host(const void *q_h, const void *k_h, const void *v_h, voi
             (e = cudaEventRecord(res->copied[c], s_in)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(res->compute, res->copied[c], 0)) != cudaSuccess)
             return cuda_fail(e, "host-to-device copy");
-        fa_status st = fa_forward(ws + L.q + off_in, ws + L.k + off_in, ws + L.v + off_in, ws + L.o + off_o,
-                                  lse_h ? reinterpret_cast<float *>(ws + L.lse + off_l) : nullptr,
-                                  1, nh, N, d, scale, causal, in_dtype, o_dtype, res->compute);
+        fa_status st = fa_forward_ws(ws + L.q + off_in, ws + L.k + off_in, ws + L.v + off_in, ws + L.o + off_o,
+                                     lse_h ? reinterpret_cast<float *>(ws + L.lse + off_l) : nullptr, 1, nh, N, d,
+                                     scale, causal, in_dtype, o_dtype, kernel_ws_bytes ? kernel_ws : nullptr,
+                                     kernel_ws_bytes, res->compute);
         if (st != FA_OK) return st;
         if ((e = cudaEventRecord(res->computed[c], res->compute)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(res->d2h, res->computed[c], 0)) != cudaSuccess ||
@@ -254,9 +346,11 @@ fa_status fa_check_device_error(void *stream)
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
-    uint32_t word = 0;
+    uint32_t word = 0, wide_word = 0;
     e = fa::tc_take_error_word(&word, s);
+    if (e == cudaSuccess) e = fa::wide_take_error_word(&wide_word, s);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    word |= wide_word;
     if (word) return fail(FA_ERR_TIMEOUT, "a device pipeline wait gave up (error word 0x%x)", word);
     return FA_OK;
 }

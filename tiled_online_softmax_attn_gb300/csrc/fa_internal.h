@@ -30,4 +30,22 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t stream, uint32_t flags, con
 // Reads and clears the device error word of the tensor-core kernel.
 cudaError_t tc_take_error_word(uint32_t *word, cudaStream_t stream);
 
+// Wide-head tensor-core path (fa_wide.cu): fp32 inputs with d % 128 == 0
+// (d <= 1024), bf16 inputs with d % 128 == 0 and 256 <= d <= 1024.
+struct WidePlan {
+    bool ok;             // the path applies to this problem
+    int nprod;           // 3: fp32 inputs as bf16 hi + lo pairs; 1: bf16 inputs
+    int dv;              // width of the O slice a CTA owns (256 or 128)
+    int n_q, n_kv, n_dv; // query tiles, key tiles, O slices
+    int n_split, tiles_per_split;
+    size_t off_split[6]; // workspace offsets of Q/K/V hi and lo copies (fp32 inputs)
+    size_t off_opart, off_m, off_l, off_d;  // partial results when n_split > 1
+    size_t workspace_bytes;
+};
+// max_splits = 1 plans a launch that needs no partials.
+WidePlan wide_plan(const Problem &p, int max_splits);
+cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cudaStream_t stream, uint32_t flags,
+                        const char **detail);
+cudaError_t wide_take_error_word(uint32_t *word, cudaStream_t stream);
+
 }  // namespace fa
