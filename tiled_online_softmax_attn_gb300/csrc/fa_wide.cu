@@ -407,10 +407,19 @@ fa_wide_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_constant_
     }
 }
 
-// x = hi + lo with hi = bf16(x), lo = bf16(x - hi); four elements per thread.
-__global__ void fa_split_kernel(const float4 *__restrict__ x, uint2 *__restrict__ hi, uint2 *__restrict__ lo,
-                                size_t n4)
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi), for Q, K and V in one
+// launch (blockIdx.y picks the tensor); four elements per thread.
+struct SplitArgs {
+    const float4 *x[3];
+    uint2 *hi[3];
+    uint2 *lo[3];
+};
+
+__global__ void fa_split_kernel(const SplitArgs a, size_t n4)
 {
+    const float4 *__restrict__ x = a.x[blockIdx.y];
+    uint2 *__restrict__ hi = a.hi[blockIdx.y];
+    uint2 *__restrict__ lo = a.lo[blockIdx.y];
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
         const float4 v = x[i];
         const uint32_t h01 = pack_bf16x2(v.x, v.y), h23 = pack_bf16x2(v.z, v.w);
@@ -421,36 +430,52 @@ __global__ void fa_split_kernel(const float4 *__restrict__ x, uint2 *__restrict_
     }
 }
 
-// Merge of the per-split partial results, one CTA per query row.
+// Merge of the per-split partial results, one CTA per query row and one
+// float4 of the row per thread, every split's load in flight together.
 template <typename Tout>
-__global__ void fa_combine_kernel(const float *__restrict__ o_part, const float *__restrict__ m_part,
-                                  const float *__restrict__ l_part, const float *__restrict__ d_part,
-                                  Tout *__restrict__ o, float *__restrict__ lse, int BH, int N, int D, int n_split)
+__global__ void __launch_bounds__(256)
+fa_combine_kernel(const float *__restrict__ o_part, const float *__restrict__ m_part,
+                  const float *__restrict__ l_part, const float *__restrict__ d_part,
+                  Tout *__restrict__ o, float *__restrict__ lse, int BH, int N, int D, int n_split)
 {
+    __shared__ float w_s[MAX_SPLITS];
+    __shared__ float inv_s;
     const size_t row = blockIdx.x;
     const size_t stride = (size_t)BH * N;
-    float w[MAX_SPLITS];
-    float M = -INFINITY;
-    for (int s = 0; s < n_split; ++s) M = fmaxf(M, m_part[s * stride + row]);
-    float L = 0.f, Lq = 0.f;
-    for (int s = 0; s < n_split; ++s) {
-        const float ms = m_part[s * stride + row];
-        w[s] = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-        if (w[s] != 0.f) {
-            L += w[s] * l_part[s * stride + row];
-            Lq += w[s] * (l_part[s * stride + row] + d_part[s * stride + row]);
+    if (threadIdx.x < 32) {
+        // warp 0: reference maximum, weights 2^(m_s - m), denominators
+        const int s = threadIdx.x;
+        const float ms = s < n_split ? m_part[s * stride + row] : -INFINITY;
+        float M = ms;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float wt = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+        float L = wt != 0.f ? wt * l_part[s * stride + row] : 0.f;
+        float Lq = wt != 0.f ? wt * (l_part[s * stride + row] + d_part[s * stride + row]) : 0.f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            L += __shfl_xor_sync(0xffffffffu, L, off);
+            Lq += __shfl_xor_sync(0xffffffffu, Lq, off);
+        }
+        if (s < n_split) w_s[s] = wt;
+        if (s == 0) {
+            inv_s = 1.f / Lq;
+            if (lse) lse[row] = (M + log2f(L)) * 0.69314718055994530942f;
         }
     }
-    const float inv = 1.f / Lq;
+    __syncthreads();
+    const float inv = inv_s;
     for (int c = threadIdx.x * 4; c < D; c += blockDim.x * 4) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
         for (int s = 0; s < n_split; ++s) {
-            if (w[s] == 0.f) continue;  // empty splits hold no partial O
-            const float4 v = *reinterpret_cast<const float4 *>(o_part + (s * stride + row) * D + c);
-            acc.x += w[s] * v.x;
-            acc.y += w[s] * v.y;
-            acc.z += w[s] * v.z;
-            acc.w += w[s] * v.w;
+            const float wt = w_s[s];
+            if (wt == 0.f) continue;  // empty splits hold no partial O
+            const float4 v = __ldcs(reinterpret_cast<const float4 *>(o_part + (s * stride + row) * D + c));
+            acc.x = fmaf(wt, v.x, acc.x);
+            acc.y = fmaf(wt, v.y, acc.y);
+            acc.z = fmaf(wt, v.z, acc.z);
+            acc.w = fmaf(wt, v.w, acc.w);
         }
         Tout *dst = o + row * D + c;
         if constexpr (sizeof(Tout) == 4) {
@@ -460,7 +485,6 @@ __global__ void fa_combine_kernel(const float *__restrict__ o_part, const float 
                 make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
         }
     }
-    if (threadIdx.x == 0 && lse) lse[row] = (M + log2f(L)) * 0.69314718055994530942f;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -519,7 +543,7 @@ WidePlan wide_plan(const Problem &p, int max_splits)
     w.n_kv = (int)((p.N + BN - 1) / BN);
     w.n_dv = (int)(p.d / w.dv);
     const int64_t base = (int64_t)w.n_q * w.n_dv * BH;
-    const int64_t target = 2 * (int64_t)sm_count();
+    const int64_t target = (int64_t)sm_count();  // one wave: more splits only add partials to merge
     int splits = (int)std::min<int64_t>({(int64_t)std::max(1, std::min(max_splits, MAX_SPLITS)), (int64_t)w.n_kv,
                                          std::max<int64_t>(1, (target + base - 1) / base)});
     w.tiles_per_split = (w.n_kv + splits - 1) / splits;
@@ -552,14 +576,18 @@ cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cu
     if (w.nprod == 3) {
         void *buf[6];
         for (int i = 0; i < 6; ++i) buf[i] = ws + w.off_split[i];
-        const float *src[3] = {static_cast<const float *>(p.q), static_cast<const float *>(p.k), static_cast<const float *>(p.v)};
-        const size_t n4 = n / 4;
-        const int blocks = (int)std::min<size_t>((n4 + 255) / 256, (size_t)sm_count() * 8);
+        SplitArgs sa;
+        sa.x[0] = static_cast<const float4 *>(p.q);
+        sa.x[1] = static_cast<const float4 *>(p.k);
+        sa.x[2] = static_cast<const float4 *>(p.v);
         for (int t = 0; t < 3; ++t) {
-            fa_split_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4 *>(src[t]),
-                                                        static_cast<uint2 *>(buf[2 * t]), static_cast<uint2 *>(buf[2 * t + 1]), n4);
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            sa.hi[t] = static_cast<uint2 *>(buf[2 * t]);
+            sa.lo[t] = static_cast<uint2 *>(buf[2 * t + 1]);
         }
+        const size_t n4 = n / 4;
+        const unsigned blocks = (unsigned)std::min<size_t>((n4 + 255) / 256, (size_t)sm_count() * 4);
+        fa_split_kernel<<<dim3(blocks, 3), 256, 0, stream>>>(sa, n4);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
         qh = buf[0]; ql = buf[1]; kh = buf[2]; kl = buf[3]; vh = buf[4]; vl = buf[5];
     }
     CUtensorMap m[6];
@@ -608,11 +636,12 @@ cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cu
     if (e != cudaSuccess) return e;
     if (!prm.direct) {
         const unsigned rows = (unsigned)(BH * p.N);
+        const int threads = (int)std::min<int64_t>(256, std::max<int64_t>(32, p.d / 4));
         if (p.o_dtype == 1)
-            fa_combine_kernel<float><<<rows, 128, 0, stream>>>(prm.o_part, prm.m_part, prm.l_part, prm.d_part,
+            fa_combine_kernel<float><<<rows, threads, 0, stream>>>(prm.o_part, prm.m_part, prm.l_part, prm.d_part,
                                                                static_cast<float *>(p.o), p.lse, (int)BH, (int)p.N, (int)p.d, w.n_split);
         else
-            fa_combine_kernel<__nv_bfloat16><<<rows, 128, 0, stream>>>(prm.o_part, prm.m_part, prm.l_part, prm.d_part,
+            fa_combine_kernel<__nv_bfloat16><<<rows, threads, 0, stream>>>(prm.o_part, prm.m_part, prm.l_part, prm.d_part,
                                                                        static_cast<__nv_bfloat16 *>(p.o), p.lse, (int)BH, (int)p.N,
                                                                        (int)p.d, w.n_split);
         e = cudaGetLastError();
