@@ -170,6 +170,36 @@ fa_status fa_forward_host(const void *q_h, const void *k_h, const void *v_h, voi
                           void *stream);
 
 /*
+ * fa_forward_noalloc -- the wide-head path of fa_forward_ws for callers that
+ * cannot allocate device memory.  The pages have no counterpart: it exists
+ * for code that must not call cudaMalloc while it runs (a plugin inside a
+ * framework that owns all device memory through its own allocator, or a
+ * service that plans its memory up front because a run-time allocation can
+ * stall the device or fail under memory pressure).
+ *
+ * Arguments, layouts and the result are those of fa_forward; the caller
+ * still owns Q, K, V, O and LSE.  The scratch comes from a device array of
+ * FA_NOALLOC_SCRATCH_BYTES inside this library, which every GPU that loads
+ * the library holds until the process exits.  The call allocates nothing.
+ *   - Covers the wide-head path only: fp32 inputs with d a multiple of 128,
+ *     or bf16 inputs with d a multiple of 128 in 256..1024 (scale > 0,
+ *     16-byte aligned pointers).  Other problems return FA_ERR_UNSUPPORTED:
+ *     fa_forward needs no scratch for them.
+ *   - A problem whose scratch exceeds FA_NOALLOC_SCRATCH_BYTES (after falling
+ *     back to a single key split) returns FA_ERR_UNSUPPORTED with the sizes
+ *     in fa_last_error.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents (nothing needs to start at zero).  Calls whose work can
+ *     overlap on the GPU race on it: order them, e.g. on one stream.
+ *   - The first call on a device looks up the array's address with that
+ *     device current; make it before any stream capture begins.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
+fa_status fa_forward_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+                             int in_dtype, int o_dtype, void *stream);
+
+/*
  * fa_check_device_error -- synchronise `stream`, then read and clear the
  * device-side error word the kernels set when a bounded pipeline wait gives
  * up.  Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if the stream itself

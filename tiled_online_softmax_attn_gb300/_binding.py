@@ -42,6 +42,8 @@ SIGNATURES = {
     "fa_host_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int]),
     "fa_forward_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, ctypes.c_size_t, _P]),
+    "fa_forward_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]),
     "fa_check_device_error": (ctypes.c_int, [_P]),
     "fa_last_error": (ctypes.c_char_p, []),
     "fa_version": (ctypes.c_char_p, []),

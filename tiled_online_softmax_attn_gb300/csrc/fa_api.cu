@@ -360,3 +360,8 @@ const char *fa_last_error(void) { return g_last_error.c_str(); }
 const char *fa_version(void) { return "0.1.0 sm_103a"; }
 
 }  // extern "C"
+
+namespace fa {
+// Lets other translation units of the library report through fa_last_error.
+void set_last_error(const char *msg) { g_last_error = msg ? msg : ""; }
+}  // namespace fa

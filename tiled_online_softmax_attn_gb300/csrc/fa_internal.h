@@ -48,4 +48,7 @@ cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cu
                         const char **detail);
 cudaError_t wide_take_error_word(uint32_t *word, cudaStream_t stream);
 
+// Sets the text fa_last_error returns on this host thread.
+void set_last_error(const char *msg);
+
 }  // namespace fa
