@@ -42,9 +42,9 @@ def _load():
     with _lock:
         if _lib is None:
             lib = ctypes.CDLL(build())
-            f = lib.oracle_attention_rows
+            f = lib.oracle_attention_rows_qkv
             f.restype = ctypes.c_int
-            f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 4 + [
+            f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 6 + [
                 ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
             _lib = lib
@@ -56,19 +56,22 @@ def default_threads() -> int:
 
 
 def attention_rows(q, k, v, scale, causal, rows, threads=None):
-    """Exact O rows and LSE for the given row ids (bh * N + i), in float64.
+    """Exact O rows and LSE for the given row ids (bh * Nq + i), in float64.
 
-    q, k, v: float32 arrays shaped [B, H, N, d], holding the exact input values.
-    Returns (o[len(rows), d], lse[len(rows)]).
+    q: [B, H, Nq, dk], k: [B, H, Nk, dk], v: [B, H, Nk, dv] float32 arrays
+    holding the exact input values.  Returns (o[len(rows), dv], lse[len(rows)]).
     """
     q = np.ascontiguousarray(q, dtype=np.float32)
     k = np.ascontiguousarray(k, dtype=np.float32)
     v = np.ascontiguousarray(v, dtype=np.float32)
-    if q.ndim != 4 or q.shape != k.shape or q.shape != v.shape:
-        raise ValueError("q, k, v must be [B, H, N, d] arrays of one shape")
+    if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
+        raise ValueError("q, k, v must be 4-D [B, H, N, d] arrays")
     B, H, N, d = q.shape
+    Nk, dv = k.shape[2], v.shape[3]
+    if k.shape != (B, H, Nk, d) or v.shape != (B, H, Nk, dv):
+        raise ValueError("k must be [B, H, Nk, dk] and v [B, H, Nk, dv] with q's B, H, dk")
     rows = np.ascontiguousarray(rows, dtype=np.int64).ravel()
-    o = np.empty((rows.size, d), dtype=np.float64)
+    o = np.empty((rows.size, dv), dtype=np.float64)
     lse = np.empty(rows.size, dtype=np.float64)
     if rows.size == 0:
         return o, lse
@@ -81,9 +84,9 @@ def attention_rows(q, k, v, scale, causal, rows, threads=None):
         lo, hi = int(bounds[c]), int(bounds[c + 1])
         if hi <= lo:
             return 0
-        work = np.empty(N, dtype=np.float64)
-        return lib.oracle_attention_rows(
-            q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, N, d,
+        work = np.empty(Nk, dtype=np.float64)
+        return lib.oracle_attention_rows_qkv(
+            q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, N, Nk, d, dv,
             float(scale), int(bool(causal)), rows[lo:].ctypes.data, hi - lo,
             o[lo:].ctypes.data, lse[lo:].ctypes.data, work.ctypes.data)
 
@@ -99,8 +102,9 @@ def attention_rows(q, k, v, scale, causal, rows, threads=None):
 
 
 def attention(q, k, v, scale, causal=False, threads=None):
-    """Exact O [B, H, N, d] and LSE [B, H, N] for every row, in float64."""
-    B, H, N, d = np.shape(q)
+    """Exact O [B, H, Nq, dv] and LSE [B, H, Nq] for every row, in float64."""
+    B, H, N, _ = np.shape(q)
+    dv = np.shape(v)[3]
     rows = np.arange(B * H * N, dtype=np.int64)
     o, lse = attention_rows(q, k, v, scale, causal, rows, threads)
-    return o.reshape(B, H, N, d), lse.reshape(B, H, N)
+    return o.reshape(B, H, N, dv), lse.reshape(B, H, N)

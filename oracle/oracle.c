@@ -25,39 +25,45 @@
  * one row are kept in a work buffer of N doubles between the passes; no
  * N x N matrix is ever formed.
  *
- * Layout: Q, K, V are contiguous [B, H, N, d] row-major float32.  A "row id"
- * is bh * N + i with bh = b * H + h.
+ * Layout: contiguous row-major float32, Q [B, H, Nq, dk], K [B, H, Nk, dk],
+ * V [B, H, Nk, dv].  A "row id" is bh * Nq + i with bh = b * H + h.
  */
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
 
 /* Returns 0 on success, 1 on a bad argument, 2 when a row has no key in
- * range (cannot happen for N >= 1: the causal row i always sees key 0). */
-int oracle_attention_rows(const float *q, const float *k, const float *v,
-                          int64_t B, int64_t H, int64_t N, int64_t d,
-                          double scale, int causal,
-                          const int64_t *rows, int64_t nrows,
-                          double *o, double *lse, double *work)
+ * range (cannot happen for Nk >= 1: the causal row i always sees key 0).
+ *
+ * Q is [B, H, Nq, dk], K is [B, H, Nk, dk], V is [B, H, Nk, dv] (the shapes
+ * (n, d_k), (m, d_k), (m, d_v) per head of "The Attention Formula" in
+ * "Transformer Attention: A Mathematical Deep Dive"); a row id is
+ * bh * Nq + i; O rows are dv wide.  Under the causal mask query i sees keys
+ * j <= i. */
+int oracle_attention_rows_qkv(const float *q, const float *k, const float *v,
+                              int64_t B, int64_t H, int64_t Nq, int64_t Nk,
+                              int64_t dk, int64_t dv, double scale, int causal,
+                              const int64_t *rows, int64_t nrows,
+                              double *o, double *lse, double *work)
 {
     if (!q || !k || !v || !rows || !o || !work) return 1;
-    if (B < 1 || H < 1 || N < 1 || d < 1 || nrows < 0) return 1;
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || dk < 1 || dv < 1 || nrows < 0) return 1;
     for (int64_t r = 0; r < nrows; ++r) {
         int64_t id = rows[r];
-        if (id < 0 || id >= B * H * N) return 1;
-        int64_t bh = id / N;
-        int64_t i = id % N;
-        const float *qi = q + (bh * N + i) * d;
-        const float *kh = k + bh * N * d;
-        const float *vh = v + bh * N * d;
-        int64_t nkeys = causal ? i + 1 : N;
+        if (id < 0 || id >= B * H * Nq) return 1;
+        int64_t bh = id / Nq;
+        int64_t i = id % Nq;
+        const float *qi = q + (bh * Nq + i) * dk;
+        const float *kh = k + bh * Nk * dk;
+        const float *vh = v + bh * Nk * dv;
+        int64_t nkeys = causal ? (i + 1 < Nk ? i + 1 : Nk) : Nk;
         if (nkeys < 1) return 2;
 
         /* scores x_j */
         for (int64_t j = 0; j < nkeys; ++j) {
             double dot = 0.0;
-            for (int64_t t = 0; t < d; ++t)
-                dot += (double)qi[t] * (double)kh[j * d + t];
+            for (int64_t t = 0; t < dk; ++t)
+                dot += (double)qi[t] * (double)kh[j * dk + t];
             work[j] = scale * dot;
         }
         /* pass 1: the row maximum m */
@@ -69,14 +75,25 @@ int oracle_attention_rows(const float *q, const float *k, const float *v,
         for (int64_t j = 0; j < nkeys; ++j)
             dT += exp(work[j] - m);
         /* pass 3: the weighted sum of the value rows */
-        double *oi = o + r * d;
-        for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
+        double *oi = o + r * dv;
+        for (int64_t t = 0; t < dv; ++t) oi[t] = 0.0;
         for (int64_t j = 0; j < nkeys; ++j) {
             double w = exp(work[j] - m) / dT;
-            for (int64_t t = 0; t < d; ++t)
-                oi[t] += w * (double)vh[j * d + t];
+            for (int64_t t = 0; t < dv; ++t)
+                oi[t] += w * (double)vh[j * dv + t];
         }
         if (lse) lse[r] = m + log(dT);
     }
     return 0;
+}
+
+/* The self-attention case: Nq = Nk = N, dk = dv = d. */
+int oracle_attention_rows(const float *q, const float *k, const float *v,
+                          int64_t B, int64_t H, int64_t N, int64_t d,
+                          double scale, int causal,
+                          const int64_t *rows, int64_t nrows,
+                          double *o, double *lse, double *work)
+{
+    return oracle_attention_rows_qkv(q, k, v, B, H, N, N, d, d, scale, causal,
+                                     rows, nrows, o, lse, work);
 }

@@ -38,7 +38,7 @@ def tiled_attention(Q, K, V, scale, block_q=2, block_k=2, causal=False, trace=No
         for ks in range(0, K.shape[0], block_k):
             ke = min(ks + block_k, K.shape[0])
             S = (Q[qs:qe] @ K[ks:ke].T) * scale
-            if causal:
+            if causal:  # key j visible to query i when j <= i
                 qi = np.arange(qs, qe)[:, None]
                 kj = np.arange(ks, ke)[None, :]
                 S = np.where(kj <= qi, S, -np.inf)

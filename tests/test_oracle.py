@@ -30,8 +30,8 @@ def brute_force(q, k, v, scale, causal):
     q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
     s = np.einsum("bhid,bhjd->bhij", q, k) * scale
     if causal:
-        n = s.shape[-1]
-        s = np.where(np.tril(np.ones((n, n), dtype=bool)), s, -np.inf)
+        nq, nk = s.shape[-2:]
+        s = np.where(np.arange(nk)[None, :] <= np.arange(nq)[:, None], s, -np.inf)
     mx = s.max(axis=-1, keepdims=True)
     e = np.exp(s - mx)
     den = e.sum(axis=-1, keepdims=True)
@@ -275,3 +275,51 @@ def test_bad_rows_are_rejected():
         oracle.attention_rows(q, q, q, 1.0, False, np.array([4]))
     with pytest.raises(ValueError):
         oracle.attention_rows(q, q[..., :1], q, 1.0, False, np.array([0]))
+
+
+# --------------------------------------------------------------------------
+# Cross-attention shapes: Nq != Nk and d_v != d_k ("Transformer Attention: A
+# Mathematical Deep Dive", "The Attention Formula": Q (n, d_k), K (m, d_k),
+# V (m, d_v))
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("causal", [False, True])
+def test_cross_shapes_match_materialised_softmax(seed, causal):
+    rng = np.random.default_rng(200 + seed)
+    B, H = 1 + seed % 2, 2
+    nq, nk = int(rng.integers(1, 50)), int(rng.integers(1, 50))
+    dk, dv = int(rng.integers(1, 12)), int(rng.integers(1, 12))
+    q = rng.standard_normal((B, H, nq, dk)).astype(np.float32)
+    k = rng.standard_normal((B, H, nk, dk)).astype(np.float32)
+    v = rng.standard_normal((B, H, nk, dv)).astype(np.float32)
+    o, lse = oracle.attention(q, k, v, 0.7, causal)
+    assert o.shape == (B, H, nq, dv)
+    ob, lb = brute_force(q, k, v, 0.7, causal)
+    np.testing.assert_allclose(o, ob, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lb, rtol=0, atol=1e-12)
+
+
+def test_cross_shapes_reduce_to_self_attention_pieces():
+    """Queries 0..nq-1 against the first nk keys equal the self-attention of
+    the padded problem restricted to those keys when causal (rows i < nk see
+    only keys j <= i either way)."""
+    rng = np.random.default_rng(300)
+    n, d = 40, 6
+    q, k, v = (rng.standard_normal((1, 1, n, d)).astype(np.float32) for _ in range(3))
+    o_sq, l_sq = oracle.attention(q, k, v, 0.5, True)
+    o_x, l_x = oracle.attention(q[:, :, :25], k[:, :, :30], v[:, :, :30], 0.5, True)
+    np.testing.assert_array_equal(o_x, o_sq[:, :, :25])
+    np.testing.assert_array_equal(l_x, l_sq[:, :, :25])
+
+
+def test_values_wider_than_keys_are_column_independent():
+    """Each output column depends on its own value column only: splitting V's
+    columns splits O's."""
+    rng = np.random.default_rng(301)
+    q = rng.standard_normal((1, 1, 9, 3)).astype(np.float32)
+    k = rng.standard_normal((1, 1, 13, 3)).astype(np.float32)
+    v = rng.standard_normal((1, 1, 13, 10)).astype(np.float32)
+    o, _ = oracle.attention(q, k, v, 0.8)
+    o1, _ = oracle.attention(q, k, v[..., :4], 0.8)
+    o2, _ = oracle.attention(q, k, v[..., 4:], 0.8)
+    np.testing.assert_array_equal(o, np.concatenate([o1, o2], axis=-1))
