@@ -170,6 +170,40 @@ fa_status fa_forward_host(const void *q_h, const void *k_h, const void *v_h, voi
                           void *stream);
 
 /*
+ * fa_attention -- the general form: cross-attention shapes and strided
+ * layouts ("Transformer Attention: A Mathematical Deep Dive", "The Attention
+ * Formula": Q is (n, d_k), K is (m, d_k), V is (m, d_v) per head).
+ *
+ *   Q [B, H, Nq, dk], K [B, H, Nk, dk], V [B, H, Nk, dv], O [B, H, Nq, dv];
+ *   element (b, h, n, c) of a tensor lives at ptr + b*s[0] + h*s[1] + n*s[2] + c
+ *   (elements, the last dimension contiguous); an all-zero stride triple means
+ *   the contiguous layout.  The (batch, seq, heads, dim) layout of the
+ *   flash_attn_func usage is s = {N*H*d, d, H*d}.  Strides must be >= 0;
+ *   O's must not make two of its elements share an address.
+ *   LSE is a contiguous [B, H, Nq] float32 tensor or NULL.
+ *   causal masks key j > query i (the same rule as for Nq = Nk).
+ *   workspace as for fa_forward_ws (may be NULL).
+ *
+ * The 64/128 tensor-core kernel covers bf16 inputs with dk and dv each 64
+ * or 128, scale > 0, 16-byte aligned pointers and every stride a non-zero
+ * multiple of 16 bytes; the wide-head path covers the contiguous Nq = Nk,
+ * dk = dv layouts of fa_forward_ws; the general-d kernel covers the rest
+ * (dk, dv <= 1024, any strides).
+ */
+typedef struct fa_params {
+    const void *q, *k, *v;
+    void *o;
+    float *lse;
+    int64_t B, H, Nq, Nk, dk, dv;
+    int64_t q_stride[3], k_stride[3], v_stride[3], o_stride[3];
+    float scale;
+    int causal;
+    int in_dtype, o_dtype;
+} fa_params;
+
+fa_status fa_attention(const fa_params *p, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * fa_forward_noalloc -- the wide-head path of fa_forward_ws for callers that
  * cannot allocate device memory.  The pages have no counterpart: it exists
  * for code that must not call cudaMalloc while it runs (a plugin inside a

@@ -73,3 +73,42 @@ def test_fa_forward_requires_cuda_tensors():
     x = torch.zeros((1, 1, 4, 64), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.fa_forward(x, x, x)
+
+
+def _params(**kw):
+    p = fa.FaParams()
+    p.q, p.k, p.v, p.o = 1 << 40, 2 << 40, 3 << 40, 4 << 40
+    p.B, p.H, p.Nq, p.Nk, p.dk, p.dv = 2, 4, 100, 70, 64, 32
+    p.scale, p.causal, p.in_dtype, p.o_dtype = 0.125, 0, fa.FA_BF16, fa.FA_BF16
+    for name, val in kw.items():
+        if name.endswith("stride"):
+            getattr(p, name)[:] = val
+        else:
+            setattr(p, name, val)
+    return p
+
+
+@pytest.mark.parametrize("kw,expect,text", [
+    (dict(o_stride=[4 * 100 * 32, 32, 16]), fa.FA_ERR_INVALID_ARG, "overlap"),   # rows of 32 every 16
+    (dict(q_stride=[-1, 64, 64]), fa.FA_ERR_INVALID_ARG, ">= 0"),
+    (dict(o=(1 << 40) + 64), fa.FA_ERR_INVALID_ARG, "overlap"),
+    (dict(Nk=0), fa.FA_ERR_INVALID_ARG, ">= 1"),
+    (dict(dv=2048), fa.FA_ERR_UNSUPPORTED, "1024"),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG, "finite"),
+])
+def test_attention_params_validation(lib, kw, expect, text):
+    import ctypes
+    p = _params(**kw)
+    assert lib.fa_attention(ctypes.byref(p), None, 0, None) == expect
+    assert text in fa.last_error()
+
+
+def test_attention_accepts_sequence_major_layout_on_the_host(lib):
+    """(batch, seq, heads, dim) strides pass validation; with no GPU the call
+    then fails at the launch, not before."""
+    import ctypes
+    B, H, Nq, Nk, dk, dv = 2, 4, 100, 70, 64, 32
+    p = _params(q_stride=[Nq * H * dk, dk, H * dk], k_stride=[Nk * H * dk, dk, H * dk],
+                v_stride=[Nk * H * dv, dv, H * dv], o_stride=[Nq * H * dv, dv, H * dv])
+    st = lib.fa_attention(ctypes.byref(p), None, 0, None)
+    assert st == fa.FA_ERR_CUDA, fa.last_error()

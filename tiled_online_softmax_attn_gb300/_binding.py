@@ -26,9 +26,20 @@ FA_FLAG_TEST_SKIP_KV_LOAD = 0x100
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa_gb300.so")
 
-# name -> (restype, argtypes) for every function include/fa.h declares
 _I64 = ctypes.c_int64
 _P = ctypes.c_void_p
+
+
+class FaParams(ctypes.Structure):
+    """struct fa_params of include/fa.h."""
+    _fields_ = [("q", _P), ("k", _P), ("v", _P), ("o", _P), ("lse", _P),
+                ("B", _I64), ("H", _I64), ("Nq", _I64), ("Nk", _I64), ("dk", _I64), ("dv", _I64),
+                ("q_stride", _I64 * 3), ("k_stride", _I64 * 3), ("v_stride", _I64 * 3),
+                ("o_stride", _I64 * 3), ("scale", ctypes.c_float), ("causal", ctypes.c_int),
+                ("in_dtype", ctypes.c_int), ("o_dtype", ctypes.c_int)]
+
+
+# name -> (restype, argtypes) for every function include/fa.h declares
 SIGNATURES = {
     "fa_forward": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]),
@@ -42,6 +53,7 @@ SIGNATURES = {
     "fa_host_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int]),
     "fa_forward_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, ctypes.c_size_t, _P]),
+    "fa_attention": (ctypes.c_int, [ctypes.POINTER(FaParams), _P, ctypes.c_size_t, _P]),
     "fa_forward_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]),
     "fa_check_device_error": (ctypes.c_int, [_P]),
@@ -208,4 +220,46 @@ def forward_host(q, k, v, o, lse, workspace, scale=None, causal=False, stream=No
                                 _dtype_code(o.dtype), workspace.data_ptr(),
                                 workspace.numel() * workspace.element_size(), stream)
     check(st)
+    return o, lse
+
+
+def fa_attention(q, k, v, o=None, lse=None, scale=None, causal=False, o_dtype=None,
+                 return_lse=True, workspace=None, stream=None):
+    """Attention on [B, H, Nq, dk] / [B, H, Nk, dk] / [B, H, Nk, dv] CUDA tensors
+    with any strides (the last dimension contiguous), e.g. transposed views of
+    (batch, seq, heads, dim) tensors.  O defaults to a contiguous
+    [B, H, Nq, dv] tensor; an existing (possibly strided) view may be passed."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or t.dim() != 4 or t.stride(-1) != 1:
+            raise ValueError(f"{name} must be a 4-D CUDA tensor whose last dimension is contiguous")
+    B, H, Nq, dk = q.shape
+    Nk, dv = k.shape[2], v.shape[3]
+    if k.shape != (B, H, Nk, dk) or v.shape != (B, H, Nk, dv) or q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError("k must be [B, H, Nk, dk] and v [B, H, Nk, dv], one dtype")
+    if o is None:
+        o = torch.empty((B, H, Nq, dv), dtype=o_dtype or q.dtype, device=q.device)
+    elif o.shape != (B, H, Nq, dv) or o.stride(-1) != 1:
+        raise ValueError("o must be [B, H, Nq, dv] with a contiguous last dimension")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or lse.shape != (B, H, Nq)):
+        raise ValueError("lse must be a contiguous float32 [B, H, Nq] tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    prm = FaParams()
+    prm.q, prm.k, prm.v, prm.o = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
+    prm.lse = lse.data_ptr() if lse is not None else None
+    prm.B, prm.H, prm.Nq, prm.Nk, prm.dk, prm.dv = B, H, Nq, Nk, dk, dv
+    for name, t in (("q_stride", q), ("k_stride", k), ("v_stride", v), ("o_stride", o)):
+        getattr(prm, name)[:] = list(t.stride()[:3])
+    prm.scale, prm.causal = float(scale), int(bool(causal))
+    prm.in_dtype, prm.o_dtype = _dtype_code(q.dtype), _dtype_code(o.dtype)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(load().fa_attention(ctypes.byref(prm), ws_ptr, ws_bytes, stream))
     return o, lse

@@ -135,6 +135,81 @@ cudaError_t pipeline_res(PipelineRes **out)
     return cudaSuccess;
 }
 
+// Byte range [lo, hi) a strided tensor can touch.
+struct Extent {
+    uintptr_t lo, hi;
+};
+
+Extent extent_of(const void *ptr, const int64_t st[3], const int64_t size[3], int64_t width, size_t elt)
+{
+    int64_t last = width - 1;
+    for (int i = 0; i < 3; ++i) last += (size[i] - 1) * st[i];
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr);
+    return {lo, lo + (uintptr_t)(last + 1) * elt};
+}
+
+// No two elements of a strided tensor share an address: with the dimensions
+// sorted by stride, each stride exceeds the span of the smaller ones.
+bool no_self_overlap(const int64_t st[3], const int64_t size[3], int64_t width)
+{
+    struct D {
+        int64_t stride, size;
+    } dd[4] = {{1, width}, {st[0], size[0]}, {st[1], size[1]}, {st[2], size[2]}};
+    for (int i = 1; i < 4; ++i)
+        for (int j = i; j > 0 && dd[j].stride < dd[j - 1].stride; --j) {
+            D t = dd[j];
+            dd[j] = dd[j - 1];
+            dd[j - 1] = t;
+        }
+    int64_t span = 0;  // largest offset reachable with the dimensions so far
+    for (int i = 0; i < 4; ++i) {
+        if (dd[i].size <= 1) continue;
+        if (dd[i].stride <= span) return false;
+        span += (dd[i].size - 1) * dd[i].stride;
+    }
+    return true;
+}
+
+fa_status validate_general(const fa::Problem &p)
+{
+    if (!p.q || !p.k || !p.v || !p.o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
+    if (p.in_dtype != FA_BF16 && p.in_dtype != FA_FP32)
+        return fail(FA_ERR_INVALID_ARG, "in_dtype %d is not an fa_dtype", p.in_dtype);
+    if (p.o_dtype != FA_BF16 && p.o_dtype != FA_FP32)
+        return fail(FA_ERR_INVALID_ARG, "o_dtype %d is not an fa_dtype", p.o_dtype);
+    const int64_t Nk = p.Nk, dv = p.dv;
+    if (p.B < 1 || p.H < 1 || p.N < 1 || Nk < 1 || p.d < 1 || dv < 1)
+        return fail(FA_ERR_INVALID_ARG, "B, H, Nq, Nk, dk, dv must be >= 1");
+    if (p.d > 1024 || dv > 1024) return fail(FA_ERR_UNSUPPORTED, "dk and dv must be <= 1024");
+    const int64_t nmax = std::max(p.N, Nk);
+    if (p.B > (int64_t)INT32_MAX || p.H > (int64_t)INT32_MAX || nmax > (int64_t)INT32_MAX ||
+        p.B * p.H > (int64_t)INT32_MAX / nmax)
+        return fail(FA_ERR_UNSUPPORTED, "B * H * max(Nq, Nk) must be below 2^31");
+    if (!std::isfinite(p.scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+    const size_t ei = dtype_size(p.in_dtype), eo = dtype_size(p.o_dtype);
+    if (!aligned(p.q, ei) || !aligned(p.k, ei) || !aligned(p.v, ei) || !aligned(p.o, eo) ||
+        (p.lse && !aligned(p.lse, 4)))
+        return fail(FA_ERR_INVALID_ARG, "pointers must be aligned to their element size");
+    int64_t st[4][3];
+    for (int t = 0; t < 4; ++t) {
+        fa::strides_of(p, t, st[t]);
+        for (int i = 0; i < 3; ++i)
+            if (st[t][i] < 0) return fail(FA_ERR_INVALID_ARG, "strides must be >= 0");
+    }
+    const int64_t sq[3] = {p.B, p.H, p.N}, sk[3] = {p.B, p.H, Nk};
+    if (!no_self_overlap(st[3], sq, dv)) return fail(FA_ERR_INVALID_ARG, "o's strides make its elements overlap");
+    const Extent eo_ = extent_of(p.o, st[3], sq, dv, eo);
+    const Extent ins[3] = {extent_of(p.q, st[0], sq, p.d, ei), extent_of(p.k, st[1], sk, p.d, ei),
+                           extent_of(p.v, st[2], sk, dv, ei)};
+    for (const Extent &x : ins)
+        if (eo_.lo < x.hi && x.lo < eo_.hi) return fail(FA_ERR_INVALID_ARG, "o must not overlap q, k or v");
+    if (p.lse) {
+        const uintptr_t l0 = reinterpret_cast<uintptr_t>(p.lse), l1 = l0 + (uintptr_t)(p.B * p.H * p.N) * 4;
+        if (eo_.lo < l1 && l0 < eo_.hi) return fail(FA_ERR_INVALID_ARG, "o must not overlap lse");
+    }
+    return FA_OK;
+}
+
 // Heads per pipelined chunk of fa_forward_host: up to MAX_CHUNKS chunks of
 // at least ~4 MB of input each.
 int host_chunks(const fa::Problem &p)
@@ -229,6 +304,25 @@ int fa_plan(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int o_dtyp
     }
     if (desc && desc_len) snprintf(desc, desc_len, "%s", buf);
     return launches;
+}
+
+fa_status fa_attention(const fa_params *a, void *workspace, size_t workspace_bytes, void *stream)
+{
+    g_last_error.clear();
+    if (!a) return fail(FA_ERR_INVALID_ARG, "params must be non-NULL");
+    fa::Problem p{a->q, a->k, a->v, a->o, a->lse, a->B, a->H, a->Nq, a->dk, a->scale, a->causal != 0,
+                  a->in_dtype, a->o_dtype};
+    p.Nk = a->Nk;
+    p.dv = a->dv;
+    for (int i = 0; i < 3; ++i) {
+        p.qs[i] = a->q_stride[i];
+        p.ks[i] = a->k_stride[i];
+        p.vs[i] = a->v_stride[i];
+        p.os[i] = a->o_stride[i];
+    }
+    fa_status st = validate_general(p);
+    if (st != FA_OK) return st;
+    return dispatch(p, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), 0u);
 }
 
 fa_status fa_forward_ws(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B, int64_t H,

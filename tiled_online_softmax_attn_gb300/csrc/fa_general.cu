@@ -58,11 +58,17 @@ __device__ __forceinline__ float group8_sum(float x) {
     return x;
 }
 
+// Element strides (batch, head, row) of the four tensors; the last dimension
+// is contiguous.
+struct Strides {
+    int64_t q[3], k[3], v[3], o[3];
+};
+
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(NT)
 fa_general_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
-                  Tout *__restrict__ o, float *__restrict__ lse, int N, int d, int n_qblocks,
-                  int BH, float scale_log2, int causal)
+                  Tout *__restrict__ o, float *__restrict__ lse, int N, int Nk, int d, int dv, int H,
+                  int n_qblocks, int BH, float scale_log2, int causal, const Strides st)
 {
     extern __shared__ float smem[];
     float *Qs = smem;              // [BR][QS]  query chunk
@@ -81,9 +87,11 @@ fa_general_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
     }
     const int q0 = qb * BR;
     const int dv0 = blockIdx.y * DV;
-    const int dvn = min(DV, d - dv0);
-    const size_t head = (size_t)bh * N * d;
-    const Tin *qh = q + head, *kh = k + head, *vh = v + head;
+    const int dvn = min(DV, dv - dv0);
+    const int b = bh / H, h = bh % H;
+    const Tin *qh = q + b * st.q[0] + h * st.q[1];
+    const Tin *kh = k + b * st.k[0] + h * st.k[1];
+    const Tin *vh = v + b * st.v[0] + h * st.v[1];
 
     const int r = tid >> 3;        // query row of this thread in the block
     const int cg = tid & 7;        // lane in the row's 8-thread group
@@ -95,7 +103,7 @@ fa_general_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
 #pragma unroll
     for (int x = 0; x < 16; ++x) acc[x] = 0.f;
 
-    const int kv_end = causal ? min(N, q0 + BR) : N;
+    const int kv_end = causal ? min(Nk, q0 + BR) : Nk;
     for (int k0 = 0; k0 < kv_end; k0 += BC) {
         // ---- S = Q_i K_j^T for this thread's 8 keys: cg + 8u
         float s[8];
@@ -104,11 +112,11 @@ fa_general_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
         for (int dc = 0; dc < d; dc += DK) {
             for (int e = tid; e < BR * DK; e += NT) {
                 int rr = e / DK, cc = e % DK, gr = q0 + rr, gc = dc + cc;
-                Qs[rr * QS + cc] = (gr < N && gc < d) ? load_f(qh + (size_t)gr * d + gc) : 0.f;
+                Qs[rr * QS + cc] = (gr < N && gc < d) ? load_f(qh + gr * st.q[2] + gc) : 0.f;
             }
             for (int e = tid; e < BC * DK; e += NT) {
                 int rr = e / DK, cc = e % DK, gr = k0 + rr, gc = dc + cc;
-                Ks[rr * QS + cc] = (gr < N && gc < d) ? load_f(kh + (size_t)gr * d + gc) : 0.f;
+                Ks[rr * QS + cc] = (gr < Nk && gc < d) ? load_f(kh + gr * st.k[2] + gc) : 0.f;
             }
             __syncthreads();
 #pragma unroll 8
@@ -125,7 +133,7 @@ fa_general_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             int j = k0 + cg + 8 * u;
-            bool keep = j < N && (!causal || j <= row);
+            bool keep = j < Nk && (!causal || j <= row);
             s[u] = keep ? s[u] * scale_log2 : -INFINITY;
             tmax = fmaxf(tmax, s[u]);
         }
@@ -147,7 +155,7 @@ fa_general_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
         // ---- value tile, this CTA's columns
         for (int e = tid; e < BC * DV; e += NT) {
             int jj = e / DV, cc = e % DV, gj = k0 + jj;
-            Vs[jj * DV + cc] = (gj < N && cc < dvn) ? load_f(vh + (size_t)gj * d + dv0 + cc) : 0.f;
+            Vs[jj * DV + cc] = (gj < Nk && cc < dvn) ? load_f(vh + gj * st.v[2] + dv0 + cc) : 0.f;
         }
         __syncthreads();
 
@@ -172,7 +180,7 @@ fa_general_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
     // ---- O / l and LSE = (m + log2 l) * ln 2
     if (row < N) {
         const float inv_l = 1.f / l;
-        Tout *orow = o + head + (size_t)row * d + dv0;
+        Tout *orow = o + b * st.o[0] + h * st.o[1] + row * st.o[2] + dv0;
 #pragma unroll
         for (int u = 0; u < 4; ++u)
 #pragma unroll
@@ -191,13 +199,18 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream)
     auto kern = fa_general_kernel<Tin, Tout>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    const int N = (int)p.N, d = (int)p.d, BH = (int)(p.B * p.H);
+    const int N = (int)p.N, Nk = (int)keys_of(p), d = (int)p.d, dv = (int)dv_of(p), BH = (int)(p.B * p.H);
     const int n_qblocks = (N + BR - 1) / BR;
-    dim3 grid((unsigned)((int64_t)n_qblocks * BH), (unsigned)((d + DV - 1) / DV));
+    dim3 grid((unsigned)((int64_t)n_qblocks * BH), (unsigned)((dv + DV - 1) / DV));
     const float scale_log2 = p.scale * 1.4426950408889634f;
+    Strides st;
+    strides_of(p, 0, st.q);
+    strides_of(p, 1, st.k);
+    strides_of(p, 2, st.v);
+    strides_of(p, 3, st.o);
     kern<<<grid, NT, SMEM_BYTES, stream>>>(
         static_cast<const Tin *>(p.q), static_cast<const Tin *>(p.k), static_cast<const Tin *>(p.v),
-        static_cast<Tout *>(p.o), p.lse, N, d, n_qblocks, BH, scale_log2, p.causal);
+        static_cast<Tout *>(p.o), p.lse, N, Nk, d, dv, (int)p.H, n_qblocks, BH, scale_log2, p.causal, st);
     return cudaGetLastError();
 }
 

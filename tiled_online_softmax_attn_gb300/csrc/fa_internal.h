@@ -7,6 +7,10 @@
 namespace fa {
 
 // One forward problem, already validated by the C ABI.
+//   Q [B, H, N, d], K [B, H, Nk, d], V [B, H, Nk, dv], O [B, H, N, dv],
+//   LSE [B, H, N] contiguous.  Nk = 0 means N, dv = 0 means d.  Strides are
+//   in elements for (batch, head, sequence), the head dimension contiguous;
+//   all-zero strides mean the contiguous layout.
 struct Problem {
     const void *q, *k, *v;
     void *o;
@@ -16,7 +20,48 @@ struct Problem {
     int causal;
     int in_dtype;          // fa_dtype
     int o_dtype;           // fa_dtype
+    int64_t Nk = 0, dv = 0;
+    int64_t qs[3] = {0, 0, 0}, ks[3] = {0, 0, 0}, vs[3] = {0, 0, 0}, os[3] = {0, 0, 0};
 };
+
+inline int64_t keys_of(const Problem &p) { return p.Nk ? p.Nk : p.N; }
+inline int64_t dv_of(const Problem &p) { return p.dv ? p.dv : p.d; }
+
+// Element strides (batch, head, sequence) of tensor t: 0 = Q, 1 = K, 2 = V, 3 = O.
+inline void strides_of(const Problem &p, int t, int64_t out[3])
+{
+    const int64_t *s = t == 0 ? p.qs : t == 1 ? p.ks : t == 2 ? p.vs : p.os;
+    if (s[0] || s[1] || s[2]) {
+        out[0] = s[0];
+        out[1] = s[1];
+        out[2] = s[2];
+        return;
+    }
+    const int64_t n = (t == 0 || t == 3) ? p.N : keys_of(p);
+    const int64_t w = (t <= 1) ? p.d : dv_of(p);
+    out[0] = p.H * n * w;
+    out[1] = n * w;
+    out[2] = w;
+}
+
+// True when every tensor has the contiguous layout and Nk = N, dv = d.
+inline bool plain_layout(const Problem &p)
+{
+    for (int t = 0; t < 4; ++t) {
+        const int64_t *s = t == 0 ? p.qs : t == 1 ? p.ks : t == 2 ? p.vs : p.os;
+        if (s[0] || s[1] || s[2]) {
+            int64_t c[3];
+            Problem z = p;
+            z.qs[0] = z.qs[1] = z.qs[2] = 0;
+            z.ks[0] = z.ks[1] = z.ks[2] = 0;
+            z.vs[0] = z.vs[1] = z.vs[2] = 0;
+            z.os[0] = z.os[1] = z.os[2] = 0;
+            strides_of(z, t, c);
+            if (s[0] != c[0] || s[1] != c[1] || s[2] != c[2]) return false;
+        }
+    }
+    return keys_of(p) == p.N && dv_of(p) == p.d;
+}
 
 // General-d CUDA-core kernel (any d <= 1024, bf16 or fp32 in and out).
 cudaError_t launch_general(const Problem &p, cudaStream_t stream);

@@ -71,22 +71,28 @@ constexpr uint32_t ERR_WAIT_MMA = 2u;       // MMA thread gave up waiting for da
 constexpr uint32_t ERR_WAIT_SOFTMAX = 4u;   // softmax gave up waiting for S or O
 constexpr uint32_t ERR_DRAIN = 8u;          // teardown could not confirm in-flight work
 
-template <int D>
+template <int DK, int DV>
 struct Cfg {
-    static constexpr int CHUNKS = D / 64;                  // 128-byte swizzle chunks per row
-    static constexpr uint32_t TILE_BYTES = BM * D * 2;     // one 128 x D bf16 tile
-    static constexpr int KS = (D == 128) ? 2 : 3;          // K ring slots
-    static constexpr int VS = (D == 128) ? 2 : 3;          // V ring slots
+    static constexpr int QCH = DK / 64;                    // 128-byte swizzle chunks of a Q/K row
+    static constexpr int VCH = DV / 64;                    // ... of a V row
+    static constexpr uint32_t Q_BYTES = BM * DK * 2;       // one 128 x DK bf16 tile
+    static constexpr uint32_t K_BYTES = BN * DK * 2;
+    static constexpr uint32_t V_BYTES = BN * DV * 2;
+    // three K and V ring slots when they fit in shared memory, else two
+    static constexpr int KS = (2 * Q_BYTES + 3 * (K_BYTES + V_BYTES) + 1024 <= 227u * 1024u) ? 3 : 2;
+    static constexpr int VS = KS;
     static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = 2 * TILE_BYTES;
-    static constexpr uint32_t OFF_V = OFF_K + KS * TILE_BYTES;
-    static constexpr uint32_t SMEM_TILES = OFF_V + VS * TILE_BYTES;
+    static constexpr uint32_t OFF_K = 2 * Q_BYTES;
+    static constexpr uint32_t OFF_V = OFF_K + KS * K_BYTES;
+    static constexpr uint32_t SMEM_TILES = OFF_V + VS * V_BYTES;
     static constexpr uint32_t SMEM_BYTES = SMEM_TILES + 1024;  // + alignment slack
-    static constexpr uint32_t COL_O = 256;                 // O0 at 256, O1 at 256 + D
+    static constexpr uint32_t COL_O = 256;                 // O0 at 256, O1 at 256 + DV
 };
 
 struct Params {
-    int N;             // sequence length
+    int N;             // query sequence length
+    int Nk;            // key sequence length
+    int H;             // heads
     int BH;            // batch * heads
     int n_qblocks;     // CTAs per head (256 query rows each)
     int n_kv;          // key tiles per head
@@ -95,6 +101,8 @@ struct Params {
     int skip_load;     // fault injection: never issue the K load of this tile (-1 = off)
     uint64_t wait_limit_ns;
     void *o;
+    int64_t os_b, os_h, os_n;  // O element strides (batch, head, sequence)
+    int qperm, kperm, vperm;   // which of (sequence, head, batch) each outer map dimension holds
     float *lse;
     int o_fp32;
 };
@@ -109,13 +117,23 @@ struct __align__(8) Barriers {
     uint64_t drain;
 };
 
+// Map coordinate for dimension slot s of a tensor map whose outer dimensions
+// are ordered by stride: 0 = sequence row, 1 = head, 2 = batch.
+__device__ __forceinline__ int pick(int s, int row, int h, int b) { return s == 0 ? row : (s == 1 ? h : b); }
+
+__device__ __forceinline__ void tma_load_rows(uint32_t dst, const void *tmap, uint32_t bar, int col, int perm, int row,
+                                              int h, int b, uint64_t pol)
+{
+    tma_load_4d(dst, tmap, bar, col, pick(perm & 3, row, h, b), pick((perm >> 2) & 3, row, h, b),
+                pick((perm >> 4) & 3, row, h, b), pol);
+}
+
 __device__ __forceinline__ void raise_error(uint32_t bit, volatile int *abort_flag)
 {
     atomicOr(&g_tc_error_word, bit);
     *abort_flag = 1;
 }
 
-template <int D>
 __device__ __forceinline__ void store_o_row(void *o, int o_fp32, size_t row_elem, const float *vals,
                                             int col0, int ncols)
 {
@@ -139,12 +157,12 @@ __device__ __forceinline__ void store_o_row(void *o, int o_fp32, size_t row_elem
     }
 }
 
-template <int D, bool CAUSAL>
+template <int DK, int DV, bool CAUSAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const Params prm)
 {
-    using C = Cfg<D>;
+    using C = Cfg<DK, DV>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ Barriers bars;
     __shared__ uint32_t tmem_base_s;
@@ -164,7 +182,8 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         qb = (int)(blockIdx.x % prm.n_qblocks);
         bh = (int)(blockIdx.x / prm.n_qblocks);
     }
-    const int N = prm.N;
+    const int N = prm.N, Nk = prm.Nk;
+    const int b = bh / prm.H, h = bh % prm.H;
     const int qrow0 = qb * 2 * BM;  // first row of Q0; Q1 starts BM later
     // key tiles each query tile needs: all, or up to its diagonal under the mask
     const int n0 = CAUSAL ? min(prm.n_kv, 2 * qb + 1) : prm.n_kv;
@@ -212,10 +231,10 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             auto load_q = [&](int t) {
                 q_issued = t + 1;
                 const uint32_t bar = smem_addr(&bars.q_full[t]);
-                mbar_arrive_expect_tx(bar, C::TILE_BYTES);
-                for (int c = 0; c < C::CHUNKS; ++c)
-                    tma_load_3d(s_base + C::OFF_Q + t * C::TILE_BYTES + c * (BM * 128), &tm_q, bar, c * 64,
-                                qrow0 + t * BM, bh, pol_q);
+                mbar_arrive_expect_tx(bar, C::Q_BYTES);
+                for (int c = 0; c < C::QCH; ++c)
+                    tma_load_rows(s_base + C::OFF_Q + t * C::Q_BYTES + c * (BM * 128), &tm_q, bar, c * 64,
+                                  prm.qperm, qrow0 + t * BM, h, b, pol_q);
             };
             auto load_kv = [&](bool is_k, int j) -> bool {
                 const int S = is_k ? C::KS : C::VS;
@@ -225,10 +244,11 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 const uint32_t full = smem_addr(is_k ? &bars.k_full[slot] : &bars.v_full[slot]);
                 if (!wait_or_abort(empty, (n_use & 1u) ^ 1u, limit, &abort_flag)) return false;
                 if (is_k && j == prm.skip_load) return true;  // fault injection: never arrives
-                mbar_arrive_expect_tx(full, C::TILE_BYTES);
-                const uint32_t dst = s_base + (is_k ? C::OFF_K : C::OFF_V) + slot * C::TILE_BYTES;
-                for (int c = 0; c < C::CHUNKS; ++c)
-                    tma_load_3d(dst + c * (BN * 128), is_k ? &tm_k : &tm_v, full, c * 64, j * BN, bh, pol_kv);
+                mbar_arrive_expect_tx(full, is_k ? C::K_BYTES : C::V_BYTES);
+                const uint32_t dst = s_base + (is_k ? C::OFF_K + slot * C::K_BYTES : C::OFF_V + slot * C::V_BYTES);
+                for (int c = 0; c < (is_k ? C::QCH : C::VCH); ++c)
+                    tma_load_rows(dst + c * (BN * 128), is_k ? &tm_k : &tm_v, full, c * 64, is_k ? prm.kperm : prm.vperm,
+                                  j * BN, h, b, pol_kv);
                 return true;
             };
             load_q(0);
@@ -264,7 +284,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         // ================================================================ MMA issuer
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
-            const uint32_t idesc_o = idesc_bf16_f32(BM, D, 0, 1);
+            const uint32_t idesc_o = idesc_bf16_f32(BM, DV, 0, 1);
             const uint32_t sQ = s_base + C::OFF_Q, sK = s_base + C::OFF_K, sV = s_base + C::OFF_V;
             bool ok = true;
             bool issued_any = false;
@@ -281,15 +301,15 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             // (field bits 0-13 hold address >> 4, and every shared-memory
             // address here is below 256 KB, so adding offset >> 4 never carries
             // out of the field).
-            const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024), dq1 = sdesc_sw128(sQ + C::TILE_BYTES, 16, 1024);
+            const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024), dq1 = sdesc_sw128(sQ + C::Q_BYTES, 16, 1024);
             const uint64_t dk0 = sdesc_sw128(sK, 16, 1024), dv0 = sdesc_sw128(sV, BN * 128, 1024);
-            constexpr uint64_t TILE_STEP = C::TILE_BYTES >> 4;  // one ring slot, in descriptor units
+            constexpr uint64_t K_STEP = C::K_BYTES >> 4, V_STEP = C::V_BYTES >> 4;  // one ring slot, descriptor units
             // S_t = Q_t K_j^T   (M = 128 rows, N = 128 keys, K = D in steps of 16)
             auto mma_s = [&](int t, int j) {
-                const uint64_t q = t ? dq1 : dq0, k = dk0 + (uint64_t)(j % C::KS) * TILE_STEP;
+                const uint64_t q = t ? dq1 : dq0, k = dk0 + (uint64_t)(j % C::KS) * K_STEP;
                 const uint32_t d_s = tmem + t * 128;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4);
                     mma_ss(d_s, q + off, k + off, idesc_s, kk > 0 ? 1u : 0u);
                 }
@@ -297,8 +317,8 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             };
             // O_t += P_t V_j   (M = 128 rows, N = D, K = 128 keys in steps of 16)
             auto mma_o = [&](int t, int j) {
-                const uint64_t v = dv0 + (uint64_t)(j % C::VS) * TILE_STEP;
-                const uint32_t d_o = tmem + C::COL_O + t * D, a_p = tmem + t * 128;
+                const uint64_t v = dv0 + (uint64_t)(j % C::VS) * V_STEP;
+                const uint32_t d_o = tmem + C::COL_O + t * DV, a_p = tmem + t * 128;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                     mma_ts(d_o, a_p + kk * 8, v + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
@@ -371,7 +391,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const int n_t = t == 0 ? n0 : n1;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const uint32_t tS = lane_base + t * 128;
-        const uint32_t tO = lane_base + C::COL_O + t * D;
+        const uint32_t tO = lane_base + C::COL_O + t * DV;
         const float sl = prm.scale_log2;
         float m = -INFINITY;  // running maximum, log2 units
         float l = 0.f;        // running denominator (exact weights): LSE
@@ -391,7 +411,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 for (int x = 0; x < BN; ++x) s[x] = __uint_as_float(raw[x]);
             }
             const int kv0 = j * BN;
-            int lim = N - kv0;                          // keys >= N are padding
+            int lim = Nk - kv0;                         // keys >= Nk are padding
             if (CAUSAL) lim = min(lim, grow - kv0 + 1);  // keys after this query
             if (lim < BN) {
 #pragma unroll
@@ -440,7 +460,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < DV / 32; ++c) {
                     uint32_t raw[32];
                     tmem_ld32(tO + c * 32, raw);
 #pragma unroll
@@ -461,15 +481,15 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (ok && wait_or_abort(smem_addr(&bars.o_full[t]), 0, limit, &abort_flag)) {
             tc_fence_after();
             const float inv_l = 1.f / (l + dq);
-            const size_t row_elem = ((size_t)bh * N + (size_t)grow) * D;
+            const size_t row_elem = (size_t)(b * prm.os_b + h * prm.os_h + (int64_t)grow * prm.os_n);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < DV / 32; ++c) {
                 uint32_t raw[32];
                 tmem_ld32(tO + c * 32, raw);
                 float vals[32];
 #pragma unroll
                 for (int x = 0; x < 32; ++x) vals[x] = __uint_as_float(raw[x]) * inv_l;
-                if (grow < N) store_o_row<D>(prm.o, prm.o_fp32, row_elem, vals, c * 32, 32);
+                if (grow < N) store_o_row(prm.o, prm.o_fp32, row_elem, vals, c * 32, 32);
             }
             if (prm.lse && grow < N) prm.lse[(size_t)bh * N + grow] = (m + log2f(l)) * 0.69314718055994530942f;
         } else if (!abort_flag) {
@@ -503,37 +523,60 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// [BH, N, d] bf16 viewed as a 3-D tensor (d innermost); box = 64 columns
-// (128 bytes, the swizzle width) x 128 rows x 1 head.  Rows past N of a head
-// read as zeros.
-bool make_map(CUtensorMap *map, const void *ptr, int64_t BH, int64_t N, int64_t d)
+// A [B, H, n, w] bf16 tensor with element strides st = (batch, head, row)
+// and contiguous w, as a 4-D tensor map: w innermost, then the three outer
+// dimensions in increasing stride; box = 64 columns (128 bytes, the swizzle
+// width) x 128 rows x 1 x 1.  *perm records which of (row, head, batch) each
+// outer map dimension holds.  Rows past n read as zeros.
+bool make_map(CUtensorMap *map, const void *ptr, int64_t w, int64_t n, int64_t H, int64_t B, const int64_t st[3],
+              int *perm)
 {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)(N * d * 2)};
-    cuuint32_t box[3] = {64, 128, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+    struct Dim {
+        int64_t size, stride;
+        int which;
+        uint32_t box;
+    } dd[3] = {{n, st[2], 0, 128}, {H, st[1], 1, 1}, {B, st[0], 2, 1}};
+    for (int i = 1; i < 3; ++i)  // insertion sort by stride, stable
+        for (int j = i; j > 0 && dd[j].stride < dd[j - 1].stride; --j) {
+            Dim t = dd[j];
+            dd[j] = dd[j - 1];
+            dd[j - 1] = t;
+        }
+    cuuint64_t dims[4] = {(cuuint64_t)w, (cuuint64_t)dd[0].size, (cuuint64_t)dd[1].size, (cuuint64_t)dd[2].size};
+    cuuint64_t strides[3] = {(cuuint64_t)dd[0].stride * 2, (cuuint64_t)dd[1].stride * 2, (cuuint64_t)dd[2].stride * 2};
+    cuuint32_t box[4] = {64, dd[0].box, dd[1].box, dd[2].box};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    *perm = dd[0].which | (dd[1].which << 2) | (dd[2].which << 4);
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool CAUSAL>
+template <int DK, int DV, bool CAUSAL>
 cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, const char **detail)
 {
-    using Cf = Cfg<D>;
+    using Cf = Cfg<DK, DV>;
     CUtensorMap mq, mk, mv;
-    const int64_t BH = p.B * p.H;
-    if (!make_map(&mq, p.q, BH, p.N, D) || !make_map(&mk, p.k, BH, p.N, D) || !make_map(&mv, p.v, BH, p.N, D)) {
+    const int64_t BH = p.B * p.H, Nk = keys_of(p);
+    int64_t sq[3], sk[3], sv[3], so[3];
+    strides_of(p, 0, sq);
+    strides_of(p, 1, sk);
+    strides_of(p, 2, sv);
+    strides_of(p, 3, so);
+    Params prm;
+    if (!make_map(&mq, p.q, DK, p.N, p.H, p.B, sq, &prm.qperm) || !make_map(&mk, p.k, DK, Nk, p.H, p.B, sk, &prm.kperm) ||
+        !make_map(&mv, p.v, DV, Nk, p.H, p.B, sv, &prm.vperm)) {
         *detail = "cuTensorMapEncodeTiled failed or is unavailable";
         return cudaErrorInvalidValue;
     }
-    Params prm;
     prm.N = (int)p.N;
+    prm.Nk = (int)Nk;
+    prm.H = (int)p.H;
     prm.BH = (int)BH;
     prm.n_qblocks = (int)((p.N + 2 * BM - 1) / (2 * BM));
-    prm.n_kv = (int)((p.N + BN - 1) / BN);
+    prm.n_kv = (int)((Nk + BN - 1) / BN);
     prm.scale_log2 = p.scale * 1.4426950408889634f;
     prm.causal = CAUSAL;
     const bool inject = (flags & FA_FLAG_TEST_SKIP_KV_LOAD) != 0;
@@ -541,9 +584,12 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     // 2 s is far above any legitimate wait; the fault-injection test uses 20 ms
     prm.wait_limit_ns = inject ? 20000000ull : 2000000000ull;
     prm.o = p.o;
+    prm.os_b = so[0];
+    prm.os_h = so[1];
+    prm.os_n = so[2];
     prm.lse = p.lse;
     prm.o_fp32 = p.o_dtype == 1;
-    auto kern = fa_tc_kernel<D, CAUSAL>;
+    auto kern = fa_tc_kernel<DK, DV, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int64_t grid = (int64_t)prm.n_qblocks * BH;
@@ -551,20 +597,39 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     return cudaGetLastError();
 }
 
+template <int DK, int DV>
+cudaError_t launch_dims(const Problem &p, cudaStream_t stream, uint32_t flags, const char **detail)
+{
+    return p.causal ? launch_typed<DK, DV, true>(p, stream, flags, detail)
+                    : launch_typed<DK, DV, false>(p, stream, flags, detail);
+}
+
 }  // namespace
 
 bool tc_supported(const Problem &p)
 {
-    if (p.in_dtype != 0 || !(p.d == 64 || p.d == 128) || !(p.scale > 0.f)) return false;
+    const int64_t dv = dv_of(p);
+    if (p.in_dtype != 0 || !(p.d == 64 || p.d == 128) || !(dv == 64 || dv == 128) || !(p.scale > 0.f)) return false;
     auto al16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
-    return al16(p.q) && al16(p.k) && al16(p.v) && al16(p.o);
+    if (!(al16(p.q) && al16(p.k) && al16(p.v) && al16(p.o))) return false;
+    // TMA: every stride a non-zero multiple of 16 bytes; O rows start 16-byte aligned
+    const int64_t o_elt = p.o_dtype == 1 ? 4 : 2;
+    for (int t = 0; t < 4; ++t) {
+        int64_t st[3];
+        strides_of(p, t, st);
+        const int64_t elt = t == 3 ? o_elt : 2;
+        for (int i = 0; i < 3; ++i)
+            if (st[i] <= 0 || (st[i] * elt) % 16 != 0) return false;
+    }
+    return true;
 }
 
 cudaError_t launch_tc(const Problem &p, cudaStream_t stream, uint32_t flags, const char **detail)
 {
-    if (p.d == 128) return p.causal ? launch_typed<128, true>(p, stream, flags, detail)
-                                    : launch_typed<128, false>(p, stream, flags, detail);
-    return p.causal ? launch_typed<64, true>(p, stream, flags, detail) : launch_typed<64, false>(p, stream, flags, detail);
+    const int64_t dv = dv_of(p);
+    if (p.d == 128) return dv == 128 ? launch_dims<128, 128>(p, stream, flags, detail)
+                                     : launch_dims<128, 64>(p, stream, flags, detail);
+    return dv == 128 ? launch_dims<64, 128>(p, stream, flags, detail) : launch_dims<64, 64>(p, stream, flags, detail);
 }
 
 cudaError_t tc_take_error_word(uint32_t *word, cudaStream_t stream)

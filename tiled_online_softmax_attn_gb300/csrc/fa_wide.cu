@@ -534,7 +534,7 @@ WidePlan wide_plan(const Problem &p, int max_splits)
     const bool fp32_in = p.in_dtype == 1;
     auto al16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
     w.ok = p.d % 128 == 0 && p.d <= 1024 && (fp32_in ? p.d >= 128 : p.d >= 256) && p.scale > 0.f &&
-           p.B * p.H <= 65535 && al16(p.q) && al16(p.k) && al16(p.v) && al16(p.o);
+           p.B * p.H <= 65535 && plain_layout(p) && al16(p.q) && al16(p.k) && al16(p.v) && al16(p.o);
     if (!w.ok) return w;
     const int64_t BH = p.B * p.H;
     w.nprod = fp32_in ? 3 : 1;
