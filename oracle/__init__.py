@@ -7,7 +7,8 @@ CUDA path.
 
 ``attention_rows`` / ``attention`` wrap ``oracle.c`` (the three passes of
 "Safe Softmax and the Three Passes" in "The Details of Flash Attention",
-fp64); ``tiled_model`` holds a second, tile-by-tile restatement of the online
+fp64); ``attention_backward`` is the gradient of that definition written
+out; ``tiled_model`` holds a second, tile-by-tile restatement of the online
 recurrence used only to pin the intermediate numbers of the worked example.
 Row chunks run on host threads (ctypes releases the GIL during the C call).
 """
@@ -47,6 +48,10 @@ def _load():
             f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 6 + [
                 ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+            g = lib.oracle_attention_backward_head
+            g.restype = ctypes.c_int
+            g.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 4 + [
+                ctypes.c_double, ctypes.c_int, ctypes.c_int64] + [ctypes.c_void_p] * 4
             _lib = lib
     return _lib
 
@@ -108,3 +113,30 @@ def attention(q, k, v, scale, causal=False, threads=None):
     rows = np.arange(B * H * N, dtype=np.int64)
     o, lse = attention_rows(q, k, v, scale, causal, rows, threads)
     return o.reshape(B, H, N, dv), lse.reshape(B, H, N)
+
+
+def attention_backward(q, k, v, dout, scale, causal=False, threads=None):
+    """Gradients (dq, dk, dv) of L = sum(O * dout) for the forward pass on
+    q, k, v [B, H, N, d] (float32 arrays of the exact input values), float64.
+    Heads run on host threads; each materialises its N x N weights."""
+    q, k, v, dout = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k, v, dout))
+    if q.ndim != 4 or not (q.shape == k.shape == v.shape == dout.shape):
+        raise ValueError("q, k, v, dout must be [B, H, N, d] arrays of one shape")
+    B, H, N, d = q.shape
+    dq, dk, dv = (np.empty((B * H, N, d), dtype=np.float64) for _ in range(3))
+    lib = _load()
+
+    def run(bh):
+        work = np.empty(N * N, dtype=np.float64)
+        return lib.oracle_attention_backward_head(
+            q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, B, H, N, d,
+            float(scale), int(bool(causal)), bh, dq[bh].ctypes.data, dk[bh].ctypes.data,
+            dv[bh].ctypes.data, work.ctypes.data)
+
+    threads = threads or default_threads()
+    with ThreadPoolExecutor(max_workers=max(1, min(threads, B * H))) as ex:
+        codes = list(ex.map(run, range(B * H)))
+    if any(codes):
+        raise RuntimeError("oracle_attention_backward_head failed")
+    shape = (B, H, N, d)
+    return dq.reshape(shape), dk.reshape(shape), dv.reshape(shape)

@@ -97,3 +97,69 @@ int oracle_attention_rows(const float *q, const float *k, const float *v,
     return oracle_attention_rows_qkv(q, k, v, B, H, N, N, d, d, scale, causal,
                                      rows, nrows, o, lse, work);
 }
+
+/*
+ * Gradients of the forward pass for one head (bh), fp64, from the plain
+ * definition: with L = sum_i dO_i . O_i, P the softmax weights above and
+ * S_ij = scale * q_i . k_j (masked entries have P_ij = 0),
+ *
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = dO_i . v_j
+ *   dS_ij = P_ij (dP_ij - delta_i),   delta_i = sum_j P_ij dP_ij
+ *   dQ_i  = scale * sum_j dS_ij k_j
+ *   dK_j  = scale * sum_i dS_ij q_i
+ *
+ * This is what "FlashAttention" (ai360xpert.com, "Recomputation in the
+ * backward pass") recomputes tile by tile from the stored row statistics.
+ * Layout: Q, K, V, dO contiguous [B, H, N, d]; dq, dk, dv receive this
+ * head's [N, d] blocks; work holds N * N doubles (P).  Returns 0 on success.
+ */
+int oracle_attention_backward_head(const float *q, const float *k, const float *v, const float *dout,
+                                   int64_t B, int64_t H, int64_t N, int64_t d, double scale, int causal,
+                                   int64_t bh, double *dq, double *dk, double *dv, double *work)
+{
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || !work) return 1;
+    if (B < 1 || H < 1 || N < 1 || d < 1 || bh < 0 || bh >= B * H) return 1;
+    const float *qh = q + bh * N * d, *kh = k + bh * N * d, *vh = v + bh * N * d, *gh = dout + bh * N * d;
+    double *P = work;
+    /* the softmax weights, row by row, by the three passes */
+    for (int64_t i = 0; i < N; ++i) {
+        int64_t nkeys = causal ? i + 1 : N;
+        double *pr = P + i * N;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < N; ++j) {
+            if (j >= nkeys) { pr[j] = 0.0; continue; }
+            double dot = 0.0;
+            for (int64_t t = 0; t < d; ++t) dot += (double)qh[i * d + t] * (double)kh[j * d + t];
+            pr[j] = scale * dot;
+            if (pr[j] > m) m = pr[j];
+        }
+        double den = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j) den += exp(pr[j] - m);
+        for (int64_t j = 0; j < nkeys; ++j) pr[j] = exp(pr[j] - m) / den;
+    }
+    for (int64_t x = 0; x < N * d; ++x) { dq[x] = 0.0; dk[x] = 0.0; dv[x] = 0.0; }
+    for (int64_t i = 0; i < N; ++i) {
+        const double *pr = P + i * N;
+        /* delta_i = sum_j P_ij (dO_i . v_j) */
+        double delta = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            if (pr[j] == 0.0) continue;
+            double dp = 0.0;
+            for (int64_t t = 0; t < d; ++t) dp += (double)gh[i * d + t] * (double)vh[j * d + t];
+            delta += pr[j] * dp;
+        }
+        for (int64_t j = 0; j < N; ++j) {
+            if (pr[j] == 0.0) continue;
+            double dp = 0.0;
+            for (int64_t t = 0; t < d; ++t) dp += (double)gh[i * d + t] * (double)vh[j * d + t];
+            const double ds = pr[j] * (dp - delta);
+            for (int64_t t = 0; t < d; ++t) {
+                dv[j * d + t] += pr[j] * (double)gh[i * d + t];
+                dq[i * d + t] += scale * ds * (double)kh[j * d + t];
+                dk[j * d + t] += scale * ds * (double)qh[i * d + t];
+            }
+        }
+    }
+    return 0;
+}
