@@ -204,6 +204,31 @@ typedef struct fa_params {
 fa_status fa_attention(const fa_params *p, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * fa_backward_workspace_size / fa_backward -- gradients of the forward pass
+ * by recomputation from the stored per-row statistics ("FlashAttention",
+ * ai360xpert.com, "Recomputation in the backward pass"): with
+ * P_ij = exp(scale q_i.k_j - LSE_i) and L = sum_i dO_i . O_i,
+ *   dV = P^T dO,  dS = P o (dO V^T - delta),  delta_i = dO_i . O_i,
+ *   dQ = scale dS K,  dK = scale dS^T Q.
+ *
+ *   q, k, v, o, dout  device pointers, contiguous [B, H, N, d] of in_dtype
+ *                     (o is the forward output, dout the gradient of O).
+ *   lse               device pointer, [B, H, N] fp32 from the forward pass.
+ *   dq, dk, dv        device pointers, [B, H, N, d] of grad_dtype; written.
+ *   workspace         device pointer, >= fa_backward_workspace_size bytes,
+ *                     256-byte aligned (per-row delta and LSE in log2 units).
+ *   scale, causal     as in the forward call that produced o and lse.
+ * Asynchronous on `stream`; no result is accumulated across CTAs, so the
+ * gradients are deterministic.  Gradients must not overlap the inputs.
+ */
+size_t fa_backward_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d);
+fa_status fa_backward(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                      const float *lse, void *dq, void *dk, void *dv,
+                      int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+                      int in_dtype, int grad_dtype, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
+/*
  * fa_forward_noalloc -- the wide-head path of fa_forward_ws for callers that
  * cannot allocate device memory.  The pages have no counterpart: it exists
  * for code that must not call cudaMalloc while it runs (a plugin inside a

@@ -54,6 +54,9 @@ SIGNATURES = {
     "fa_forward_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "fa_attention": (ctypes.c_int, [ctypes.POINTER(FaParams), _P, ctypes.c_size_t, _P]),
+    "fa_backward_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
+    "fa_backward": (ctypes.c_int, [_P] * 9 + [_I64, _I64, _I64, _I64, ctypes.c_float, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "fa_forward_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]),
     "fa_check_device_error": (ctypes.c_int, [_P]),
@@ -263,3 +266,33 @@ def fa_attention(q, k, v, o=None, lse=None, scale=None, causal=False, o_dtype=No
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     check(load().fa_attention(ctypes.byref(prm), ws_ptr, ws_bytes, stream))
     return o, lse
+
+
+def fa_backward(q, k, v, o, dout, lse, scale=None, causal=False, grad_dtype=None, dq=None, dk=None,
+                dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of the forward pass that produced (o, lse) from
+    q, k, v, given dout = dL/dO; contiguous [B, H, N, d] CUDA tensors."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        if not t.is_cuda or not t.is_contiguous() or t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor like q")
+    B, H, N, d = q.shape
+    gdt = grad_dtype or q.dtype
+    dq = torch.empty(q.shape, dtype=gdt, device=q.device) if dq is None else dq
+    dk = torch.empty(q.shape, dtype=gdt, device=q.device) if dk is None else dk
+    dv = torch.empty(q.shape, dtype=gdt, device=q.device) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(load().fa_backward_workspace_size(B, H, N, d), dtype=torch.uint8,
+                                device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    st = load().fa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                            float(scale), int(bool(causal)), _dtype_code(q.dtype), _dtype_code(gdt),
+                            workspace.data_ptr(), workspace.numel() * workspace.element_size(), stream)
+    check(st)
+    return dq, dk, dv

@@ -325,6 +325,56 @@ fa_status fa_attention(const fa_params *a, void *workspace, size_t workspace_byt
     return dispatch(p, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), 0u);
 }
 
+size_t fa_backward_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d)
+{
+    if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+    fa::BackwardProblem p{};
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.d = d;
+    return fa::backward_workspace_bytes(p);
+}
+
+fa_status fa_backward(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
+                      void *dq, void *dk, void *dv, int64_t B, int64_t H, int64_t N, int64_t d, float scale,
+                      int causal, int in_dtype, int grad_dtype, void *workspace, size_t workspace_bytes, void *stream)
+{
+    g_last_error.clear();
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv)
+        return fail(FA_ERR_INVALID_ARG, "q, k, v, o, dout, lse, dq, dk, dv must be non-NULL");
+    fa::Problem fwd{q, k, v, const_cast<void *>(o), nullptr, B, H, N, d, scale, causal != 0, in_dtype, in_dtype};
+    if (!size_ok(fwd)) return fail(FA_ERR_INVALID_ARG, "invalid sizes or dtypes");
+    if (grad_dtype != FA_BF16 && grad_dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, "grad_dtype %d is not an fa_dtype", grad_dtype);
+    if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+    const size_t ei = dtype_size(in_dtype), eg = dtype_size(grad_dtype), n = (size_t)(B * H * N * d);
+    const void *ins[5] = {q, k, v, o, dout};
+    void *outs[3] = {dq, dk, dv};
+    for (const void *x : ins)
+        if (!aligned(x, ei)) return fail(FA_ERR_INVALID_ARG, "pointers must be aligned to their element size");
+    for (const void *x : outs)
+        if (!aligned(x, eg)) return fail(FA_ERR_INVALID_ARG, "pointers must be aligned to their element size");
+    auto overlap = [](const void *a, size_t na, const void *b, size_t nb) {
+        uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+        return x < y + nb && y < x + na;
+    };
+    for (int a = 0; a < 3; ++a) {
+        for (const void *x : ins)
+            if (overlap(outs[a], n * eg, x, n * ei)) return fail(FA_ERR_INVALID_ARG, "gradients must not overlap the inputs");
+        if (overlap(outs[a], n * eg, lse, (size_t)(B * H * N) * 4))
+            return fail(FA_ERR_INVALID_ARG, "gradients must not overlap the inputs");
+        for (int c = a + 1; c < 3; ++c)
+            if (overlap(outs[a], n * eg, outs[c], n * eg)) return fail(FA_ERR_INVALID_ARG, "dq, dk, dv must not overlap");
+    }
+    fa::BackwardProblem p{q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal != 0, in_dtype, grad_dtype};
+    const size_t need = fa::backward_workspace_bytes(p);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+        return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned and hold %zu bytes", need);
+    cudaError_t e = fa::launch_backward_general(p, workspace, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return FA_OK;
+}
+
 fa_status fa_forward_ws(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B, int64_t H,
                         int64_t N, int64_t d, float scale, int causal, int in_dtype, int o_dtype, void *workspace,
                         size_t workspace_bytes, void *stream)

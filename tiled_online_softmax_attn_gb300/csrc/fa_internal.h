@@ -93,6 +93,20 @@ cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cu
                         const char **detail);
 cudaError_t wide_take_error_word(uint32_t *word, cudaStream_t stream);
 
+// Backward problem: contiguous [B, H, N, d] Q, K, V, O, dO of in_dtype,
+// LSE [B, H, N] fp32 from the forward pass, gradients of grad_dtype.
+struct BackwardProblem {
+    const void *q, *k, *v, *o, *dout;
+    const float *lse;
+    void *dq, *dk, *dv;
+    int64_t B, H, N, d;
+    float scale;
+    int causal;
+    int in_dtype, grad_dtype;
+};
+size_t backward_workspace_bytes(const BackwardProblem &p);
+cudaError_t launch_backward_general(const BackwardProblem &p, void *workspace, cudaStream_t stream);
+
 // Sets the text fa_last_error returns on this host thread.
 void set_last_error(const char *msg);
 
