@@ -370,6 +370,13 @@ fa_status fa_backward(const void *q, const void *k, const void *v, const void *o
     const size_t need = fa::backward_workspace_bytes(p);
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
         return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned and hold %zu bytes", need);
+    if (fa::backward_tc_supported(p)) {
+        const char *detail = nullptr;
+        cudaError_t e = fa::launch_backward_tc(p, workspace, static_cast<cudaStream_t>(stream), &detail);
+        if (e != cudaSuccess)
+            return detail ? fail(FA_ERR_CUDA, "tensor-core backward: %s", detail) : cuda_fail(e, "tensor-core backward");
+        return FA_OK;
+    }
     cudaError_t e = fa::launch_backward_general(p, workspace, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return FA_OK;
@@ -490,11 +497,12 @@ fa_status fa_check_device_error(void *stream)
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
-    uint32_t word = 0, wide_word = 0;
+    uint32_t word = 0, wide_word = 0, bwd_word = 0;
     e = fa::tc_take_error_word(&word, s);
     if (e == cudaSuccess) e = fa::wide_take_error_word(&wide_word, s);
+    if (e == cudaSuccess) e = fa::bwd_take_error_word(&bwd_word, s);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
-    word |= wide_word;
+    word |= wide_word | bwd_word;
     if (word) return fail(FA_ERR_TIMEOUT, "a device pipeline wait gave up (error word 0x%x)", word);
     return FA_OK;
 }

@@ -42,10 +42,12 @@ __device__ __forceinline__ float ld(const __nv_bfloat16 *p) { return __bfloat162
 __device__ __forceinline__ void st(float *p, float x) { *p = x; }
 __device__ __forceinline__ void st(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 
-// delta_i = dO_i . O_i, one warp per row, lse2_i = LSE_i * log2(e).
+// delta_i = dO_i . O_i, one warp per row, lse2_i = LSE_i * log2(e); row i of
+// head bh goes to index bh * pitch + i (pitch >= N).
 template <typename T>
 __global__ void fa_bwd_delta_kernel(const T *__restrict__ o, const T *__restrict__ dout, const float *__restrict__ lse,
-                                    float *__restrict__ delta, float *__restrict__ lse2, int64_t rows, int d)
+                                    float *__restrict__ delta, float *__restrict__ lse2, int64_t rows, int d, int N,
+                                    int pitch)
 {
     const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
@@ -55,8 +57,9 @@ __global__ void fa_bwd_delta_kernel(const T *__restrict__ o, const T *__restrict
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
-        delta[row] = acc;
-        lse2[row] = lse[row] * 1.4426950408889634f;
+        const int64_t idx = (row / N) * pitch + row % N;
+        delta[idx] = acc;
+        lse2[idx] = lse[row] * 1.4426950408889634f;
     }
 }
 
@@ -216,7 +219,7 @@ cudaError_t launch_typed(const BackwardProblem &p, float *delta, float *lse2, cu
     const int N = (int)p.N, d = (int)p.d, BH = (int)(p.B * p.H);
     const int64_t rows = (int64_t)BH * N;
     fa_bwd_delta_kernel<Tin><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
-        static_cast<const Tin *>(p.o), static_cast<const Tin *>(p.dout), p.lse, delta, lse2, rows, d);
+        static_cast<const Tin *>(p.o), static_cast<const Tin *>(p.dout), p.lse, delta, lse2, rows, d, N, N);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const float sl = p.scale * 1.4426950408889634f;
@@ -241,17 +244,39 @@ cudaError_t launch_typed(const BackwardProblem &p, float *delta, float *lse2, cu
 
 }  // namespace
 
+// delta and lse2 arrays, each [B*H][N rounded up to 128] floats (the tensor-
+// core backward reads them in 128-row blocks).
 size_t backward_workspace_bytes(const BackwardProblem &p)
 {
-    const size_t rows = (size_t)(p.B * p.H * p.N);
+    const size_t rows = (size_t)(p.B * p.H) * (size_t)((p.N + 127) / 128 * 128);
     return 2 * ((rows * 4 + 255) & ~size_t(255));
+}
+
+cudaError_t launch_backward_delta(const BackwardProblem &p, void *workspace, cudaStream_t stream, int pitch,
+                                  float **delta_out, float **lse2_out)
+{
+    const size_t rows_pad = (size_t)(p.B * p.H) * (size_t)((p.N + 127) / 128 * 128);
+    float *delta = static_cast<float *>(workspace);
+    float *lse2 = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + ((rows_pad * 4 + 255) & ~size_t(255)));
+    *delta_out = delta;
+    *lse2_out = lse2;
+    const int64_t rows = p.B * p.H * p.N;
+    if (p.in_dtype == 0)
+        fa_bwd_delta_kernel<__nv_bfloat16><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(p.o), static_cast<const __nv_bfloat16 *>(p.dout), p.lse, delta, lse2,
+            rows, (int)p.d, (int)p.N, pitch);
+    else
+        fa_bwd_delta_kernel<float><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+            static_cast<const float *>(p.o), static_cast<const float *>(p.dout), p.lse, delta, lse2, rows, (int)p.d,
+            (int)p.N, pitch);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_backward_general(const BackwardProblem &p, void *workspace, cudaStream_t stream)
 {
-    const size_t rows = (size_t)(p.B * p.H * p.N);
+    const size_t rows_pad = (size_t)(p.B * p.H) * (size_t)((p.N + 127) / 128 * 128);
     float *delta = static_cast<float *>(workspace);
-    float *lse2 = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + ((rows * 4 + 255) & ~size_t(255)));
+    float *lse2 = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + ((rows_pad * 4 + 255) & ~size_t(255)));
     const bool in_bf16 = p.in_dtype == 0, g_bf16 = p.grad_dtype == 0;
     if (in_bf16 && g_bf16) return launch_typed<__nv_bfloat16, __nv_bfloat16>(p, delta, lse2, stream);
     if (in_bf16) return launch_typed<__nv_bfloat16, float>(p, delta, lse2, stream);

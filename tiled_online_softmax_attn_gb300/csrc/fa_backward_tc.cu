@@ -1,0 +1,598 @@
+// Tensor-core backward pass (tcgen05 + TMA), bf16 inputs, d in {64, 128}.
+//
+// The gradients of the forward pass by recomputation from the stored per-row
+// log-sum-exp ("FlashAttention", ai360xpert.com, "Recomputation in the
+// backward pass"); definitions as in fa_backward.cu.  Two kernels, neither of
+// which accumulates across CTAs:
+//
+//   dK/dV kernel -- a CTA owns 128 keys (one per tensor-memory lane) and
+//   streams the query tiles that see them.  Per query tile:
+//     S^T  = K_j Q_i^T       (SS MMA)          -> TMEM
+//     dP^T = V_j dO_i^T      (SS MMA)          -> TMEM
+//     P^T  = exp2(S^T scale log2 e - LSE_i log2 e)   (softmax warps; written
+//            over S^T as bf16)
+//     dV  += P^T dO_i        (A = P^T from TMEM, B = dO_i MN-major)
+//     dS^T = P^T (dP^T - delta_i)   (written over dP^T as bf16)
+//     dK  += dS^T Q_i        (A = dS^T from TMEM, B = Q_i MN-major)
+//   dQ kernel -- a CTA owns 128 queries and streams the key tiles they see:
+//     S = Q_i K_j^T, dP = dO_i V_j^T, dS = P (dP - delta), dQ += dS K_j.
+//
+// So S and dP are formed twice (7 products of 128 x 128 x d instead of 5):
+// the price of no atomics and deterministic gradients.  Warps 0-3 handle one
+// tensor-memory lane (row) each thread, warp 4 issues the TMA loads, warp 5
+// the MMAs.  Every wait is bounded as in the forward kernels.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+#include "tc_common.cuh"
+
+namespace fa {
+
+__device__ uint32_t g_bwd_error_word;
+
+namespace {
+
+using namespace ptx;
+using namespace tc;
+
+constexpr int BM = 128;
+constexpr int NUM_THREADS = 192;
+constexpr int TMA_WARP = 4;
+constexpr int MMA_WARP = 5;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t BOX = 128 * 128;  // one 128-row x 64-column bf16 box
+constexpr uint32_t VEC_BYTES = 1024;  // lse2 and delta of 128 rows
+
+template <int D>
+struct BCfg {
+    static constexpr int CH = D / 64;
+    static constexpr uint32_t TILE = BM * D * 2;
+    static constexpr uint32_t RES = 2 * TILE;              // resident pair (K,V) or (Q,dO)
+    static constexpr uint32_t STAGE = 2 * TILE + VEC_BYTES;  // streamed pair (+ vectors for dK/dV)
+    static constexpr uint32_t SMEM = RES + 2 * STAGE + 1024;
+    // keep one CTA per SM (all 512 tensor-memory columns each)
+    static constexpr uint32_t SMEM_REQ = SMEM < 120u * 1024u ? 120u * 1024u : SMEM;
+};
+
+struct BwdParams {
+    int N, BH, n_q, pitch;
+    float sl, scale;
+    uint64_t limit;
+    const float *lse2, *delta;  // [BH][pitch]
+    void *dq, *dk, *dv;
+    int g_fp32;
+};
+
+__device__ __forceinline__ void store_row32(void *base, int fp32, size_t elem, const uint32_t (&raw)[32], float mul)
+{
+    if (fp32) {
+        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(base) + elem);
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+            dst[x] = make_float4(__uint_as_float(raw[4 * x]) * mul, __uint_as_float(raw[4 * x + 1]) * mul,
+                                 __uint_as_float(raw[4 * x + 2]) * mul, __uint_as_float(raw[4 * x + 3]) * mul);
+    } else {
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(base) + elem);
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+            dst[x] = make_uint4(pack_bf16x2(__uint_as_float(raw[8 * x]) * mul, __uint_as_float(raw[8 * x + 1]) * mul),
+                                pack_bf16x2(__uint_as_float(raw[8 * x + 2]) * mul, __uint_as_float(raw[8 * x + 3]) * mul),
+                                pack_bf16x2(__uint_as_float(raw[8 * x + 4]) * mul, __uint_as_float(raw[8 * x + 5]) * mul),
+                                pack_bf16x2(__uint_as_float(raw[8 * x + 6]) * mul, __uint_as_float(raw[8 * x + 7]) * mul));
+    }
+}
+
+__device__ __forceinline__ void fail_bwd(volatile int *abort_flag)
+{
+    atomicOr(&g_bwd_error_word, 64u);
+    *abort_flag = 1;
+}
+
+// ---------------------------------------------------------------- dK / dV
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g, const BwdParams prm)
+{
+    using C = BCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t res_full, full_b[2], empty_b[2], s_full, p_ready, ds_ready, o_full, drain;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N = prm.N;
+    const int kt = (int)(blockIdx.x % prm.n_q), bh = (int)(blockIdx.x / prm.n_q);
+    const int k0 = kt * BM;
+    const int first = CAUSAL ? kt : 0;  // query tiles before the key tile see none of its keys
+    const int n_steps = prm.n_q - first;
+
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s_base = smem_addr(smem);
+    const uint32_t sK = s_base, sV = s_base + C::TILE, sStage = s_base + C::RES;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_addr(&res_full), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_addr(&full_b[s]), 1);
+            mbar_init(smem_addr(&empty_b[s]), 1);
+        }
+        mbar_init(smem_addr(&s_full), 1);
+        mbar_init(smem_addr(&p_ready), 128);
+        mbar_init(smem_addr(&ds_ready), 128);
+        mbar_init(smem_addr(&o_full), 1);
+        mbar_init(smem_addr(&drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == MMA_WARP) {
+        tmem_alloc(smem_addr(&tmem_base_s), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    const uint64_t limit = prm.limit;
+    // tensor memory: S^T/P^T [0,128), dP^T/dS^T [128,256), dV [256,256+D), dK [256+D, 256+2D)
+    const uint32_t cS = 0, cP = 128, cV = 256, cK = 256 + D;
+
+    if (warp == TMA_WARP) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_last();
+            bool ok = true;
+            int issued = 0;
+            mbar_arrive_expect_tx(smem_addr(&res_full), C::RES);
+            for (int c = 0; c < C::CH; ++c) {
+                tma_load_3d(sK + c * BOX, &tm_k, smem_addr(&res_full), c * 64, k0, bh, pol);
+                tma_load_3d(sV + c * BOX, &tm_v, smem_addr(&res_full), c * 64, k0, bh, pol);
+            }
+            for (int s = 0; s < n_steps; ++s) {
+                const int st = s & 1, q0 = (first + s) * BM;
+                if (!wait_or_abort(smem_addr(&empty_b[st]), (uint32_t)(((s >> 1) & 1) ^ 1), limit, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_addr(&full_b[st]), dst = sStage + st * C::STAGE;
+                mbar_arrive_expect_tx(fb, C::STAGE);
+                for (int c = 0; c < C::CH; ++c) {
+                    tma_load_3d(dst + c * BOX, &tm_q, fb, c * 64, q0, bh, pol);
+                    tma_load_3d(dst + C::TILE + c * BOX, &tm_g, fb, c * 64, q0, bh, pol);
+                }
+                const size_t vrow = (size_t)bh * prm.pitch + q0;
+                bulk_copy_g2s(dst + 2 * C::TILE, prm.lse2 + vrow, 512, fb);
+                bulk_copy_g2s(dst + 2 * C::TILE + 512, prm.delta + vrow, 512, fb);
+                issued = s + 1;
+            }
+            if (!ok) {
+                if (!abort_flag) fail_bwd(&abort_flag);
+                for (int s = (issued > 2 ? issued - 2 : 0); s < issued; ++s)
+                    mbar_wait_bounded(smem_addr(&full_b[s & 1]), (uint32_t)((s >> 1) & 1), limit);
+                mbar_wait_bounded(smem_addr(&res_full), 0, limit);
+            }
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        if (lane == 0) {
+            const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0), id_o = idesc_bf16_f32(BM, D, 0, 1);
+            const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
+            bool ok = wait_or_abort(smem_addr(&res_full), 0, limit, &abort_flag), issued = false;
+            for (int s = 0; ok && s < n_steps; ++s) {
+                const int st = s & 1;
+                if (!wait_or_abort(smem_addr(&full_b[st]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t base = sStage + st * C::STAGE;
+                const uint64_t dQ = sdesc_sw128(base, 16, 1024), dG = sdesc_sw128(base + C::TILE, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
+                    mma_ss(tmem + cS, dK + off, dQ + off, id_s, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
+                    mma_ss(tmem + cP, dV + off, dG + off, id_s, kk > 0 ? 1u : 0u);
+                }
+                issued = true;
+                mma_commit(smem_addr(&s_full));
+                // dV += P^T dO_i once P^T is in tensor memory
+                if (!wait_or_abort(smem_addr(&p_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t dGmn = sdesc_sw128(base + C::TILE, BOX, 1024), dQmn = sdesc_sw128(base, BOX, 1024);
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk)
+                    mma_ts(tmem + cV, tmem + cS + kk * 8, dGmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                           (s > 0 || kk > 0) ? 1u : 0u);
+                // dK += dS^T Q_i once dS^T is in tensor memory
+                if (!wait_or_abort(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk)
+                    mma_ts(tmem + cK, tmem + cP + kk * 8, dQmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                           (s > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(smem_addr(&empty_b[st]));
+            }
+            if (ok) {
+                mma_commit(smem_addr(&o_full));
+            } else {
+                if (!abort_flag) fail_bwd(&abort_flag);
+                if (issued) {
+                    mma_commit(smem_addr(&drain));
+                    mbar_wait_bounded(smem_addr(&drain), 0, limit);
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // one key per thread: key kj on tensor-memory lane warp*32 + lane
+        const int jr = warp * 32 + lane, kj = k0 + jr;
+        const uint32_t lb = tmem + ((uint32_t)(warp * 32) << 16);
+        const float sl = prm.sl;
+        bool ok = true;
+        for (int s = 0; s < n_steps; ++s) {
+            const int st = s & 1, q0 = (first + s) * BM;
+            if (!wait_or_abort(smem_addr(&s_full), (uint32_t)(s & 1), limit, &abort_flag) ||
+                !wait_or_abort(smem_addr(&full_b[st]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float *vec = reinterpret_cast<const float *>(smem + C::RES + st * C::STAGE + 2 * C::TILE);
+            // P^T row: weights of this key for the 128 queries of the tile
+            float p[BM];
+            {
+                uint32_t raw[BM];
+                tmem_ld128(lb + cS, raw);
+#pragma unroll
+                for (int c = 0; c < BM; ++c) {
+                    const int q = q0 + c;
+                    const bool keep = kj < N && q < N && (!CAUSAL || kj <= q);
+                    p[c] = keep ? ex2(fmaf(__uint_as_float(raw[c]), sl, -vec[c])) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(p[h * 64 + 2 * x], p[h * 64 + 2 * x + 1]);
+                tmem_st32(lb + cS + h * 32, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_addr(&p_ready));
+            // dS^T row = P^T (dP^T - delta)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t raw[64];
+                tmem_ld64(lb + cP + h * 64, raw);
+                uint32_t pk[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    const int c = h * 64 + 2 * x;
+                    const float d0 = p[c] * (__uint_as_float(raw[2 * x]) - vec[128 + c]);
+                    const float d1 = p[c + 1] * (__uint_as_float(raw[2 * x + 1]) - vec[128 + c + 1]);
+                    pk[x] = pack_bf16x2(p[c] != 0.f ? d0 : 0.f, p[c + 1] != 0.f ? d1 : 0.f);
+                }
+                tmem_st32(lb + cP + h * 32, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_addr(&ds_ready));
+        }
+        if (ok && wait_or_abort(smem_addr(&o_full), 0, limit, &abort_flag)) {
+            tc_fence_after();
+            const size_t row = ((size_t)bh * N + kj) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(lb + cV + c * 32, raw);
+                if (kj < N) store_row32(prm.dv, prm.g_fp32, row + c * 32, raw, 1.f);
+                tmem_ld32(lb + cK + c * 32, raw);
+                if (kj < N) store_row32(prm.dk, prm.g_fp32, row + c * 32, raw, prm.scale);
+            }
+        } else if (!abort_flag) {
+            fail_bwd(&abort_flag);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- dQ
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g, const BwdParams prm)
+{
+    using C = BCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t res_full, full_b[2], empty_b[2], s_full, ds_ready, o_full, drain;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N = prm.N;
+    const int qt = CAUSAL ? prm.n_q - 1 - (int)(blockIdx.x / prm.BH) : (int)(blockIdx.x % prm.n_q);
+    const int bh = CAUSAL ? (int)(blockIdx.x % prm.BH) : (int)(blockIdx.x / prm.n_q);
+    const int q0 = qt * BM;
+    const int n_steps = CAUSAL ? qt + 1 : prm.n_q;  // key tiles this query tile sees
+
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s_base = smem_addr(smem);
+    const uint32_t sQ = s_base, sG = s_base + C::TILE, sStage = s_base + C::RES;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_addr(&res_full), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_addr(&full_b[s]), 1);
+            mbar_init(smem_addr(&empty_b[s]), 1);
+        }
+        mbar_init(smem_addr(&s_full), 1);
+        mbar_init(smem_addr(&ds_ready), 128);
+        mbar_init(smem_addr(&o_full), 1);
+        mbar_init(smem_addr(&drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == MMA_WARP) {
+        tmem_alloc(smem_addr(&tmem_base_s), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    const uint64_t limit = prm.limit;
+    // tensor memory: S / dS [0,128), dP [128,256), dQ [256, 256+D)
+    const uint32_t cS = 0, cP = 128, cQ = 256;
+
+    if (warp == TMA_WARP) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_last();
+            bool ok = true;
+            int issued = 0;
+            mbar_arrive_expect_tx(smem_addr(&res_full), C::RES);
+            for (int c = 0; c < C::CH; ++c) {
+                tma_load_3d(sQ + c * BOX, &tm_q, smem_addr(&res_full), c * 64, q0, bh, pol);
+                tma_load_3d(sG + c * BOX, &tm_g, smem_addr(&res_full), c * 64, q0, bh, pol);
+            }
+            for (int s = 0; s < n_steps; ++s) {
+                const int st = s & 1, k0 = s * BM;
+                if (!wait_or_abort(smem_addr(&empty_b[st]), (uint32_t)(((s >> 1) & 1) ^ 1), limit, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_addr(&full_b[st]), dst = sStage + st * C::STAGE;
+                mbar_arrive_expect_tx(fb, 2 * C::TILE);
+                for (int c = 0; c < C::CH; ++c) {
+                    tma_load_3d(dst + c * BOX, &tm_k, fb, c * 64, k0, bh, pol);
+                    tma_load_3d(dst + C::TILE + c * BOX, &tm_v, fb, c * 64, k0, bh, pol);
+                }
+                issued = s + 1;
+            }
+            if (!ok) {
+                if (!abort_flag) fail_bwd(&abort_flag);
+                for (int s = (issued > 2 ? issued - 2 : 0); s < issued; ++s)
+                    mbar_wait_bounded(smem_addr(&full_b[s & 1]), (uint32_t)((s >> 1) & 1), limit);
+                mbar_wait_bounded(smem_addr(&res_full), 0, limit);
+            }
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        if (lane == 0) {
+            const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0), id_o = idesc_bf16_f32(BM, D, 0, 1);
+            const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), dG = sdesc_sw128(sG, 16, 1024);
+            bool ok = wait_or_abort(smem_addr(&res_full), 0, limit, &abort_flag), issued = false;
+            for (int s = 0; ok && s < n_steps; ++s) {
+                const int st = s & 1;
+                if (!wait_or_abort(smem_addr(&full_b[st]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t base = sStage + st * C::STAGE;
+                const uint64_t dK = sdesc_sw128(base, 16, 1024), dV = sdesc_sw128(base + C::TILE, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
+                    mma_ss(tmem + cS, dQ + off, dK + off, id_s, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
+                    mma_ss(tmem + cP, dG + off, dV + off, id_s, kk > 0 ? 1u : 0u);
+                }
+                issued = true;
+                mma_commit(smem_addr(&s_full));
+                if (!wait_or_abort(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t dKmn = sdesc_sw128(base, BOX, 1024);
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk)
+                    mma_ts(tmem + cQ, tmem + cS + kk * 8, dKmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                           (s > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(smem_addr(&empty_b[st]));
+            }
+            if (ok) {
+                mma_commit(smem_addr(&o_full));
+            } else {
+                if (!abort_flag) fail_bwd(&abort_flag);
+                if (issued) {
+                    mma_commit(smem_addr(&drain));
+                    mbar_wait_bounded(smem_addr(&drain), 0, limit);
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        const int r = warp * 32 + lane, qi = q0 + r;
+        const uint32_t lb = tmem + ((uint32_t)(warp * 32) << 16);
+        const float sl = prm.sl;
+        const float l2 = qi < N ? prm.lse2[(size_t)bh * prm.pitch + qi] : 0.f;
+        const float de = qi < N ? prm.delta[(size_t)bh * prm.pitch + qi] : 0.f;
+        bool ok = true;
+        for (int s = 0; s < n_steps; ++s) {
+            const int k0 = s * BM;
+            if (!wait_or_abort(smem_addr(&s_full), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            float p[BM];
+            {
+                uint32_t raw[BM];
+                tmem_ld128(lb + cS, raw);
+#pragma unroll
+                for (int c = 0; c < BM; ++c) {
+                    const int kj = k0 + c;
+                    const bool keep = qi < N && kj < N && (!CAUSAL || kj <= qi);
+                    p[c] = keep ? ex2(fmaf(__uint_as_float(raw[c]), sl, -l2)) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t raw[64];
+                tmem_ld64(lb + cP + h * 64, raw);
+                uint32_t pk[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    const int c = h * 64 + 2 * x;
+                    const float d0 = p[c] * (__uint_as_float(raw[2 * x]) - de);
+                    const float d1 = p[c + 1] * (__uint_as_float(raw[2 * x + 1]) - de);
+                    pk[x] = pack_bf16x2(p[c] != 0.f ? d0 : 0.f, p[c + 1] != 0.f ? d1 : 0.f);
+                }
+                tmem_st32(lb + cS + h * 32, pk);  // dS over S
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_addr(&ds_ready));
+        }
+        if (ok && wait_or_abort(smem_addr(&o_full), 0, limit, &abort_flag)) {
+            tc_fence_after();
+            const size_t row = ((size_t)bh * N + qi) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(lb + cQ + c * 32, raw);
+                if (qi < N) store_row32(prm.dq, prm.g_fp32, row + c * 32, raw, prm.scale);
+            }
+        } else if (!abort_flag) {
+            fail_bwd(&abort_flag);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool make_map(CUtensorMap *map, const void *ptr, int64_t BH, int64_t N, int64_t d)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)(N * d * 2)};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_dims(const BackwardProblem &p, float *delta, float *lse2, int pitch, cudaStream_t stream,
+                        const char **detail)
+{
+    using C = BCfg<D>;
+    const int64_t BH = p.B * p.H;
+    CUtensorMap mq, mk, mv, mg;
+    if (!make_map(&mq, p.q, BH, p.N, D) || !make_map(&mk, p.k, BH, p.N, D) || !make_map(&mv, p.v, BH, p.N, D) ||
+        !make_map(&mg, p.dout, BH, p.N, D)) {
+        *detail = "cuTensorMapEncodeTiled failed or is unavailable";
+        return cudaErrorInvalidValue;
+    }
+    BwdParams prm;
+    prm.N = (int)p.N;
+    prm.BH = (int)BH;
+    prm.n_q = (int)((p.N + BM - 1) / BM);
+    prm.pitch = pitch;
+    prm.sl = p.scale * 1.4426950408889634f;
+    prm.scale = p.scale;
+    prm.limit = 2000000000ull;
+    prm.lse2 = lse2;
+    prm.delta = delta;
+    prm.dq = p.dq;
+    prm.dk = p.dk;
+    prm.dv = p.dv;
+    prm.g_fp32 = p.grad_dtype == 1;
+    auto kv = fa_bwd_dkdv_tc<D, CAUSAL>;
+    auto kq = fa_bwd_dq_tc<D, CAUSAL>;
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_REQ)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_REQ)) != cudaSuccess) return e;
+    const unsigned grid = (unsigned)((int64_t)prm.n_q * BH);
+    kv<<<grid, NUM_THREADS, C::SMEM_REQ, stream>>>(mq, mk, mv, mg, prm);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    kq<<<grid, NUM_THREADS, C::SMEM_REQ, stream>>>(mq, mk, mv, mg, prm);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool backward_tc_supported(const BackwardProblem &p)
+{
+    if (p.in_dtype != 0 || !(p.d == 64 || p.d == 128) || !(p.scale > 0.f)) return false;
+    auto al16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
+    return al16(p.q) && al16(p.k) && al16(p.v) && al16(p.dout) && al16(p.dq) && al16(p.dk) && al16(p.dv);
+}
+
+cudaError_t launch_backward_tc(const BackwardProblem &p, void *workspace, cudaStream_t stream, const char **detail)
+{
+    const int pitch = (int)((p.N + 127) / 128 * 128);
+    float *delta = nullptr, *lse2 = nullptr;
+    cudaError_t e = launch_backward_delta(p, workspace, stream, pitch, &delta, &lse2);
+    if (e != cudaSuccess) return e;
+    if (p.d == 128)
+        return p.causal ? launch_dims<128, true>(p, delta, lse2, pitch, stream, detail)
+                        : launch_dims<128, false>(p, delta, lse2, pitch, stream, detail);
+    return p.causal ? launch_dims<64, true>(p, delta, lse2, pitch, stream, detail)
+                    : launch_dims<64, false>(p, delta, lse2, pitch, stream, detail);
+}
+
+cudaError_t bwd_take_error_word(uint32_t *word, cudaStream_t stream)
+{
+    cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_bwd_error_word, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess || *word == 0) return e;
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_bwd_error_word, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(stream);
+}
+
+}  // namespace fa

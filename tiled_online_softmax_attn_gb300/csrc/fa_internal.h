@@ -106,6 +106,13 @@ struct BackwardProblem {
 };
 size_t backward_workspace_bytes(const BackwardProblem &p);
 cudaError_t launch_backward_general(const BackwardProblem &p, void *workspace, cudaStream_t stream);
+// delta and lse2 (LSE * log2 e) into the workspace with the given row pitch per head.
+cudaError_t launch_backward_delta(const BackwardProblem &p, void *workspace, cudaStream_t stream, int pitch,
+                                  float **delta, float **lse2);
+// Tensor-core backward: bf16 inputs, d in {64, 128}, scale > 0, 16-byte aligned.
+bool backward_tc_supported(const BackwardProblem &p);
+cudaError_t launch_backward_tc(const BackwardProblem &p, void *workspace, cudaStream_t stream, const char **detail);
+cudaError_t bwd_take_error_word(uint32_t *word, cudaStream_t stream);
 
 // Sets the text fa_last_error returns on this host thread.
 void set_last_error(const char *msg);

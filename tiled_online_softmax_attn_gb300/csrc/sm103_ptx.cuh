@@ -106,6 +106,15 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int c0, int
                  : "memory");
 }
 
+// Plain bulk copy global -> shared (no tensor map), completion on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // 3-D tiled store shared -> global (bulk async group).  Coordinates must be
 // non-negative; elements outside the tensor are not written.
 __device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int c0, int c1, int c2)
