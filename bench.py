@@ -247,6 +247,73 @@ def aggregate_tflops(flops_per_rank: float, ms_max: float, world: int) -> float:
     return world * flops_per_rank / (ms_max * 1e-3) / 1e12
 
 
+def bench_backward(args, w, world, rank, local_rank):
+    """fa_backward on the workload: one step = dQ, dK, dV from (Q, K, V, O, dO,
+    LSE) by recomputation; FLOPs counted as the five products of 2 N^2 d each
+    per head (2.5 times the forward's), halved under the causal mask."""
+    import torch
+    import tiled_online_softmax_attn_gb300 as fa
+    from tiled_online_softmax_attn_gb300 import build as fa_build
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    fa_build.build()
+    q_np, k_np, v_np = w.inputs()
+    g_np = synth.tensor(3 * w.seed + 9, w.shape, w.dtype)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    q, k, v, g = (torch.from_numpy(x).to(tdt).to(dev) for x in (q_np, k_np, v_np, g_np))
+    o, lse = fa.fa_forward(q, k, v, scale=w.scale, causal=w.causal)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(fa.load().fa_backward_workspace_size(*w.shape), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fa_backward(q, k, v, o, g, lse, scale=w.scale, causal=w.causal, dq=dq, dk=dk, dv=dv,
+                       workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    with ClockSampler(local_rank) as clocks:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    if fa.check_device_error(stream.cuda_stream) != fa.FA_OK:
+        raise RuntimeError(fa.last_error())
+    ms = reduce_max(e0.elapsed_time(e1), dist, dev) / args.steps
+    flops = 2.5 * w.flops
+    value = world * flops / (ms * 1e-3) / 1e12
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    tc = w.dtype == "bf16" and w.d in (64, 128)
+    line = {
+        "metric": "attention bwd TFLOP/s (10·B·H·N²·d/time, halved for causal)", "value": value,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "pass": "backward", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "parallelism": "replicas"},
+        "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
+                     "frac": value / world / peak, "peak_source": peak_kind,
+                     "note": "5 products counted; the kernels form S and dP twice (7 products)"},
+        "gpu_launches": args.steps * 3,  # delta, dK/dV, dQ
+        "kernel": "tensor-core backward" if tc else "general backward",
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -258,6 +325,8 @@ def main():
     ap.add_argument("--heads", type=int, help="override H of the workload")
     ap.add_argument("--e2e-steps", type=int, default=20, help="0 skips the end-to-end measurement")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--pass", dest="which", choices=["forward", "backward"], default="forward",
+                    help="backward times fa_backward (dQ, dK, dV by recomputation from LSE)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -281,6 +350,9 @@ def main():
     import torch
     import tiled_online_softmax_attn_gb300 as fa
     from tiled_online_softmax_attn_gb300 import build as fa_build
+
+    if args.which == "backward":
+        return bench_backward(args, w, world, rank, local_rank)
 
     dist = None
     if world > 1:
