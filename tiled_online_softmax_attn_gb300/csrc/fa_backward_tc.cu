@@ -186,25 +186,42 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0), id_o = idesc_bf16_f32(BM, D, 0, 1);
             const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
             bool ok = wait_or_abort(smem_addr(&res_full), 0, limit, &abort_flag), issued = false;
-            for (int s = 0; ok && s < n_steps; ++s) {
-                const int st = s & 1;
-                if (!wait_or_abort(smem_addr(&full_b[st]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t base = sStage + st * C::STAGE;
-                const uint64_t dQ = sdesc_sw128(base, 16, 1024), dG = sdesc_sw128(base + C::TILE, 16, 1024);
+            // S^T(s) = K Q_s^T into cS, dP^T(s) = V dO_s^T into cP
+            auto mma_st = [&](int s) {
+                const uint32_t base = sStage + (s & 1) * C::STAGE;
+                const uint64_t dQ = sdesc_sw128(base, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
                     mma_ss(tmem + cS, dK + off, dQ + off, id_s, kk > 0 ? 1u : 0u);
                 }
+                issued = true;
+            };
+            auto mma_dpt = [&](int s) {
+                const uint32_t base = sStage + (s & 1) * C::STAGE;
+                const uint64_t dG = sdesc_sw128(base + C::TILE, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
                     mma_ss(tmem + cP, dV + off, dG + off, id_s, kk > 0 ? 1u : 0u);
                 }
-                issued = true;
+            };
+            auto wait_stage = [&](int s) -> bool {
+                if (!wait_or_abort(smem_addr(&full_b[s & 1]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) return false;
+                tc_fence_after();
+                return true;
+            };
+            if (ok && (ok = wait_stage(0))) {
+                mma_st(0);
+                mma_dpt(0);
                 mma_commit(smem_addr(&s_full));
-                // dV += P^T dO_i once P^T is in tensor memory
+            }
+            // Per step: dV(s) once P^T(s) is written; then S^T(s+1) into the
+            // columns dV(s) has just read (same-thread MMAs run in order), so
+            // it overlaps the softmax warps' dS^T(s); then dK(s) and dP^T(s+1).
+            for (int s = 0; ok && s < n_steps; ++s) {
+                const int st = s & 1;
+                const uint32_t base = sStage + st * C::STAGE;
                 if (!wait_or_abort(smem_addr(&p_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t dGmn = sdesc_sw128(base + C::TILE, BOX, 1024), dQmn = sdesc_sw128(base, BOX, 1024);
@@ -212,7 +229,11 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 for (int kk = 0; kk < BM / 16; ++kk)
                     mma_ts(tmem + cV, tmem + cS + kk * 8, dGmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
-                // dK += dS^T Q_i once dS^T is in tensor memory
+                const bool more = s + 1 < n_steps;
+                if (more) {
+                    if (!wait_stage(s + 1)) { ok = false; break; }
+                    mma_st(s + 1);
+                }
                 if (!wait_or_abort(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
@@ -220,6 +241,10 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     mma_ts(tmem + cK, tmem + cP + kk * 8, dQmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(smem_addr(&empty_b[st]));
+                if (more) {
+                    mma_dpt(s + 1);
+                    mma_commit(smem_addr(&s_full));
+                }
             }
             if (ok) {
                 mma_commit(smem_addr(&o_full));
@@ -319,7 +344,7 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 {
     using C = BCfg<D>;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t res_full, full_b[2], empty_b[2], s_full, ds_ready, o_full, drain;
+    __shared__ __align__(8) uint64_t res_full, full_b[2], empty_b[2], s_full, s_read, ds_ready, o_full, drain;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
 
@@ -342,6 +367,7 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             mbar_init(smem_addr(&empty_b[s]), 1);
         }
         mbar_init(smem_addr(&s_full), 1);
+        mbar_init(smem_addr(&s_read), 128);
         mbar_init(smem_addr(&ds_ready), 128);
         mbar_init(smem_addr(&o_full), 1);
         mbar_init(smem_addr(&drain), 1);
@@ -356,7 +382,7 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
     const uint64_t limit = prm.limit;
-    // tensor memory: S / dS [0,128), dP [128,256), dQ [256, 256+D)
+    // tensor memory: S [0,128), dP / dS [128,256), dQ [256, 256+D)
     const uint32_t cS = 0, cP = 128, cQ = 256;
 
     if (warp == TMA_WARP) {
@@ -396,32 +422,59 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0), id_o = idesc_bf16_f32(BM, D, 0, 1);
             const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), dG = sdesc_sw128(sG, 16, 1024);
             bool ok = wait_or_abort(smem_addr(&res_full), 0, limit, &abort_flag), issued = false;
-            for (int s = 0; ok && s < n_steps; ++s) {
-                const int st = s & 1;
-                if (!wait_or_abort(smem_addr(&full_b[st]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) { ok = false; break; }
+            auto wait_stage = [&](int s) -> bool {
+                if (!wait_or_abort(smem_addr(&full_b[s & 1]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t base = sStage + st * C::STAGE;
-                const uint64_t dK = sdesc_sw128(base, 16, 1024), dV = sdesc_sw128(base + C::TILE, 16, 1024);
+                return true;
+            };
+            // S(s) = Q K_s^T into cS; dP(s) = dO V_s^T into cP
+            auto mma_s = [&](int s) {
+                const uint64_t dK = sdesc_sw128(sStage + (s & 1) * C::STAGE, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
                     mma_ss(tmem + cS, dQ + off, dK + off, id_s, kk > 0 ? 1u : 0u);
                 }
+                issued = true;
+            };
+            auto mma_dp = [&](int s) {
+                const uint64_t dV = sdesc_sw128(sStage + (s & 1) * C::STAGE + C::TILE, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
                     mma_ss(tmem + cP, dG + off, dV + off, id_s, kk > 0 ? 1u : 0u);
                 }
-                issued = true;
+            };
+            if (ok && (ok = wait_stage(0))) {
+                mma_s(0);
+                mma_dp(0);
                 mma_commit(smem_addr(&s_full));
+            }
+            // Per step: S(s+1) as soon as the softmax warps have read S(s) (it
+            // overlaps their dS(s)); dQ(s) once dS(s) is written over dP(s);
+            // then dP(s+1) into the columns dQ(s) has just read.
+            for (int s = 0; ok && s < n_steps; ++s) {
+                const int st = s & 1;
+                const bool more = s + 1 < n_steps;
+                if (more) {
+                    if (!wait_or_abort(smem_addr(&s_read), (uint32_t)(s & 1), limit, &abort_flag) || !wait_stage(s + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mma_s(s + 1);
+                }
                 if (!wait_or_abort(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint64_t dKmn = sdesc_sw128(base, BOX, 1024);
+                const uint64_t dKmn = sdesc_sw128(sStage + st * C::STAGE, BOX, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts(tmem + cQ, tmem + cS + kk * 8, dKmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                    mma_ts(tmem + cQ, tmem + cP + kk * 8, dKmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(smem_addr(&empty_b[st]));
+                if (more) {
+                    mma_dp(s + 1);
+                    mma_commit(smem_addr(&s_full));
+                }
             }
             if (ok) {
                 mma_commit(smem_addr(&o_full));
@@ -456,6 +509,8 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     p[c] = keep ? ex2(fmaf(__uint_as_float(raw[c]), sl, -l2)) : 0.f;
                 }
             }
+            tc_fence_before();
+            mbar_arrive(smem_addr(&s_read));  // S(s) is in registers: the MMA may overwrite it
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t raw[64];
@@ -468,7 +523,7 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     const float d1 = p[c + 1] * (__uint_as_float(raw[2 * x + 1]) - de);
                     pk[x] = pack_bf16x2(p[c] != 0.f ? d0 : 0.f, p[c + 1] != 0.f ? d1 : 0.f);
                 }
-                tmem_st32(lb + cS + h * 32, pk);  // dS over S
+                tmem_st32(lb + cP + h * 32, pk);  // dS over the dP columns already read
             }
             tmem_wait_st();
             tc_fence_before();
