@@ -14,7 +14,7 @@
 //
 //   warp 8  (TMA)      loads Q0, Q1 once and K_j, V_j into the K and V rings
 //                      (full/empty mbarrier pairs per slot);
-//   warp 9  (MMA)      allocates tensor memory and, from one thread, issues
+//   warp 9  (MMA)      allocates tensor memory and issues (one elected lane)
 //                      S_t = Q_t K_j^T (SS form) and O_t += P_t V_j (A operand
 //                      read from tensor memory), alternating the two tiles so
 //                      the tensor core works on one tile while the other
@@ -282,7 +282,9 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ================================================================ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs this branch converged; elect.sync picks the lane
+        // that issues each MMA and commit.
+        {
             const uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
             const uint32_t idesc_o = idesc_bf16_f32(BM, DV, 0, 1);
             const uint32_t sQ = s_base + C::OFF_Q, sK = s_base + C::OFF_K, sV = s_base + C::OFF_V;
@@ -290,7 +292,8 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             bool issued_any = false;
             auto wait = [&](uint64_t *b, uint32_t parity) -> bool {
                 if (!ok) return false;
-                if (!wait_or_abort(smem_addr(b), parity, limit, &abort_flag)) {
+                const bool done = wait_or_abort(smem_addr(b), parity, limit, &abort_flag);
+                if (!__all_sync(0xffffffffu, done)) {  // reconverges the warp; one verdict for all lanes
                     ok = false;
                     if (!abort_flag) raise_error(ERR_WAIT_MMA, &abort_flag);
                     return false;
@@ -311,7 +314,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4);
-                    mma_ss(d_s, q + off, k + off, idesc_s, kk > 0 ? 1u : 0u);
+                    mma_ss_w(d_s, q + off, k + off, idesc_s, kk > 0 ? 1u : 0u);
                 }
                 issued_any = true;
             };
@@ -321,20 +324,20 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 const uint32_t d_o = tmem + C::COL_O + t * DV, a_p = tmem + t * 128;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(d_o, a_p + kk * 8, v + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
+                    mma_ts_w(d_o, a_p + kk * 8, v + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 issued_any = true;
             };
             if (wait(&bars.q_full[0], 0) && wait(&bars.k_full[0], 0)) {
                 tc_fence_after();
                 mma_s(0, 0);
-                mma_commit(smem_addr(&bars.s_full[0]));
+                mma_commit_w(smem_addr(&bars.s_full[0]));
             }
             if (wait(&bars.q_full[1], 0)) {
                 tc_fence_after();
                 mma_s(1, 0);
-                mma_commit(smem_addr(&bars.s_full[1]));
-                mma_commit(smem_addr(&bars.k_empty[0]));
+                mma_commit_w(smem_addr(&bars.s_full[1]));
+                mma_commit_w(smem_addr(&bars.k_empty[0]));
             }
             for (int j = 1; ok && j < n1; ++j) {
                 if (!wait(&bars.k_full[j % C::KS], (uint32_t)((j / C::KS) & 1))) break;
@@ -346,9 +349,9 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     mma_o(0, j - 1);
                     if (j < n0) {
                         mma_s(0, j);
-                        mma_commit(smem_addr(&bars.s_full[0]));
+                        mma_commit_w(smem_addr(&bars.s_full[0]));
                     } else {
-                        mma_commit(smem_addr(&bars.o_full[0]));
+                        mma_commit_w(smem_addr(&bars.o_full[0]));
                     }
                 }
                 // tile 1
@@ -356,9 +359,9 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 tc_fence_after();
                 mma_o(1, j - 1);
                 mma_s(1, j);
-                mma_commit(smem_addr(&bars.s_full[1]));
-                mma_commit(smem_addr(&bars.k_empty[j % C::KS]));
-                mma_commit(smem_addr(&bars.v_empty[(j - 1) % C::VS]));
+                mma_commit_w(smem_addr(&bars.s_full[1]));
+                mma_commit_w(smem_addr(&bars.k_empty[j % C::KS]));
+                mma_commit_w(smem_addr(&bars.v_empty[(j - 1) % C::VS]));
             }
             if (ok) {
                 const int last = n1 - 1;
@@ -366,19 +369,20 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     if (n0 == n1 && wait(&bars.p_full[0], (uint32_t)(last & 1))) {
                         tc_fence_after();
                         mma_o(0, last);
-                        mma_commit(smem_addr(&bars.o_full[0]));
+                        mma_commit_w(smem_addr(&bars.o_full[0]));
                     }
                     if (wait(&bars.p_full[1], (uint32_t)(last & 1))) {
                         tc_fence_after();
                         mma_o(1, last);
-                        mma_commit(smem_addr(&bars.o_full[1]));
+                        mma_commit_w(smem_addr(&bars.o_full[1]));
                     }
                 }
             }
             if (!ok && issued_any) {
                 // every MMA issued so far must finish before tensor memory is freed
-                mma_commit(smem_addr(&bars.drain));
-                if (!mbar_wait_bounded(smem_addr(&bars.drain), 0, limit)) atomicOr(&g_tc_error_word, ERR_DRAIN);
+                mma_commit_w(smem_addr(&bars.drain));
+                if (!mbar_wait_bounded(smem_addr(&bars.drain), 0, limit) && lane == 0)
+                    atomicOr(&g_tc_error_word, ERR_DRAIN);
             }
         }
         __syncwarp();
