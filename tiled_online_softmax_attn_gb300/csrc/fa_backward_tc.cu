@@ -182,10 +182,10 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
-        if (lane == 0) {
+        {  // whole warp, converged; elect.sync picks the issuing lane
             const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0), id_o = idesc_bf16_f32(BM, D, 0, 1);
             const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
-            bool ok = wait_or_abort(smem_addr(&res_full), 0, limit, &abort_flag), issued = false;
+            bool ok = wait_or_abort_w(smem_addr(&res_full), 0, limit, &abort_flag), issued = false;
             // S^T(s) = K Q_s^T into cS, dP^T(s) = V dO_s^T into cP
             auto mma_st = [&](int s) {
                 const uint32_t base = sStage + (s & 1) * C::STAGE;
@@ -193,7 +193,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
-                    mma_ss(tmem + cS, dK + off, dQ + off, id_s, kk > 0 ? 1u : 0u);
+                    mma_ss_w(tmem + cS, dK + off, dQ + off, id_s, kk > 0 ? 1u : 0u);
                 }
                 issued = true;
             };
@@ -203,18 +203,18 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
-                    mma_ss(tmem + cP, dV + off, dG + off, id_s, kk > 0 ? 1u : 0u);
+                    mma_ss_w(tmem + cP, dV + off, dG + off, id_s, kk > 0 ? 1u : 0u);
                 }
             };
             auto wait_stage = [&](int s) -> bool {
-                if (!wait_or_abort(smem_addr(&full_b[s & 1]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) return false;
+                if (!wait_or_abort_w(smem_addr(&full_b[s & 1]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) return false;
                 tc_fence_after();
                 return true;
             };
             if (ok && (ok = wait_stage(0))) {
                 mma_st(0);
                 mma_dpt(0);
-                mma_commit(smem_addr(&s_full));
+                mma_commit_w(smem_addr(&s_full));
             }
             // Per step: dV(s) once P^T(s) is written; then S^T(s+1) into the
             // columns dV(s) has just read (same-thread MMAs run in order), so
@@ -222,36 +222,36 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int s = 0; ok && s < n_steps; ++s) {
                 const int st = s & 1;
                 const uint32_t base = sStage + st * C::STAGE;
-                if (!wait_or_abort(smem_addr(&p_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
+                if (!wait_or_abort_w(smem_addr(&p_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t dGmn = sdesc_sw128(base + C::TILE, BOX, 1024), dQmn = sdesc_sw128(base, BOX, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts(tmem + cV, tmem + cS + kk * 8, dGmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                    mma_ts_w(tmem + cV, tmem + cS + kk * 8, dGmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
                 const bool more = s + 1 < n_steps;
                 if (more) {
                     if (!wait_stage(s + 1)) { ok = false; break; }
                     mma_st(s + 1);
                 }
-                if (!wait_or_abort(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
+                if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts(tmem + cK, tmem + cP + kk * 8, dQmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                    mma_ts_w(tmem + cK, tmem + cP + kk * 8, dQmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(smem_addr(&empty_b[st]));
+                mma_commit_w(smem_addr(&empty_b[st]));
                 if (more) {
                     mma_dpt(s + 1);
-                    mma_commit(smem_addr(&s_full));
+                    mma_commit_w(smem_addr(&s_full));
                 }
             }
             if (ok) {
-                mma_commit(smem_addr(&o_full));
+                mma_commit_w(smem_addr(&o_full));
             } else {
                 if (!abort_flag) fail_bwd(&abort_flag);
                 if (issued) {
-                    mma_commit(smem_addr(&drain));
+                    mma_commit_w(smem_addr(&drain));
                     mbar_wait_bounded(smem_addr(&drain), 0, limit);
                 }
             }
@@ -418,12 +418,12 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
-        if (lane == 0) {
+        {  // whole warp, converged; elect.sync picks the issuing lane
             const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0), id_o = idesc_bf16_f32(BM, D, 0, 1);
             const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), dG = sdesc_sw128(sG, 16, 1024);
-            bool ok = wait_or_abort(smem_addr(&res_full), 0, limit, &abort_flag), issued = false;
+            bool ok = wait_or_abort_w(smem_addr(&res_full), 0, limit, &abort_flag), issued = false;
             auto wait_stage = [&](int s) -> bool {
-                if (!wait_or_abort(smem_addr(&full_b[s & 1]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) return false;
+                if (!wait_or_abort_w(smem_addr(&full_b[s & 1]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) return false;
                 tc_fence_after();
                 return true;
             };
@@ -433,7 +433,7 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
-                    mma_ss(tmem + cS, dQ + off, dK + off, id_s, kk > 0 ? 1u : 0u);
+                    mma_ss_w(tmem + cS, dQ + off, dK + off, id_s, kk > 0 ? 1u : 0u);
                 }
                 issued = true;
             };
@@ -442,13 +442,13 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
-                    mma_ss(tmem + cP, dG + off, dV + off, id_s, kk > 0 ? 1u : 0u);
+                    mma_ss_w(tmem + cP, dG + off, dV + off, id_s, kk > 0 ? 1u : 0u);
                 }
             };
             if (ok && (ok = wait_stage(0))) {
                 mma_s(0);
                 mma_dp(0);
-                mma_commit(smem_addr(&s_full));
+                mma_commit_w(smem_addr(&s_full));
             }
             // Per step: S(s+1) as soon as the softmax warps have read S(s) (it
             // overlaps their dS(s)); dQ(s) once dS(s) is written over dP(s);
@@ -457,31 +457,31 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 const int st = s & 1;
                 const bool more = s + 1 < n_steps;
                 if (more) {
-                    if (!wait_or_abort(smem_addr(&s_read), (uint32_t)(s & 1), limit, &abort_flag) || !wait_stage(s + 1)) {
+                    if (!wait_or_abort_w(smem_addr(&s_read), (uint32_t)(s & 1), limit, &abort_flag) || !wait_stage(s + 1)) {
                         ok = false;
                         break;
                     }
                     mma_s(s + 1);
                 }
-                if (!wait_or_abort(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
+                if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t dKmn = sdesc_sw128(sStage + st * C::STAGE, BOX, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts(tmem + cQ, tmem + cP + kk * 8, dKmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                    mma_ts_w(tmem + cQ, tmem + cP + kk * 8, dKmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(smem_addr(&empty_b[st]));
+                mma_commit_w(smem_addr(&empty_b[st]));
                 if (more) {
                     mma_dp(s + 1);
-                    mma_commit(smem_addr(&s_full));
+                    mma_commit_w(smem_addr(&s_full));
                 }
             }
             if (ok) {
-                mma_commit(smem_addr(&o_full));
+                mma_commit_w(smem_addr(&o_full));
             } else {
                 if (!abort_flag) fail_bwd(&abort_flag);
                 if (issued) {
-                    mma_commit(smem_addr(&drain));
+                    mma_commit_w(smem_addr(&drain));
                     mbar_wait_bounded(smem_addr(&drain), 0, limit);
                 }
             }

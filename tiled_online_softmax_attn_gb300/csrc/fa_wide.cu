@@ -200,7 +200,7 @@ fa_wide_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_constant_
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ================================================================ MMA issuer
-        if (lane == 0) {
+        {  // whole warp, converged; elect.sync picks the issuing lane
             const uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
             const uint32_t idesc_o = idesc_bf16_f32(BM, DV, 0, 1);
             const uint32_t tS = tmem, tO = tmem + COL_O;
@@ -208,7 +208,7 @@ fa_wide_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_constant_
             bool ok = true, issued = false;
             auto wait_full = [&]() -> int {
                 const int st = it % STAGES;
-                if (!wait_or_abort(smem_addr(&full_b[st]), (uint32_t)((it / STAGES) & 1), limit, &abort_flag))
+                if (!wait_or_abort_w(smem_addr(&full_b[st]), (uint32_t)((it / STAGES) & 1), limit, &abort_flag))
                     return -1;
                 tc_fence_after();
                 return st;
@@ -224,19 +224,19 @@ fa_wide_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_constant_
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t off = (uint64_t)(kk * 2);  // 32 bytes along K
-                        mma_ss(tS, dqh + off, dkh + off, idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
+                        mma_ss_w(tS, dqh + off, dkh + off, idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
                         if (NPROD == 3) {
-                            mma_ss(tS, dqh + off, dkl + off, idesc_s, 1u);
-                            mma_ss(tS, dql + off, dkh + off, idesc_s, 1u);
+                            mma_ss_w(tS, dqh + off, dkl + off, idesc_s, 1u);
+                            mma_ss_w(tS, dql + off, dkh + off, idesc_s, 1u);
                         }
                     }
                     issued = true;
-                    mma_commit(smem_addr(&empty_b[st]));
+                    mma_commit_w(smem_addr(&empty_b[st]));
                     ++it;
                 }
                 if (!ok) break;
-                mma_commit(smem_addr(&s_full));
-                if (!wait_or_abort(smem_addr(&p_full), (uint32_t)(jj & 1), limit, &abort_flag)) { ok = false; break; }
+                mma_commit_w(smem_addr(&s_full));
+                if (!wait_or_abort_w(smem_addr(&p_full), (uint32_t)(jj & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 for (int part = 0; part < (NPROD == 3 ? 2 : 1); ++part) {
                     const int st = wait_full();
@@ -246,22 +246,22 @@ fa_wide_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_constant_
                     for (int kk = 0; kk < BN / 16; ++kk) {
                         const uint64_t voff = (uint64_t)((kk * 16 * 128) >> 4);
                         if (part == 0) {
-                            mma_ts(tO, tS + kk * 8, dv + voff, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
-                            if (NPROD == 3) mma_ts(tO, tS + 64 + kk * 8, dv + voff, idesc_o, 1u);
+                            mma_ts_w(tO, tS + kk * 8, dv + voff, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                            if (NPROD == 3) mma_ts_w(tO, tS + 64 + kk * 8, dv + voff, idesc_o, 1u);
                         } else {
-                            mma_ts(tO, tS + kk * 8, dv + voff, idesc_o, 1u);
+                            mma_ts_w(tO, tS + kk * 8, dv + voff, idesc_o, 1u);
                         }
                     }
-                    mma_commit(smem_addr(&empty_b[st]));
+                    mma_commit_w(smem_addr(&empty_b[st]));
                     ++it;
                 }
             }
             if (ok) {
-                mma_commit(smem_addr(&o_full));
+                mma_commit_w(smem_addr(&o_full));
             } else {
                 if (!abort_flag) raise_wide(ERR_WAIT, &abort_flag);
                 if (issued) {
-                    mma_commit(smem_addr(&drain));
+                    mma_commit_w(smem_addr(&drain));
                     if (!mbar_wait_bounded(smem_addr(&drain), 0, limit)) atomicOr(&g_wide_error_word, ERR_DRAIN);
                 }
             }

@@ -25,6 +25,15 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
     }
 }
 
+// The same wait made by a whole warp: every lane waits, and the warp leaves
+// converged with one verdict (true only if every lane saw the phase).
+__device__ __forceinline__ bool wait_or_abort_w(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                volatile int *abort_flag)
+{
+    const bool done = wait_or_abort(bar, parity, limit_ns, abort_flag);
+    return __all_sync(0xffffffffu, done);
+}
+
 // Maximum of 128 scores: eight independent chains of three-input maxima,
 // then a short combine (depth 11 instead of a 127-long dependency chain).
 __device__ __forceinline__ float row_max_128(const float (&s)[128])
