@@ -78,13 +78,14 @@ struct Cfg {
     static constexpr uint32_t Q_BYTES = BM * DK * 2;       // one 128 x DK bf16 tile
     static constexpr uint32_t K_BYTES = BN * DK * 2;
     static constexpr uint32_t V_BYTES = BN * DV * 2;
-    // three K and V ring slots when they fit in shared memory, else two
-    static constexpr int KS = (2 * Q_BYTES + 3 * (K_BYTES + V_BYTES) + 1024 <= 227u * 1024u) ? 3 : 2;
-    static constexpr int VS = KS;
+    // Ring of key/value stages: stage j holds K_j and V_(j-1), the two tiles
+    // that iteration j of the MMA loop reads.  Three stages when they fit in
+    // shared memory, else two.
+    static constexpr int KVS = (2 * Q_BYTES + 3 * (K_BYTES + V_BYTES) + 1024 <= 227u * 1024u) ? 3 : 2;
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = 2 * Q_BYTES;
-    static constexpr uint32_t OFF_V = OFF_K + KS * K_BYTES;
-    static constexpr uint32_t SMEM_TILES = OFF_V + VS * V_BYTES;
+    static constexpr uint32_t OFF_V = OFF_K + KVS * K_BYTES;
+    static constexpr uint32_t SMEM_TILES = OFF_V + KVS * V_BYTES;
     static constexpr uint32_t SMEM_BYTES = SMEM_TILES + 1024;  // + alignment slack
     static constexpr uint32_t COL_O = 256;                 // O0 at 256, O1 at 256 + DV
 };
@@ -109,8 +110,7 @@ struct Params {
 
 struct __align__(8) Barriers {
     uint64_t q_full[2];
-    uint64_t k_full[3], k_empty[3];
-    uint64_t v_full[3], v_empty[3];
+    uint64_t kv_full[3], kv_empty[3];
     uint64_t s_full[2];
     uint64_t p_full[2];
     uint64_t o_full[2];
@@ -195,10 +195,8 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         mbar_init(smem_addr(&bars.q_full[0]), 1);
         mbar_init(smem_addr(&bars.q_full[1]), 1);
         for (int s = 0; s < 3; ++s) {
-            mbar_init(smem_addr(&bars.k_full[s]), 1);
-            mbar_init(smem_addr(&bars.k_empty[s]), 1);
-            mbar_init(smem_addr(&bars.v_full[s]), 1);
-            mbar_init(smem_addr(&bars.v_empty[s]), 1);
+            mbar_init(smem_addr(&bars.kv_full[s]), 1);
+            mbar_init(smem_addr(&bars.kv_empty[s]), 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_addr(&bars.s_full[t]), 1);
@@ -226,7 +224,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             tma_prefetch_desc(&tm_v);
             const uint64_t pol_q = policy_evict_first();
             const uint64_t pol_kv = policy_evict_last();
-            int k_issued = 0, v_issued = 0, q_issued = 0;  // tiles whose loads were issued
+            int issued = 0, q_issued = 0;  // stages and Q tiles whose loads were issued
             bool ok = true;
             auto load_q = [&](int t) {
                 q_issued = t + 1;
@@ -236,45 +234,42 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     tma_load_rows(s_base + C::OFF_Q + t * C::Q_BYTES + c * (BM * 128), &tm_q, bar, c * 64,
                                   prm.qperm, qrow0 + t * BM, h, b, pol_q);
             };
-            auto load_kv = [&](bool is_k, int j) -> bool {
-                const int S = is_k ? C::KS : C::VS;
-                const int slot = j % S;
-                const uint32_t n_use = (uint32_t)(j / S);
-                const uint32_t empty = smem_addr(is_k ? &bars.k_empty[slot] : &bars.v_empty[slot]);
-                const uint32_t full = smem_addr(is_k ? &bars.k_full[slot] : &bars.v_full[slot]);
-                if (!wait_or_abort(empty, (n_use & 1u) ^ 1u, limit, &abort_flag)) return false;
-                if (is_k && j == prm.skip_load) return true;  // fault injection: never arrives
-                mbar_arrive_expect_tx(full, is_k ? C::K_BYTES : C::V_BYTES);
-                const uint32_t dst = s_base + (is_k ? C::OFF_K + slot * C::K_BYTES : C::OFF_V + slot * C::V_BYTES);
-                for (int c = 0; c < (is_k ? C::QCH : C::VCH); ++c)
-                    tma_load_rows(dst + c * (BN * 128), is_k ? &tm_k : &tm_v, full, c * 64, is_k ? prm.kperm : prm.vperm,
-                                  j * BN, h, b, pol_kv);
+            // stage s = K_s (s < n1) and V_(s-1) (s >= 1), s = 0 .. n1
+            auto load_stage = [&](int s) -> bool {
+                const int slot = s % C::KVS;
+                const uint32_t n_use = (uint32_t)(s / C::KVS);
+                const uint32_t full = smem_addr(&bars.kv_full[slot]);
+                if (!wait_or_abort(smem_addr(&bars.kv_empty[slot]), (n_use & 1u) ^ 1u, limit, &abort_flag)) return false;
+                if (s == prm.skip_load && s < n1) return true;  // fault injection: this stage never fills
+                const bool has_k = s < n1, has_v = s >= 1;
+                mbar_arrive_expect_tx(full, (has_k ? C::K_BYTES : 0u) + (has_v ? C::V_BYTES : 0u));
+                if (has_k)
+                    for (int c = 0; c < C::QCH; ++c)
+                        tma_load_rows(s_base + C::OFF_K + slot * C::K_BYTES + c * (BN * 128), &tm_k, full, c * 64,
+                                      prm.kperm, s * BN, h, b, pol_kv);
+                if (has_v)
+                    for (int c = 0; c < C::VCH; ++c)
+                        tma_load_rows(s_base + C::OFF_V + slot * C::V_BYTES + c * (BN * 128), &tm_v, full, c * 64,
+                                      prm.vperm, (s - 1) * BN, h, b, pol_kv);
                 return true;
             };
             load_q(0);
-            ok = load_kv(true, 0);
-            if (ok) { k_issued = 1; load_q(1); }
-            if (ok) { ok = load_kv(false, 0); if (ok) v_issued = 1; }
-            for (int j = 1; ok && j < n1; ++j) {
-                ok = load_kv(true, j);
-                if (ok) { k_issued = j + 1; ok = load_kv(false, j); }
-                if (ok) v_issued = j + 1;
+            ok = load_stage(0);
+            if (ok) { issued = 1; load_q(1); }
+            for (int s = 1; ok && s <= n1; ++s) {
+                ok = load_stage(s);
+                if (ok) issued = s + 1;
             }
             if (!ok) {
                 if (!abort_flag) raise_error(ERR_WAIT_TMA, &abort_flag);
             }
             // Before the CTA exits, every load issued must have landed.
-            auto drain = [&](bool is_k, int issued) {
-                const int S = is_k ? C::KS : C::VS;
-                for (int j = max(0, issued - S); j < issued; ++j) {
-                    if (is_k && j == prm.skip_load) continue;
-                    const uint32_t full = smem_addr(is_k ? &bars.k_full[j % S] : &bars.v_full[j % S]);
-                    if (!mbar_wait_bounded(full, (uint32_t)((j / S) & 1), limit)) atomicOr(&g_tc_error_word, ERR_DRAIN);
-                }
-            };
             if (abort_flag) {
-                drain(true, k_issued);
-                drain(false, v_issued);
+                for (int s = max(0, issued - C::KVS); s < issued; ++s) {
+                    if (s == prm.skip_load && s < n1) continue;
+                    const uint32_t full = smem_addr(&bars.kv_full[s % C::KVS]);
+                    if (!mbar_wait_bounded(full, (uint32_t)((s / C::KVS) & 1), limit)) atomicOr(&g_tc_error_word, ERR_DRAIN);
+                }
                 for (int t = 0; t < q_issued; ++t)
                     if (!mbar_wait_bounded(smem_addr(&bars.q_full[t]), 0, limit)) atomicOr(&g_tc_error_word, ERR_DRAIN);
             }
@@ -307,9 +302,9 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024), dq1 = sdesc_sw128(sQ + C::Q_BYTES, 16, 1024);
             const uint64_t dk0 = sdesc_sw128(sK, 16, 1024), dv0 = sdesc_sw128(sV, BN * 128, 1024);
             constexpr uint64_t K_STEP = C::K_BYTES >> 4, V_STEP = C::V_BYTES >> 4;  // one ring slot, descriptor units
-            // S_t = Q_t K_j^T   (M = 128 rows, N = 128 keys, K = D in steps of 16)
-            auto mma_s = [&](int t, int j) {
-                const uint64_t q = t ? dq1 : dq0, k = dk0 + (uint64_t)(j % C::KS) * K_STEP;
+            // S_t = Q_t K^T from ring slot `slot` (M = 128 rows, N = 128 keys, K = D in steps of 16)
+            auto mma_s = [&](int t, int slot) {
+                const uint64_t q = t ? dq1 : dq0, k = dk0 + (uint64_t)slot * K_STEP;
                 const uint32_t d_s = tmem + t * 128;
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
@@ -318,17 +313,19 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 }
                 issued_any = true;
             };
-            // O_t += P_t V_j   (M = 128 rows, N = D, K = 128 keys in steps of 16)
-            auto mma_o = [&](int t, int j) {
-                const uint64_t v = dv0 + (uint64_t)(j % C::VS) * V_STEP;
+            // O_t += P_t V from ring slot `slot` (M = 128 rows, N = D, K = 128 keys in steps of 16);
+            // `first` starts the accumulator (key tile 0)
+            auto mma_o = [&](int t, int slot, bool first) {
+                const uint64_t v = dv0 + (uint64_t)slot * V_STEP;
                 const uint32_t d_o = tmem + C::COL_O + t * DV, a_p = tmem + t * 128;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                     mma_ts_w(d_o, a_p + kk * 8, v + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+                             (!first || kk > 0) ? 1u : 0u);
                 issued_any = true;
             };
-            if (wait(&bars.q_full[0], 0) && wait(&bars.k_full[0], 0)) {
+            // stage 0: K_0
+            if (wait(&bars.q_full[0], 0) && wait(&bars.kv_full[0], 0)) {
                 tc_fence_after();
                 mma_s(0, 0);
                 mma_commit_w(smem_addr(&bars.s_full[0]));
@@ -337,43 +334,47 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 tc_fence_after();
                 mma_s(1, 0);
                 mma_commit_w(smem_addr(&bars.s_full[1]));
-                mma_commit_w(smem_addr(&bars.k_empty[0]));
+                mma_commit_w(smem_addr(&bars.kv_empty[0]));
             }
+            // iteration j reads stage j (K_j, V_(j-1)): P_t V_(j-1), then S_t = Q_t K_j^T
+            int slot = 0;
+            uint32_t phase = 0;
             for (int j = 1; ok && j < n1; ++j) {
-                if (!wait(&bars.k_full[j % C::KS], (uint32_t)((j / C::KS) & 1))) break;
-                if (!wait(&bars.v_full[(j - 1) % C::VS], (uint32_t)(((j - 1) / C::VS) & 1))) break;
+                if (++slot == C::KVS) { slot = 0; phase ^= 1u; }
+                if (!wait(&bars.kv_full[slot], phase)) break;
+                const uint32_t pp = (uint32_t)((j - 1) & 1);
                 // tile 0
                 if (j <= n0) {
-                    if (!wait(&bars.p_full[0], (uint32_t)((j - 1) & 1))) break;
+                    if (!wait(&bars.p_full[0], pp)) break;
                     tc_fence_after();
-                    mma_o(0, j - 1);
+                    mma_o(0, slot, j == 1);
                     if (j < n0) {
-                        mma_s(0, j);
+                        mma_s(0, slot);
                         mma_commit_w(smem_addr(&bars.s_full[0]));
                     } else {
                         mma_commit_w(smem_addr(&bars.o_full[0]));
                     }
                 }
                 // tile 1
-                if (!wait(&bars.p_full[1], (uint32_t)((j - 1) & 1))) break;
+                if (!wait(&bars.p_full[1], pp)) break;
                 tc_fence_after();
-                mma_o(1, j - 1);
-                mma_s(1, j);
+                mma_o(1, slot, j == 1);
+                mma_s(1, slot);
                 mma_commit_w(smem_addr(&bars.s_full[1]));
-                mma_commit_w(smem_addr(&bars.k_empty[j % C::KS]));
-                mma_commit_w(smem_addr(&bars.v_empty[(j - 1) % C::VS]));
+                mma_commit_w(smem_addr(&bars.kv_empty[slot]));
             }
-            if (ok) {
+            if (ok) {  // stage n1: V of the last key tile
                 const int last = n1 - 1;
-                if (wait(&bars.v_full[last % C::VS], (uint32_t)((last / C::VS) & 1))) {
+                const int ls = n1 % C::KVS;
+                if (wait(&bars.kv_full[ls], (uint32_t)((n1 / C::KVS) & 1))) {
                     if (n0 == n1 && wait(&bars.p_full[0], (uint32_t)(last & 1))) {
                         tc_fence_after();
-                        mma_o(0, last);
+                        mma_o(0, ls, last == 0);
                         mma_commit_w(smem_addr(&bars.o_full[0]));
                     }
                     if (wait(&bars.p_full[1], (uint32_t)(last & 1))) {
                         tc_fence_after();
-                        mma_o(1, last);
+                        mma_o(1, ls, last == 0);
                         mma_commit_w(smem_addr(&bars.o_full[1]));
                     }
                 }
