@@ -59,9 +59,12 @@ using namespace tc;
 
 constexpr int BM = 128;           // query rows per tile (tensor-memory lanes)
 constexpr int BN = 128;           // keys per tile
-constexpr int NUM_THREADS = 320;  // 10 warps
-constexpr int TMA_WARP = 8;
-constexpr int MMA_WARP = 9;
+constexpr int RH = 1;             // softmax threads per query row
+constexpr int HC = BN / RH;       // key columns of a tile per softmax thread
+constexpr int SOFTMAX_WARPS = 8 * RH;
+constexpr int TMA_WARP = SOFTMAX_WARPS;
+constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
+constexpr int NUM_THREADS = 32 * (SOFTMAX_WARPS + 2);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;  // lazy-rescale threshold, log2 units
 
@@ -115,6 +118,7 @@ struct __align__(8) Barriers {
     uint64_t p_full[2];
     uint64_t o_full[2];
     uint64_t drain;
+    uint64_t pair[8];  // the RH softmax threads of a row exchange partial results (per tile and lane quarter)
 };
 
 // Map coordinate for dimension slot s of a tensor map whose outer dimensions
@@ -127,6 +131,10 @@ __device__ __forceinline__ void tma_load_rows(uint32_t dst, const void *tmap, ui
     tma_load_4d(dst, tmap, bar, col, pick(perm & 3, row, h, b), pick((perm >> 2) & 3, row, h, b),
                 pick((perm >> 4) & 3, row, h, b), pol);
 }
+
+// One row slice of tensor memory (32 lanes x 64 or 128 columns), loaded and waited for.
+__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t (&r)[64]) { tmem_ld64(taddr, r); }
+__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t (&r)[128]) { tmem_ld128(taddr, r); }
 
 __device__ __forceinline__ void raise_error(uint32_t bit, volatile int *abort_flag)
 {
@@ -166,6 +174,8 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     extern __shared__ uint8_t smem_raw[];
     __shared__ Barriers bars;
     __shared__ uint32_t tmem_base_s;
+    __shared__ float xch_max[2][2][RH][BM];  // [iteration parity][tile][row thread][row]: partial row maxima
+    __shared__ float2 xch_l[2][RH][BM];      // [tile][row thread][row]: partial (l, dq) for the epilogue
     __shared__ volatile int abort_flag;
 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -200,10 +210,11 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_addr(&bars.s_full[t]), 1);
-            mbar_init(smem_addr(&bars.p_full[t]), 128);
+            mbar_init(smem_addr(&bars.p_full[t]), 128 * RH);
             mbar_init(smem_addr(&bars.o_full[t]), 1);
         }
         mbar_init(smem_addr(&bars.drain), 1);
+        for (int i = 0; i < 8; ++i) mbar_init(smem_addr(&bars.pair[i]), 32 * RH);
         fence_mbar_init();
     }
     if (warp == MMA_WARP) {
@@ -389,46 +400,74 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         __syncwarp();
     } else {
         // ================================================================ softmax + epilogue
-        const int t = warp >> 2;          // query tile 0 or 1
-        const int quarter = warp & 3;     // tensor-memory lanes 32*quarter ...
+        // RH threads per query row: warps w, w + 8, ... read the same
+        // tensor-memory lanes (lane quarter w % 4) and take consecutive
+        // HC-column slices of the row's keys.  They agree on the row maximum
+        // through shared memory and a per-pair mbarrier; l and dq stay partial
+        // until the epilogue.
+        const int rh = warp >> 3;               // which slice of the row
+        const int t = (warp >> 2) & 1;          // query tile 0 or 1
+        const int quarter = warp & 3;           // tensor-memory lanes 32*quarter ...
         const int r = quarter * 32 + lane;
-        const int grow = qrow0 + t * BM + r;  // global query row of this thread
+        const int grow = qrow0 + t * BM + r;    // global query row of this thread
         const int n_t = t == 0 ? n0 : n1;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t tS = lane_base + t * 128;
-        const uint32_t tO = lane_base + C::COL_O + t * DV;
+        const uint32_t tS = lane_base + t * 128 + rh * HC;        // this slice of S_t (fp32)
+        const uint32_t tP = lane_base + t * 128 + rh * (HC / 2);  // its weights, bf16 pairs
+        constexpr int OC = DV / RH;                               // output columns per thread
+        const uint32_t tO = lane_base + C::COL_O + t * DV + rh * OC;
+        const uint32_t pair_bar = smem_addr(&bars.pair[t * 4 + quarter]);
         const float sl = prm.scale_log2;
         float m = -INFINITY;  // running maximum, log2 units
-        float l = 0.f;        // running denominator (exact weights): LSE
+        float l = 0.f;        // running denominator of this slice (exact weights): LSE
         float dq = 0.f;       // bf16 rounding of each tile's largest weight: O / (l + dq)
         bool ok = true;
+        auto fail = [&]() {
+            ok = false;
+            if (!abort_flag) raise_error(ERR_WAIT_SOFTMAX, &abort_flag);
+            else atomicOr(&g_tc_error_word, ERR_WAIT_SOFTMAX);
+        };
         for (int j = 0; j < n_t; ++j) {
             if (!wait_or_abort(smem_addr(&bars.s_full[t]), (uint32_t)(j & 1), limit, &abort_flag)) {
-                ok = false;
+                fail();
                 break;
             }
             tc_fence_after();
-            float s[BN];
+            float s[HC];
             {
-                uint32_t raw[BN];
-                tmem_ld128(tS, raw);
+                uint32_t raw[HC];
+                tmem_ld_row(tS, raw);
 #pragma unroll
-                for (int x = 0; x < BN; ++x) s[x] = __uint_as_float(raw[x]);
+                for (int x = 0; x < HC; ++x) s[x] = __uint_as_float(raw[x]);
             }
-            const int kv0 = j * BN;
+            const int kv0 = j * BN + rh * HC;
             int lim = Nk - kv0;                         // keys >= Nk are padding
             if (CAUSAL) lim = min(lim, grow - kv0 + 1);  // keys after this query
-            if (lim < BN) {
+            if (lim < HC) {
 #pragma unroll
-                for (int c = 0; c < BN; ++c)
+                for (int c = 0; c < HC; ++c)
                     if (c >= lim) s[c] = -INFINITY;
             }
-            const float mx = row_max_128(s);
+            const float mh = row_max<HC>(s);
+            float mx = mh, mo = -INFINITY;
+            if constexpr (RH > 1) {
+                xch_max[j & 1][t][rh][r] = mh;
+                mbar_arrive(pair_bar);
+                if (!wait_or_abort(pair_bar, (uint32_t)(j & 1), limit, &abort_flag)) {
+                    fail();
+                    break;
+                }
+#pragma unroll
+                for (int o = 0; o < RH; ++o)
+                    if (o != rh) mo = fmaxf(mo, xch_max[j & 1][t][o][r]);
+                mx = fmaxf(mh, mo);
+            }
             const float m_tile = mx * sl;
             // Lazy rescaling: the reference maximum m moves only when the tile's
             // maximum exceeds it by more than RESCALE_LOG2 (weights then stay
             // below 2^RESCALE_LOG2).  Softmax is invariant to the shift, so O / l
-            // and m + log2 l are unchanged; alpha is 1 on most tiles.
+            // and m + log2 l are unchanged; alpha is 1 on most tiles.  Every
+            // thread of the row sees the same mx, so all take the same steps.
             float alpha = 1.f;
             if (m_tile > m + RESCALE_LOG2) {
                 alpha = ex2(m - m_tile);  // 0 on the first tile (m = -inf)
@@ -438,7 +477,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const uint64_t sl2 = f2_pack(sl, sl), nb2 = f2_pack(-base, -base);
             uint64_t rs2[2] = {0ull, 0ull};
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < HC / 32; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
@@ -448,7 +487,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     pk[x] = pack_bf16x2(p0, p1);
                     rs2[x & 1] = f2_add(rs2[x & 1], f2_pack(p0, p1));
                 }
-                tmem_st16(tS + c * 16, pk);
+                tmem_st16(tP + c * 16, pk);
             }
             float r0, r1;
             f2_unpack(f2_add(rs2[0], rs2[1]), r0, r1);
@@ -457,15 +496,20 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             // tile dominates a peaked row, so the normaliser of O gets that
             // weight's rounding error added: O's numerator and denominator then
             // agree on the terms that matter (the same FFMA and ex2 as above,
-            // so p_top is bit-identical to that element's weight).
-            const float p_top = ex2(fmaf(mx, sl, -base));
-            dq = dq * alpha + (__uint_as_float(pack_bf16x2(p_top, 0.f) << 16) - p_top);
+            // so p_top is bit-identical to that element's weight).  The slice
+            // holding the row maximum adds it (the lowest such slice on a tie).
+            float corr = 0.f;
+            if (mh == mx && (rh == 0 || mo != mx)) {
+                const float p_top = ex2(fmaf(mx, sl, -base));
+                corr = __uint_as_float(pack_bf16x2(p_top, 0.f) << 16) - p_top;
+            }
+            dq = dq * alpha + corr;
             // O_t already holds every earlier P V product: the commit that
             // signalled this S tile covers all MMAs issued before it.
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-                for (int c = 0; c < DV / 32; ++c) {
+                for (int c = 0; c < OC / 32; ++c) {
                     uint32_t raw[32];
                     tmem_ld32(tO + c * 32, raw);
 #pragma unroll
@@ -485,22 +529,39 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         // ---- epilogue: O / l, LSE
         if (ok && wait_or_abort(smem_addr(&bars.o_full[t]), 0, limit, &abort_flag)) {
             tc_fence_after();
-            const float inv_l = 1.f / (l + dq);
-            const size_t row_elem = (size_t)(b * prm.os_b + h * prm.os_h + (int64_t)grow * prm.os_n);
+            float lt = l, dqt = dq;
+            if constexpr (RH > 1) {
+                xch_l[t][rh][r] = make_float2(l, dq);
+                mbar_arrive(pair_bar);
+                if (!wait_or_abort(pair_bar, (uint32_t)(n_t & 1), limit, &abort_flag)) {
+                    fail();
+                } else {
 #pragma unroll
-            for (int c = 0; c < DV / 32; ++c) {
-                uint32_t raw[32];
-                tmem_ld32(tO + c * 32, raw);
-                float vals[32];
-#pragma unroll
-                for (int x = 0; x < 32; ++x) vals[x] = __uint_as_float(raw[x]) * inv_l;
-                if (grow < N) store_o_row(prm.o, prm.o_fp32, row_elem, vals, c * 32, 32);
+                    for (int o = 0; o < RH; ++o)
+                        if (o != rh) {
+                            const float2 x = xch_l[t][o][r];
+                            lt += x.x;
+                            dqt += x.y;
+                        }
+                }
             }
-            if (prm.lse && grow < N) prm.lse[(size_t)bh * N + grow] = (m + log2f(l)) * 0.69314718055994530942f;
-        } else if (!abort_flag) {
-            raise_error(ERR_WAIT_SOFTMAX, &abort_flag);
-        } else {
-            atomicOr(&g_tc_error_word, ERR_WAIT_SOFTMAX);
+            if (ok) {
+                const float inv_l = 1.f / (lt + dqt);
+                const size_t row_elem = (size_t)(b * prm.os_b + h * prm.os_h + (int64_t)grow * prm.os_n);
+#pragma unroll
+                for (int c = 0; c < OC / 32; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(tO + c * 32, raw);
+                    float vals[32];
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) vals[x] = __uint_as_float(raw[x]) * inv_l;
+                    if (grow < N) store_o_row(prm.o, prm.o_fp32, row_elem, vals, rh * OC + c * 32, 32);
+                }
+                if (rh == 0 && prm.lse && grow < N)
+                    prm.lse[(size_t)bh * N + grow] = (m + log2f(lt)) * 0.69314718055994530942f;
+            }
+        } else if (ok) {
+            fail();
         }
     }
 

@@ -34,21 +34,29 @@ __device__ __forceinline__ bool wait_or_abort_w(uint32_t bar, uint32_t parity, u
     return __all_sync(0xffffffffu, done);
 }
 
-// Maximum of 128 scores: eight independent chains of three-input maxima,
-// then a short combine (depth 11 instead of a 127-long dependency chain).
-__device__ __forceinline__ float row_max_128(const float (&s)[128])
+// Maximum of NV scores (NV a multiple of 8): eight independent chains of
+// three-input maxima, then a short combine (depth about NV / 16 + 3 instead
+// of an NV-long dependency chain).
+template <int NV>
+__device__ __forceinline__ float row_max(const float (&s)[NV])
 {
+    static_assert(NV % 8 == 0 && NV >= 16, "row_max: NV must be a multiple of 8, at least 16");
+    constexpr int C = NV / 8;
     float a[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = max3f(s[16 * i], s[16 * i + 1], s[16 * i + 2]);
+    for (int i = 0; i < 8; ++i) a[i] = s[i * C];
 #pragma unroll
-    for (int k = 3; k < 15; k += 2)
+    for (int k = 1; k + 1 < C; k += 2)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = max3f(a[i], s[16 * i + k], s[16 * i + k + 1]);
+        for (int i = 0; i < 8; ++i) a[i] = max3f(a[i], s[i * C + k], s[i * C + k + 1]);
+    if constexpr (C % 2 == 0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = fmaxf(a[i], s[16 * i + 15]);
+        for (int i = 0; i < 8; ++i) a[i] = fmaxf(a[i], s[i * C + C - 1]);
+    }
     return max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
 }
+
+__device__ __forceinline__ float row_max_128(const float (&s)[128]) { return row_max<128>(s); }
 
 }  // namespace tc
 }  // namespace fa
