@@ -18,9 +18,13 @@
 //     S = Q_i K_j^T, dP = dO_i V_j^T, dS = P (dP - delta), dQ += dS K_j.
 //
 // So S and dP are formed twice (7 products of 128 x 128 x d instead of 5):
-// the price of no atomics and deterministic gradients.  Warps 0-3 handle one
-// tensor-memory lane (row) each thread, warp 4 issues the TMA loads, warp 5
-// the MMAs.  Every wait is bounded as in the forward kernels.
+// the price of no atomics and deterministic gradients.  Warps 0-7 do the
+// elementwise work: warp w reads tensor-memory lanes 32 (w % 4) .. + 31 (one
+// row per thread) and the half w / 4 of the 128 columns, so two warps share
+// each row and each SM sub-partition runs two of them; no reduction crosses
+// columns.  Warp 8 issues the TMA loads, warp 9 the MMAs.  The two score
+// products of a tile signal separate barriers, so the exponentials start as
+// soon as the first is done.  Every wait is bounded as in the forward kernels.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -45,9 +49,12 @@ using namespace ptx;
 using namespace tc;
 
 constexpr int BM = 128;
-constexpr int NUM_THREADS = 192;
-constexpr int TMA_WARP = 4;
-constexpr int MMA_WARP = 5;
+constexpr int EW_WARPS = 8;  // elementwise warps: 4 lane quarters x 2 column halves
+constexpr int EW_THREADS = 32 * EW_WARPS;
+constexpr int NUM_THREADS = EW_THREADS + 64;
+constexpr int TMA_WARP = EW_WARPS;
+constexpr int MMA_WARP = EW_WARPS + 1;
+constexpr int HALF = BM / 2;  // columns per elementwise thread
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t BOX = 128 * 128;  // one 128-row x 64-column bf16 box
 constexpr uint32_t VEC_BYTES = 1024;  // lse2 and delta of 128 rows
@@ -91,6 +98,11 @@ __device__ __forceinline__ void store_row32(void *base, int fp32, size_t elem, c
     }
 }
 
+// Tensor-memory column of K step kk (16 elements) of a 128-wide bf16 A
+// operand whose two 64-element halves were written by the two column-half
+// warps at col0 and col0 + 64 (32 packed columns each).
+__device__ __forceinline__ uint32_t a_col(uint32_t col0, int kk) { return col0 + kk * 8 + (kk >= 4 ? 32 : 0); }
+
 __device__ __forceinline__ void fail_bwd(volatile int *abort_flag)
 {
     atomicOr(&g_bwd_error_word, 64u);
@@ -105,7 +117,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 {
     using C = BCfg<D>;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t res_full, full_b[2], empty_b[2], s_full, p_ready, ds_ready, o_full, drain;
+    __shared__ __align__(8) uint64_t res_full, full_b[2], empty_b[2], st_full, dp_full, p_ready, ds_ready, o_full, drain;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
 
@@ -127,9 +139,10 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             mbar_init(smem_addr(&full_b[s]), 1);
             mbar_init(smem_addr(&empty_b[s]), 1);
         }
-        mbar_init(smem_addr(&s_full), 1);
-        mbar_init(smem_addr(&p_ready), 128);
-        mbar_init(smem_addr(&ds_ready), 128);
+        mbar_init(smem_addr(&st_full), 1);
+        mbar_init(smem_addr(&dp_full), 1);
+        mbar_init(smem_addr(&p_ready), EW_THREADS);
+        mbar_init(smem_addr(&ds_ready), EW_THREADS);
         mbar_init(smem_addr(&o_full), 1);
         mbar_init(smem_addr(&drain), 1);
         fence_mbar_init();
@@ -143,7 +156,8 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
     const uint64_t limit = prm.limit;
-    // tensor memory: S^T/P^T [0,128), dP^T/dS^T [128,256), dV [256,256+D), dK [256+D, 256+2D)
+    // tensor memory: S^T/P^T [0,128), dP^T/dS^T [128,256), dV [256,256+D), dK [256+D, 256+2D);
+    // the column half h of P^T (dS^T) is written over columns [64h, 64h + 32) of S^T (dP^T)
     const uint32_t cS = 0, cP = 128, cV = 256, cK = 256 + D;
 
     if (warp == TMA_WARP) {
@@ -213,12 +227,13 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             };
             if (ok && (ok = wait_stage(0))) {
                 mma_st(0);
+                mma_commit_w(smem_addr(&st_full));
                 mma_dpt(0);
-                mma_commit_w(smem_addr(&s_full));
+                mma_commit_w(smem_addr(&dp_full));
             }
             // Per step: dV(s) once P^T(s) is written; then S^T(s+1) into the
             // columns dV(s) has just read (same-thread MMAs run in order), so
-            // it overlaps the softmax warps' dS^T(s); then dK(s) and dP^T(s+1).
+            // it overlaps the elementwise warps' dS^T(s); then dK(s) and dP^T(s+1).
             for (int s = 0; ok && s < n_steps; ++s) {
                 const int st = s & 1;
                 const uint32_t base = sStage + st * C::STAGE;
@@ -227,23 +242,24 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const uint64_t dGmn = sdesc_sw128(base + C::TILE, BOX, 1024), dQmn = sdesc_sw128(base, BOX, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts_w(tmem + cV, tmem + cS + kk * 8, dGmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                    mma_ts_w(tmem + cV, tmem + a_col(cS, kk), dGmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
                 const bool more = s + 1 < n_steps;
                 if (more) {
                     if (!wait_stage(s + 1)) { ok = false; break; }
                     mma_st(s + 1);
+                    mma_commit_w(smem_addr(&st_full));
                 }
                 if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts_w(tmem + cK, tmem + cP + kk * 8, dQmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                    mma_ts_w(tmem + cK, tmem + a_col(cP, kk), dQmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
                 mma_commit_w(smem_addr(&empty_b[st]));
                 if (more) {
                     mma_dpt(s + 1);
-                    mma_commit_w(smem_addr(&s_full));
+                    mma_commit_w(smem_addr(&dp_full));
                 }
             }
             if (ok) {
@@ -258,56 +274,71 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         __syncwarp();
     } else {
-        // one key per thread: key kj on tensor-memory lane warp*32 + lane
-        const int jr = warp * 32 + lane, kj = k0 + jr;
-        const uint32_t lb = tmem + ((uint32_t)(warp * 32) << 16);
+        // one key per thread (tensor-memory lane), queries [64 hf, 64 hf + 64) of each tile
+        const int quarter = warp & 3, hf = warp >> 2;
+        const int jr = quarter * 32 + lane, kj = k0 + jr;
+        const uint32_t lb = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t cSh = cS + hf * HALF, cPh = cP + hf * HALF;
         const float sl = prm.sl;
         bool ok = true;
         for (int s = 0; s < n_steps; ++s) {
-            const int st = s & 1, q0 = (first + s) * BM;
-            if (!wait_or_abort(smem_addr(&s_full), (uint32_t)(s & 1), limit, &abort_flag) ||
+            const int st = s & 1, q0 = (first + s) * BM + hf * HALF;
+            if (!wait_or_abort(smem_addr(&st_full), (uint32_t)(s & 1), limit, &abort_flag) ||
                 !wait_or_abort(smem_addr(&full_b[st]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const float *vec = reinterpret_cast<const float *>(smem + C::RES + st * C::STAGE + 2 * C::TILE);
-            // P^T row: weights of this key for the 128 queries of the tile
-            float p[BM];
+            const float4 *vec = reinterpret_cast<const float4 *>(smem + C::RES + st * C::STAGE + 2 * C::TILE) + hf * (HALF / 4);
+            // P^T row: weights of this key for this half of the tile's queries
+            float p[HALF];
             {
-                uint32_t raw[BM];
-                tmem_ld128(lb + cS, raw);
+                uint32_t raw[HALF];
+                tmem_ld64(lb + cSh, raw);
 #pragma unroll
-                for (int c = 0; c < BM; ++c) {
-                    const int q = q0 + c;
-                    const bool keep = kj < N && q < N && (!CAUSAL || kj <= q);
-                    p[c] = keep ? ex2(fmaf(__uint_as_float(raw[c]), sl, -vec[c])) : 0.f;
+                for (int c4 = 0; c4 < HALF / 4; ++c4) {
+                    const float4 l4 = vec[c4];  // LSE * log2 e of queries q0 + 4 c4 ...
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = 4 * c4 + e, q = q0 + c;
+                        const bool keep = kj < N && q < N && (!CAUSAL || kj <= q);
+                        p[c] = keep ? ex2(fmaf(__uint_as_float(raw[c]), sl, -lv[e])) : 0.f;
+                    }
                 }
             }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            {
                 uint32_t pk[32];
 #pragma unroll
-                for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(p[h * 64 + 2 * x], p[h * 64 + 2 * x + 1]);
-                tmem_st32(lb + cS + h * 32, pk);
+                for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(p[2 * x], p[2 * x + 1]);
+                tmem_st32(lb + cSh, pk);
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_addr(&p_ready));
             // dS^T row = P^T (dP^T - delta)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t raw[64];
-                tmem_ld64(lb + cP + h * 64, raw);
+            if (!wait_or_abort(smem_addr(&dp_full), (uint32_t)(s & 1), limit, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            {
+                uint32_t raw[HALF];
+                tmem_ld64(lb + cPh, raw);
                 uint32_t pk[32];
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    const int c = h * 64 + 2 * x;
-                    const float d0 = p[c] * (__uint_as_float(raw[2 * x]) - vec[128 + c]);
-                    const float d1 = p[c + 1] * (__uint_as_float(raw[2 * x + 1]) - vec[128 + c + 1]);
-                    pk[x] = pack_bf16x2(p[c] != 0.f ? d0 : 0.f, p[c + 1] != 0.f ? d1 : 0.f);
+                for (int c4 = 0; c4 < HALF / 4; ++c4) {
+                    const float4 d4 = vec[BM / 4 + c4];  // delta of queries q0 + 4 c4 ...
+                    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; e += 2) {
+                        const int c = 4 * c4 + e;
+                        const float d0 = p[c] * (__uint_as_float(raw[c]) - dv[e]);
+                        const float d1 = p[c + 1] * (__uint_as_float(raw[c + 1]) - dv[e + 1]);
+                        pk[c / 2] = pack_bf16x2(p[c] != 0.f ? d0 : 0.f, p[c + 1] != 0.f ? d1 : 0.f);
+                    }
                 }
-                tmem_st32(lb + cP + h * 32, pk);
+                tmem_st32(lb + cPh, pk);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -317,7 +348,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc_fence_after();
             const size_t row = ((size_t)bh * N + kj) * D;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {  // this warp's half of the columns
                 uint32_t raw[32];
                 tmem_ld32(lb + cV + c * 32, raw);
                 if (kj < N) store_row32(prm.dv, prm.g_fp32, row + c * 32, raw, 1.f);
@@ -344,7 +375,7 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 {
     using C = BCfg<D>;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t res_full, full_b[2], empty_b[2], s_full, s_read, ds_ready, o_full, drain;
+    __shared__ __align__(8) uint64_t res_full, full_b[2], empty_b[2], s_full, dp_full, s_read, ds_ready, o_full, drain;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
 
@@ -367,8 +398,9 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             mbar_init(smem_addr(&empty_b[s]), 1);
         }
         mbar_init(smem_addr(&s_full), 1);
-        mbar_init(smem_addr(&s_read), 128);
-        mbar_init(smem_addr(&ds_ready), 128);
+        mbar_init(smem_addr(&dp_full), 1);
+        mbar_init(smem_addr(&s_read), EW_THREADS);
+        mbar_init(smem_addr(&ds_ready), EW_THREADS);
         mbar_init(smem_addr(&o_full), 1);
         mbar_init(smem_addr(&drain), 1);
         fence_mbar_init();
@@ -382,7 +414,8 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
     const uint64_t limit = prm.limit;
-    // tensor memory: S [0,128), dP / dS [128,256), dQ [256, 256+D)
+    // tensor memory: S [0,128), dP / dS [128,256), dQ [256, 256+D); the column half h
+    // of dS is written over columns [64h, 64h + 32) of dP
     const uint32_t cS = 0, cP = 128, cQ = 256;
 
     if (warp == TMA_WARP) {
@@ -447,8 +480,9 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             };
             if (ok && (ok = wait_stage(0))) {
                 mma_s(0);
-                mma_dp(0);
                 mma_commit_w(smem_addr(&s_full));
+                mma_dp(0);
+                mma_commit_w(smem_addr(&dp_full));
             }
             // Per step: S(s+1) as soon as the softmax warps have read S(s) (it
             // overlaps their dS(s)); dQ(s) once dS(s) is written over dP(s);
@@ -462,18 +496,19 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         break;
                     }
                     mma_s(s + 1);
+                    mma_commit_w(smem_addr(&s_full));
                 }
                 if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t dKmn = sdesc_sw128(sStage + st * C::STAGE, BOX, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts_w(tmem + cQ, tmem + cP + kk * 8, dKmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                    mma_ts_w(tmem + cQ, tmem + a_col(cP, kk), dKmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
                 mma_commit_w(smem_addr(&empty_b[st]));
                 if (more) {
                     mma_dp(s + 1);
-                    mma_commit_w(smem_addr(&s_full));
+                    mma_commit_w(smem_addr(&dp_full));
                 }
             }
             if (ok) {
@@ -488,22 +523,25 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         __syncwarp();
     } else {
-        const int r = warp * 32 + lane, qi = q0 + r;
-        const uint32_t lb = tmem + ((uint32_t)(warp * 32) << 16);
+        // one query per thread (tensor-memory lane), keys [64 hf, 64 hf + 64) of each tile
+        const int quarter = warp & 3, hf = warp >> 2;
+        const int r = quarter * 32 + lane, qi = q0 + r;
+        const uint32_t lb = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t cSh = cS + hf * HALF, cPh = cP + hf * HALF;
         const float sl = prm.sl;
         const float l2 = qi < N ? prm.lse2[(size_t)bh * prm.pitch + qi] : 0.f;
         const float de = qi < N ? prm.delta[(size_t)bh * prm.pitch + qi] : 0.f;
         bool ok = true;
         for (int s = 0; s < n_steps; ++s) {
-            const int k0 = s * BM;
+            const int k0 = s * BM + hf * HALF;
             if (!wait_or_abort(smem_addr(&s_full), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
             tc_fence_after();
-            float p[BM];
+            float p[HALF];
             {
-                uint32_t raw[BM];
-                tmem_ld128(lb + cS, raw);
+                uint32_t raw[HALF];
+                tmem_ld64(lb + cSh, raw);
 #pragma unroll
-                for (int c = 0; c < BM; ++c) {
+                for (int c = 0; c < HALF; ++c) {
                     const int kj = k0 + c;
                     const bool keep = qi < N && kj < N && (!CAUSAL || kj <= qi);
                     p[c] = keep ? ex2(fmaf(__uint_as_float(raw[c]), sl, -l2)) : 0.f;
@@ -511,19 +549,20 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
             tc_fence_before();
             mbar_arrive(smem_addr(&s_read));  // S(s) is in registers: the MMA may overwrite it
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t raw[64];
-                tmem_ld64(lb + cP + h * 64, raw);
+            if (!wait_or_abort(smem_addr(&dp_full), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            {
+                uint32_t raw[HALF];
+                tmem_ld64(lb + cPh, raw);
                 uint32_t pk[32];
 #pragma unroll
                 for (int x = 0; x < 32; ++x) {
-                    const int c = h * 64 + 2 * x;
-                    const float d0 = p[c] * (__uint_as_float(raw[2 * x]) - de);
-                    const float d1 = p[c + 1] * (__uint_as_float(raw[2 * x + 1]) - de);
+                    const int c = 2 * x;
+                    const float d0 = p[c] * (__uint_as_float(raw[c]) - de);
+                    const float d1 = p[c + 1] * (__uint_as_float(raw[c + 1]) - de);
                     pk[x] = pack_bf16x2(p[c] != 0.f ? d0 : 0.f, p[c + 1] != 0.f ? d1 : 0.f);
                 }
-                tmem_st32(lb + cP + h * 32, pk);  // dS over the dP columns already read
+                tmem_st32(lb + cPh, pk);  // dS over the dP columns already read
             }
             tmem_wait_st();
             tc_fence_before();
@@ -533,7 +572,7 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             tc_fence_after();
             const size_t row = ((size_t)bh * N + qi) * D;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {  // this warp's half of the columns
                 uint32_t raw[32];
                 tmem_ld32(lb + cQ + c * 32, raw);
                 if (qi < N) store_row32(prm.dq, prm.g_fp32, row + c * 32, raw, prm.scale);
