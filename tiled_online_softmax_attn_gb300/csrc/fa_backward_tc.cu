@@ -33,6 +33,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/fa.h"
 #include "fa_internal.h"
@@ -290,22 +291,32 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             tc_fence_after();
             const float4 *vec = reinterpret_cast<const float4 *>(smem + C::RES + st * C::STAGE + 2 * C::TILE) + hf * (HALF / 4);
+            // Tiles with no padded key or query and wholly below the diagonal
+            // take the unmasked path (no per-element tests or selects).
+            const int qt0 = (first + s) * BM;
+            const bool masked = k0 + BM > N || qt0 + BM > N || (CAUSAL && qt0 < k0 + BM);
             // P^T row: weights of this key for this half of the tile's queries
             float p[HALF];
             {
                 uint32_t raw[HALF];
                 tmem_ld64(lb + cSh, raw);
+                auto weights = [&](auto mask) {
+                    constexpr bool M = decltype(mask)::value;
 #pragma unroll
-                for (int c4 = 0; c4 < HALF / 4; ++c4) {
-                    const float4 l4 = vec[c4];  // LSE * log2 e of queries q0 + 4 c4 ...
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                    for (int c4 = 0; c4 < HALF / 4; ++c4) {
+                        const float4 l4 = vec[c4];  // LSE * log2 e of queries q0 + 4 c4 ...
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = 4 * c4 + e, q = q0 + c;
-                        const bool keep = kj < N && q < N && (!CAUSAL || kj <= q);
-                        p[c] = keep ? ex2(fmaf(__uint_as_float(raw[c]), sl, -lv[e])) : 0.f;
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = 4 * c4 + e, q = q0 + c;
+                            const float w = ex2(fmaf(__uint_as_float(raw[c]), sl, -lv[e]));
+                            if (M) p[c] = (kj < N && q < N && (!CAUSAL || kj <= q)) ? w : 0.f;
+                            else p[c] = w;
+                        }
                     }
-                }
+                };
+                if (masked) weights(std::true_type{});
+                else weights(std::false_type{});
             }
             {
                 uint32_t pk[32];
@@ -326,18 +337,29 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 uint32_t raw[HALF];
                 tmem_ld64(lb + cPh, raw);
                 uint32_t pk[32];
+                // a masked weight is exactly 0 and its dP may be anything, so the
+                // masked path selects 0 instead of multiplying
+                auto grads = [&](auto mask) {
+                    constexpr bool M = decltype(mask)::value;
 #pragma unroll
-                for (int c4 = 0; c4 < HALF / 4; ++c4) {
-                    const float4 d4 = vec[BM / 4 + c4];  // delta of queries q0 + 4 c4 ...
-                    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                    for (int c4 = 0; c4 < HALF / 4; ++c4) {
+                        const float4 d4 = vec[BM / 4 + c4];  // delta of queries q0 + 4 c4 ...
+                        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-                    for (int e = 0; e < 4; e += 2) {
-                        const int c = 4 * c4 + e;
-                        const float d0 = p[c] * (__uint_as_float(raw[c]) - dv[e]);
-                        const float d1 = p[c + 1] * (__uint_as_float(raw[c + 1]) - dv[e + 1]);
-                        pk[c / 2] = pack_bf16x2(p[c] != 0.f ? d0 : 0.f, p[c + 1] != 0.f ? d1 : 0.f);
+                        for (int e = 0; e < 4; e += 2) {
+                            const int c = 4 * c4 + e;
+                            float d0 = p[c] * (__uint_as_float(raw[c]) - dv[e]);
+                            float d1 = p[c + 1] * (__uint_as_float(raw[c + 1]) - dv[e + 1]);
+                            if (M) {
+                                d0 = p[c] != 0.f ? d0 : 0.f;
+                                d1 = p[c + 1] != 0.f ? d1 : 0.f;
+                            }
+                            pk[c / 2] = pack_bf16x2(d0, d1);
+                        }
                     }
-                }
+                };
+                if (masked) grads(std::true_type{});
+                else grads(std::false_type{});
                 tmem_st32(lb + cPh, pk);
             }
             tmem_wait_st();
@@ -536,16 +558,26 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const int k0 = s * BM + hf * HALF;
             if (!wait_or_abort(smem_addr(&s_full), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
             tc_fence_after();
+            // Tiles with no padded key or query and wholly below the diagonal
+            // take the unmasked path (no per-element tests or selects).
+            const int kt0 = s * BM;
+            const bool masked = kt0 + BM > N || q0 + BM > N || (CAUSAL && kt0 + BM > q0);
             float p[HALF];
             {
                 uint32_t raw[HALF];
                 tmem_ld64(lb + cSh, raw);
+                auto weights = [&](auto mask) {
+                    constexpr bool M = decltype(mask)::value;
 #pragma unroll
-                for (int c = 0; c < HALF; ++c) {
-                    const int kj = k0 + c;
-                    const bool keep = qi < N && kj < N && (!CAUSAL || kj <= qi);
-                    p[c] = keep ? ex2(fmaf(__uint_as_float(raw[c]), sl, -l2)) : 0.f;
-                }
+                    for (int c = 0; c < HALF; ++c) {
+                        const int kj = k0 + c;
+                        const float w = ex2(fmaf(__uint_as_float(raw[c]), sl, -l2));
+                        if (M) p[c] = (qi < N && kj < N && (!CAUSAL || kj <= qi)) ? w : 0.f;
+                        else p[c] = w;
+                    }
+                };
+                if (masked) weights(std::true_type{});
+                else weights(std::false_type{});
             }
             tc_fence_before();
             mbar_arrive(smem_addr(&s_read));  // S(s) is in registers: the MMA may overwrite it
@@ -555,13 +587,22 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 uint32_t raw[HALF];
                 tmem_ld64(lb + cPh, raw);
                 uint32_t pk[32];
+                auto grads = [&](auto mask) {
+                    constexpr bool M = decltype(mask)::value;
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    const int c = 2 * x;
-                    const float d0 = p[c] * (__uint_as_float(raw[c]) - de);
-                    const float d1 = p[c + 1] * (__uint_as_float(raw[c + 1]) - de);
-                    pk[x] = pack_bf16x2(p[c] != 0.f ? d0 : 0.f, p[c + 1] != 0.f ? d1 : 0.f);
-                }
+                    for (int x = 0; x < 32; ++x) {
+                        const int c = 2 * x;
+                        float d0 = p[c] * (__uint_as_float(raw[c]) - de);
+                        float d1 = p[c + 1] * (__uint_as_float(raw[c + 1]) - de);
+                        if (M) {
+                            d0 = p[c] != 0.f ? d0 : 0.f;
+                            d1 = p[c + 1] != 0.f ? d1 : 0.f;
+                        }
+                        pk[x] = pack_bf16x2(d0, d1);
+                    }
+                };
+                if (masked) grads(std::true_type{});
+                else grads(std::false_type{});
                 tmem_st32(lb + cPh, pk);  // dS over the dP columns already read
             }
             tmem_wait_st();
