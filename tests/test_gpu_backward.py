@@ -55,6 +55,7 @@ SHAPES = [
     (1, 2, 64, 16, "fp32"),
     (1, 1, 1, 64, "bf16"),
     (1, 2, 640, 128, "bf16"),
+    (1, 2, 384, 64, "bf16"),
     (1, 1, 130, 256, "fp32"),
 ]
 
