@@ -295,39 +295,43 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // take the unmasked path (no per-element tests or selects).
             const int qt0 = (first + s) * BM;
             const bool masked = k0 + BM > N || qt0 + BM > N || (CAUSAL && qt0 < k0 + BM);
-            // P^T row: weights of this key for this half of the tile's queries
-            float p[HALF];
+            // P^T row: weights of this key for this half of the tile's queries,
+            // as bf16 pairs (kept in registers for dS^T and written to tensor
+            // memory for the dV product)
+            uint32_t pw[HALF / 2];
             {
                 uint32_t raw[HALF];
                 tmem_ld64(lb + cSh, raw);
+                const uint64_t sl2 = f2_pack(sl, sl);
                 auto weights = [&](auto mask) {
                     constexpr bool M = decltype(mask)::value;
 #pragma unroll
                     for (int c4 = 0; c4 < HALF / 4; ++c4) {
                         const float4 l4 = vec[c4];  // LSE * log2 e of queries q0 + 4 c4 ...
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c = 4 * c4 + e, q = q0 + c;
-                            const float w = ex2(fmaf(__uint_as_float(raw[c]), sl, -lv[e]));
-                            if (M) p[c] = (kj < N && q < N && (!CAUSAL || kj <= q)) ? w : 0.f;
-                            else p[c] = w;
+                        for (int e = 0; e < 4; e += 2) {
+                            const int c = 4 * c4 + e;
+                            const uint64_t nl = e ? f2_pack(-l4.z, -l4.w) : f2_pack(-l4.x, -l4.y);
+                            float a0, a1;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1])), sl2, nl), a0, a1);
+                            float w0 = ex2(a0), w1 = ex2(a1);
+                            if (M) {
+                                const int q = q0 + c;
+                                w0 = (kj < N && q < N && (!CAUSAL || kj <= q)) ? w0 : 0.f;
+                                w1 = (kj < N && q + 1 < N && (!CAUSAL || kj <= q + 1)) ? w1 : 0.f;
+                            }
+                            pw[c / 2] = pack_bf16x2(w0, w1);
                         }
                     }
                 };
                 if (masked) weights(std::true_type{});
                 else weights(std::false_type{});
-            }
-            {
-                uint32_t pk[32];
-#pragma unroll
-                for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(p[2 * x], p[2 * x + 1]);
-                tmem_st32(lb + cSh, pk);
+                tmem_st32(lb + cSh, pw);
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_addr(&p_ready));
-            // dS^T row = P^T (dP^T - delta)
+            // dS^T row = P^T (dP^T - delta), with the bf16 weights the dV product uses
             if (!wait_or_abort(smem_addr(&dp_full), (uint32_t)(s & 1), limit, &abort_flag)) {
                 ok = false;
                 break;
@@ -336,7 +340,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             {
                 uint32_t raw[HALF];
                 tmem_ld64(lb + cPh, raw);
-                uint32_t pk[32];
+                uint32_t pk[HALF / 2];
                 // a masked weight is exactly 0 and its dP may be anything, so the
                 // masked path selects 0 instead of multiplying
                 auto grads = [&](auto mask) {
@@ -344,15 +348,17 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                     for (int c4 = 0; c4 < HALF / 4; ++c4) {
                         const float4 d4 = vec[BM / 4 + c4];  // delta of queries q0 + 4 c4 ...
-                        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
                         for (int e = 0; e < 4; e += 2) {
                             const int c = 4 * c4 + e;
-                            float d0 = p[c] * (__uint_as_float(raw[c]) - dv[e]);
-                            float d1 = p[c + 1] * (__uint_as_float(raw[c + 1]) - dv[e + 1]);
+                            const uint64_t nd = e ? f2_pack(-d4.z, -d4.w) : f2_pack(-d4.x, -d4.y);
+                            const float p0 = __uint_as_float(pw[c / 2] << 16), p1 = __uint_as_float(pw[c / 2] & 0xffff0000u);
+                            const uint64_t t = f2_add(f2_pack(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1])), nd);
+                            float d0, d1;
+                            f2_unpack(f2_mul(f2_pack(p0, p1), t), d0, d1);
                             if (M) {
-                                d0 = p[c] != 0.f ? d0 : 0.f;
-                                d1 = p[c + 1] != 0.f ? d1 : 0.f;
+                                d0 = p0 != 0.f ? d0 : 0.f;
+                                d1 = p1 != 0.f ? d1 : 0.f;
                             }
                             pk[c / 2] = pack_bf16x2(d0, d1);
                         }
@@ -566,14 +572,22 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             {
                 uint32_t raw[HALF];
                 tmem_ld64(lb + cSh, raw);
+                const uint64_t sl2 = f2_pack(sl, sl), nl2 = f2_pack(-l2, -l2);
                 auto weights = [&](auto mask) {
                     constexpr bool M = decltype(mask)::value;
 #pragma unroll
-                    for (int c = 0; c < HALF; ++c) {
-                        const int kj = k0 + c;
-                        const float w = ex2(fmaf(__uint_as_float(raw[c]), sl, -l2));
-                        if (M) p[c] = (qi < N && kj < N && (!CAUSAL || kj <= qi)) ? w : 0.f;
-                        else p[c] = w;
+                    for (int c = 0; c < HALF; c += 2) {
+                        float a0, a1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1])), sl2, nl2), a0, a1);
+                        const float w0 = ex2(a0), w1 = ex2(a1);
+                        if (M) {
+                            const int kj = k0 + c;
+                            p[c] = (qi < N && kj < N && (!CAUSAL || kj <= qi)) ? w0 : 0.f;
+                            p[c + 1] = (qi < N && kj + 1 < N && (!CAUSAL || kj + 1 <= qi)) ? w1 : 0.f;
+                        } else {
+                            p[c] = w0;
+                            p[c + 1] = w1;
+                        }
                     }
                 };
                 if (masked) weights(std::true_type{});
@@ -587,13 +601,15 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 uint32_t raw[HALF];
                 tmem_ld64(lb + cPh, raw);
                 uint32_t pk[32];
+                const uint64_t nd2 = f2_pack(-de, -de);
                 auto grads = [&](auto mask) {
                     constexpr bool M = decltype(mask)::value;
 #pragma unroll
                     for (int x = 0; x < 32; ++x) {
                         const int c = 2 * x;
-                        float d0 = p[c] * (__uint_as_float(raw[c]) - de);
-                        float d1 = p[c + 1] * (__uint_as_float(raw[c + 1]) - de);
+                        const uint64_t t = f2_add(f2_pack(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1])), nd2);
+                        float d0, d1;
+                        f2_unpack(f2_mul(f2_pack(p[c], p[c + 1]), t), d0, d1);
                         if (M) {
                             d0 = p[c] != 0.f ? d0 : 0.f;
                             d1 = p[c + 1] != 0.f ? d1 : 0.f;
