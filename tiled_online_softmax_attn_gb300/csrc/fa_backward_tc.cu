@@ -129,7 +129,10 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int first = CAUSAL ? kt : 0;  // query tiles before the key tile see none of its keys
     const int n_steps = prm.n_q - first;
 
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived from smem_raw by an offset so the
+    // compiler keeps the shared address space (plain shared loads for the
+    // per-query vectors)
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t s_base = smem_addr(smem);
     const uint32_t sK = s_base, sV = s_base + C::TILE, sStage = s_base + C::RES;
 
@@ -414,7 +417,10 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     const int q0 = qt * BM;
     const int n_steps = CAUSAL ? qt + 1 : prm.n_q;  // key tiles this query tile sees
 
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived from smem_raw by an offset so the
+    // compiler keeps the shared address space (plain shared loads for the
+    // per-query vectors)
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t s_base = smem_addr(smem);
     const uint32_t sQ = s_base, sG = s_base + C::TILE, sStage = s_base + C::RES;
 
