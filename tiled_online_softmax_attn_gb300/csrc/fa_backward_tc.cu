@@ -118,7 +118,10 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 {
     using C = BCfg<D>;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t res_full, full_b[2], empty_b[2], st_full, dp_full, p_ready, ds_ready, o_full, drain;
+    // per stage slot: fq/eq for Q_i and its LSE/delta vectors, fg/eg for dO_i (dO_i is
+    // freed by the earlier dV product and loaded second, so Q_i, needed first, lands sooner)
+    __shared__ __align__(8) uint64_t res_full, fq[2], eq[2], fg[2], eg[2], st_full, dp_full, p_ready, ds_ready, o_full,
+        drain;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
 
@@ -140,8 +143,10 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         abort_flag = 0;
         mbar_init(smem_addr(&res_full), 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(smem_addr(&full_b[s]), 1);
-            mbar_init(smem_addr(&empty_b[s]), 1);
+            mbar_init(smem_addr(&fq[s]), 1);
+            mbar_init(smem_addr(&eq[s]), 1);
+            mbar_init(smem_addr(&fg[s]), 1);
+            mbar_init(smem_addr(&eg[s]), 1);
         }
         mbar_init(smem_addr(&st_full), 1);
         mbar_init(smem_addr(&dp_full), 1);
@@ -168,7 +173,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
             bool ok = true;
-            int issued = 0;
+            int issued_q = 0, issued_g = 0;
             mbar_arrive_expect_tx(smem_addr(&res_full), C::RES);
             for (int c = 0; c < C::CH; ++c) {
                 tma_load_3d(sK + c * BOX, &tm_k, smem_addr(&res_full), c * 64, k0, bh, pol);
@@ -176,25 +181,33 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             for (int s = 0; s < n_steps; ++s) {
                 const int st = s & 1, q0 = (first + s) * BM;
-                if (!wait_or_abort(smem_addr(&empty_b[st]), (uint32_t)(((s >> 1) & 1) ^ 1), limit, &abort_flag)) {
+                const uint32_t par = (uint32_t)(((s >> 1) & 1) ^ 1), dst = sStage + st * C::STAGE;
+                if (!wait_or_abort(smem_addr(&eq[st]), par, limit, &abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint32_t fb = smem_addr(&full_b[st]), dst = sStage + st * C::STAGE;
-                mbar_arrive_expect_tx(fb, C::STAGE);
-                for (int c = 0; c < C::CH; ++c) {
-                    tma_load_3d(dst + c * BOX, &tm_q, fb, c * 64, q0, bh, pol);
-                    tma_load_3d(dst + C::TILE + c * BOX, &tm_g, fb, c * 64, q0, bh, pol);
-                }
+                const uint32_t bq = smem_addr(&fq[st]);
+                mbar_arrive_expect_tx(bq, C::TILE + VEC_BYTES);
+                for (int c = 0; c < C::CH; ++c) tma_load_3d(dst + c * BOX, &tm_q, bq, c * 64, q0, bh, pol);
                 const size_t vrow = (size_t)bh * prm.pitch + q0;
-                bulk_copy_g2s(dst + 2 * C::TILE, prm.lse2 + vrow, 512, fb);
-                bulk_copy_g2s(dst + 2 * C::TILE + 512, prm.delta + vrow, 512, fb);
-                issued = s + 1;
+                bulk_copy_g2s(dst + 2 * C::TILE, prm.lse2 + vrow, 512, bq);
+                bulk_copy_g2s(dst + 2 * C::TILE + 512, prm.delta + vrow, 512, bq);
+                issued_q = s + 1;
+                if (!wait_or_abort(smem_addr(&eg[st]), par, limit, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t bg = smem_addr(&fg[st]);
+                mbar_arrive_expect_tx(bg, C::TILE);
+                for (int c = 0; c < C::CH; ++c) tma_load_3d(dst + C::TILE + c * BOX, &tm_g, bg, c * 64, q0, bh, pol);
+                issued_g = s + 1;
             }
             if (!ok) {
                 if (!abort_flag) fail_bwd(&abort_flag);
-                for (int s = (issued > 2 ? issued - 2 : 0); s < issued; ++s)
-                    mbar_wait_bounded(smem_addr(&full_b[s & 1]), (uint32_t)((s >> 1) & 1), limit);
+                for (int s = (issued_q > 2 ? issued_q - 2 : 0); s < issued_q; ++s)
+                    mbar_wait_bounded(smem_addr(&fq[s & 1]), (uint32_t)((s >> 1) & 1), limit);
+                for (int s = (issued_g > 2 ? issued_g - 2 : 0); s < issued_g; ++s)
+                    mbar_wait_bounded(smem_addr(&fg[s & 1]), (uint32_t)((s >> 1) & 1), limit);
                 mbar_wait_bounded(smem_addr(&res_full), 0, limit);
             }
         }
@@ -224,16 +237,18 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     mma_ss_w(tmem + cP, dV + off, dG + off, id_s, kk > 0 ? 1u : 0u);
                 }
             };
-            auto wait_stage = [&](int s) -> bool {
-                if (!wait_or_abort_w(smem_addr(&full_b[s & 1]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) return false;
+            auto wait_stage = [&](uint64_t *bars, int s) -> bool {
+                if (!wait_or_abort_w(smem_addr(&bars[s & 1]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) return false;
                 tc_fence_after();
                 return true;
             };
-            if (ok && (ok = wait_stage(0))) {
+            if (ok && (ok = wait_stage(fq, 0))) {
                 mma_st(0);
                 mma_commit_w(smem_addr(&st_full));
-                mma_dpt(0);
-                mma_commit_w(smem_addr(&dp_full));
+                if ((ok = wait_stage(fg, 0))) {
+                    mma_dpt(0);
+                    mma_commit_w(smem_addr(&dp_full));
+                }
             }
             // Per step: dV(s) once P^T(s) is written; then S^T(s+1) into the
             // columns dV(s) has just read (same-thread MMAs run in order), so
@@ -248,9 +263,10 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 for (int kk = 0; kk < BM / 16; ++kk)
                     mma_ts_w(tmem + cV, tmem + a_col(cS, kk), dGmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
+                mma_commit_w(smem_addr(&eg[st]));  // dO_s read for the last time
                 const bool more = s + 1 < n_steps;
                 if (more) {
-                    if (!wait_stage(s + 1)) { ok = false; break; }
+                    if (!wait_stage(fq, s + 1)) { ok = false; break; }
                     mma_st(s + 1);
                     mma_commit_w(smem_addr(&st_full));
                 }
@@ -260,8 +276,9 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 for (int kk = 0; kk < BM / 16; ++kk)
                     mma_ts_w(tmem + cK, tmem + a_col(cP, kk), dQmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_w(smem_addr(&empty_b[st]));
+                mma_commit_w(smem_addr(&eq[st]));  // Q_s read for the last time (its vectors by the elementwise warps before ds_ready)
                 if (more) {
+                    if (!wait_stage(fg, s + 1)) { ok = false; break; }
                     mma_dpt(s + 1);
                     mma_commit_w(smem_addr(&dp_full));
                 }
@@ -288,7 +305,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int s = 0; s < n_steps; ++s) {
             const int st = s & 1, q0 = (first + s) * BM + hf * HALF;
             if (!wait_or_abort(smem_addr(&st_full), (uint32_t)(s & 1), limit, &abort_flag) ||
-                !wait_or_abort(smem_addr(&full_b[st]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) {
+                !wait_or_abort(smem_addr(&fq[st]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) {
                 ok = false;
                 break;
             }
@@ -406,7 +423,10 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 {
     using C = BCfg<D>;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t res_full, full_b[2], empty_b[2], s_full, dp_full, s_read, ds_ready, o_full, drain;
+    // per stage slot: fk/ek for K_j, fv/ev for V_j (V_j is freed by the earlier dP
+    // product and loaded second, so K_j, needed first, lands sooner)
+    __shared__ __align__(8) uint64_t res_full, fk[2], ek[2], fv[2], ev[2], s_full, dp_full, s_read, ds_ready, o_full,
+        drain;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
 
@@ -428,8 +448,10 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         abort_flag = 0;
         mbar_init(smem_addr(&res_full), 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(smem_addr(&full_b[s]), 1);
-            mbar_init(smem_addr(&empty_b[s]), 1);
+            mbar_init(smem_addr(&fk[s]), 1);
+            mbar_init(smem_addr(&ek[s]), 1);
+            mbar_init(smem_addr(&fv[s]), 1);
+            mbar_init(smem_addr(&ev[s]), 1);
         }
         mbar_init(smem_addr(&s_full), 1);
         mbar_init(smem_addr(&dp_full), 1);
@@ -456,7 +478,7 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
             bool ok = true;
-            int issued = 0;
+            int issued_k = 0, issued_v = 0;
             mbar_arrive_expect_tx(smem_addr(&res_full), C::RES);
             for (int c = 0; c < C::CH; ++c) {
                 tma_load_3d(sQ + c * BOX, &tm_q, smem_addr(&res_full), c * 64, q0, bh, pol);
@@ -464,22 +486,30 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
             for (int s = 0; s < n_steps; ++s) {
                 const int st = s & 1, k0 = s * BM;
-                if (!wait_or_abort(smem_addr(&empty_b[st]), (uint32_t)(((s >> 1) & 1) ^ 1), limit, &abort_flag)) {
+                const uint32_t par = (uint32_t)(((s >> 1) & 1) ^ 1), dst = sStage + st * C::STAGE;
+                if (!wait_or_abort(smem_addr(&ek[st]), par, limit, &abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint32_t fb = smem_addr(&full_b[st]), dst = sStage + st * C::STAGE;
-                mbar_arrive_expect_tx(fb, 2 * C::TILE);
-                for (int c = 0; c < C::CH; ++c) {
-                    tma_load_3d(dst + c * BOX, &tm_k, fb, c * 64, k0, bh, pol);
-                    tma_load_3d(dst + C::TILE + c * BOX, &tm_v, fb, c * 64, k0, bh, pol);
+                const uint32_t bk = smem_addr(&fk[st]);
+                mbar_arrive_expect_tx(bk, C::TILE);
+                for (int c = 0; c < C::CH; ++c) tma_load_3d(dst + c * BOX, &tm_k, bk, c * 64, k0, bh, pol);
+                issued_k = s + 1;
+                if (!wait_or_abort(smem_addr(&ev[st]), par, limit, &abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                issued = s + 1;
+                const uint32_t bv = smem_addr(&fv[st]);
+                mbar_arrive_expect_tx(bv, C::TILE);
+                for (int c = 0; c < C::CH; ++c) tma_load_3d(dst + C::TILE + c * BOX, &tm_v, bv, c * 64, k0, bh, pol);
+                issued_v = s + 1;
             }
             if (!ok) {
                 if (!abort_flag) fail_bwd(&abort_flag);
-                for (int s = (issued > 2 ? issued - 2 : 0); s < issued; ++s)
-                    mbar_wait_bounded(smem_addr(&full_b[s & 1]), (uint32_t)((s >> 1) & 1), limit);
+                for (int s = (issued_k > 2 ? issued_k - 2 : 0); s < issued_k; ++s)
+                    mbar_wait_bounded(smem_addr(&fk[s & 1]), (uint32_t)((s >> 1) & 1), limit);
+                for (int s = (issued_v > 2 ? issued_v - 2 : 0); s < issued_v; ++s)
+                    mbar_wait_bounded(smem_addr(&fv[s & 1]), (uint32_t)((s >> 1) & 1), limit);
                 mbar_wait_bounded(smem_addr(&res_full), 0, limit);
             }
         }
@@ -489,8 +519,8 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0), id_o = idesc_bf16_f32(BM, D, 0, 1);
             const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), dG = sdesc_sw128(sG, 16, 1024);
             bool ok = wait_or_abort_w(smem_addr(&res_full), 0, limit, &abort_flag), issued = false;
-            auto wait_stage = [&](int s) -> bool {
-                if (!wait_or_abort_w(smem_addr(&full_b[s & 1]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) return false;
+            auto wait_stage = [&](uint64_t *bars, int s) -> bool {
+                if (!wait_or_abort_w(smem_addr(&bars[s & 1]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) return false;
                 tc_fence_after();
                 return true;
             };
@@ -512,11 +542,14 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     mma_ss_w(tmem + cP, dG + off, dV + off, id_s, kk > 0 ? 1u : 0u);
                 }
             };
-            if (ok && (ok = wait_stage(0))) {
+            if (ok && (ok = wait_stage(fk, 0))) {
                 mma_s(0);
                 mma_commit_w(smem_addr(&s_full));
-                mma_dp(0);
-                mma_commit_w(smem_addr(&dp_full));
+                if ((ok = wait_stage(fv, 0))) {
+                    mma_dp(0);
+                    mma_commit_w(smem_addr(&dp_full));
+                    mma_commit_w(smem_addr(&ev[0]));  // V_0 read for the last time
+                }
             }
             // Per step: S(s+1) as soon as the softmax warps have read S(s) (it
             // overlaps their dS(s)); dQ(s) once dS(s) is written over dP(s);
@@ -525,7 +558,7 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 const int st = s & 1;
                 const bool more = s + 1 < n_steps;
                 if (more) {
-                    if (!wait_or_abort_w(smem_addr(&s_read), (uint32_t)(s & 1), limit, &abort_flag) || !wait_stage(s + 1)) {
+                    if (!wait_or_abort_w(smem_addr(&s_read), (uint32_t)(s & 1), limit, &abort_flag) || !wait_stage(fk, s + 1)) {
                         ok = false;
                         break;
                     }
@@ -539,10 +572,12 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 for (int kk = 0; kk < BM / 16; ++kk)
                     mma_ts_w(tmem + cQ, tmem + a_col(cP, kk), dKmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_w(smem_addr(&empty_b[st]));
+                mma_commit_w(smem_addr(&ek[st]));  // K_s read for the last time
                 if (more) {
+                    if (!wait_stage(fv, s + 1)) { ok = false; break; }
                     mma_dp(s + 1);
                     mma_commit_w(smem_addr(&dp_full));
+                    mma_commit_w(smem_addr(&ev[(s + 1) & 1]));  // V_(s+1) read for the last time
                 }
             }
             if (ok) {
