@@ -18,7 +18,7 @@
 //     S = Q_i K_j^T, dP = dO_i V_j^T, dS = P (dP - delta), dQ += dS K_j.
 //
 // So S and dP are formed twice (7 products of 128 x 128 x d instead of 5):
-// the price of no atomics and deterministic gradients.  Warps 0-7 do the
+// the price of no atomics and deterministic gradients.  The eight elementwise warps do the
 // elementwise work: warp w reads tensor-memory lanes 32 (w % 4) .. + 31 (one
 // row per thread) and the half w / 4 of the 128 columns, so two warps share
 // each row and each SM sub-partition runs two of them; no reduction crosses
@@ -50,12 +50,21 @@ using namespace ptx;
 using namespace tc;
 
 constexpr int BM = 128;
-constexpr int EW_WARPS = 8;  // elementwise warps: 4 lane quarters x 2 column halves
-constexpr int EW_THREADS = 32 * EW_WARPS;
-constexpr int NUM_THREADS = EW_THREADS + 64;
-constexpr int TMA_WARP = EW_WARPS;
-constexpr int MMA_WARP = EW_WARPS + 1;
-constexpr int HALF = BM / 2;  // columns per elementwise thread
+// Elementwise warps: 4 lane quarters x NH column groups of W = 128 / NH columns.
+// Two groups for both head dimensions: four groups at d = 64 (16 elementwise
+// warps) measured no faster, the d = 64 step being bound by the issue of its
+// 24 MMAs (16 of them N = 64) rather than by the elementwise work.
+__host__ __device__ constexpr int ew_groups(int) { return 2; }
+template <int D>
+struct EW {
+    static constexpr int NH = ew_groups(D);
+    static constexpr int W = BM / NH;               // columns per elementwise thread
+    static constexpr int WARPS = 4 * NH;
+    static constexpr int THREADS = 32 * WARPS;
+    static constexpr int NUM_THREADS = THREADS + 64;
+    static constexpr int TMA_WARP = WARPS;
+    static constexpr int MMA_WARP = WARPS + 1;
+};
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t BOX = 128 * 128;  // one 128-row x 64-column bf16 box
 constexpr uint32_t VEC_BYTES = 1024;  // lse2 and delta of 128 rows
@@ -100,9 +109,20 @@ __device__ __forceinline__ void store_row32(void *base, int fp32, size_t elem, c
 }
 
 // Tensor-memory column of K step kk (16 elements) of a 128-wide bf16 A
-// operand whose two 64-element halves were written by the two column-half
-// warps at col0 and col0 + 64 (32 packed columns each).
-__device__ __forceinline__ uint32_t a_col(uint32_t col0, int kk) { return col0 + kk * 8 + (kk >= 4 ? 32 : 0); }
+// operand whose W-element column groups were written by the group's warps
+// at col0 + g W (W / 2 packed columns each, over the group's own fp32 columns).
+template <int W>
+__device__ __forceinline__ uint32_t a_col(uint32_t col0, int kk)
+{
+    const int e = 16 * kk;
+    return col0 + (uint32_t)((e / W) * W + (e % W) / 2);
+}
+
+// Row slices of tensor memory by width (32 lanes; loads include the wait).
+__device__ __forceinline__ void tmem_ld_cols(uint32_t a, uint32_t (&r)[32]) { tmem_ld32(a, r); }
+__device__ __forceinline__ void tmem_ld_cols(uint32_t a, uint32_t (&r)[64]) { tmem_ld64(a, r); }
+__device__ __forceinline__ void tmem_st_cols(uint32_t a, const uint32_t (&r)[16]) { tmem_st16(a, r); }
+__device__ __forceinline__ void tmem_st_cols(uint32_t a, const uint32_t (&r)[32]) { tmem_st32(a, r); }
 
 __device__ __forceinline__ void fail_bwd(volatile int *abort_flag)
 {
@@ -112,11 +132,13 @@ __device__ __forceinline__ void fail_bwd(volatile int *abort_flag)
 
 // ---------------------------------------------------------------- dK / dV
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(EW<D>::NUM_THREADS, 1)
 fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g, const BwdParams prm)
 {
     using C = BCfg<D>;
+    using E = EW<D>;
+    constexpr int W = E::W, TMA_WARP = E::TMA_WARP, MMA_WARP = E::MMA_WARP;
     extern __shared__ uint8_t smem_raw[];
     // per stage slot: fq/eq for Q_i and its LSE/delta vectors, fg/eg for dO_i (dO_i is
     // freed by the earlier dV product and loaded second, so Q_i, needed first, lands sooner)
@@ -150,8 +172,8 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         mbar_init(smem_addr(&st_full), 1);
         mbar_init(smem_addr(&dp_full), 1);
-        mbar_init(smem_addr(&p_ready), EW_THREADS);
-        mbar_init(smem_addr(&ds_ready), EW_THREADS);
+        mbar_init(smem_addr(&p_ready), E::THREADS);
+        mbar_init(smem_addr(&ds_ready), E::THREADS);
         mbar_init(smem_addr(&o_full), 1);
         mbar_init(smem_addr(&drain), 1);
         fence_mbar_init();
@@ -261,7 +283,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const uint64_t dGmn = sdesc_sw128(base + C::TILE, BOX, 1024), dQmn = sdesc_sw128(base, BOX, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts_w(tmem + cV, tmem + a_col(cS, kk), dGmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                    mma_ts_w(tmem + cV, tmem + a_col<W>(cS, kk), dGmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
                 mma_commit_w(smem_addr(&eg[st]));  // dO_s read for the last time
                 const bool more = s + 1 < n_steps;
@@ -274,7 +296,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts_w(tmem + cK, tmem + a_col(cP, kk), dQmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                    mma_ts_w(tmem + cK, tmem + a_col<W>(cP, kk), dQmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
                 mma_commit_w(smem_addr(&eq[st]));  // Q_s read for the last time (its vectors by the elementwise warps before ds_ready)
                 if (more) {
@@ -295,22 +317,22 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         __syncwarp();
     } else {
-        // one key per thread (tensor-memory lane), queries [64 hf, 64 hf + 64) of each tile
+        // one key per thread (tensor-memory lane), queries [W hf, W hf + W) of each tile
         const int quarter = warp & 3, hf = warp >> 2;
         const int jr = quarter * 32 + lane, kj = k0 + jr;
         const uint32_t lb = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t cSh = cS + hf * HALF, cPh = cP + hf * HALF;
+        const uint32_t cSh = cS + hf * W, cPh = cP + hf * W;
         const float sl = prm.sl;
         bool ok = true;
         for (int s = 0; s < n_steps; ++s) {
-            const int st = s & 1, q0 = (first + s) * BM + hf * HALF;
+            const int st = s & 1, q0 = (first + s) * BM + hf * W;
             if (!wait_or_abort(smem_addr(&st_full), (uint32_t)(s & 1), limit, &abort_flag) ||
                 !wait_or_abort(smem_addr(&fq[st]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const float4 *vec = reinterpret_cast<const float4 *>(smem + C::RES + st * C::STAGE + 2 * C::TILE) + hf * (HALF / 4);
+            const float4 *vec = reinterpret_cast<const float4 *>(smem + C::RES + st * C::STAGE + 2 * C::TILE) + hf * (W / 4);
             // Tiles with no padded key or query and wholly below the diagonal
             // take the unmasked path (no per-element tests or selects).
             const int qt0 = (first + s) * BM;
@@ -318,15 +340,15 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // P^T row: weights of this key for this half of the tile's queries,
             // as bf16 pairs (kept in registers for dS^T and written to tensor
             // memory for the dV product)
-            uint32_t pw[HALF / 2];
+            uint32_t pw[W / 2];
             {
-                uint32_t raw[HALF];
-                tmem_ld64(lb + cSh, raw);
+                uint32_t raw[W];
+                tmem_ld_cols(lb + cSh, raw);
                 const uint64_t sl2 = f2_pack(sl, sl);
                 auto weights = [&](auto mask) {
                     constexpr bool M = decltype(mask)::value;
 #pragma unroll
-                    for (int c4 = 0; c4 < HALF / 4; ++c4) {
+                    for (int c4 = 0; c4 < W / 4; ++c4) {
                         const float4 l4 = vec[c4];  // LSE * log2 e of queries q0 + 4 c4 ...
 #pragma unroll
                         for (int e = 0; e < 4; e += 2) {
@@ -346,7 +368,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 };
                 if (masked) weights(std::true_type{});
                 else weights(std::false_type{});
-                tmem_st32(lb + cSh, pw);
+                tmem_st_cols(lb + cSh, pw);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -358,15 +380,15 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             tc_fence_after();
             {
-                uint32_t raw[HALF];
-                tmem_ld64(lb + cPh, raw);
-                uint32_t pk[HALF / 2];
+                uint32_t raw[W];
+                tmem_ld_cols(lb + cPh, raw);
+                uint32_t pk[W / 2];
                 // a masked weight is exactly 0 and its dP may be anything, so the
                 // masked path selects 0 instead of multiplying
                 auto grads = [&](auto mask) {
                     constexpr bool M = decltype(mask)::value;
 #pragma unroll
-                    for (int c4 = 0; c4 < HALF / 4; ++c4) {
+                    for (int c4 = 0; c4 < W / 4; ++c4) {
                         const float4 d4 = vec[BM / 4 + c4];  // delta of queries q0 + 4 c4 ...
 #pragma unroll
                         for (int e = 0; e < 4; e += 2) {
@@ -386,7 +408,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 };
                 if (masked) grads(std::true_type{});
                 else grads(std::false_type{});
-                tmem_st32(lb + cPh, pk);
+                tmem_st_cols(lb + cPh, pk);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -396,7 +418,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc_fence_after();
             const size_t row = ((size_t)bh * N + kj) * D;
 #pragma unroll 1
-            for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {  // this warp's half of the columns
+            for (int c = hf; c < D / 32; c += E::NH) {  // this warp's 32-column chunks
                 uint32_t raw[32];
                 tmem_ld32(lb + cV + c * 32, raw);
                 if (kj < N) store_row32(prm.dv, prm.g_fp32, row + c * 32, raw, 1.f);
@@ -417,11 +439,13 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
 // ---------------------------------------------------------------- dQ
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(EW<D>::NUM_THREADS, 1)
 fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g, const BwdParams prm)
 {
     using C = BCfg<D>;
+    using E = EW<D>;
+    constexpr int W = E::W, TMA_WARP = E::TMA_WARP, MMA_WARP = E::MMA_WARP;
     extern __shared__ uint8_t smem_raw[];
     // per stage slot: fk/ek for K_j, fv/ev for V_j (V_j is freed by the earlier dP
     // product and loaded second, so K_j, needed first, lands sooner)
@@ -455,8 +479,8 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         mbar_init(smem_addr(&s_full), 1);
         mbar_init(smem_addr(&dp_full), 1);
-        mbar_init(smem_addr(&s_read), EW_THREADS);
-        mbar_init(smem_addr(&ds_ready), EW_THREADS);
+        mbar_init(smem_addr(&s_read), E::THREADS);
+        mbar_init(smem_addr(&ds_ready), E::THREADS);
         mbar_init(smem_addr(&o_full), 1);
         mbar_init(smem_addr(&drain), 1);
         fence_mbar_init();
@@ -570,7 +594,7 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 const uint64_t dKmn = sdesc_sw128(sStage + st * C::STAGE, BOX, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts_w(tmem + cQ, tmem + a_col(cP, kk), dKmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                    mma_ts_w(tmem + cQ, tmem + a_col<W>(cP, kk), dKmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
                 mma_commit_w(smem_addr(&ek[st]));  // K_s read for the last time
                 if (more) {
@@ -592,32 +616,32 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         __syncwarp();
     } else {
-        // one query per thread (tensor-memory lane), keys [64 hf, 64 hf + 64) of each tile
+        // one query per thread (tensor-memory lane), keys [W hf, W hf + W) of each tile
         const int quarter = warp & 3, hf = warp >> 2;
         const int r = quarter * 32 + lane, qi = q0 + r;
         const uint32_t lb = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t cSh = cS + hf * HALF, cPh = cP + hf * HALF;
+        const uint32_t cSh = cS + hf * W, cPh = cP + hf * W;
         const float sl = prm.sl;
         const float l2 = qi < N ? prm.lse2[(size_t)bh * prm.pitch + qi] : 0.f;
         const float de = qi < N ? prm.delta[(size_t)bh * prm.pitch + qi] : 0.f;
         bool ok = true;
         for (int s = 0; s < n_steps; ++s) {
-            const int k0 = s * BM + hf * HALF;
+            const int k0 = s * BM + hf * W;
             if (!wait_or_abort(smem_addr(&s_full), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
             tc_fence_after();
             // Tiles with no padded key or query and wholly below the diagonal
             // take the unmasked path (no per-element tests or selects).
             const int kt0 = s * BM;
             const bool masked = kt0 + BM > N || q0 + BM > N || (CAUSAL && kt0 + BM > q0);
-            float p[HALF];
+            float p[W];
             {
-                uint32_t raw[HALF];
-                tmem_ld64(lb + cSh, raw);
+                uint32_t raw[W];
+                tmem_ld_cols(lb + cSh, raw);
                 const uint64_t sl2 = f2_pack(sl, sl), nl2 = f2_pack(-l2, -l2);
                 auto weights = [&](auto mask) {
                     constexpr bool M = decltype(mask)::value;
 #pragma unroll
-                    for (int c = 0; c < HALF; c += 2) {
+                    for (int c = 0; c < W; c += 2) {
                         float a0, a1;
                         f2_unpack(f2_fma(f2_pack(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1])), sl2, nl2), a0, a1);
                         const float w0 = ex2(a0), w1 = ex2(a1);
@@ -639,14 +663,14 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             if (!wait_or_abort(smem_addr(&dp_full), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
             tc_fence_after();
             {
-                uint32_t raw[HALF];
-                tmem_ld64(lb + cPh, raw);
-                uint32_t pk[32];
+                uint32_t raw[W];
+                tmem_ld_cols(lb + cPh, raw);
+                uint32_t pk[W / 2];
                 const uint64_t nd2 = f2_pack(-de, -de);
                 auto grads = [&](auto mask) {
                     constexpr bool M = decltype(mask)::value;
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) {
+                    for (int x = 0; x < W / 2; ++x) {
                         const int c = 2 * x;
                         const uint64_t t = f2_add(f2_pack(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1])), nd2);
                         float d0, d1;
@@ -660,7 +684,7 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 };
                 if (masked) grads(std::true_type{});
                 else grads(std::false_type{});
-                tmem_st32(lb + cPh, pk);  // dS over the dP columns already read
+                tmem_st_cols(lb + cPh, pk);  // dS over the dP columns already read
             }
             tmem_wait_st();
             tc_fence_before();
@@ -670,7 +694,7 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             tc_fence_after();
             const size_t row = ((size_t)bh * N + qi) * D;
 #pragma unroll 1
-            for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {  // this warp's half of the columns
+            for (int c = hf; c < D / 32; c += E::NH) {  // this warp's 32-column chunks
                 uint32_t raw[32];
                 tmem_ld32(lb + cQ + c * 32, raw);
                 if (qi < N) store_row32(prm.dq, prm.g_fp32, row + c * 32, raw, prm.scale);
@@ -747,9 +771,9 @@ cudaError_t launch_dims(const BackwardProblem &p, float *delta, float *lse2, int
     if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_REQ)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_REQ)) != cudaSuccess) return e;
     const unsigned grid = (unsigned)((int64_t)prm.n_q * BH);
-    kv<<<grid, NUM_THREADS, C::SMEM_REQ, stream>>>(mq, mk, mv, mg, prm);
+    kv<<<grid, EW<D>::NUM_THREADS, C::SMEM_REQ, stream>>>(mq, mk, mv, mg, prm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    kq<<<grid, NUM_THREADS, C::SMEM_REQ, stream>>>(mq, mk, mv, mg, prm);
+    kq<<<grid, EW<D>::NUM_THREADS, C::SMEM_REQ, stream>>>(mq, mk, mv, mg, prm);
     return cudaGetLastError();
 }
 
