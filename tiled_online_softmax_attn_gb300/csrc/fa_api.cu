@@ -210,6 +210,32 @@ fa_status validate_general(const fa::Problem &p)
     return FA_OK;
 }
 
+// The error words of the three kernel families, read with one synchronisation
+// of the stream (after the work already queued on it) into pinned memory of
+// this host thread, and cleared where set.
+cudaError_t take_error_words(uint32_t *word, cudaStream_t s)
+{
+    thread_local uint32_t *host = nullptr;  // pinned, 3 words, one block per host thread
+    if (!host) {
+        cudaError_t e = cudaHostAlloc(reinterpret_cast<void **>(&host), 4 * sizeof(uint32_t), cudaHostAllocDefault);
+        if (e != cudaSuccess) return e;
+    }
+    uint32_t *dev[3] = {nullptr, nullptr, nullptr};
+    cudaError_t e = fa::tc_error_word_ptr(&dev[0]);
+    if (e == cudaSuccess) e = fa::wide_error_word_ptr(&dev[1]);
+    if (e == cudaSuccess) e = fa::bwd_error_word_ptr(&dev[2]);
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+        e = cudaMemcpyAsync(&host[i], dev[i], sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    *word = host[0] | host[1] | host[2];
+    if (*word == 0) return cudaSuccess;
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+        if (host[i]) e = cudaMemsetAsync(dev[i], 0, sizeof(uint32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return e;
+}
+
 // Heads per pipelined chunk of fa_forward_host: up to MAX_CHUNKS chunks of
 // at least ~4 MB of input each.
 int host_chunks(const fa::Problem &p)
@@ -220,14 +246,28 @@ int host_chunks(const fa::Problem &p)
     return std::max(chunks, 1);
 }
 
+// First head of chunk c of fa_forward_host.  Chunk sizes fall linearly
+// (boundaries at BH (1 - (1 - c / K)^2)): the copies in are the bottleneck and
+// the kernel and the copy out of the last chunk are the only work not hidden
+// behind them, so the last chunk is the smallest.
+int64_t chunk_head(int64_t BH, int chunks, int c)
+{
+    if (c >= chunks) return BH;
+    const double r = 1.0 - (double)c / chunks;
+    return std::min<int64_t>(BH, (int64_t)std::llround((double)BH * (1.0 - r * r)));
+}
+
 // Kernel workspace for one chunk of fa_forward_host (the largest chunk).
 size_t chunk_workspace(const fa::Problem &p)
 {
     const int64_t BH = p.B * p.H;
     const int chunks = host_chunks(p);
+    int64_t largest = 1;
+    for (int c = 0; c < chunks; ++c)
+        largest = std::max(largest, chunk_head(BH, chunks, c + 1) - chunk_head(BH, chunks, c));
     fa::Problem c = p;
     c.B = 1;
-    c.H = (BH + chunks - 1) / chunks;
+    c.H = largest;
     if (fa::tc_supported(c)) return 0;
     const fa::WidePlan w = fa::wide_plan(c, 1 << 20);
     return w.ok ? w.workspace_bytes : 0;
@@ -459,7 +499,7 @@ fa_status fa_forward_host(const void *q_h, const void *k_h, const void *v_h, voi
     if ((e = cudaStreamWaitEvent(res->d2h, res->start, 0)) != cudaSuccess) return cuda_fail(e, "stream wait");
 
     for (int c = 0; c < chunks; ++c) {
-        const int64_t h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks, nh = h1 - h0;
+        const int64_t h0 = chunk_head(BH, chunks, c), h1 = chunk_head(BH, chunks, c + 1), nh = h1 - h0;
         if (nh == 0) continue;
         const size_t off_in = (size_t)h0 * head_elems * ei, n_in = (size_t)nh * head_elems * ei;
         const size_t off_o = (size_t)h0 * head_elems * eo, n_o = (size_t)nh * head_elems * eo;
@@ -495,14 +535,9 @@ fa_status fa_check_device_error(void *stream)
 {
     g_last_error.clear();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
-    uint32_t word = 0, wide_word = 0, bwd_word = 0;
-    e = fa::tc_take_error_word(&word, s);
-    if (e == cudaSuccess) e = fa::wide_take_error_word(&wide_word, s);
-    if (e == cudaSuccess) e = fa::bwd_take_error_word(&bwd_word, s);
-    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
-    word |= wide_word | bwd_word;
+    uint32_t word = 0;
+    cudaError_t e = take_error_words(&word, s);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize / reading the device error words");
     if (word) return fail(FA_ERR_TIMEOUT, "a device pipeline wait gave up (error word 0x%x)", word);
     return FA_OK;
 }

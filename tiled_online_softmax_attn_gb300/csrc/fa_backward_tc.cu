@@ -799,16 +799,9 @@ cudaError_t launch_backward_tc(const BackwardProblem &p, void *workspace, cudaSt
                     : launch_dims<64, false>(p, delta, lse2, pitch, stream, detail);
 }
 
-cudaError_t bwd_take_error_word(uint32_t *word, cudaStream_t stream)
+cudaError_t bwd_error_word_ptr(uint32_t **ptr)
 {
-    cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_bwd_error_word, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost, stream);
-    if (e != cudaSuccess) return e;
-    e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess || *word == 0) return e;
-    const uint32_t zero = 0;
-    e = cudaMemcpyToSymbolAsync(g_bwd_error_word, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, stream);
-    if (e != cudaSuccess) return e;
-    return cudaStreamSynchronize(stream);
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(ptr), g_bwd_error_word);
 }
 
 }  // namespace fa

@@ -72,8 +72,9 @@ bool tc_supported(const Problem &p);
 // failures that are not CUDA errors (tensor-map encoding).
 cudaError_t launch_tc(const Problem &p, cudaStream_t stream, uint32_t flags, const char **detail);
 
-// Reads and clears the device error word of the tensor-core kernel.
-cudaError_t tc_take_error_word(uint32_t *word, cudaStream_t stream);
+// Device address of the error word of the tensor-core kernel (ORed bits of
+// waits that gave up; cleared by the host after reading).
+cudaError_t tc_error_word_ptr(uint32_t **ptr);
 
 // Wide-head tensor-core path (fa_wide.cu): fp32 inputs with d % 128 == 0
 // (d <= 1024), bf16 inputs with d % 128 == 0 and 256 <= d <= 1024.
@@ -91,7 +92,7 @@ struct WidePlan {
 WidePlan wide_plan(const Problem &p, int max_splits);
 cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cudaStream_t stream, uint32_t flags,
                         const char **detail);
-cudaError_t wide_take_error_word(uint32_t *word, cudaStream_t stream);
+cudaError_t wide_error_word_ptr(uint32_t **ptr);
 
 // Backward problem: contiguous [B, H, N, d] Q, K, V, O, dO of in_dtype,
 // LSE [B, H, N] fp32 from the forward pass, gradients of grad_dtype.
@@ -112,7 +113,7 @@ cudaError_t launch_backward_delta(const BackwardProblem &p, void *workspace, cud
 // Tensor-core backward: bf16 inputs, d in {64, 128}, scale > 0, 16-byte aligned.
 bool backward_tc_supported(const BackwardProblem &p);
 cudaError_t launch_backward_tc(const BackwardProblem &p, void *workspace, cudaStream_t stream, const char **detail);
-cudaError_t bwd_take_error_word(uint32_t *word, cudaStream_t stream);
+cudaError_t bwd_error_word_ptr(uint32_t **ptr);
 
 // Sets the text fa_last_error returns on this host thread.
 void set_last_error(const char *msg);

@@ -698,16 +698,9 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t stream, uint32_t flags, con
     return dv == 128 ? launch_dims<64, 128>(p, stream, flags, detail) : launch_dims<64, 64>(p, stream, flags, detail);
 }
 
-cudaError_t tc_take_error_word(uint32_t *word, cudaStream_t stream)
+cudaError_t tc_error_word_ptr(uint32_t **ptr)
 {
-    cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_tc_error_word, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost, stream);
-    if (e != cudaSuccess) return e;
-    e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess || *word == 0) return e;
-    const uint32_t zero = 0;
-    e = cudaMemcpyToSymbolAsync(g_tc_error_word, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, stream);
-    if (e != cudaSuccess) return e;
-    return cudaStreamSynchronize(stream);
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(ptr), g_tc_error_word);
 }
 
 }  // namespace fa

@@ -649,16 +649,9 @@ cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cu
     return e;
 }
 
-cudaError_t wide_take_error_word(uint32_t *word, cudaStream_t stream)
+cudaError_t wide_error_word_ptr(uint32_t **ptr)
 {
-    cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_wide_error_word, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost, stream);
-    if (e != cudaSuccess) return e;
-    e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess || *word == 0) return e;
-    const uint32_t zero = 0;
-    e = cudaMemcpyToSymbolAsync(g_wide_error_word, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, stream);
-    if (e != cudaSuccess) return e;
-    return cudaStreamSynchronize(stream);
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(ptr), g_wide_error_word);
 }
 
 }  // namespace fa
