@@ -98,6 +98,21 @@ def test_full_size_workloads_sampled(name):
     _sampled(synth.WORKLOADS[name])
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_persistent_ctas_with_ragged_rows(d):
+    """More items (256-row query blocks x heads) than SMs, few key tiles and a
+    ragged N: CTAs loop over several items each, so the per-item barrier
+    phases and the release of O between items are exercised; every row of the
+    last, partial query block is checked too."""
+    w = synth.Workload("persistent", 2, 40, 1000, d, "bf16", False, seed=7100 + d)
+    q, k, v = w.inputs()
+    o, lse = run(q, k, v, w.dtype, w.scale, w.causal)
+    rows = np.unique(np.concatenate([sample_rows(w.B, w.H, w.N, 512, seed=w.seed),
+                                     np.arange(w.N - 232, w.N, dtype=np.int64) + (w.B * w.H - 1) * w.N]))
+    o_ref, lse_ref = oracle.attention_rows(q, k, v, w.scale, w.causal, rows)
+    compare(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, w.dtype, w.dtype)
+
+
 def test_peaked_workload_fp32_output():
     """With fp32 O the plain bounds hold without the bf16 rounding floor."""
     _sampled(synth.WORKLOADS["peaked"], o_dtype="fp32")

@@ -9,11 +9,14 @@
 // divided by l once after the last key tile.  Scores live in log2 units so
 // each weight is one FFMA and one ex2.
 //
-// One CTA owns two 128-row query tiles (Q0, Q1) of one (batch, head) and
-// streams that head's K/V tiles (128 keys) through a shared-memory ring:
+// A work item is two 128-row query tiles (Q0, Q1) of one (batch, head); a CTA
+// processes one item, or (short items) loops over items c, c + gridDim.x, ...
+// with one CTA per SM.  It streams the head's K/V tiles (128 keys) through a
+// shared-memory ring:
 //
-//   warp 8  (TMA)      loads Q0, Q1 once and K_j, V_j into the K and V rings
-//                      (full/empty mbarrier pairs per slot);
+//   warp 8  (TMA)      loads Q0, Q1 once per item (after the previous item's
+//                      last S MMA) and stage j = (K_j, V_(j-1)) into the ring
+//                      (one full/empty mbarrier pair per stage);
 //   warp 9  (MMA)      allocates tensor memory and issues (one elected lane)
 //                      S_t = Q_t K_j^T (SS form) and O_t += P_t V_j (A operand
 //                      read from tensor memory), alternating the two tiles so
@@ -22,7 +25,9 @@
 //   warps 0-3 / 4-7    softmax for Q0 / Q1: one query row per thread (a warp
 //                      reads its 32 tensor-memory lanes), row max, weights,
 //                      row sum, bf16 P written back over S, the alpha rescale
-//                      of O in tensor memory, and the epilogue (O / l, LSE).
+//                      of O in tensor memory, and the epilogue (O / l, LSE),
+//                      which releases O_t (o_empty) as soon as it is read so
+//                      the next item's first P V product can start.
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   [  0,128) S0 / P0   [128,256) S1 / P1   [256, 256+D) O0   [256+D, 256+2D) O1
@@ -39,6 +44,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -59,12 +65,9 @@ using namespace tc;
 
 constexpr int BM = 128;           // query rows per tile (tensor-memory lanes)
 constexpr int BN = 128;           // keys per tile
-constexpr int RH = 1;             // softmax threads per query row
-constexpr int HC = BN / RH;       // key columns of a tile per softmax thread
-constexpr int SOFTMAX_WARPS = 8 * RH;
-constexpr int TMA_WARP = SOFTMAX_WARPS;
-constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
-constexpr int NUM_THREADS = 32 * (SOFTMAX_WARPS + 2);
+constexpr int TMA_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr int NUM_THREADS = 320;  // 10 warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;  // lazy-rescale threshold, log2 units
 
@@ -98,7 +101,8 @@ struct Params {
     int Nk;            // key sequence length
     int H;             // heads
     int BH;            // batch * heads
-    int n_qblocks;     // CTAs per head (256 query rows each)
+    int n_qblocks;     // work items per head (256 query rows each)
+    int n_items;       // n_qblocks * BH; CTA c takes items c, c + gridDim.x, ...
     int n_kv;          // key tiles per head
     float scale_log2;  // scale * log2(e), > 0
     int causal;
@@ -112,14 +116,41 @@ struct Params {
 };
 
 struct __align__(8) Barriers {
-    uint64_t q_full[2];
+    uint64_t q_full[2], q_empty;      // query tiles of an item; free after its last S MMA
     uint64_t kv_full[3], kv_empty[3];
     uint64_t s_full[2];
     uint64_t p_full[2];
-    uint64_t o_full[2];
+    uint64_t o_full[2], o_empty[2];   // O_t complete / read by the epilogue
     uint64_t drain;
-    uint64_t pair[8];  // the RH softmax threads of a row exchange partial results (per tile and lane quarter)
 };
+
+// A work item: two 128-row query tiles (256 rows) of one (batch, head).
+struct Item {
+    int bh, b, h;
+    int qrow0;   // first row of Q0; Q1 starts BM later
+    int n0, n1;  // key tiles each query tile needs: all, or up to its diagonal under the mask
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Item item_of(const Params &prm, int w)
+{
+    int qb, bh;
+    if (CAUSAL) {  // longest query blocks first
+        qb = prm.n_qblocks - 1 - w / prm.BH;
+        bh = w % prm.BH;
+    } else {       // items of one head are adjacent: concurrent CTAs share its K/V in L2
+        qb = w % prm.n_qblocks;
+        bh = w / prm.n_qblocks;
+    }
+    Item it;
+    it.bh = bh;
+    it.b = bh / prm.H;
+    it.h = bh % prm.H;
+    it.qrow0 = qb * 2 * BM;
+    it.n0 = CAUSAL ? min(prm.n_kv, 2 * qb + 1) : prm.n_kv;
+    it.n1 = CAUSAL ? min(prm.n_kv, 2 * qb + 2) : prm.n_kv;
+    return it;
+}
 
 // Map coordinate for dimension slot s of a tensor map whose outer dimensions
 // are ordered by stride: 0 = sequence row, 1 = head, 2 = batch.
@@ -131,10 +162,6 @@ __device__ __forceinline__ void tma_load_rows(uint32_t dst, const void *tmap, ui
     tma_load_4d(dst, tmap, bar, col, pick(perm & 3, row, h, b), pick((perm >> 2) & 3, row, h, b),
                 pick((perm >> 4) & 3, row, h, b), pol);
 }
-
-// One row slice of tensor memory (32 lanes x 64 or 128 columns), loaded and waited for.
-__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t (&r)[64]) { tmem_ld64(taddr, r); }
-__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t (&r)[128]) { tmem_ld128(taddr, r); }
 
 __device__ __forceinline__ void raise_error(uint32_t bit, volatile int *abort_flag)
 {
@@ -174,47 +201,30 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     extern __shared__ uint8_t smem_raw[];
     __shared__ Barriers bars;
     __shared__ uint32_t tmem_base_s;
-    __shared__ float xch_max[2][2][RH][BM];  // [iteration parity][tile][row thread][row]: partial row maxima
-    __shared__ float2 xch_l[2][RH][BM];      // [tile][row thread][row]: partial (l, dq) for the epilogue
     __shared__ volatile int abort_flag;
 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_base = smem_addr(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // ---- work item: (query block of 256 rows, head)
-    int qb, bh;
-    if (CAUSAL) {  // longest query blocks first
-        qb = prm.n_qblocks - 1 - (int)(blockIdx.x / prm.BH);
-        bh = (int)(blockIdx.x % prm.BH);
-    } else {       // CTAs of one head run together and share its K/V in L2
-        qb = (int)(blockIdx.x % prm.n_qblocks);
-        bh = (int)(blockIdx.x / prm.n_qblocks);
-    }
     const int N = prm.N, Nk = prm.Nk;
-    const int b = bh / prm.H, h = bh % prm.H;
-    const int qrow0 = qb * 2 * BM;  // first row of Q0; Q1 starts BM later
-    // key tiles each query tile needs: all, or up to its diagonal under the mask
-    const int n0 = CAUSAL ? min(prm.n_kv, 2 * qb + 1) : prm.n_kv;
-    const int n1 = CAUSAL ? min(prm.n_kv, 2 * qb + 2) : prm.n_kv;
 
-    // ---- setup
+    // ---- setup (once per CTA; the CTA then loops over work items)
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(smem_addr(&bars.q_full[0]), 1);
-        mbar_init(smem_addr(&bars.q_full[1]), 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_addr(&bars.q_full[t]), 1);
+            mbar_init(smem_addr(&bars.s_full[t]), 1);
+            mbar_init(smem_addr(&bars.p_full[t]), 128);
+            mbar_init(smem_addr(&bars.o_full[t]), 1);
+            mbar_init(smem_addr(&bars.o_empty[t]), 128);
+        }
+        mbar_init(smem_addr(&bars.q_empty), 1);
         for (int s = 0; s < 3; ++s) {
             mbar_init(smem_addr(&bars.kv_full[s]), 1);
             mbar_init(smem_addr(&bars.kv_empty[s]), 1);
         }
-        for (int t = 0; t < 2; ++t) {
-            mbar_init(smem_addr(&bars.s_full[t]), 1);
-            mbar_init(smem_addr(&bars.p_full[t]), 128 * RH);
-            mbar_init(smem_addr(&bars.o_full[t]), 1);
-        }
         mbar_init(smem_addr(&bars.drain), 1);
-        for (int i = 0; i < 8; ++i) mbar_init(smem_addr(&bars.pair[i]), 32 * RH);
         fence_mbar_init();
     }
     if (warp == MMA_WARP) {
@@ -235,54 +245,66 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             tma_prefetch_desc(&tm_v);
             const uint64_t pol_q = policy_evict_first();
             const uint64_t pol_kv = policy_evict_last();
-            int issued = 0, q_issued = 0;  // stages and Q tiles whose loads were issued
+            int g = 0;                     // stages issued over all items (ring position)
+            int q_items = 0;               // items whose Q loads were issued
+            int skipped = -1;              // ring position of the injected, never-filled stage
             bool ok = true;
-            auto load_q = [&](int t) {
-                q_issued = t + 1;
-                const uint32_t bar = smem_addr(&bars.q_full[t]);
-                mbar_arrive_expect_tx(bar, C::Q_BYTES);
-                for (int c = 0; c < C::QCH; ++c)
-                    tma_load_rows(s_base + C::OFF_Q + t * C::Q_BYTES + c * (BM * 128), &tm_q, bar, c * 64,
-                                  prm.qperm, qrow0 + t * BM, h, b, pol_q);
-            };
-            // stage s = K_s (s < n1) and V_(s-1) (s >= 1), s = 0 .. n1
-            auto load_stage = [&](int s) -> bool {
-                const int slot = s % C::KVS;
-                const uint32_t n_use = (uint32_t)(s / C::KVS);
-                const uint32_t full = smem_addr(&bars.kv_full[slot]);
-                if (!wait_or_abort(smem_addr(&bars.kv_empty[slot]), (n_use & 1u) ^ 1u, limit, &abort_flag)) return false;
-                if (s == prm.skip_load && s < n1) return true;  // fault injection: this stage never fills
-                const bool has_k = s < n1, has_v = s >= 1;
-                mbar_arrive_expect_tx(full, (has_k ? C::K_BYTES : 0u) + (has_v ? C::V_BYTES : 0u));
-                if (has_k)
-                    for (int c = 0; c < C::QCH; ++c)
-                        tma_load_rows(s_base + C::OFF_K + slot * C::K_BYTES + c * (BN * 128), &tm_k, full, c * 64,
-                                      prm.kperm, s * BN, h, b, pol_kv);
-                if (has_v)
-                    for (int c = 0; c < C::VCH; ++c)
-                        tma_load_rows(s_base + C::OFF_V + slot * C::V_BYTES + c * (BN * 128), &tm_v, full, c * 64,
-                                      prm.vperm, (s - 1) * BN, h, b, pol_kv);
-                return true;
-            };
-            load_q(0);
-            ok = load_stage(0);
-            if (ok) { issued = 1; load_q(1); }
-            for (int s = 1; ok && s <= n1; ++s) {
-                ok = load_stage(s);
-                if (ok) issued = s + 1;
+            for (int w = blockIdx.x, it = 0; ok && w < prm.n_items; w += gridDim.x, ++it) {
+                const Item wi = item_of<CAUSAL>(prm, w);
+                // stage s of the item = K_s (s < n1) and V_(s-1) (s >= 1), s = 0 .. n1
+                auto load_stage = [&](int s) -> bool {
+                    const int slot = g % C::KVS;
+                    const uint32_t n_use = (uint32_t)(g / C::KVS);
+                    const uint32_t full = smem_addr(&bars.kv_full[slot]);
+                    if (!wait_or_abort(smem_addr(&bars.kv_empty[slot]), (n_use & 1u) ^ 1u, limit, &abort_flag)) return false;
+                    ++g;
+                    if (it == 0 && s == prm.skip_load && s < wi.n1) {  // fault injection: this stage never fills
+                        skipped = g - 1;
+                        return true;
+                    }
+                    const bool has_k = s < wi.n1, has_v = s >= 1;
+                    mbar_arrive_expect_tx(full, (has_k ? C::K_BYTES : 0u) + (has_v ? C::V_BYTES : 0u));
+                    if (has_k)
+                        for (int c = 0; c < C::QCH; ++c)
+                            tma_load_rows(s_base + C::OFF_K + slot * C::K_BYTES + c * (BN * 128), &tm_k, full, c * 64,
+                                          prm.kperm, s * BN, wi.h, wi.b, pol_kv);
+                    if (has_v)
+                        for (int c = 0; c < C::VCH; ++c)
+                            tma_load_rows(s_base + C::OFF_V + slot * C::V_BYTES + c * (BN * 128), &tm_v, full, c * 64,
+                                          prm.vperm, (s - 1) * BN, wi.h, wi.b, pol_kv);
+                    return true;
+                };
+                // the first key tile may load before the previous item's last S MMA
+                // frees the query tiles
+                ok = load_stage(0);
+                if (ok && it > 0 && !wait_or_abort(smem_addr(&bars.q_empty), (uint32_t)((it - 1) & 1), limit, &abort_flag))
+                    ok = false;
+                if (ok) {
+                    for (int t = 0; t < 2; ++t) {
+                        const uint32_t bar = smem_addr(&bars.q_full[t]);
+                        mbar_arrive_expect_tx(bar, C::Q_BYTES);
+                        for (int c = 0; c < C::QCH; ++c)
+                            tma_load_rows(s_base + C::OFF_Q + t * C::Q_BYTES + c * (BM * 128), &tm_q, bar, c * 64,
+                                          prm.qperm, wi.qrow0 + t * BM, wi.h, wi.b, pol_q);
+                    }
+                    q_items = it + 1;
+                }
+                for (int s = 1; ok && s <= wi.n1; ++s) ok = load_stage(s);
             }
             if (!ok) {
                 if (!abort_flag) raise_error(ERR_WAIT_TMA, &abort_flag);
             }
             // Before the CTA exits, every load issued must have landed.
             if (abort_flag) {
-                for (int s = max(0, issued - C::KVS); s < issued; ++s) {
-                    if (s == prm.skip_load && s < n1) continue;
-                    const uint32_t full = smem_addr(&bars.kv_full[s % C::KVS]);
-                    if (!mbar_wait_bounded(full, (uint32_t)((s / C::KVS) & 1), limit)) atomicOr(&g_tc_error_word, ERR_DRAIN);
+                for (int p = max(0, g - C::KVS); p < g; ++p) {
+                    if (p == skipped) continue;
+                    const uint32_t full = smem_addr(&bars.kv_full[p % C::KVS]);
+                    if (!mbar_wait_bounded(full, (uint32_t)((p / C::KVS) & 1), limit)) atomicOr(&g_tc_error_word, ERR_DRAIN);
                 }
-                for (int t = 0; t < q_issued; ++t)
-                    if (!mbar_wait_bounded(smem_addr(&bars.q_full[t]), 0, limit)) atomicOr(&g_tc_error_word, ERR_DRAIN);
+                if (q_items > 0)
+                    for (int t = 0; t < 2; ++t)
+                        if (!mbar_wait_bounded(smem_addr(&bars.q_full[t]), (uint32_t)((q_items - 1) & 1), limit))
+                            atomicOr(&g_tc_error_word, ERR_DRAIN);
             }
         }
         __syncwarp();
@@ -335,60 +357,81 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                              (!first || kk > 0) ? 1u : 0u);
                 issued_any = true;
             };
-            // stage 0: K_0
-            if (wait(&bars.q_full[0], 0) && wait(&bars.kv_full[0], 0)) {
-                tc_fence_after();
-                mma_s(0, 0);
-                mma_commit_w(smem_addr(&bars.s_full[0]));
-            }
-            if (wait(&bars.q_full[1], 0)) {
-                tc_fence_after();
-                mma_s(1, 0);
-                mma_commit_w(smem_addr(&bars.s_full[1]));
-                mma_commit_w(smem_addr(&bars.kv_empty[0]));
-            }
-            // iteration j reads stage j (K_j, V_(j-1)): P_t V_(j-1), then S_t = Q_t K_j^T
-            int slot = 0;
-            uint32_t phase = 0;
-            for (int j = 1; ok && j < n1; ++j) {
-                if (++slot == C::KVS) { slot = 0; phase ^= 1u; }
-                if (!wait(&bars.kv_full[slot], phase)) break;
-                const uint32_t pp = (uint32_t)((j - 1) & 1);
-                // tile 0
-                if (j <= n0) {
-                    if (!wait(&bars.p_full[0], pp)) break;
+            int slot = 0;            // ring slot of the current stage
+            uint32_t phase = 0;      // its fill parity
+            auto next_stage = [&]() {
+                if (++slot == C::KVS) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+            };
+            uint32_t pp[2] = {0u, 0u};  // p_full waits so far, per tile
+            for (int w = blockIdx.x, it = 0; ok && w < prm.n_items; w += gridDim.x, ++it) {
+                const Item wi = item_of<CAUSAL>(prm, w);
+                const int n0 = wi.n0, n1 = wi.n1;
+                // the first P_t V product of an item overwrites O_t: the previous
+                // item's epilogue must have read it
+                auto o_free = [&](int t) -> bool { return it == 0 || wait(&bars.o_empty[t], (uint32_t)((it - 1) & 1)); };
+                auto p_ready = [&](int t) -> bool {
+                    const bool r = wait(&bars.p_full[t], pp[t] & 1u);
+                    ++pp[t];
+                    return r;
+                };
+                // stage 0: K_0
+                if (wait(&bars.q_full[0], (uint32_t)(it & 1)) && wait(&bars.kv_full[slot], phase)) {
                     tc_fence_after();
-                    mma_o(0, slot, j == 1);
-                    if (j < n0) {
-                        mma_s(0, slot);
-                        mma_commit_w(smem_addr(&bars.s_full[0]));
-                    } else {
-                        mma_commit_w(smem_addr(&bars.o_full[0]));
-                    }
+                    mma_s(0, slot);
+                    mma_commit_w(smem_addr(&bars.s_full[0]));
                 }
-                // tile 1
-                if (!wait(&bars.p_full[1], pp)) break;
-                tc_fence_after();
-                mma_o(1, slot, j == 1);
-                mma_s(1, slot);
-                mma_commit_w(smem_addr(&bars.s_full[1]));
-                mma_commit_w(smem_addr(&bars.kv_empty[slot]));
-            }
-            if (ok) {  // stage n1: V of the last key tile
+                if (wait(&bars.q_full[1], (uint32_t)(it & 1))) {
+                    tc_fence_after();
+                    mma_s(1, slot);
+                    mma_commit_w(smem_addr(&bars.s_full[1]));
+                    if (n1 == 1) mma_commit_w(smem_addr(&bars.q_empty));
+                    mma_commit_w(smem_addr(&bars.kv_empty[slot]));
+                }
+                next_stage();
+                // iteration j reads stage j (K_j, V_(j-1)): P_t V_(j-1), then S_t = Q_t K_j^T
+                for (int j = 1; ok && j < n1; ++j) {
+                    if (!wait(&bars.kv_full[slot], phase)) break;
+                    // tile 0
+                    if (j <= n0) {
+                        if (!p_ready(0) || (j == 1 && !o_free(0))) break;
+                        tc_fence_after();
+                        mma_o(0, slot, j == 1);
+                        if (j < n0) {
+                            mma_s(0, slot);
+                            mma_commit_w(smem_addr(&bars.s_full[0]));
+                        } else {
+                            mma_commit_w(smem_addr(&bars.o_full[0]));
+                        }
+                    }
+                    // tile 1
+                    if (!p_ready(1) || (j == 1 && !o_free(1))) break;
+                    tc_fence_after();
+                    mma_o(1, slot, j == 1);
+                    mma_s(1, slot);
+                    mma_commit_w(smem_addr(&bars.s_full[1]));
+                    if (j == n1 - 1) mma_commit_w(smem_addr(&bars.q_empty));  // the item's last S MMA
+                    mma_commit_w(smem_addr(&bars.kv_empty[slot]));
+                    next_stage();
+                }
+                if (!ok) break;
+                // stage n1: V of the last key tile
                 const int last = n1 - 1;
-                const int ls = n1 % C::KVS;
-                if (wait(&bars.kv_full[ls], (uint32_t)((n1 / C::KVS) & 1))) {
-                    if (n0 == n1 && wait(&bars.p_full[0], (uint32_t)(last & 1))) {
-                        tc_fence_after();
-                        mma_o(0, ls, last == 0);
-                        mma_commit_w(smem_addr(&bars.o_full[0]));
-                    }
-                    if (wait(&bars.p_full[1], (uint32_t)(last & 1))) {
-                        tc_fence_after();
-                        mma_o(1, ls, last == 0);
-                        mma_commit_w(smem_addr(&bars.o_full[1]));
-                    }
+                if (!wait(&bars.kv_full[slot], phase)) break;
+                if (n0 == n1) {
+                    if (!p_ready(0) || (last == 0 && !o_free(0))) break;
+                    tc_fence_after();
+                    mma_o(0, slot, last == 0);
+                    mma_commit_w(smem_addr(&bars.o_full[0]));
                 }
+                if (!p_ready(1) || (last == 0 && !o_free(1))) break;
+                tc_fence_after();
+                mma_o(1, slot, last == 0);
+                mma_commit_w(smem_addr(&bars.o_full[1]));
+                mma_commit_w(smem_addr(&bars.kv_empty[slot]));
+                next_stage();
             }
             if (!ok && issued_any) {
                 // every MMA issued so far must finish before tensor memory is freed
@@ -400,168 +443,136 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         __syncwarp();
     } else {
         // ================================================================ softmax + epilogue
-        // RH threads per query row: warps w, w + 8, ... read the same
-        // tensor-memory lanes (lane quarter w % 4) and take consecutive
-        // HC-column slices of the row's keys.  They agree on the row maximum
-        // through shared memory and a per-pair mbarrier; l and dq stay partial
-        // until the epilogue.
-        const int rh = warp >> 3;               // which slice of the row
-        const int t = (warp >> 2) & 1;          // query tile 0 or 1
-        const int quarter = warp & 3;           // tensor-memory lanes 32*quarter ...
+        const int t = warp >> 2;          // query tile 0 or 1
+        const int quarter = warp & 3;     // tensor-memory lanes 32*quarter ...
         const int r = quarter * 32 + lane;
-        const int grow = qrow0 + t * BM + r;    // global query row of this thread
-        const int n_t = t == 0 ? n0 : n1;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t tS = lane_base + t * 128 + rh * HC;        // this slice of S_t (fp32)
-        const uint32_t tP = lane_base + t * 128 + rh * (HC / 2);  // its weights, bf16 pairs
-        constexpr int OC = DV / RH;                               // output columns per thread
-        const uint32_t tO = lane_base + C::COL_O + t * DV + rh * OC;
-        const uint32_t pair_bar = smem_addr(&bars.pair[t * 4 + quarter]);
+        const uint32_t tS = lane_base + t * 128;
+        const uint32_t tO = lane_base + C::COL_O + t * DV;
         const float sl = prm.scale_log2;
-        float m = -INFINITY;  // running maximum, log2 units
-        float l = 0.f;        // running denominator of this slice (exact weights): LSE
-        float dq = 0.f;       // bf16 rounding of each tile's largest weight: O / (l + dq)
+        uint32_t sp = 0;                  // s_full waits so far
         bool ok = true;
         auto fail = [&]() {
             ok = false;
             if (!abort_flag) raise_error(ERR_WAIT_SOFTMAX, &abort_flag);
             else atomicOr(&g_tc_error_word, ERR_WAIT_SOFTMAX);
         };
-        for (int j = 0; j < n_t; ++j) {
-            if (!wait_or_abort(smem_addr(&bars.s_full[t]), (uint32_t)(j & 1), limit, &abort_flag)) {
+        for (int w = blockIdx.x, it = 0; ok && w < prm.n_items; w += gridDim.x, ++it) {
+            const Item wi = item_of<CAUSAL>(prm, w);
+            const int grow = wi.qrow0 + t * BM + r;  // global query row of this thread
+            const int n_t = t == 0 ? wi.n0 : wi.n1;
+            float m = -INFINITY;  // running maximum, log2 units
+            float l = 0.f;        // running denominator (exact weights): LSE
+            float dq = 0.f;       // bf16 rounding of each tile's largest weight: O / (l + dq)
+            for (int j = 0; j < n_t; ++j) {
+                if (!wait_or_abort(smem_addr(&bars.s_full[t]), sp & 1u, limit, &abort_flag)) {
+                    fail();
+                    break;
+                }
+                ++sp;
+                tc_fence_after();
+                float s[BN];
+                {
+                    uint32_t raw[BN];
+                    tmem_ld128(tS, raw);
+#pragma unroll
+                    for (int x = 0; x < BN; ++x) s[x] = __uint_as_float(raw[x]);
+                }
+                const int kv0 = j * BN;
+                int lim = Nk - kv0;                         // keys >= Nk are padding
+                if (CAUSAL) lim = min(lim, grow - kv0 + 1);  // keys after this query
+                if (lim < BN) {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c)
+                        if (c >= lim) s[c] = -INFINITY;
+                }
+                const float mx = row_max<BN>(s);
+                const float m_tile = mx * sl;
+                // Lazy rescaling: the reference maximum m moves only when the tile's
+                // maximum exceeds it by more than RESCALE_LOG2 (weights then stay
+                // below 2^RESCALE_LOG2).  Softmax is invariant to the shift, so O / l
+                // and m + log2 l are unchanged; alpha is 1 on most tiles.
+                float alpha = 1.f;
+                if (m_tile > m + RESCALE_LOG2) {
+                    alpha = ex2(m - m_tile);  // 0 on the first tile (m = -inf)
+                    m = m_tile;
+                }
+                const float base = (m == -INFINITY) ? 0.f : m;  // a row with no key yet
+                const uint64_t sl2 = f2_pack(sl, sl), nb2 = f2_pack(-base, -base);
+                uint64_t rs2[2] = {0ull, 0ull};
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        float a0, a1;
+                        f2_unpack(f2_fma(f2_pack(s[c * 32 + 2 * x], s[c * 32 + 2 * x + 1]), sl2, nb2), a0, a1);
+                        const float p0 = ex2(a0), p1 = ex2(a1);
+                        pk[x] = pack_bf16x2(p0, p1);
+                        rs2[x & 1] = f2_add(rs2[x & 1], f2_pack(p0, p1));
+                    }
+                    tmem_st16(tS + c * 16, pk);
+                }
+                float r0, r1;
+                f2_unpack(f2_add(rs2[0], rs2[1]), r0, r1);
+                l = l * alpha + (r0 + r1);
+                // The P V product sees bf16 weights.  The largest weight of the
+                // tile dominates a peaked row, so the normaliser of O gets that
+                // weight's rounding error added: O's numerator and denominator then
+                // agree on the terms that matter (the same FFMA and ex2 as above,
+                // so p_top is bit-identical to that element's weight).
+                const float p_top = ex2(fmaf(mx, sl, -base));
+                dq = dq * alpha + (__uint_as_float(pack_bf16x2(p_top, 0.f) << 16) - p_top);
+                // O_t already holds every earlier P V product of this item: the
+                // commit that signalled this S tile covers all MMAs issued before it.
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+                    for (int c = 0; c < DV / 32; ++c) {
+                        uint32_t raw[32];
+                        tmem_ld32(tO + c * 32, raw);
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) {
+                            float o0, o1;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(raw[2 * x]), __uint_as_float(raw[2 * x + 1])), a2), o0, o1);
+                            raw[2 * x] = __float_as_uint(o0);
+                            raw[2 * x + 1] = __float_as_uint(o1);
+                        }
+                        tmem_st32(tO + c * 32, raw);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(smem_addr(&bars.p_full[t]));
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l, LSE.  O_t is read whole, then released to the
+            // next item's first P V product before the stores.
+            if (!wait_or_abort(smem_addr(&bars.o_full[t]), (uint32_t)(it & 1), limit, &abort_flag)) {
                 fail();
                 break;
             }
             tc_fence_after();
-            float s[HC];
-            {
-                uint32_t raw[HC];
-                tmem_ld_row(tS, raw);
+            uint32_t ov[DV];
 #pragma unroll
-                for (int x = 0; x < HC; ++x) s[x] = __uint_as_float(raw[x]);
-            }
-            const int kv0 = j * BN + rh * HC;
-            int lim = Nk - kv0;                         // keys >= Nk are padding
-            if (CAUSAL) lim = min(lim, grow - kv0 + 1);  // keys after this query
-            if (lim < HC) {
+            for (int c = 0; c < DV / 32; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(tO + c * 32, raw);
 #pragma unroll
-                for (int c = 0; c < HC; ++c)
-                    if (c >= lim) s[c] = -INFINITY;
+                for (int x = 0; x < 32; ++x) ov[c * 32 + x] = raw[x];
             }
-            const float mh = row_max<HC>(s);
-            float mx = mh, mo = -INFINITY;
-            if constexpr (RH > 1) {
-                xch_max[j & 1][t][rh][r] = mh;
-                mbar_arrive(pair_bar);
-                if (!wait_or_abort(pair_bar, (uint32_t)(j & 1), limit, &abort_flag)) {
-                    fail();
-                    break;
-                }
-#pragma unroll
-                for (int o = 0; o < RH; ++o)
-                    if (o != rh) mo = fmaxf(mo, xch_max[j & 1][t][o][r]);
-                mx = fmaxf(mh, mo);
-            }
-            const float m_tile = mx * sl;
-            // Lazy rescaling: the reference maximum m moves only when the tile's
-            // maximum exceeds it by more than RESCALE_LOG2 (weights then stay
-            // below 2^RESCALE_LOG2).  Softmax is invariant to the shift, so O / l
-            // and m + log2 l are unchanged; alpha is 1 on most tiles.  Every
-            // thread of the row sees the same mx, so all take the same steps.
-            float alpha = 1.f;
-            if (m_tile > m + RESCALE_LOG2) {
-                alpha = ex2(m - m_tile);  // 0 on the first tile (m = -inf)
-                m = m_tile;
-            }
-            const float base = (m == -INFINITY) ? 0.f : m;  // a row with no key yet
-            const uint64_t sl2 = f2_pack(sl, sl), nb2 = f2_pack(-base, -base);
-            uint64_t rs2[2] = {0ull, 0ull};
-#pragma unroll
-            for (int c = 0; c < HC / 32; ++c) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    float a0, a1;
-                    f2_unpack(f2_fma(f2_pack(s[c * 32 + 2 * x], s[c * 32 + 2 * x + 1]), sl2, nb2), a0, a1);
-                    const float p0 = ex2(a0), p1 = ex2(a1);
-                    pk[x] = pack_bf16x2(p0, p1);
-                    rs2[x & 1] = f2_add(rs2[x & 1], f2_pack(p0, p1));
-                }
-                tmem_st16(tP + c * 16, pk);
-            }
-            float r0, r1;
-            f2_unpack(f2_add(rs2[0], rs2[1]), r0, r1);
-            l = l * alpha + (r0 + r1);
-            // The P V product sees bf16 weights.  The largest weight of the
-            // tile dominates a peaked row, so the normaliser of O gets that
-            // weight's rounding error added: O's numerator and denominator then
-            // agree on the terms that matter (the same FFMA and ex2 as above,
-            // so p_top is bit-identical to that element's weight).  The slice
-            // holding the row maximum adds it (the lowest such slice on a tie).
-            float corr = 0.f;
-            if (mh == mx && (rh == 0 || mo != mx)) {
-                const float p_top = ex2(fmaf(mx, sl, -base));
-                corr = __uint_as_float(pack_bf16x2(p_top, 0.f) << 16) - p_top;
-            }
-            dq = dq * alpha + corr;
-            // O_t already holds every earlier P V product: the commit that
-            // signalled this S tile covers all MMAs issued before it.
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
-                for (int c = 0; c < OC / 32; ++c) {
-                    uint32_t raw[32];
-                    tmem_ld32(tO + c * 32, raw);
-#pragma unroll
-                    for (int x = 0; x < 16; ++x) {
-                        float o0, o1;
-                        f2_unpack(f2_mul(f2_pack(__uint_as_float(raw[2 * x]), __uint_as_float(raw[2 * x + 1])), a2), o0, o1);
-                        raw[2 * x] = __float_as_uint(o0);
-                        raw[2 * x + 1] = __float_as_uint(o1);
-                    }
-                    tmem_st32(tO + c * 32, raw);
-                }
-            }
-            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(smem_addr(&bars.p_full[t]));
-        }
-        // ---- epilogue: O / l, LSE
-        if (ok && wait_or_abort(smem_addr(&bars.o_full[t]), 0, limit, &abort_flag)) {
-            tc_fence_after();
-            float lt = l, dqt = dq;
-            if constexpr (RH > 1) {
-                xch_l[t][rh][r] = make_float2(l, dq);
-                mbar_arrive(pair_bar);
-                if (!wait_or_abort(pair_bar, (uint32_t)(n_t & 1), limit, &abort_flag)) {
-                    fail();
-                } else {
+            mbar_arrive(smem_addr(&bars.o_empty[t]));
+            const float inv_l = 1.f / (l + dq);
+            const size_t row_elem = (size_t)(wi.b * prm.os_b + wi.h * prm.os_h + (int64_t)grow * prm.os_n);
 #pragma unroll
-                    for (int o = 0; o < RH; ++o)
-                        if (o != rh) {
-                            const float2 x = xch_l[t][o][r];
-                            lt += x.x;
-                            dqt += x.y;
-                        }
-                }
+            for (int c = 0; c < DV / 32; ++c) {
+                float vals[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) vals[x] = __uint_as_float(ov[c * 32 + x]) * inv_l;
+                if (grow < N) store_o_row(prm.o, prm.o_fp32, row_elem, vals, c * 32, 32);
             }
-            if (ok) {
-                const float inv_l = 1.f / (lt + dqt);
-                const size_t row_elem = (size_t)(b * prm.os_b + h * prm.os_h + (int64_t)grow * prm.os_n);
-#pragma unroll
-                for (int c = 0; c < OC / 32; ++c) {
-                    uint32_t raw[32];
-                    tmem_ld32(tO + c * 32, raw);
-                    float vals[32];
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) vals[x] = __uint_as_float(raw[x]) * inv_l;
-                    if (grow < N) store_o_row(prm.o, prm.o_fp32, row_elem, vals, rh * OC + c * 32, 32);
-                }
-                if (rh == 0 && prm.lse && grow < N)
-                    prm.lse[(size_t)bh * N + grow] = (m + log2f(lt)) * 0.69314718055994530942f;
-            }
-        } else if (ok) {
-            fail();
+            if (prm.lse && grow < N) prm.lse[(size_t)wi.bh * N + grow] = (m + log2f(l)) * 0.69314718055994530942f;
         }
     }
 
@@ -642,6 +653,7 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     prm.H = (int)p.H;
     prm.BH = (int)BH;
     prm.n_qblocks = (int)((p.N + 2 * BM - 1) / (2 * BM));
+    prm.n_items = (int)(prm.n_qblocks * BH);
     prm.n_kv = (int)((Nk + BN - 1) / BN);
     prm.scale_log2 = p.scale * 1.4426950408889634f;
     prm.causal = CAUSAL;
@@ -658,7 +670,19 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     auto kern = fa_tc_kernel<DK, DV, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int64_t grid = (int64_t)prm.n_qblocks * BH;
+    // Short items (few key tiles, no mask): one persistent CTA per SM loops over
+    // them, so an item's prologue (query loads, first S MMA) and epilogue overlap
+    // its neighbours' work.  Long items gain nothing from that, and items of
+    // unequal cost (causal) balance better one per CTA, handed out by the
+    // hardware as SMs free up (measured on the multi-head, peaked and causal
+    // workloads: +2.5 %, -2.4 %, -6 % for persistence).
+    int grid = prm.n_items;
+    if (!CAUSAL && prm.n_kv <= 64) {
+        int dev = 0, sms = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        grid = (int)std::min<int64_t>((int64_t)prm.n_items, (int64_t)std::max(sms, 1));
+    }
     kern<<<(unsigned)grid, NUM_THREADS, Cf::SMEM_BYTES, stream>>>(mq, mk, mv, prm);
     return cudaGetLastError();
 }
