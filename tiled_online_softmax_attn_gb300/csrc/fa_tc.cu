@@ -10,7 +10,7 @@
 // each weight is one FFMA and one ex2.
 //
 // A work item is two 128-row query tiles (Q0, Q1) of one (batch, head); a CTA
-// processes one item, or (short items) loops over items c, c + gridDim.x, ...
+// processes one item, or (short items) loops over items in rounds (item_index)
 // with one CTA per SM.  It streams the head's K/V tiles (128 keys) through a
 // shared-memory ring:
 //
@@ -45,6 +45,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -102,7 +103,7 @@ struct Params {
     int H;             // heads
     int BH;            // batch * heads
     int n_qblocks;     // work items per head (256 query rows each)
-    int n_items;       // n_qblocks * BH; CTA c takes items c, c + gridDim.x, ...
+    int n_items;       // n_qblocks * BH; see item_index for the CTA -> item order
     int n_kv;          // key tiles per head
     float scale_log2;  // scale * log2(e), > 0
     int causal;
@@ -130,6 +131,18 @@ struct Item {
     int qrow0;   // first row of Q0; Q1 starts BM later
     int n0, n1;  // key tiles each query tile needs: all, or up to its diagonal under the mask
 };
+
+// Item of this CTA's round `it`: rounds alternate direction over the CTAs
+// (c, then G - 1 - c, ...), so with items sorted longest first (causal) every
+// CTA's total stays close to the mean.  Increasing in `it`.
+// Without persistence a CTA takes the single item blockIdx.x.
+template <bool PERSIST>
+__device__ __forceinline__ int item_index(int it)
+{
+    if (!PERSIST) return it == 0 ? (int)blockIdx.x : INT_MAX;
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    return it * G + ((it & 1) ? G - 1 - c : c);
+}
 
 template <bool CAUSAL>
 __device__ __forceinline__ Item item_of(const Params &prm, int w)
@@ -192,7 +205,7 @@ __device__ __forceinline__ void store_o_row(void *o, int o_fp32, size_t row_elem
     }
 }
 
-template <int DK, int DV, bool CAUSAL>
+template <int DK, int DV, bool CAUSAL, bool PERSIST>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const Params prm)
@@ -249,7 +262,9 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             int q_items = 0;               // items whose Q loads were issued
             int skipped = -1;              // ring position of the injected, never-filled stage
             bool ok = true;
-            for (int w = blockIdx.x, it = 0; ok && w < prm.n_items; w += gridDim.x, ++it) {
+            for (int it = 0; ok; ++it) {
+                const int w = item_index<PERSIST>(it);
+                if (w >= prm.n_items) break;
                 const Item wi = item_of<CAUSAL>(prm, w);
                 // stage s of the item = K_s (s < n1) and V_(s-1) (s >= 1), s = 0 .. n1
                 auto load_stage = [&](int s) -> bool {
@@ -366,7 +381,9 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 }
             };
             uint32_t pp[2] = {0u, 0u};  // p_full waits so far, per tile
-            for (int w = blockIdx.x, it = 0; ok && w < prm.n_items; w += gridDim.x, ++it) {
+            for (int it = 0; ok; ++it) {
+                const int w = item_index<PERSIST>(it);
+                if (w >= prm.n_items) break;
                 const Item wi = item_of<CAUSAL>(prm, w);
                 const int n0 = wi.n0, n1 = wi.n1;
                 // the first P_t V product of an item overwrites O_t: the previous
@@ -387,7 +404,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     tc_fence_after();
                     mma_s(1, slot);
                     mma_commit_w(smem_addr(&bars.s_full[1]));
-                    if (n1 == 1) mma_commit_w(smem_addr(&bars.q_empty));
+                    if (PERSIST && n1 == 1) mma_commit_w(smem_addr(&bars.q_empty));
                     mma_commit_w(smem_addr(&bars.kv_empty[slot]));
                 }
                 next_stage();
@@ -412,7 +429,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     mma_o(1, slot, j == 1);
                     mma_s(1, slot);
                     mma_commit_w(smem_addr(&bars.s_full[1]));
-                    if (j == n1 - 1) mma_commit_w(smem_addr(&bars.q_empty));  // the item's last S MMA
+                    if (PERSIST && j == n1 - 1) mma_commit_w(smem_addr(&bars.q_empty));  // the item's last S MMA
                     mma_commit_w(smem_addr(&bars.kv_empty[slot]));
                     next_stage();
                 }
@@ -457,7 +474,9 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             if (!abort_flag) raise_error(ERR_WAIT_SOFTMAX, &abort_flag);
             else atomicOr(&g_tc_error_word, ERR_WAIT_SOFTMAX);
         };
-        for (int w = blockIdx.x, it = 0; ok && w < prm.n_items; w += gridDim.x, ++it) {
+        for (int it = 0; ok; ++it) {
+            const int w = item_index<PERSIST>(it);
+            if (w >= prm.n_items) break;
             const Item wi = item_of<CAUSAL>(prm, w);
             const int grow = wi.qrow0 + t * BM + r;  // global query row of this thread
             const int n_t = t == 0 ? wi.n0 : wi.n1;
@@ -553,24 +572,36 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 break;
             }
             tc_fence_after();
-            uint32_t ov[DV];
-#pragma unroll
-            for (int c = 0; c < DV / 32; ++c) {
-                uint32_t raw[32];
-                tmem_ld32(tO + c * 32, raw);
-#pragma unroll
-                for (int x = 0; x < 32; ++x) ov[c * 32 + x] = raw[x];
-            }
-            tc_fence_before();
-            mbar_arrive(smem_addr(&bars.o_empty[t]));
             const float inv_l = 1.f / (l + dq);
             const size_t row_elem = (size_t)(wi.b * prm.os_b + wi.h * prm.os_h + (int64_t)grow * prm.os_n);
+            if (PERSIST) {
+                uint32_t ov[DV];
 #pragma unroll
-            for (int c = 0; c < DV / 32; ++c) {
-                float vals[32];
+                for (int c = 0; c < DV / 32; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(tO + c * 32, raw);
 #pragma unroll
-                for (int x = 0; x < 32; ++x) vals[x] = __uint_as_float(ov[c * 32 + x]) * inv_l;
-                if (grow < N) store_o_row(prm.o, prm.o_fp32, row_elem, vals, c * 32, 32);
+                    for (int x = 0; x < 32; ++x) ov[c * 32 + x] = raw[x];
+                }
+                tc_fence_before();
+                mbar_arrive(smem_addr(&bars.o_empty[t]));
+#pragma unroll
+                for (int c = 0; c < DV / 32; ++c) {
+                    float vals[32];
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) vals[x] = __uint_as_float(ov[c * 32 + x]) * inv_l;
+                    if (grow < N) store_o_row(prm.o, prm.o_fp32, row_elem, vals, c * 32, 32);
+                }
+            } else {  // the only item of the CTA: no one waits for O
+#pragma unroll
+                for (int c = 0; c < DV / 32; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(tO + c * 32, raw);
+                    float vals[32];
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) vals[x] = __uint_as_float(raw[x]) * inv_l;
+                    if (grow < N) store_o_row(prm.o, prm.o_fp32, row_elem, vals, c * 32, 32);
+                }
             }
             if (prm.lse && grow < N) prm.lse[(size_t)wi.bh * N + grow] = (m + log2f(l)) * 0.69314718055994530942f;
         }
@@ -667,17 +698,19 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     prm.os_n = so[2];
     prm.lse = p.lse;
     prm.o_fp32 = p.o_dtype == 1;
-    auto kern = fa_tc_kernel<DK, DV, CAUSAL>;
+    // Short unmasked items (64 key tiles or fewer): one persistent CTA per SM
+    // loops over them, so an item's prologue (query loads, first S MMA) and
+    // epilogue overlap its neighbours' work (multi-head workload +2.5 %).  Long
+    // items gain nothing from that, and items of unequal cost (causal) balance
+    // best one per CTA, handed out by the hardware as SMs free up (measured:
+    // persistence with alternating-direction rounds gave the causal workload
+    // -1 %, the peaked one -2 %).
+    const bool persist = !CAUSAL && prm.n_kv <= 64;
+    auto kern = persist ? fa_tc_kernel<DK, DV, CAUSAL, true> : fa_tc_kernel<DK, DV, CAUSAL, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    // Short items (few key tiles, no mask): one persistent CTA per SM loops over
-    // them, so an item's prologue (query loads, first S MMA) and epilogue overlap
-    // its neighbours' work.  Long items gain nothing from that, and items of
-    // unequal cost (causal) balance better one per CTA, handed out by the
-    // hardware as SMs free up (measured on the multi-head, peaked and causal
-    // workloads: +2.5 %, -2.4 %, -6 % for persistence).
     int grid = prm.n_items;
-    if (!CAUSAL && prm.n_kv <= 64) {
+    if (persist) {
         int dev = 0, sms = 0;
         if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
