@@ -120,7 +120,7 @@ struct __align__(8) Barriers {
     uint64_t q_full[2], q_empty;      // query tiles of an item; free after its last S MMA
     uint64_t kv_full[3], kv_empty[3];
     uint64_t s_full[2];
-    uint64_t p_full[2];
+    uint64_t p_half[2], p_full[2];    // P_t keys [0, 64) written / all of P_t written
     uint64_t o_full[2], o_empty[2];   // O_t complete / read by the epilogue
     uint64_t drain;
 };
@@ -228,6 +228,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_addr(&bars.q_full[t]), 1);
             mbar_init(smem_addr(&bars.s_full[t]), 1);
+            mbar_init(smem_addr(&bars.p_half[t]), 128);
             mbar_init(smem_addr(&bars.p_full[t]), 128);
             mbar_init(smem_addr(&bars.o_full[t]), 1);
             mbar_init(smem_addr(&bars.o_empty[t]), 128);
@@ -363,11 +364,13 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             };
             // O_t += P_t V from ring slot `slot` (M = 128 rows, N = D, K = 128 keys in steps of 16);
             // `first` starts the accumulator (key tile 0)
-            auto mma_o = [&](int t, int slot, bool first) {
+            // `h` selects keys [64 h, 64 h + 64): the first half starts while the
+            // softmax warps still compute the second
+            auto mma_o = [&](int t, int slot, bool first, int h) {
                 const uint64_t v = dv0 + (uint64_t)slot * V_STEP;
                 const uint32_t d_o = tmem + C::COL_O + t * DV, a_p = tmem + t * 128;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
+                for (int kk = 4 * h; kk < 4 * h + BN / 32; ++kk)
                     mma_ts_w(d_o, a_p + kk * 8, v + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
                              (!first || kk > 0) ? 1u : 0u);
                 issued_any = true;
@@ -389,10 +392,17 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 // the first P_t V product of an item overwrites O_t: the previous
                 // item's epilogue must have read it
                 auto o_free = [&](int t) -> bool { return it == 0 || wait(&bars.o_empty[t], (uint32_t)((it - 1) & 1)); };
-                auto p_ready = [&](int t) -> bool {
-                    const bool r = wait(&bars.p_full[t], pp[t] & 1u);
+                // O_t += P_t V in two halves, each once its half of P_t is written
+                auto pv = [&](int t, int slot, bool first) -> bool {
+                    const uint32_t par = pp[t] & 1u;
                     ++pp[t];
-                    return r;
+                    if (!wait(&bars.p_half[t], par) || (first && !o_free(t))) return false;
+                    tc_fence_after();
+                    mma_o(t, slot, first, 0);
+                    if (!wait(&bars.p_full[t], par)) return false;
+                    tc_fence_after();
+                    mma_o(t, slot, first, 1);
+                    return true;
                 };
                 // stage 0: K_0
                 if (wait(&bars.q_full[0], (uint32_t)(it & 1)) && wait(&bars.kv_full[slot], phase)) {
@@ -413,9 +423,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     if (!wait(&bars.kv_full[slot], phase)) break;
                     // tile 0
                     if (j <= n0) {
-                        if (!p_ready(0) || (j == 1 && !o_free(0))) break;
-                        tc_fence_after();
-                        mma_o(0, slot, j == 1);
+                        if (!pv(0, slot, j == 1)) break;
                         if (j < n0) {
                             mma_s(0, slot);
                             mma_commit_w(smem_addr(&bars.s_full[0]));
@@ -424,9 +432,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         }
                     }
                     // tile 1
-                    if (!p_ready(1) || (j == 1 && !o_free(1))) break;
-                    tc_fence_after();
-                    mma_o(1, slot, j == 1);
+                    if (!pv(1, slot, j == 1)) break;
                     mma_s(1, slot);
                     mma_commit_w(smem_addr(&bars.s_full[1]));
                     if (PERSIST && j == n1 - 1) mma_commit_w(smem_addr(&bars.q_empty));  // the item's last S MMA
@@ -438,14 +444,10 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 const int last = n1 - 1;
                 if (!wait(&bars.kv_full[slot], phase)) break;
                 if (n0 == n1) {
-                    if (!p_ready(0) || (last == 0 && !o_free(0))) break;
-                    tc_fence_after();
-                    mma_o(0, slot, last == 0);
+                    if (!pv(0, slot, last == 0)) break;
                     mma_commit_w(smem_addr(&bars.o_full[0]));
                 }
-                if (!p_ready(1) || (last == 0 && !o_free(1))) break;
-                tc_fence_after();
-                mma_o(1, slot, last == 0);
+                if (!pv(1, slot, last == 0)) break;
                 mma_commit_w(smem_addr(&bars.o_full[1]));
                 mma_commit_w(smem_addr(&bars.kv_empty[slot]));
                 next_stage();
@@ -516,6 +518,25 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     alpha = ex2(m - m_tile);  // 0 on the first tile (m = -inf)
                     m = m_tile;
                 }
+                // O_t already holds every earlier P V product of this item (the
+                // commit that signalled this S tile covers all MMAs issued before
+                // it); rescale it before any P V product of this tile is released.
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+                    for (int c = 0; c < DV / 16; ++c) {  // 16 columns at a time: the scores are live
+                        uint32_t raw[16];
+                        tmem_ld16(tO + c * 16, raw);
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) {
+                            float o0, o1;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(raw[2 * x]), __uint_as_float(raw[2 * x + 1])), a2), o0, o1);
+                            raw[2 * x] = __float_as_uint(o0);
+                            raw[2 * x + 1] = __float_as_uint(o1);
+                        }
+                        tmem_st16(tO + c * 16, raw);
+                    }
+                }
                 const float base = (m == -INFINITY) ? 0.f : m;  // a row with no key yet
                 const uint64_t sl2 = f2_pack(sl, sl), nb2 = f2_pack(-base, -base);
                 uint64_t rs2[2] = {0ull, 0ull};
@@ -531,6 +552,11 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         rs2[x & 1] = f2_add(rs2[x & 1], f2_pack(p0, p1));
                     }
                     tmem_st16(tS + c * 16, pk);
+                    if (c == BN / 64 - 1) {  // keys [0, 64) written: the first half of P V may start
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(smem_addr(&bars.p_half[t]));
+                    }
                 }
                 float r0, r1;
                 f2_unpack(f2_add(rs2[0], rs2[1]), r0, r1);
@@ -542,24 +568,6 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 // so p_top is bit-identical to that element's weight).
                 const float p_top = ex2(fmaf(mx, sl, -base));
                 dq = dq * alpha + (__uint_as_float(pack_bf16x2(p_top, 0.f) << 16) - p_top);
-                // O_t already holds every earlier P V product of this item: the
-                // commit that signalled this S tile covers all MMAs issued before it.
-                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                    const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
-                    for (int c = 0; c < DV / 32; ++c) {
-                        uint32_t raw[32];
-                        tmem_ld32(tO + c * 32, raw);
-#pragma unroll
-                        for (int x = 0; x < 16; ++x) {
-                            float o0, o1;
-                            f2_unpack(f2_mul(f2_pack(__uint_as_float(raw[2 * x]), __uint_as_float(raw[2 * x + 1])), a2), o0, o1);
-                            raw[2 * x] = __float_as_uint(o0);
-                            raw[2 * x + 1] = __float_as_uint(o1);
-                        }
-                        tmem_st32(tO + c * 32, raw);
-                    }
-                }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(smem_addr(&bars.p_full[t]));
