@@ -71,6 +71,8 @@ constexpr int MMA_WARP = 9;
 constexpr int NUM_THREADS = 320;  // 10 warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;  // lazy-rescale threshold, log2 units
+constexpr int P_PARTS = 2;            // P_t is released to the P V product in this many key slices
+                                      // (two halves: +3-5 %; four quarters measured 8 % slower than halves)
 
 // error word bits
 constexpr uint32_t ERR_WAIT_TMA = 1u;       // producer gave up waiting for a free slot
@@ -120,7 +122,7 @@ struct __align__(8) Barriers {
     uint64_t q_full[2], q_empty;      // query tiles of an item; free after its last S MMA
     uint64_t kv_full[3], kv_empty[3];
     uint64_t s_full[2];
-    uint64_t p_half[2], p_full[2];    // P_t keys [0, 64) written / all of P_t written
+    uint64_t p_part[2][P_PARTS];      // P_t keys [0, (k + 1) BN / P_PARTS) written
     uint64_t o_full[2], o_empty[2];   // O_t complete / read by the epilogue
     uint64_t drain;
 };
@@ -228,8 +230,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_addr(&bars.q_full[t]), 1);
             mbar_init(smem_addr(&bars.s_full[t]), 1);
-            mbar_init(smem_addr(&bars.p_half[t]), 128);
-            mbar_init(smem_addr(&bars.p_full[t]), 128);
+            for (int k = 0; k < P_PARTS; ++k) mbar_init(smem_addr(&bars.p_part[t][k]), 128);
             mbar_init(smem_addr(&bars.o_full[t]), 1);
             mbar_init(smem_addr(&bars.o_empty[t]), 128);
         }
@@ -364,13 +365,14 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             };
             // O_t += P_t V from ring slot `slot` (M = 128 rows, N = D, K = 128 keys in steps of 16);
             // `first` starts the accumulator (key tile 0)
-            // `h` selects keys [64 h, 64 h + 64): the first half starts while the
-            // softmax warps still compute the second
+            // slice `h` of the keys (BN / P_PARTS of them): a slice starts while the
+            // softmax warps still compute the later ones
             auto mma_o = [&](int t, int slot, bool first, int h) {
                 const uint64_t v = dv0 + (uint64_t)slot * V_STEP;
                 const uint32_t d_o = tmem + C::COL_O + t * DV, a_p = tmem + t * 128;
+                constexpr int KS = BN / 16 / P_PARTS;  // K steps per slice
 #pragma unroll
-                for (int kk = 4 * h; kk < 4 * h + BN / 32; ++kk)
+                for (int kk = KS * h; kk < KS * h + KS; ++kk)
                     mma_ts_w(d_o, a_p + kk * 8, v + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
                              (!first || kk > 0) ? 1u : 0u);
                 issued_any = true;
@@ -383,7 +385,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     phase ^= 1u;
                 }
             };
-            uint32_t pp[2] = {0u, 0u};  // p_full waits so far, per tile
+            uint32_t pp[2] = {0u, 0u};  // P releases waited for so far, per tile
             for (int it = 0; ok; ++it) {
                 const int w = item_index<PERSIST>(it);
                 if (w >= prm.n_items) break;
@@ -392,16 +394,16 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 // the first P_t V product of an item overwrites O_t: the previous
                 // item's epilogue must have read it
                 auto o_free = [&](int t) -> bool { return it == 0 || wait(&bars.o_empty[t], (uint32_t)((it - 1) & 1)); };
-                // O_t += P_t V in two halves, each once its half of P_t is written
+                // O_t += P_t V slice by slice, each once its slice of P_t is written
                 auto pv = [&](int t, int slot, bool first) -> bool {
                     const uint32_t par = pp[t] & 1u;
                     ++pp[t];
-                    if (!wait(&bars.p_half[t], par) || (first && !o_free(t))) return false;
-                    tc_fence_after();
-                    mma_o(t, slot, first, 0);
-                    if (!wait(&bars.p_full[t], par)) return false;
-                    tc_fence_after();
-                    mma_o(t, slot, first, 1);
+#pragma unroll
+                    for (int h = 0; h < P_PARTS; ++h) {
+                        if (!wait(&bars.p_part[t][h], par) || (h == 0 && first && !o_free(t))) return false;
+                        tc_fence_after();
+                        mma_o(t, slot, first, h);
+                    }
                     return true;
                 };
                 // stage 0: K_0
@@ -552,10 +554,11 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         rs2[x & 1] = f2_add(rs2[x & 1], f2_pack(p0, p1));
                     }
                     tmem_st16(tS + c * 16, pk);
-                    if (c == BN / 64 - 1) {  // keys [0, 64) written: the first half of P V may start
+                    constexpr int CPP = BN / 32 / P_PARTS;  // 32-key chunks per slice
+                    if ((c + 1) % CPP == 0 && c + 1 < BN / 32) {  // a slice of P is written: its P V may start
                         tmem_wait_st();
                         tc_fence_before();
-                        mbar_arrive(smem_addr(&bars.p_half[t]));
+                        mbar_arrive(smem_addr(&bars.p_part[t][c / CPP]));
                     }
                 }
                 float r0, r1;
@@ -570,7 +573,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 dq = dq * alpha + (__uint_as_float(pack_bf16x2(p_top, 0.f) << 16) - p_top);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(smem_addr(&bars.p_full[t]));
+                mbar_arrive(smem_addr(&bars.p_part[t][P_PARTS - 1]));
             }
             if (!ok) break;
             // ---- epilogue: O / l, LSE.  O_t is read whole, then released to the
