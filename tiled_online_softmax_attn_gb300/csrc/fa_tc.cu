@@ -97,6 +97,11 @@ struct Cfg {
     static constexpr uint32_t SMEM_TILES = OFF_V + KVS * V_BYTES;
     static constexpr uint32_t SMEM_BYTES = SMEM_TILES + 1024;  // + alignment slack
     static constexpr uint32_t COL_O = 256;                 // O0 at 256, O1 at 256 + DV
+    // DV = 64 leaves 128 tensor-memory columns free: P_t gets columns of its
+    // own (64 packed columns each) instead of overwriting S_t, so S_t(j+1) can
+    // be issued as soon as the softmax warps have read S_t(j)
+    static constexpr bool SEP_P = DV == 64;
+    static constexpr uint32_t COL_P = 256 + 2 * DV;        // P0 at COL_P, P1 at COL_P + 64 (SEP_P)
 };
 
 struct Params {
@@ -123,6 +128,7 @@ struct __align__(8) Barriers {
     uint64_t kv_full[3], kv_empty[3];
     uint64_t s_full[2];
     uint64_t p_part[2][P_PARTS];      // P_t keys [0, (k + 1) BN / P_PARTS) written
+    uint64_t s_read[2], p_free[2];    // SEP_P: S_t read by the softmax warps / P_t read by the P V product
     uint64_t o_full[2], o_empty[2];   // O_t complete / read by the epilogue
     uint64_t drain;
 };
@@ -231,6 +237,8 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             mbar_init(smem_addr(&bars.q_full[t]), 1);
             mbar_init(smem_addr(&bars.s_full[t]), 1);
             for (int k = 0; k < P_PARTS; ++k) mbar_init(smem_addr(&bars.p_part[t][k]), 128);
+            mbar_init(smem_addr(&bars.s_read[t]), 128);
+            mbar_init(smem_addr(&bars.p_free[t]), 1);
             mbar_init(smem_addr(&bars.o_full[t]), 1);
             mbar_init(smem_addr(&bars.o_empty[t]), 128);
         }
@@ -369,7 +377,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             // softmax warps still compute the later ones
             auto mma_o = [&](int t, int slot, bool first, int h) {
                 const uint64_t v = dv0 + (uint64_t)slot * V_STEP;
-                const uint32_t d_o = tmem + C::COL_O + t * DV, a_p = tmem + t * 128;
+                const uint32_t d_o = tmem + C::COL_O + t * DV, a_p = tmem + (C::SEP_P ? C::COL_P + t * 64 : t * 128);
                 constexpr int KS = BN / 16 / P_PARTS;  // K steps per slice
 #pragma unroll
                 for (int kk = KS * h; kk < KS * h + KS; ++kk)
@@ -386,6 +394,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 }
             };
             uint32_t pp[2] = {0u, 0u};  // P releases waited for so far, per tile
+            uint32_t ns[2] = {0u, 0u};  // S_t products issued so far (SEP_P)
             for (int it = 0; ok; ++it) {
                 const int w = item_index<PERSIST>(it);
                 if (w >= prm.n_items) break;
@@ -406,53 +415,105 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     }
                     return true;
                 };
-                // stage 0: K_0
-                if (wait(&bars.q_full[0], (uint32_t)(it & 1)) && wait(&bars.kv_full[slot], phase)) {
-                    tc_fence_after();
-                    mma_s(0, slot);
-                    mma_commit_w(smem_addr(&bars.s_full[0]));
-                }
-                if (wait(&bars.q_full[1], (uint32_t)(it & 1))) {
-                    tc_fence_after();
-                    mma_s(1, slot);
-                    mma_commit_w(smem_addr(&bars.s_full[1]));
-                    if (PERSIST && n1 == 1) mma_commit_w(smem_addr(&bars.q_empty));
-                    mma_commit_w(smem_addr(&bars.kv_empty[slot]));
-                }
-                next_stage();
-                // iteration j reads stage j (K_j, V_(j-1)): P_t V_(j-1), then S_t = Q_t K_j^T
-                for (int j = 1; ok && j < n1; ++j) {
-                    if (!wait(&bars.kv_full[slot], phase)) break;
-                    // tile 0
-                    if (j <= n0) {
-                        if (!pv(0, slot, j == 1)) break;
-                        if (j < n0) {
+                if constexpr (C::SEP_P) {
+                    // Before S_t is overwritten the softmax warps must have read the
+                    // previous S_t (ns[t] S_t products so far over all items).
+                    auto s_free = [&](int t) -> bool {
+                        const bool r = ns[t] == 0 || wait(&bars.s_read[t], (ns[t] - 1) & 1u);
+                        ++ns[t];
+                        return r;
+                    };
+                    // stage 0: K_0
+                    if (wait(&bars.q_full[0], (uint32_t)(it & 1)) && wait(&bars.kv_full[slot], phase) && s_free(0)) {
+                        tc_fence_after();
+                        mma_s(0, slot);
+                        mma_commit_w(smem_addr(&bars.s_full[0]));
+                    }
+                    if (wait(&bars.q_full[1], (uint32_t)(it & 1)) && s_free(1)) {
+                        tc_fence_after();
+                        mma_s(1, slot);
+                        mma_commit_w(smem_addr(&bars.s_full[1]));
+                        if (PERSIST && n1 == 1) mma_commit_w(smem_addr(&bars.q_empty));
+                        mma_commit_w(smem_addr(&bars.kv_empty[slot]));
+                    }
+                    next_stage();
+                    // iteration j reads stage j + 1 (K_(j+1), V_j): S_t(j+1) as soon as
+                    // S_t(j) is read, then P_t(j) V_j
+                    for (int j = 0; ok && j < n1; ++j) {
+                        if (!wait(&bars.kv_full[slot], phase)) break;
+                        if (j + 1 < n0) {
+                            if (!s_free(0)) break;
+                            tc_fence_after();
                             mma_s(0, slot);
                             mma_commit_w(smem_addr(&bars.s_full[0]));
-                        } else {
-                            mma_commit_w(smem_addr(&bars.o_full[0]));
                         }
+                        if (j + 1 < n1) {
+                            if (!s_free(1)) break;
+                            tc_fence_after();
+                            mma_s(1, slot);
+                            mma_commit_w(smem_addr(&bars.s_full[1]));
+                            if (PERSIST && j + 1 == n1 - 1) mma_commit_w(smem_addr(&bars.q_empty));
+                        }
+                        if (j < n0) {
+                            if (!pv(0, slot, j == 0)) break;
+                            mma_commit_w(smem_addr(&bars.p_free[0]));
+                            if (j == n0 - 1) mma_commit_w(smem_addr(&bars.o_full[0]));
+                        }
+                        if (!pv(1, slot, j == 0)) break;
+                        mma_commit_w(smem_addr(&bars.p_free[1]));
+                        if (j == n1 - 1) mma_commit_w(smem_addr(&bars.o_full[1]));
+                        mma_commit_w(smem_addr(&bars.kv_empty[slot]));
+                        next_stage();
                     }
-                    // tile 1
-                    if (!pv(1, slot, j == 1)) break;
-                    mma_s(1, slot);
-                    mma_commit_w(smem_addr(&bars.s_full[1]));
-                    if (PERSIST && j == n1 - 1) mma_commit_w(smem_addr(&bars.q_empty));  // the item's last S MMA
+                } else {
+                    // stage 0: K_0
+                    if (wait(&bars.q_full[0], (uint32_t)(it & 1)) && wait(&bars.kv_full[slot], phase)) {
+                        tc_fence_after();
+                        mma_s(0, slot);
+                        mma_commit_w(smem_addr(&bars.s_full[0]));
+                    }
+                    if (wait(&bars.q_full[1], (uint32_t)(it & 1))) {
+                        tc_fence_after();
+                        mma_s(1, slot);
+                        mma_commit_w(smem_addr(&bars.s_full[1]));
+                        if (PERSIST && n1 == 1) mma_commit_w(smem_addr(&bars.q_empty));
+                        mma_commit_w(smem_addr(&bars.kv_empty[slot]));
+                    }
+                    next_stage();
+                    // iteration j reads stage j (K_j, V_(j-1)): P_t V_(j-1), then S_t = Q_t K_j^T
+                    for (int j = 1; ok && j < n1; ++j) {
+                        if (!wait(&bars.kv_full[slot], phase)) break;
+                        // tile 0
+                        if (j <= n0) {
+                            if (!pv(0, slot, j == 1)) break;
+                            if (j < n0) {
+                                mma_s(0, slot);
+                                mma_commit_w(smem_addr(&bars.s_full[0]));
+                            } else {
+                                mma_commit_w(smem_addr(&bars.o_full[0]));
+                            }
+                        }
+                        // tile 1
+                        if (!pv(1, slot, j == 1)) break;
+                        mma_s(1, slot);
+                        mma_commit_w(smem_addr(&bars.s_full[1]));
+                        if (PERSIST && j == n1 - 1) mma_commit_w(smem_addr(&bars.q_empty));  // the item's last S MMA
+                        mma_commit_w(smem_addr(&bars.kv_empty[slot]));
+                        next_stage();
+                    }
+                    if (!ok) break;
+                    // stage n1: V of the last key tile
+                    const int last = n1 - 1;
+                    if (!wait(&bars.kv_full[slot], phase)) break;
+                    if (n0 == n1) {
+                        if (!pv(0, slot, last == 0)) break;
+                        mma_commit_w(smem_addr(&bars.o_full[0]));
+                    }
+                    if (!pv(1, slot, last == 0)) break;
+                    mma_commit_w(smem_addr(&bars.o_full[1]));
                     mma_commit_w(smem_addr(&bars.kv_empty[slot]));
                     next_stage();
                 }
-                if (!ok) break;
-                // stage n1: V of the last key tile
-                const int last = n1 - 1;
-                if (!wait(&bars.kv_full[slot], phase)) break;
-                if (n0 == n1) {
-                    if (!pv(0, slot, last == 0)) break;
-                    mma_commit_w(smem_addr(&bars.o_full[0]));
-                }
-                if (!pv(1, slot, last == 0)) break;
-                mma_commit_w(smem_addr(&bars.o_full[1]));
-                mma_commit_w(smem_addr(&bars.kv_empty[slot]));
-                next_stage();
             }
             if (!ok && issued_any) {
                 // every MMA issued so far must finish before tensor memory is freed
@@ -470,8 +531,10 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const uint32_t tS = lane_base + t * 128;
         const uint32_t tO = lane_base + C::COL_O + t * DV;
+        const uint32_t tP = C::SEP_P ? lane_base + C::COL_P + t * 64 : tS;  // where P_t goes
         const float sl = prm.scale_log2;
         uint32_t sp = 0;                  // s_full waits so far
+        uint32_t np = 0;                  // P_t tiles written so far (SEP_P: p_free phases)
         bool ok = true;
         auto fail = [&]() {
             ok = false;
@@ -501,6 +564,10 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll
                     for (int x = 0; x < BN; ++x) s[x] = __uint_as_float(raw[x]);
                 }
+                if constexpr (C::SEP_P) {  // S_t is in registers: the next S_t product may start
+                    tc_fence_before();
+                    mbar_arrive(smem_addr(&bars.s_read[t]));
+                }
                 const int kv0 = j * BN;
                 int lim = Nk - kv0;                         // keys >= Nk are padding
                 if (CAUSAL) lim = min(lim, grow - kv0 + 1);  // keys after this query
@@ -522,7 +589,14 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 }
                 // O_t already holds every earlier P V product of this item (the
                 // commit that signalled this S tile covers all MMAs issued before
-                // it); rescale it before any P V product of this tile is released.
+                // it; with P_t in columns of its own, the wait for the previous
+                // P_t's product to finish reading them covers it); rescale it
+                // before any P V product of this tile is released.
+                if (C::SEP_P && np > 0 && !wait_or_abort(smem_addr(&bars.p_free[t]), (np - 1) & 1u, limit, &abort_flag)) {
+                    fail();
+                    break;
+                }
+                ++np;
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                     const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
@@ -553,7 +627,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         pk[x] = pack_bf16x2(p0, p1);
                         rs2[x & 1] = f2_add(rs2[x & 1], f2_pack(p0, p1));
                     }
-                    tmem_st16(tS + c * 16, pk);
+                    tmem_st16(tP + c * 16, pk);
                     constexpr int CPP = BN / 32 / P_PARTS;  // 32-key chunks per slice
                     if ((c + 1) % CPP == 0 && c + 1 < BN / 32) {  // a slice of P is written: its P V may start
                         tmem_wait_st();
