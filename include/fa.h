@@ -101,12 +101,14 @@ fa_status fa_forward_ex(const void *q, const void *k, const void *v, void *o, fl
 
 /*
  * fa_workspace_size -- bytes of device workspace that let fa_forward_ws run
- * this problem on the wide-head tensor-core path at full parallelism: the
+ * this problem at full parallelism.  On the wide-head tensor-core path: the
  * bf16 hi/lo copies of fp32 inputs and, when the key range is split across
  * CTAs, the per-split partial O, m and l that a combine step merges with
  * the rule of "FlashAttention Engine: Hardware-Aware Exact Attention & SRAM
- * Tiling" ("Core FlashAttention Mechanics", item 3).  0 means the problem
- * needs none (the 64/128 tensor-core kernel, or no tensor-core path).
+ * Tiling" ("Core FlashAttention Mechanics", item 3).  On the 64/128
+ * tensor-core kernel: the same partials when the problem has too few
+ * 256-row query blocks to fill the GPU (no mask, long key range), so that
+ * CTAs split the keys.  0 means the problem needs none.
  */
 size_t fa_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int o_dtype, int causal);
 
@@ -202,6 +204,15 @@ typedef struct fa_params {
 } fa_params;
 
 fa_status fa_attention(const fa_params *p, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * fa_attention_workspace_size -- bytes of device workspace that let
+ * fa_attention run `p` at full parallelism (the key-range partials described
+ * under fa_workspace_size; a shorter workspace runs it without the split).
+ * Reads only the sizes, strides and dtypes of *p.  0 for none or for an
+ * invalid *p.
+ */
+size_t fa_attention_workspace_size(const fa_params *p);
 
 /*
  * fa_backward_workspace_size / fa_backward -- gradients of the forward pass

@@ -54,6 +54,7 @@ SIGNATURES = {
     "fa_forward_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "fa_attention": (ctypes.c_int, [ctypes.POINTER(FaParams), _P, ctypes.c_size_t, _P]),
+    "fa_attention_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(FaParams)]),
     "fa_backward_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
     "fa_backward": (ctypes.c_int, [_P] * 9 + [_I64, _I64, _I64, _I64, ctypes.c_float, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_int, _P, ctypes.c_size_t, _P]),
@@ -226,6 +227,33 @@ def forward_host(q, k, v, o, lse, workspace, scale=None, causal=False, stream=No
     return o, lse
 
 
+def _fa_params(q, k, v, o, lse, scale, causal):
+    B, H, Nq, dk = q.shape
+    Nk, dv = k.shape[2], v.shape[3]
+    prm = FaParams()
+    prm.q, prm.k, prm.v, prm.o = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
+    prm.lse = lse.data_ptr() if lse is not None else None
+    prm.B, prm.H, prm.Nq, prm.Nk, prm.dk, prm.dv = B, H, Nq, Nk, dk, dv
+    for name, t in (("q_stride", q), ("k_stride", k), ("v_stride", v), ("o_stride", o)):
+        getattr(prm, name)[:] = list(t.stride()[:3])
+    prm.scale, prm.causal = float(scale), int(bool(causal))
+    prm.in_dtype, prm.o_dtype = _dtype_code(q.dtype), _dtype_code(o.dtype)
+    return prm
+
+
+def attention_workspace_size(q, k, v, o=None, causal=False, o_dtype=None) -> int:
+    """fa_attention_workspace_size: device workspace bytes that let
+    fa_attention run these tensors at full parallelism (o: the output view,
+    or a contiguous [B, H, Nq, dv] tensor of o_dtype when None)."""
+    prm = _fa_params(q, k, v, q if o is None else o, None, 1.0, causal)  # the size query reads no pointer
+    if o is None:
+        B, H, Nq, _ = q.shape
+        dv = v.shape[3]
+        prm.o_stride[:] = [H * Nq * dv, Nq * dv, dv]
+        prm.o_dtype = _dtype_code(o_dtype or q.dtype)
+    return int(load().fa_attention_workspace_size(ctypes.byref(prm)))
+
+
 def fa_attention(q, k, v, o=None, lse=None, scale=None, causal=False, o_dtype=None,
                  return_lse=True, workspace=None, stream=None):
     """Attention on [B, H, Nq, dk] / [B, H, Nk, dk] / [B, H, Nk, dv] CUDA tensors
@@ -254,14 +282,7 @@ def fa_attention(q, k, v, o=None, lse=None, scale=None, causal=False, o_dtype=No
         stream = torch.cuda.current_stream(q.device).cuda_stream
     elif not isinstance(stream, int):
         stream = stream.cuda_stream
-    prm = FaParams()
-    prm.q, prm.k, prm.v, prm.o = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
-    prm.lse = lse.data_ptr() if lse is not None else None
-    prm.B, prm.H, prm.Nq, prm.Nk, prm.dk, prm.dv = B, H, Nq, Nk, dk, dv
-    for name, t in (("q_stride", q), ("k_stride", k), ("v_stride", v), ("o_stride", o)):
-        getattr(prm, name)[:] = list(t.stride()[:3])
-    prm.scale, prm.causal = float(scale), int(bool(causal))
-    prm.in_dtype, prm.o_dtype = _dtype_code(q.dtype), _dtype_code(o.dtype)
+    prm = _fa_params(q, k, v, o, lse, scale, causal)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     check(load().fa_attention(ctypes.byref(prm), ws_ptr, ws_bytes, stream))

@@ -285,7 +285,12 @@ fa_status dispatch(const fa::Problem &p, void *workspace, size_t workspace_bytes
     const char *detail = nullptr;
     if (!(flags & FA_FLAG_GENERAL_PATH)) {
         if (fa::tc_supported(p)) {
-            e = fa::launch_tc(p, s, flags, &detail);
+            // with a workspace, too few work items are spread over key-range splits
+            const fa::TcSplit sp = (workspace && !flags) ? fa::tc_split_plan(p) : fa::TcSplit{1, 0, 0};
+            if (sp.n_split > 1 && workspace_bytes >= sp.workspace_bytes)
+                e = fa::launch_tc_split(p, sp, workspace, s, &detail);
+            else
+                e = fa::launch_tc(p, s, flags, &detail);
             if (e != cudaSuccess)
                 return detail ? fail(FA_ERR_CUDA, "tensor-core launch: %s", detail) : cuda_fail(e, "tensor-core launch");
             return FA_OK;
@@ -313,7 +318,8 @@ size_t fa_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtyp
     const uintptr_t a = 256;  // placeholder, aligned pointers for planning only
     fa::Problem p{reinterpret_cast<const void *>(a), reinterpret_cast<const void *>(a), reinterpret_cast<const void *>(a),
                   reinterpret_cast<void *>(a), nullptr, B, H, N, d, 1.0f, causal != 0, in_dtype, o_dtype};
-    if (!size_ok(p) || fa::tc_supported(p)) return 0;
+    if (!size_ok(p)) return 0;
+    if (fa::tc_supported(p)) return fa::tc_split_plan(p).workspace_bytes;
     const fa::WidePlan w = fa::wide_plan(p, 1 << 20);
     return w.ok ? w.workspace_bytes : 0;
 }
@@ -328,8 +334,14 @@ int fa_plan(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int o_dtyp
     char buf[160];
     int launches;
     if (fa::tc_supported(p)) {
-        launches = 1;
-        snprintf(buf, sizeof(buf), "tensor-core d=%lld", (long long)d);
+        const fa::TcSplit sp = fa::tc_split_plan(p);
+        if (sp.n_split > 1 && workspace_bytes >= sp.workspace_bytes) {
+            launches = 2;
+            snprintf(buf, sizeof(buf), "tensor-core d=%lld key splits=%d", (long long)d, sp.n_split);
+        } else {
+            launches = 1;
+            snprintf(buf, sizeof(buf), "tensor-core d=%lld", (long long)d);
+        }
     } else {
         fa::WidePlan w = fa::wide_plan(p, workspace_bytes ? 1 << 20 : 1);
         if (w.ok && workspace_bytes && workspace_bytes < w.workspace_bytes) w = fa::wide_plan(p, 1);
@@ -346,10 +358,9 @@ int fa_plan(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int o_dtyp
     return launches;
 }
 
-fa_status fa_attention(const fa_params *a, void *workspace, size_t workspace_bytes, void *stream)
+namespace {
+fa::Problem problem_of(const fa_params *a)
 {
-    g_last_error.clear();
-    if (!a) return fail(FA_ERR_INVALID_ARG, "params must be non-NULL");
     fa::Problem p{a->q, a->k, a->v, a->o, a->lse, a->B, a->H, a->Nq, a->dk, a->scale, a->causal != 0,
                   a->in_dtype, a->o_dtype};
     p.Nk = a->Nk;
@@ -360,6 +371,36 @@ fa_status fa_attention(const fa_params *a, void *workspace, size_t workspace_byt
         p.vs[i] = a->v_stride[i];
         p.os[i] = a->o_stride[i];
     }
+    return p;
+}
+}  // namespace
+
+size_t fa_attention_workspace_size(const fa_params *a)
+{
+    if (!a) return 0;
+    fa::Problem p = problem_of(a);
+    // sizes, strides and dtypes only: distinct, aligned placeholder addresses
+    // stand in for the pointers (never dereferenced)
+    const uintptr_t base = 1024, gap = (uintptr_t)1 << 44;
+    p.q = reinterpret_cast<const void *>(base);
+    p.k = reinterpret_cast<const void *>(base + gap);
+    p.v = reinterpret_cast<const void *>(base + 2 * gap);
+    p.o = reinterpret_cast<void *>(base + 3 * gap);
+    p.lse = nullptr;
+    if (validate_general(p) != FA_OK) {
+        g_last_error.clear();
+        return 0;
+    }
+    if (fa::tc_supported(p)) return fa::tc_split_plan(p).workspace_bytes;
+    const fa::WidePlan w = fa::wide_plan(p, 1 << 20);
+    return w.ok ? w.workspace_bytes : 0;
+}
+
+fa_status fa_attention(const fa_params *a, void *workspace, size_t workspace_bytes, void *stream)
+{
+    g_last_error.clear();
+    if (!a) return fail(FA_ERR_INVALID_ARG, "params must be non-NULL");
+    const fa::Problem p = problem_of(a);
     fa_status st = validate_general(p);
     if (st != FA_OK) return st;
     return dispatch(p, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), 0u);

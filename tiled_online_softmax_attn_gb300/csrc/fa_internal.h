@@ -93,6 +93,22 @@ WidePlan wide_plan(const Problem &p, int max_splits);
 cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cudaStream_t stream, uint32_t flags,
                         const char **detail);
 cudaError_t wide_error_word_ptr(uint32_t **ptr);
+// Merge of key-range partials (fa_wide.cu): per split s, unnormalised O rows
+// o_part[s][row][D] (fp32), the row's reference maximum m_part (log2 units),
+// its exact weight sum l_part and its bf16-rounding correction d_part, rows =
+// BH * N; writes O (contiguous [BH * N][D]) and LSE.  n_split <= 16.
+cudaError_t launch_combine(const float *o_part, const float *m_part, const float *l_part, const float *d_part, void *o,
+                           bool o_fp32, float *lse, int64_t BH, int64_t N, int D, int n_split, cudaStream_t stream);
+
+// Key-range split of the tensor-core kernel (fa_tc.cu) for problems with too
+// few work items to fill the GPU: unmasked, O contiguous; n_split <= 1 means
+// no split.  The partials need `workspace_bytes`.
+struct TcSplit {
+    int n_split, kv_per;
+    size_t workspace_bytes;
+};
+TcSplit tc_split_plan(const Problem &p);
+cudaError_t launch_tc_split(const Problem &p, const TcSplit &sp, void *workspace, cudaStream_t stream, const char **detail);
 
 // Backward problem: contiguous [B, H, N, d] Q, K, V, O, dO of in_dtype,
 // LSE [B, H, N] fp32 from the forward pass, gradients of grad_dtype.

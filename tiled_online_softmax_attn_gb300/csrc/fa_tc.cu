@@ -121,6 +121,10 @@ struct Params {
     int qperm, kperm, vperm;   // which of (sequence, head, batch) each outer map dimension holds
     float *lse;
     int o_fp32;
+    // key-range split (n_split > 1): each item covers key tiles [kv_per sp, kv_per (sp + 1))
+    // and writes unnormalised partials instead of O and LSE
+    int n_split, kv_per;
+    float *o_part, *m_part, *l_part, *d_part;
 };
 
 struct __align__(8) Barriers {
@@ -138,6 +142,8 @@ struct Item {
     int bh, b, h;
     int qrow0;   // first row of Q0; Q1 starts BM later
     int n0, n1;  // key tiles each query tile needs: all, or up to its diagonal under the mask
+    int kv_lo;   // first key tile (key-range split; 0 otherwise)
+    int sp;      // split index
 };
 
 // Item of this CTA's round `it`: rounds alternate direction over the CTAs
@@ -155,7 +161,11 @@ __device__ __forceinline__ int item_index(int it)
 template <bool CAUSAL>
 __device__ __forceinline__ Item item_of(const Params &prm, int w)
 {
-    int qb, bh;
+    int qb, bh, sp = 0;
+    if (!CAUSAL && prm.n_split > 1) {
+        sp = w % prm.n_split;
+        w /= prm.n_split;
+    }
     if (CAUSAL) {  // longest query blocks first
         qb = prm.n_qblocks - 1 - w / prm.BH;
         bh = w % prm.BH;
@@ -164,12 +174,14 @@ __device__ __forceinline__ Item item_of(const Params &prm, int w)
         bh = w / prm.n_qblocks;
     }
     Item it;
+    it.sp = sp;
+    it.kv_lo = sp * prm.kv_per;
     it.bh = bh;
     it.b = bh / prm.H;
     it.h = bh % prm.H;
     it.qrow0 = qb * 2 * BM;
-    it.n0 = CAUSAL ? min(prm.n_kv, 2 * qb + 1) : prm.n_kv;
-    it.n1 = CAUSAL ? min(prm.n_kv, 2 * qb + 2) : prm.n_kv;
+    it.n0 = CAUSAL ? min(prm.n_kv, 2 * qb + 1) : min(prm.n_kv - it.kv_lo, prm.n_split > 1 ? prm.kv_per : prm.n_kv);
+    it.n1 = CAUSAL ? min(prm.n_kv, 2 * qb + 2) : it.n0;
     return it;
 }
 
@@ -292,11 +304,11 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     if (has_k)
                         for (int c = 0; c < C::QCH; ++c)
                             tma_load_rows(s_base + C::OFF_K + slot * C::K_BYTES + c * (BN * 128), &tm_k, full, c * 64,
-                                          prm.kperm, s * BN, wi.h, wi.b, pol_kv);
+                                          prm.kperm, (wi.kv_lo + s) * BN, wi.h, wi.b, pol_kv);
                     if (has_v)
                         for (int c = 0; c < C::VCH; ++c)
                             tma_load_rows(s_base + C::OFF_V + slot * C::V_BYTES + c * (BN * 128), &tm_v, full, c * 64,
-                                          prm.vperm, (s - 1) * BN, wi.h, wi.b, pol_kv);
+                                          prm.vperm, (wi.kv_lo + s - 1) * BN, wi.h, wi.b, pol_kv);
                     return true;
                 };
                 // the first key tile may load before the previous item's last S MMA
@@ -568,7 +580,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     tc_fence_before();
                     mbar_arrive(smem_addr(&bars.s_read[t]));
                 }
-                const int kv0 = j * BN;
+                const int kv0 = (wi.kv_lo + j) * BN;
                 int lim = Nk - kv0;                         // keys >= Nk are padding
                 if (CAUSAL) lim = min(lim, grow - kv0 + 1);  // keys after this query
                 if (lim < BN) {
@@ -657,6 +669,31 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 break;
             }
             tc_fence_after();
+            if (prm.n_split > 1) {  // key-range partials: unnormalised O, m, l, dq
+                const size_t prow = ((size_t)wi.sp * prm.BH + wi.bh) * N + grow;
+#pragma unroll
+                for (int c = 0; c < DV / 32; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(tO + c * 32, raw);
+                    if (grow < N) {
+                        float4 *dst = reinterpret_cast<float4 *>(prm.o_part + prow * DV + c * 32);
+#pragma unroll
+                        for (int x = 0; x < 8; ++x)
+                            dst[x] = make_float4(__uint_as_float(raw[4 * x]), __uint_as_float(raw[4 * x + 1]),
+                                                 __uint_as_float(raw[4 * x + 2]), __uint_as_float(raw[4 * x + 3]));
+                    }
+                }
+                if (PERSIST) {
+                    tc_fence_before();
+                    mbar_arrive(smem_addr(&bars.o_empty[t]));
+                }
+                if (grow < N) {
+                    prm.m_part[prow] = m;
+                    prm.l_part[prow] = l;
+                    prm.d_part[prow] = dq;
+                }
+                continue;
+            }
             const float inv_l = 1.f / (l + dq);
             const size_t row_elem = (size_t)(wi.b * prm.os_b + wi.h * prm.os_h + (int64_t)grow * prm.os_n);
             if (PERSIST) {
@@ -747,8 +784,35 @@ bool make_map(CUtensorMap *map, const void *ptr, int64_t w, int64_t n, int64_t H
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int sm_count(cudaError_t *e)
+{
+    int dev = 0, sms = 0;
+    if ((*e = cudaGetDevice(&dev)) != cudaSuccess) return 0;
+    if ((*e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return 0;
+    return std::max(sms, 1);
+}
+
+// Workspace layout of a key-range split: o_part [n_split][BH N][DV] fp32, then
+// m, l and dq [n_split][BH N] fp32 each (256-byte aligned pieces).
+struct SplitLayout {
+    size_t o, m, l, d, total;
+};
+SplitLayout split_layout(const Problem &p, int n_split)
+{
+    auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t rows = (size_t)(p.B * p.H * p.N) * (size_t)n_split;
+    SplitLayout L;
+    L.o = 0;
+    L.m = al(rows * (size_t)dv_of(p) * 4);
+    L.l = L.m + al(rows * 4);
+    L.d = L.l + al(rows * 4);
+    L.total = L.d + al(rows * 4);
+    return L;
+}
+
 template <int DK, int DV, bool CAUSAL>
-cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, const char **detail)
+cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, const char **detail,
+                         const TcSplit *split = nullptr, void *workspace = nullptr)
 {
     using Cf = Cfg<DK, DV>;
     CUtensorMap mq, mk, mv;
@@ -783,6 +847,20 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     prm.os_n = so[2];
     prm.lse = p.lse;
     prm.o_fp32 = p.o_dtype == 1;
+    prm.n_split = 1;
+    prm.kv_per = prm.n_kv;
+    prm.o_part = prm.m_part = prm.l_part = prm.d_part = nullptr;
+    if (split && split->n_split > 1) {
+        const SplitLayout L = split_layout(p, split->n_split);
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        prm.n_split = split->n_split;
+        prm.kv_per = split->kv_per;
+        prm.o_part = reinterpret_cast<float *>(ws + L.o);
+        prm.m_part = reinterpret_cast<float *>(ws + L.m);
+        prm.l_part = reinterpret_cast<float *>(ws + L.l);
+        prm.d_part = reinterpret_cast<float *>(ws + L.d);
+        prm.n_items *= prm.n_split;
+    }
     // Short unmasked items (64 key tiles or fewer): one persistent CTA per SM
     // loops over them, so an item's prologue (query loads, first S MMA) and
     // epilogue overlap its neighbours' work (multi-head workload +2.5 %).  Long
@@ -790,26 +868,28 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     // best one per CTA, handed out by the hardware as SMs free up (measured:
     // persistence with alternating-direction rounds gave the causal workload
     // -1 %, the peaked one -2 %).
-    const bool persist = !CAUSAL && prm.n_kv <= 64;
+    const bool persist = !CAUSAL && prm.n_kv <= 64 && prm.n_split == 1;
     auto kern = persist ? fa_tc_kernel<DK, DV, CAUSAL, true> : fa_tc_kernel<DK, DV, CAUSAL, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     int grid = prm.n_items;
     if (persist) {
-        int dev = 0, sms = 0;
-        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-        grid = (int)std::min<int64_t>((int64_t)prm.n_items, (int64_t)std::max(sms, 1));
+        const int sms = sm_count(&e);
+        if (e != cudaSuccess) return e;
+        grid = std::min(prm.n_items, sms);
     }
     kern<<<(unsigned)grid, NUM_THREADS, Cf::SMEM_BYTES, stream>>>(mq, mk, mv, prm);
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess || prm.n_split == 1) return e;
+    return launch_combine(prm.o_part, prm.m_part, prm.l_part, prm.d_part, p.o, p.o_dtype == 1, p.lse, BH, p.N, DV,
+                          prm.n_split, stream);
 }
 
 template <int DK, int DV>
-cudaError_t launch_dims(const Problem &p, cudaStream_t stream, uint32_t flags, const char **detail)
+cudaError_t launch_dims(const Problem &p, cudaStream_t stream, uint32_t flags, const char **detail,
+                        const TcSplit *split = nullptr, void *workspace = nullptr)
 {
     return p.causal ? launch_typed<DK, DV, true>(p, stream, flags, detail)
-                    : launch_typed<DK, DV, false>(p, stream, flags, detail);
+                    : launch_typed<DK, DV, false>(p, stream, flags, detail, split, workspace);
 }
 
 }  // namespace
@@ -838,6 +918,43 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t stream, uint32_t flags, con
     if (p.d == 128) return dv == 128 ? launch_dims<128, 128>(p, stream, flags, detail)
                                      : launch_dims<128, 64>(p, stream, flags, detail);
     return dv == 128 ? launch_dims<64, 128>(p, stream, flags, detail) : launch_dims<64, 64>(p, stream, flags, detail);
+}
+
+// Flash-decoding style split for problems with few work items: unmasked, O
+// contiguous, at most one wave of (item, split) CTAs, two key tiles or more
+// per split, 16 splits at most (the combine kernel's limit).
+TcSplit tc_split_plan(const Problem &p)
+{
+    TcSplit sp{1, 0, 0};
+    if (p.causal || !tc_supported(p)) return sp;
+    const int64_t dv = dv_of(p);
+    int64_t os[3];
+    strides_of(p, 3, os);
+    if (os[2] != dv || os[1] != p.N * dv || os[0] != p.H * p.N * dv) return sp;  // combine writes contiguous O
+    cudaError_t e = cudaSuccess;
+    const int sms = sm_count(&e);
+    if (e != cudaSuccess) return sp;
+    const int64_t items = (p.N + 2 * BM - 1) / (2 * BM) * p.B * p.H;
+    const int64_t n_kv = (keys_of(p) + BN - 1) / BN;
+    if (2 * items > sms || n_kv < 4) return sp;
+    int64_t n = std::min<int64_t>({16, sms / items, n_kv / 2});
+    if (n < 2) return sp;
+    const int64_t per = (n_kv + n - 1) / n;
+    n = (n_kv + per - 1) / per;
+    if (n < 2) return sp;
+    sp.n_split = (int)n;
+    sp.kv_per = (int)per;
+    sp.workspace_bytes = split_layout(p, sp.n_split).total;
+    return sp;
+}
+
+cudaError_t launch_tc_split(const Problem &p, const TcSplit &sp, void *workspace, cudaStream_t stream, const char **detail)
+{
+    const int64_t dv = dv_of(p);
+    if (p.d == 128) return dv == 128 ? launch_dims<128, 128>(p, stream, 0, detail, &sp, workspace)
+                                     : launch_dims<128, 64>(p, stream, 0, detail, &sp, workspace);
+    return dv == 128 ? launch_dims<64, 128>(p, stream, 0, detail, &sp, workspace)
+                     : launch_dims<64, 64>(p, stream, 0, detail, &sp, workspace);
 }
 
 cudaError_t tc_error_word_ptr(uint32_t **ptr)

@@ -634,19 +634,25 @@ cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cu
         else e = p.causal ? go(fa_wide_kernel<1, 128, true>) : go(fa_wide_kernel<1, 128, false>);
     }
     if (e != cudaSuccess) return e;
-    if (!prm.direct) {
-        const unsigned rows = (unsigned)(BH * p.N);
-        const int threads = (int)std::min<int64_t>(256, std::max<int64_t>(32, p.d / 4));
-        if (p.o_dtype == 1)
-            fa_combine_kernel<float><<<rows, threads, 0, stream>>>(prm.o_part, prm.m_part, prm.l_part, prm.d_part,
-                                                               static_cast<float *>(p.o), p.lse, (int)BH, (int)p.N, (int)p.d, w.n_split);
-        else
-            fa_combine_kernel<__nv_bfloat16><<<rows, threads, 0, stream>>>(prm.o_part, prm.m_part, prm.l_part, prm.d_part,
-                                                                       static_cast<__nv_bfloat16 *>(p.o), p.lse, (int)BH, (int)p.N,
-                                                                       (int)p.d, w.n_split);
-        e = cudaGetLastError();
-    }
+    if (!prm.direct)
+        e = launch_combine(prm.o_part, prm.m_part, prm.l_part, prm.d_part, p.o, p.o_dtype == 1, p.lse, BH, p.N,
+                           (int)p.d, w.n_split, stream);
     return e;
+}
+
+cudaError_t launch_combine(const float *o_part, const float *m_part, const float *l_part, const float *d_part, void *o,
+                           bool o_fp32, float *lse, int64_t BH, int64_t N, int D, int n_split, cudaStream_t stream)
+{
+    if (n_split < 1 || n_split > MAX_SPLITS || D % 4 != 0) return cudaErrorInvalidValue;
+    const unsigned rows = (unsigned)(BH * N);
+    const int threads = (int)std::min<int64_t>(256, std::max<int64_t>(32, D / 4));
+    if (o_fp32)
+        fa_combine_kernel<float><<<rows, threads, 0, stream>>>(o_part, m_part, l_part, d_part, static_cast<float *>(o),
+                                                               lse, (int)BH, (int)N, D, n_split);
+    else
+        fa_combine_kernel<__nv_bfloat16><<<rows, threads, 0, stream>>>(
+            o_part, m_part, l_part, d_part, static_cast<__nv_bfloat16 *>(o), lse, (int)BH, (int)N, D, n_split);
+    return cudaGetLastError();
 }
 
 cudaError_t wide_error_word_ptr(uint32_t **ptr)
