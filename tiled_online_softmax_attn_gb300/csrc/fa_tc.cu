@@ -158,11 +158,11 @@ __device__ __forceinline__ int item_index(int it)
     return it * G + ((it & 1) ? G - 1 - c : c);
 }
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool SPLIT>
 __device__ __forceinline__ Item item_of(const Params &prm, int w)
 {
     int qb, bh, sp = 0;
-    if (!CAUSAL && prm.n_split > 1) {
+    if (SPLIT) {
         sp = w % prm.n_split;
         w /= prm.n_split;
     }
@@ -175,12 +175,12 @@ __device__ __forceinline__ Item item_of(const Params &prm, int w)
     }
     Item it;
     it.sp = sp;
-    it.kv_lo = sp * prm.kv_per;
+    it.kv_lo = SPLIT ? sp * prm.kv_per : 0;
     it.bh = bh;
     it.b = bh / prm.H;
     it.h = bh % prm.H;
     it.qrow0 = qb * 2 * BM;
-    it.n0 = CAUSAL ? min(prm.n_kv, 2 * qb + 1) : min(prm.n_kv - it.kv_lo, prm.n_split > 1 ? prm.kv_per : prm.n_kv);
+    it.n0 = CAUSAL ? min(prm.n_kv, 2 * qb + 1) : (SPLIT ? min(prm.n_kv - it.kv_lo, prm.kv_per) : prm.n_kv);
     it.n1 = CAUSAL ? min(prm.n_kv, 2 * qb + 2) : it.n0;
     return it;
 }
@@ -225,7 +225,7 @@ __device__ __forceinline__ void store_o_row(void *o, int o_fp32, size_t row_elem
     }
 }
 
-template <int DK, int DV, bool CAUSAL, bool PERSIST>
+template <int DK, int DV, bool CAUSAL, bool PERSIST, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const Params prm)
@@ -287,7 +287,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             for (int it = 0; ok; ++it) {
                 const int w = item_index<PERSIST>(it);
                 if (w >= prm.n_items) break;
-                const Item wi = item_of<CAUSAL>(prm, w);
+                const Item wi = item_of<CAUSAL, SPLIT>(prm, w);
                 // stage s of the item = K_s (s < n1) and V_(s-1) (s >= 1), s = 0 .. n1
                 auto load_stage = [&](int s) -> bool {
                     const int slot = g % C::KVS;
@@ -410,7 +410,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             for (int it = 0; ok; ++it) {
                 const int w = item_index<PERSIST>(it);
                 if (w >= prm.n_items) break;
-                const Item wi = item_of<CAUSAL>(prm, w);
+                const Item wi = item_of<CAUSAL, SPLIT>(prm, w);
                 const int n0 = wi.n0, n1 = wi.n1;
                 // the first P_t V product of an item overwrites O_t: the previous
                 // item's epilogue must have read it
@@ -556,7 +556,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         for (int it = 0; ok; ++it) {
             const int w = item_index<PERSIST>(it);
             if (w >= prm.n_items) break;
-            const Item wi = item_of<CAUSAL>(prm, w);
+            const Item wi = item_of<CAUSAL, SPLIT>(prm, w);
             const int grow = wi.qrow0 + t * BM + r;  // global query row of this thread
             const int n_t = t == 0 ? wi.n0 : wi.n1;
             float m = -INFINITY;  // running maximum, log2 units
@@ -669,7 +669,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 break;
             }
             tc_fence_after();
-            if (prm.n_split > 1) {  // key-range partials: unnormalised O, m, l, dq
+            if constexpr (SPLIT) {  // key-range partials: unnormalised O, m, l, dq
                 const size_t prow = ((size_t)wi.sp * prm.BH + wi.bh) * N + grow;
 #pragma unroll
                 for (int c = 0; c < DV / 32; ++c) {
@@ -869,7 +869,9 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     // persistence with alternating-direction rounds gave the causal workload
     // -1 %, the peaked one -2 %).
     const bool persist = !CAUSAL && prm.n_kv <= 64 && prm.n_split == 1;
-    auto kern = persist ? fa_tc_kernel<DK, DV, CAUSAL, true> : fa_tc_kernel<DK, DV, CAUSAL, false>;
+    auto kern = prm.n_split > 1 ? fa_tc_kernel<DK, DV, CAUSAL, false, !CAUSAL>
+                : persist       ? fa_tc_kernel<DK, DV, CAUSAL, true, false>
+                                : fa_tc_kernel<DK, DV, CAUSAL, false, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     int grid = prm.n_items;
