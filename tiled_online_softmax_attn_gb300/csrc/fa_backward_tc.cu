@@ -18,13 +18,15 @@
 //     S = Q_i K_j^T, dP = dO_i V_j^T, dS = P (dP - delta), dQ += dS K_j.
 //
 // So S and dP are formed twice (7 products of 128 x 128 x d instead of 5):
-// the price of no atomics and deterministic gradients.  The eight elementwise warps do the
-// elementwise work: warp w reads tensor-memory lanes 32 (w % 4) .. + 31 (one
-// row per thread) and the half w / 4 of the 128 columns, so two warps share
-// each row and each SM sub-partition runs two of them; no reduction crosses
-// columns.  Warp 8 issues the TMA loads, warp 9 the MMAs.  The two score
-// products of a tile signal separate barriers, so the exponentials start as
-// soon as the first is done.  Every wait is bounded as in the forward kernels.
+// the price of no atomics and deterministic gradients.  Eight elementwise
+// warps do the elementwise work: warp w reads tensor-memory lanes
+// 32 (w % 4) .. + 31 (one row per thread) and the half w / 4 of the 128
+// columns, so two warps share each row and each SM sub-partition runs two of
+// them; no reduction crosses columns.  Warp 8 issues the TMA loads, warp 9 the
+// MMAs.  The two score products of a tile signal separate barriers, so the
+// exponentials start as soon as the first is done, and the two streamed tiles
+// of a stage have barriers of their own, so the one read first lands first.
+// Every wait is bounded as in the forward kernels.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>

@@ -31,9 +31,16 @@
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   [  0,128) S0 / P0   [128,256) S1 / P1   [256, 256+D) O0   [256+D, 256+2D) O1
-// P_t (bf16, two per column) overwrites the first 64 columns of S_t; the
-// next S_t MMA is issued after the P_t V MMA, and MMAs from one thread run
-// in issue order.
+// At D = 128, P_t (bf16, two per column) overwrites the first 64 columns of
+// S_t; the next S_t MMA is issued after the P_t V MMA, and MMAs from one
+// thread run in issue order.  At D = 64, P_t has columns of its own,
+// [384 + 64 t, ...), so the next S_t MMA waits only for S_t to be read.
+// Either way the softmax warps release P_t in two halves (keys 0-63, then
+// 64-127) and the P_t V product starts on the first.
+//
+// With a caller workspace and too few items to fill the GPU, items are
+// further split over key ranges (SPLIT): each writes unnormalised O, m, l and
+// the bf16 correction of its range, and a combine kernel merges them.
 //
 // Every mbarrier wait is bounded (a caller-given limit in ns).  A wait that
 // gives up sets the device error word and a CTA-wide abort flag; every role
