@@ -24,8 +24,9 @@
 // columns, so two warps share each row and each SM sub-partition runs two of
 // them; no reduction crosses columns.  Warp 8 issues the TMA loads, warp 9 the
 // MMAs.  The two score products of a tile signal separate barriers, so the
-// exponentials start as soon as the first is done, and the two streamed tiles
-// of a stage have barriers of their own, so the one read first lands first.
+// exponentials start as soon as the first is done.  The two streamed tiles
+// travel in rings of their own (full/empty barrier pair per slot), so the one
+// read first lands first and its ring can be the deeper one.
 // Every wait is bounded as in the forward kernels.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -75,11 +76,25 @@ template <int D>
 struct BCfg {
     static constexpr int CH = D / 64;
     static constexpr uint32_t TILE = BM * D * 2;
-    static constexpr uint32_t RES = 2 * TILE;              // resident pair (K,V) or (Q,dO)
-    static constexpr uint32_t STAGE = 2 * TILE + VEC_BYTES;  // streamed pair (+ vectors for dK/dV)
-    static constexpr uint32_t SMEM = RES + 2 * STAGE + 1024;
+    static constexpr uint32_t RES = 2 * TILE;  // resident pair (K,V) or (Q,dO)
+    // Streamed tiles in rings of their own.  The score product of the next
+    // tile (S^T(s+1) / S(s+1)) is issued early, but a ring slot is freed only
+    // by the last product of the tile it held, so the operand of the score
+    // product gets one slot more than the other one where shared memory allows
+    // (at d = 128 the dK/dV kernel keeps two of each: three Q slots leave room
+    // for one dO slot, which measured slower).
+    // dK/dV kernel: Q ring (each slot with the LSE/delta vectors of its rows), dO ring
+    static constexpr int NQS = D == 64 ? 4 : 2;
+    static constexpr int NGS = D == 64 ? 3 : 2;
+    static constexpr uint32_t SMEM_KV = RES + (NQS + NGS) * TILE + NQS * VEC_BYTES + 1024;
+    // dQ kernel: K ring, V ring
+    static constexpr int NKS = D == 64 ? 4 : 3;
+    static constexpr int NVS = D == 64 ? 3 : 2;
+    static constexpr uint32_t SMEM_Q = RES + (NKS + NVS) * TILE + 1024;
     // keep one CTA per SM (all 512 tensor-memory columns each)
-    static constexpr uint32_t SMEM_REQ = SMEM < 120u * 1024u ? 120u * 1024u : SMEM;
+    static constexpr uint32_t SMEM_KV_REQ = SMEM_KV < 120u * 1024u ? 120u * 1024u : SMEM_KV;
+    static constexpr uint32_t SMEM_Q_REQ = SMEM_Q < 120u * 1024u ? 120u * 1024u : SMEM_Q;
+    static_assert(SMEM_KV <= 227u * 1024u && SMEM_Q <= 227u * 1024u, "backward rings exceed shared memory");
 };
 
 struct BwdParams {
@@ -142,9 +157,9 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     using E = EW<D>;
     constexpr int W = E::W, TMA_WARP = E::TMA_WARP, MMA_WARP = E::MMA_WARP;
     extern __shared__ uint8_t smem_raw[];
-    // per stage slot: fq/eq for Q_i and its LSE/delta vectors, fg/eg for dO_i (dO_i is
+    // per ring slot: fq/eq for Q_i and its LSE/delta vectors, fg/eg for dO_i (dO_i is
     // freed by the earlier dV product and loaded second, so Q_i, needed first, lands sooner)
-    __shared__ __align__(8) uint64_t res_full, fq[2], eq[2], fg[2], eg[2], st_full, dp_full, p_ready, ds_ready, o_full,
+    __shared__ __align__(8) uint64_t res_full, fq[C::NQS], eq[C::NQS], fg[C::NGS], eg[C::NGS], st_full, dp_full, p_ready, ds_ready, o_full,
         drain;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
@@ -161,14 +176,19 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // per-query vectors)
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t s_base = smem_addr(smem);
-    const uint32_t sK = s_base, sV = s_base + C::TILE, sStage = s_base + C::RES;
+    const uint32_t sK = s_base, sV = s_base + C::TILE;
+    // Q ring, dO ring, then the LSE/delta vectors of each Q slot
+    const uint32_t sQr = s_base + C::RES, sGr = sQr + C::NQS * C::TILE;
+    const uint32_t oVec = C::RES + (C::NQS + C::NGS) * C::TILE;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(smem_addr(&res_full), 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < C::NQS; ++s) {
             mbar_init(smem_addr(&fq[s]), 1);
             mbar_init(smem_addr(&eq[s]), 1);
+        }
+        for (int s = 0; s < C::NGS; ++s) {
             mbar_init(smem_addr(&fg[s]), 1);
             mbar_init(smem_addr(&eg[s]), 1);
         }
@@ -204,34 +224,34 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tma_load_3d(sV + c * BOX, &tm_v, smem_addr(&res_full), c * 64, k0, bh, pol);
             }
             for (int s = 0; s < n_steps; ++s) {
-                const int st = s & 1, q0 = (first + s) * BM;
-                const uint32_t par = (uint32_t)(((s >> 1) & 1) ^ 1), dst = sStage + st * C::STAGE;
-                if (!wait_or_abort(smem_addr(&eq[st]), par, limit, &abort_flag)) {
+                const int qs = s % C::NQS, gs = s % C::NGS, q0 = (first + s) * BM;
+                if (!wait_or_abort(smem_addr(&eq[qs]), (uint32_t)(((s / C::NQS) & 1) ^ 1), limit, &abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint32_t bq = smem_addr(&fq[st]);
+                const uint32_t bq = smem_addr(&fq[qs]);
                 mbar_arrive_expect_tx(bq, C::TILE + VEC_BYTES);
-                for (int c = 0; c < C::CH; ++c) tma_load_3d(dst + c * BOX, &tm_q, bq, c * 64, q0, bh, pol);
+                for (int c = 0; c < C::CH; ++c) tma_load_3d(sQr + qs * C::TILE + c * BOX, &tm_q, bq, c * 64, q0, bh, pol);
                 const size_t vrow = (size_t)bh * prm.pitch + q0;
-                bulk_copy_g2s(dst + 2 * C::TILE, prm.lse2 + vrow, 512, bq);
-                bulk_copy_g2s(dst + 2 * C::TILE + 512, prm.delta + vrow, 512, bq);
+                const uint32_t dvec = s_base + oVec + qs * VEC_BYTES;
+                bulk_copy_g2s(dvec, prm.lse2 + vrow, 512, bq);
+                bulk_copy_g2s(dvec + 512, prm.delta + vrow, 512, bq);
                 issued_q = s + 1;
-                if (!wait_or_abort(smem_addr(&eg[st]), par, limit, &abort_flag)) {
+                if (!wait_or_abort(smem_addr(&eg[gs]), (uint32_t)(((s / C::NGS) & 1) ^ 1), limit, &abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint32_t bg = smem_addr(&fg[st]);
+                const uint32_t bg = smem_addr(&fg[gs]);
                 mbar_arrive_expect_tx(bg, C::TILE);
-                for (int c = 0; c < C::CH; ++c) tma_load_3d(dst + C::TILE + c * BOX, &tm_g, bg, c * 64, q0, bh, pol);
+                for (int c = 0; c < C::CH; ++c) tma_load_3d(sGr + gs * C::TILE + c * BOX, &tm_g, bg, c * 64, q0, bh, pol);
                 issued_g = s + 1;
             }
             if (!ok) {
                 if (!abort_flag) fail_bwd(&abort_flag);
-                for (int s = (issued_q > 2 ? issued_q - 2 : 0); s < issued_q; ++s)
-                    mbar_wait_bounded(smem_addr(&fq[s & 1]), (uint32_t)((s >> 1) & 1), limit);
-                for (int s = (issued_g > 2 ? issued_g - 2 : 0); s < issued_g; ++s)
-                    mbar_wait_bounded(smem_addr(&fg[s & 1]), (uint32_t)((s >> 1) & 1), limit);
+                for (int s = (issued_q > C::NQS ? issued_q - C::NQS : 0); s < issued_q; ++s)
+                    mbar_wait_bounded(smem_addr(&fq[s % C::NQS]), (uint32_t)((s / C::NQS) & 1), limit);
+                for (int s = (issued_g > C::NGS ? issued_g - C::NGS : 0); s < issued_g; ++s)
+                    mbar_wait_bounded(smem_addr(&fg[s % C::NGS]), (uint32_t)((s / C::NGS) & 1), limit);
                 mbar_wait_bounded(smem_addr(&res_full), 0, limit);
             }
         }
@@ -243,8 +263,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             bool ok = wait_or_abort_w(smem_addr(&res_full), 0, limit, &abort_flag), issued = false;
             // S^T(s) = K Q_s^T into cS, dP^T(s) = V dO_s^T into cP
             auto mma_st = [&](int s) {
-                const uint32_t base = sStage + (s & 1) * C::STAGE;
-                const uint64_t dQ = sdesc_sw128(base, 16, 1024);
+                const uint64_t dQ = sdesc_sw128(sQr + (s % C::NQS) * C::TILE, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
@@ -253,23 +272,28 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 issued = true;
             };
             auto mma_dpt = [&](int s) {
-                const uint32_t base = sStage + (s & 1) * C::STAGE;
-                const uint64_t dG = sdesc_sw128(base + C::TILE, 16, 1024);
+                const uint64_t dG = sdesc_sw128(sGr + (s % C::NGS) * C::TILE, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
                     mma_ss_w(tmem + cP, dV + off, dG + off, id_s, kk > 0 ? 1u : 0u);
                 }
             };
-            auto wait_stage = [&](uint64_t *bars, int s) -> bool {
-                if (!wait_or_abort_w(smem_addr(&bars[s & 1]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) return false;
+            // Q_s in ring slot s % NQS, dO_s in slot s % NGS
+            auto wait_q = [&](int s) -> bool {
+                if (!wait_or_abort_w(smem_addr(&fq[s % C::NQS]), (uint32_t)((s / C::NQS) & 1), limit, &abort_flag)) return false;
                 tc_fence_after();
                 return true;
             };
-            if (ok && (ok = wait_stage(fq, 0))) {
+            auto wait_g = [&](int s) -> bool {
+                if (!wait_or_abort_w(smem_addr(&fg[s % C::NGS]), (uint32_t)((s / C::NGS) & 1), limit, &abort_flag)) return false;
+                tc_fence_after();
+                return true;
+            };
+            if (ok && (ok = wait_q(0))) {
                 mma_st(0);
                 mma_commit_w(smem_addr(&st_full));
-                if ((ok = wait_stage(fg, 0))) {
+                if ((ok = wait_g(0))) {
                     mma_dpt(0);
                     mma_commit_w(smem_addr(&dp_full));
                 }
@@ -278,19 +302,18 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // columns dV(s) has just read (same-thread MMAs run in order), so
             // it overlaps the elementwise warps' dS^T(s); then dK(s) and dP^T(s+1).
             for (int s = 0; ok && s < n_steps; ++s) {
-                const int st = s & 1;
-                const uint32_t base = sStage + st * C::STAGE;
                 if (!wait_or_abort_w(smem_addr(&p_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint64_t dGmn = sdesc_sw128(base + C::TILE, BOX, 1024), dQmn = sdesc_sw128(base, BOX, 1024);
+                const uint64_t dGmn = sdesc_sw128(sGr + (s % C::NGS) * C::TILE, BOX, 1024);
+                const uint64_t dQmn = sdesc_sw128(sQr + (s % C::NQS) * C::TILE, BOX, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)
                     mma_ts_w(tmem + cV, tmem + a_col<W>(cS, kk), dGmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_w(smem_addr(&eg[st]));  // dO_s read for the last time
+                mma_commit_w(smem_addr(&eg[s % C::NGS]));  // dO_s read for the last time
                 const bool more = s + 1 < n_steps;
                 if (more) {
-                    if (!wait_stage(fq, s + 1)) { ok = false; break; }
+                    if (!wait_q(s + 1)) { ok = false; break; }
                     mma_st(s + 1);
                     mma_commit_w(smem_addr(&st_full));
                 }
@@ -300,9 +323,9 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 for (int kk = 0; kk < BM / 16; ++kk)
                     mma_ts_w(tmem + cK, tmem + a_col<W>(cP, kk), dQmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_w(smem_addr(&eq[st]));  // Q_s read for the last time (its vectors by the elementwise warps before ds_ready)
+                mma_commit_w(smem_addr(&eq[s % C::NQS]));  // Q_s read for the last time (its vectors by the elementwise warps before ds_ready)
                 if (more) {
-                    if (!wait_stage(fg, s + 1)) { ok = false; break; }
+                    if (!wait_g(s + 1)) { ok = false; break; }
                     mma_dpt(s + 1);
                     mma_commit_w(smem_addr(&dp_full));
                 }
@@ -327,14 +350,14 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const float sl = prm.sl;
         bool ok = true;
         for (int s = 0; s < n_steps; ++s) {
-            const int st = s & 1, q0 = (first + s) * BM + hf * W;
+            const int qs = s % C::NQS, q0 = (first + s) * BM + hf * W;
             if (!wait_or_abort(smem_addr(&st_full), (uint32_t)(s & 1), limit, &abort_flag) ||
-                !wait_or_abort(smem_addr(&fq[st]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) {
+                !wait_or_abort(smem_addr(&fq[qs]), (uint32_t)((s / C::NQS) & 1), limit, &abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const float4 *vec = reinterpret_cast<const float4 *>(smem + C::RES + st * C::STAGE + 2 * C::TILE) + hf * (W / 4);
+            const float4 *vec = reinterpret_cast<const float4 *>(smem + oVec + qs * VEC_BYTES) + hf * (W / 4);
             // Tiles with no padded key or query and wholly below the diagonal
             // take the unmasked path (no per-element tests or selects).
             const int qt0 = (first + s) * BM;
@@ -449,9 +472,9 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     using E = EW<D>;
     constexpr int W = E::W, TMA_WARP = E::TMA_WARP, MMA_WARP = E::MMA_WARP;
     extern __shared__ uint8_t smem_raw[];
-    // per stage slot: fk/ek for K_j, fv/ev for V_j (V_j is freed by the earlier dP
+    // per ring slot: fk/ek for K_j, fv/ev for V_j (V_j is freed by the earlier dP
     // product and loaded second, so K_j, needed first, lands sooner)
-    __shared__ __align__(8) uint64_t res_full, fk[2], ek[2], fv[2], ev[2], s_full, dp_full, s_read, ds_ready, o_full,
+    __shared__ __align__(8) uint64_t res_full, fk[C::NKS], ek[C::NKS], fv[C::NVS], ev[C::NVS], s_full, dp_full, s_read, ds_ready, o_full,
         drain;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
@@ -468,14 +491,17 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     // per-query vectors)
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t s_base = smem_addr(smem);
-    const uint32_t sQ = s_base, sG = s_base + C::TILE, sStage = s_base + C::RES;
+    const uint32_t sQ = s_base, sG = s_base + C::TILE;
+    const uint32_t sKr = s_base + C::RES, sVr = sKr + C::NKS * C::TILE;  // K ring, V ring
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(smem_addr(&res_full), 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < C::NKS; ++s) {
             mbar_init(smem_addr(&fk[s]), 1);
             mbar_init(smem_addr(&ek[s]), 1);
+        }
+        for (int s = 0; s < C::NVS; ++s) {
             mbar_init(smem_addr(&fv[s]), 1);
             mbar_init(smem_addr(&ev[s]), 1);
         }
@@ -511,31 +537,30 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 tma_load_3d(sG + c * BOX, &tm_g, smem_addr(&res_full), c * 64, q0, bh, pol);
             }
             for (int s = 0; s < n_steps; ++s) {
-                const int st = s & 1, k0 = s * BM;
-                const uint32_t par = (uint32_t)(((s >> 1) & 1) ^ 1), dst = sStage + st * C::STAGE;
-                if (!wait_or_abort(smem_addr(&ek[st]), par, limit, &abort_flag)) {
+                const int ks = s % C::NKS, vs = s % C::NVS, k0 = s * BM;
+                if (!wait_or_abort(smem_addr(&ek[ks]), (uint32_t)(((s / C::NKS) & 1) ^ 1), limit, &abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint32_t bk = smem_addr(&fk[st]);
+                const uint32_t bk = smem_addr(&fk[ks]);
                 mbar_arrive_expect_tx(bk, C::TILE);
-                for (int c = 0; c < C::CH; ++c) tma_load_3d(dst + c * BOX, &tm_k, bk, c * 64, k0, bh, pol);
+                for (int c = 0; c < C::CH; ++c) tma_load_3d(sKr + ks * C::TILE + c * BOX, &tm_k, bk, c * 64, k0, bh, pol);
                 issued_k = s + 1;
-                if (!wait_or_abort(smem_addr(&ev[st]), par, limit, &abort_flag)) {
+                if (!wait_or_abort(smem_addr(&ev[vs]), (uint32_t)(((s / C::NVS) & 1) ^ 1), limit, &abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint32_t bv = smem_addr(&fv[st]);
+                const uint32_t bv = smem_addr(&fv[vs]);
                 mbar_arrive_expect_tx(bv, C::TILE);
-                for (int c = 0; c < C::CH; ++c) tma_load_3d(dst + C::TILE + c * BOX, &tm_v, bv, c * 64, k0, bh, pol);
+                for (int c = 0; c < C::CH; ++c) tma_load_3d(sVr + vs * C::TILE + c * BOX, &tm_v, bv, c * 64, k0, bh, pol);
                 issued_v = s + 1;
             }
             if (!ok) {
                 if (!abort_flag) fail_bwd(&abort_flag);
-                for (int s = (issued_k > 2 ? issued_k - 2 : 0); s < issued_k; ++s)
-                    mbar_wait_bounded(smem_addr(&fk[s & 1]), (uint32_t)((s >> 1) & 1), limit);
-                for (int s = (issued_v > 2 ? issued_v - 2 : 0); s < issued_v; ++s)
-                    mbar_wait_bounded(smem_addr(&fv[s & 1]), (uint32_t)((s >> 1) & 1), limit);
+                for (int s = (issued_k > C::NKS ? issued_k - C::NKS : 0); s < issued_k; ++s)
+                    mbar_wait_bounded(smem_addr(&fk[s % C::NKS]), (uint32_t)((s / C::NKS) & 1), limit);
+                for (int s = (issued_v > C::NVS ? issued_v - C::NVS : 0); s < issued_v; ++s)
+                    mbar_wait_bounded(smem_addr(&fv[s % C::NVS]), (uint32_t)((s / C::NVS) & 1), limit);
                 mbar_wait_bounded(smem_addr(&res_full), 0, limit);
             }
         }
@@ -545,14 +570,20 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0), id_o = idesc_bf16_f32(BM, D, 0, 1);
             const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), dG = sdesc_sw128(sG, 16, 1024);
             bool ok = wait_or_abort_w(smem_addr(&res_full), 0, limit, &abort_flag), issued = false;
-            auto wait_stage = [&](uint64_t *bars, int s) -> bool {
-                if (!wait_or_abort_w(smem_addr(&bars[s & 1]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) return false;
+            // K_s in ring slot s % KQ, V_s in slot s % 2
+            auto wait_k = [&](int s) -> bool {
+                if (!wait_or_abort_w(smem_addr(&fk[s % C::NKS]), (uint32_t)((s / C::NKS) & 1), limit, &abort_flag)) return false;
+                tc_fence_after();
+                return true;
+            };
+            auto wait_v = [&](int s) -> bool {
+                if (!wait_or_abort_w(smem_addr(&fv[s % C::NVS]), (uint32_t)((s / C::NVS) & 1), limit, &abort_flag)) return false;
                 tc_fence_after();
                 return true;
             };
             // S(s) = Q K_s^T into cS; dP(s) = dO V_s^T into cP
             auto mma_s = [&](int s) {
-                const uint64_t dK = sdesc_sw128(sStage + (s & 1) * C::STAGE, 16, 1024);
+                const uint64_t dK = sdesc_sw128(sKr + (s % C::NKS) * C::TILE, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
@@ -561,17 +592,17 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 issued = true;
             };
             auto mma_dp = [&](int s) {
-                const uint64_t dV = sdesc_sw128(sStage + (s & 1) * C::STAGE + C::TILE, 16, 1024);
+                const uint64_t dV = sdesc_sw128(sVr + (s % C::NVS) * C::TILE, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
                     mma_ss_w(tmem + cP, dG + off, dV + off, id_s, kk > 0 ? 1u : 0u);
                 }
             };
-            if (ok && (ok = wait_stage(fk, 0))) {
+            if (ok && (ok = wait_k(0))) {
                 mma_s(0);
                 mma_commit_w(smem_addr(&s_full));
-                if ((ok = wait_stage(fv, 0))) {
+                if ((ok = wait_v(0))) {
                     mma_dp(0);
                     mma_commit_w(smem_addr(&dp_full));
                     mma_commit_w(smem_addr(&ev[0]));  // V_0 read for the last time
@@ -581,10 +612,9 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             // overlaps their dS(s)); dQ(s) once dS(s) is written over dP(s);
             // then dP(s+1) into the columns dQ(s) has just read.
             for (int s = 0; ok && s < n_steps; ++s) {
-                const int st = s & 1;
                 const bool more = s + 1 < n_steps;
                 if (more) {
-                    if (!wait_or_abort_w(smem_addr(&s_read), (uint32_t)(s & 1), limit, &abort_flag) || !wait_stage(fk, s + 1)) {
+                    if (!wait_or_abort_w(smem_addr(&s_read), (uint32_t)(s & 1), limit, &abort_flag) || !wait_k(s + 1)) {
                         ok = false;
                         break;
                     }
@@ -593,17 +623,17 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 }
                 if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint64_t dKmn = sdesc_sw128(sStage + st * C::STAGE, BOX, 1024);
+                const uint64_t dKmn = sdesc_sw128(sKr + (s % C::NKS) * C::TILE, BOX, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)
                     mma_ts_w(tmem + cQ, tmem + a_col<W>(cP, kk), dKmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_w(smem_addr(&ek[st]));  // K_s read for the last time
+                mma_commit_w(smem_addr(&ek[s % C::NKS]));  // K_s read for the last time
                 if (more) {
-                    if (!wait_stage(fv, s + 1)) { ok = false; break; }
+                    if (!wait_v(s + 1)) { ok = false; break; }
                     mma_dp(s + 1);
                     mma_commit_w(smem_addr(&dp_full));
-                    mma_commit_w(smem_addr(&ev[(s + 1) & 1]));  // V_(s+1) read for the last time
+                    mma_commit_w(smem_addr(&ev[(s + 1) % C::NVS]));  // V_(s+1) read for the last time
                 }
             }
             if (ok) {
@@ -770,12 +800,12 @@ cudaError_t launch_dims(const BackwardProblem &p, float *delta, float *lse2, int
     auto kv = fa_bwd_dkdv_tc<D, CAUSAL>;
     auto kq = fa_bwd_dq_tc<D, CAUSAL>;
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_REQ)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_REQ)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_KV_REQ)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_Q_REQ)) != cudaSuccess) return e;
     const unsigned grid = (unsigned)((int64_t)prm.n_q * BH);
-    kv<<<grid, EW<D>::NUM_THREADS, C::SMEM_REQ, stream>>>(mq, mk, mv, mg, prm);
+    kv<<<grid, EW<D>::NUM_THREADS, C::SMEM_KV_REQ, stream>>>(mq, mk, mv, mg, prm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    kq<<<grid, EW<D>::NUM_THREADS, C::SMEM_REQ, stream>>>(mq, mk, mv, mg, prm);
+    kq<<<grid, EW<D>::NUM_THREADS, C::SMEM_Q_REQ, stream>>>(mq, mk, mv, mg, prm);
     return cudaGetLastError();
 }
 
