@@ -8,7 +8,8 @@ CUDA path.
 ``attention_rows`` / ``attention`` wrap ``oracle.c`` (the three passes of
 "Safe Softmax and the Three Passes" in "The Details of Flash Attention",
 fp64); ``attention_backward`` is the gradient of that definition written
-out; ``tiled_model`` holds a second, tile-by-tile restatement of the online
+out, and ``attention_backward_sampled`` the same gradient for chosen query
+rows and keys only (for problems too large for N x N weights); ``tiled_model`` holds a second, tile-by-tile restatement of the online
 recurrence used only to pin the intermediate numbers of the worked example.
 Row chunks run on host threads (ctypes releases the GIL during the C call).
 """
@@ -140,3 +141,60 @@ def attention_backward(q, k, v, dout, scale, causal=False, threads=None):
         raise RuntimeError("oracle_attention_backward_head failed")
     shape = (B, H, N, d)
     return dq.reshape(shape), dk.reshape(shape), dv.reshape(shape)
+
+
+def attention_backward_sampled(q, k, v, dout, scale, causal, rows, keys, threads=None):
+    """Gradients of chosen query rows (dQ) and chosen keys (dK, dV), float64.
+
+    The definition of ``attention_backward`` evaluated for a subset: with
+    S_ij = scale * q_i . k_j, the row statistics LSE_i and O_i of the forward
+    oracle, P_ij = exp(S_ij - LSE_i) (0 for a masked pair), dP_ij = dO_i . v_j
+    and delta_i = dO_i . O_i (= sum_j P_ij dP_ij):
+
+        dQ_i = scale * sum_j P_ij (dP_ij - delta_i) k_j
+        dK_j = scale * sum_i P_ij (dP_ij - delta_i) q_i
+        dV_j = sum_i P_ij dO_i
+
+    rows / keys hold flat ids bh * N + i.  A key's gradients sum over every
+    query of its head, so each head with a chosen key gets the forward oracle
+    over all of its rows.  Returns (dq[len(rows), d], dk[len(keys), d],
+    dv[len(keys), d]).
+    """
+    q, k, v, dout = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k, v, dout))
+    if q.ndim != 4 or not (q.shape == k.shape == v.shape == dout.shape):
+        raise ValueError("q, k, v, dout must be [B, H, N, d] arrays of one shape")
+    B, H, N, d = q.shape
+    rows = np.ascontiguousarray(rows, dtype=np.int64).ravel()
+    keys = np.ascontiguousarray(keys, dtype=np.int64).ravel()
+    if np.any((rows < 0) | (rows >= B * H * N)) or np.any((keys < 0) | (keys >= B * H * N)):
+        raise ValueError("row or key id out of range")
+    qf, kf, vf, gf = (x.reshape(B * H, N, d).astype(np.float64) for x in (q, k, v, dout))
+    dq = np.empty((rows.size, d))
+    dk = np.empty((keys.size, d))
+    dv = np.empty((keys.size, d))
+    # query rows: their own statistics suffice
+    if rows.size:
+        o_r, lse_r = attention_rows(q, k, v, scale, causal, rows, threads)
+        for n, r in enumerate(rows):
+            bh, i = divmod(int(r), N)
+            nk = i + 1 if causal else N
+            s = scale * (kf[bh, :nk] @ qf[bh, i])
+            p = np.exp(s - lse_r[n])
+            dp = vf[bh, :nk] @ gf[bh, i]
+            delta = float(gf[bh, i] @ o_r[n])
+            dq[n] = scale * ((p * (dp - delta)) @ kf[bh, :nk])
+    # keys: every query of the head
+    for bh in np.unique(keys // N):
+        sel = np.nonzero(keys // N == bh)[0]
+        js = keys[sel] - bh * N
+        o_h, lse_h = attention_rows(q, k, v, scale, causal, np.arange(N, dtype=np.int64) + bh * N, threads)
+        delta = np.einsum("id,id->i", gf[bh], o_h)
+        s = scale * (qf[bh] @ kf[bh, js].T)                      # [N queries, chosen keys]
+        p = np.exp(s - lse_h[:, None])
+        if causal:
+            p = np.where(np.arange(N)[:, None] >= js[None, :], p, 0.0)
+        dp = gf[bh] @ vf[bh, js].T
+        ds = p * (dp - delta[:, None])
+        dk[sel] = scale * (ds.T @ qf[bh])
+        dv[sel] = p.T @ gf[bh]
+    return dq, dk, dv

@@ -16,7 +16,7 @@ import torch
 import oracle
 import synth
 import tiled_online_softmax_attn_gb300 as fa
-from parity import half_ulp_bf16
+from parity import half_ulp_bf16, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -24,28 +24,39 @@ TORCH_DT = {"bf16": torch.bfloat16, "fp32": torch.float32}
 REL = {"bf16": 2e-2, "fp32": 1e-5}
 
 
-def run_backward(B, H, N, d, dtype, causal, grad_dtype=None, seed=0):
-    w = synth.Workload("t", B, H, N, d, dtype, causal, seed=seed)
-    q, k, v = w.inputs()
-    dout = synth.tensor(3 * seed + 9, w.shape, dtype)
-    tdt = TORCH_DT[dtype]
-    qd, kd, vd, gd = (torch.from_numpy(x).cuda().to(tdt) for x in (q, k, v, dout))
-    o, lse = fa.fa_forward(qd, kd, vd, scale=w.scale, causal=causal)
-    gdt = TORCH_DT[grad_dtype or dtype]
-    dq, dk, dv = fa.fa_backward(qd, kd, vd, o, gd, lse, scale=w.scale, causal=causal, grad_dtype=gdt)
-    torch.cuda.synchronize()
-    assert fa.check_device_error() == fa.FA_OK, fa.last_error()
-    ref = oracle.attention_backward(q, k, v, dout, w.scale, causal)
+def _check(grads, ref, dtype, grad_dtype):
     stats = {}
-    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
-        g = g.float().cpu().numpy().astype(np.float64)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        if np.size(r) == 0:
+            continue
+        g = np.asarray(g, dtype=np.float64)
         err = np.abs(g - r)
         bound = REL[dtype] * np.abs(r).max()
-        if (grad_dtype or dtype) == "bf16":
+        if grad_dtype == "bf16":
             bound = bound + half_ulp_bf16(r)
         stats[name] = (float(err.max()), float(np.abs(r).max()))
         assert np.all(err <= bound), f"{name}: max err {err.max():.3e} vs scale {np.abs(r).max():.3e}"
     return stats
+
+
+def _gpu_backward(w, q, k, v, dout, grad_dtype=None):
+    tdt = TORCH_DT[w.dtype]
+    qd, kd, vd, gd = (torch.from_numpy(x).cuda().to(tdt) for x in (q, k, v, dout))
+    o, lse = fa.fa_forward(qd, kd, vd, scale=w.scale, causal=w.causal)
+    gdt = TORCH_DT[grad_dtype or w.dtype]
+    dq, dk, dv = fa.fa_backward(qd, kd, vd, o, gd, lse, scale=w.scale, causal=w.causal, grad_dtype=gdt)
+    torch.cuda.synchronize()
+    assert fa.check_device_error() == fa.FA_OK, fa.last_error()
+    return dq, dk, dv
+
+
+def run_backward(B, H, N, d, dtype, causal, grad_dtype=None, seed=0):
+    w = synth.Workload("t", B, H, N, d, dtype, causal, seed=seed)
+    q, k, v = w.inputs()
+    dout = synth.tensor(3 * seed + 9, w.shape, dtype)
+    grads = _gpu_backward(w, q, k, v, dout, grad_dtype)
+    ref = oracle.attention_backward(q, k, v, dout, w.scale, causal)
+    return _check([g.float().cpu().numpy() for g in grads], ref, dtype, grad_dtype or dtype)
 
 
 SHAPES = [
@@ -79,3 +90,45 @@ def test_backward_is_deterministic():
     torch.cuda.synchronize()
     for u, w in zip(a, b):
         assert torch.equal(u, w)
+
+
+def test_full_size_multihead_backward_heads():
+    """The multi-head workload at full size (B=4, H=32, N=4096, d=128, the
+    inputs and launch the backward benchmark times): three whole heads, from
+    different batches and head indices, against the gradient oracle (every
+    dQ, dK and dV element of those heads)."""
+    w = synth.WORKLOADS["multihead"]
+    q, k, v = w.inputs()
+    dout = synth.tensor(3 * w.seed + 9, w.shape, w.dtype)
+    grads = _gpu_backward(w, q, k, v, dout)
+    heads = [(0, 0), (1, 17), (3, 31)]
+
+    def pick(x):
+        return np.stack([x[b, h] for b, h in heads])[None]
+
+    got = [pick(g.float().cpu().numpy()) for g in grads]
+    ref = oracle.attention_backward(pick(q), pick(k), pick(v), pick(dout), w.scale, False)
+    _check(got, ref, w.dtype, w.dtype)
+
+
+@pytest.mark.parametrize("name,key_heads", [("causal", 2), ("peaked", 0)])
+def test_full_size_backward_sampled(name, key_heads):
+    """The causal (1x32x16384x128) and peaked (1x8x65536x64, Q and K x 4)
+    workloads at full size, in the launch the backward benchmark times: dQ of
+    sampled query rows in every head (rows 0, N-1, tile edges and a seeded
+    draw) and, for the causal workload, dK and dV of sampled keys in the
+    first and last head (a key's gradients sum over all queries of its head,
+    so a head with a sampled key costs the oracle a full forward)."""
+    w = synth.WORKLOADS[name]
+    q, k, v = w.inputs()
+    dout = synth.tensor(3 * w.seed + 9, w.shape, w.dtype)
+    dq, dk, dv = (g.float().cpu().numpy().reshape(-1, w.d) for g in _gpu_backward(w, q, k, v, dout))
+    rows = sample_rows(w.B, w.H, w.N, 192, seed=w.seed)
+    rng = np.random.default_rng(w.seed + 1)
+    keys = []
+    for bh in [0, w.B * w.H - 1][:key_heads]:
+        picks = [0, 1, 127, 128, w.N // 2, w.N - 129, w.N - 128, w.N - 1]
+        keys += [bh * w.N + j for j in picks] + list(bh * w.N + rng.integers(0, w.N, size=12))
+    keys = np.unique(np.array(keys, dtype=np.int64))
+    ref = oracle.attention_backward_sampled(q, k, v, dout, w.scale, w.causal, rows, keys)
+    _check([dq[rows], dk[keys], dv[keys]], ref, w.dtype, w.dtype)

@@ -78,3 +78,22 @@ def test_value_gradient_is_linear_in_upstream_gradient():
     c = oracle.attention_backward(q, k, v, g1 + 2 * g2, 0.5, True)
     for x, y, z in zip(a, b, c):
         np.testing.assert_allclose(z, x + 2 * y, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_gradients_equal_the_full_gradients(causal):
+    """The subset form evaluates the same definition: on shapes the full
+    oracle handles it must give the same dQ rows and dK, dV rows (a wrong
+    mask direction, a row statistic of the wrong head or a missing delta
+    term would break this)."""
+    rng = np.random.default_rng(420 + causal)
+    B, H, N, d = 2, 3, 37, 6
+    q, k, v, dout = (rng.standard_normal((B, H, N, d)).astype(np.float32) for _ in range(4))
+    scale = 0.4
+    dq, dk, dv = (x.reshape(-1, d) for x in oracle.attention_backward(q, k, v, dout, scale, causal))
+    rows = np.array([0, 5, N - 1, N, 2 * N + 17, B * H * N - 1])
+    keys = np.array([0, 1, N - 1, 3 * N, 3 * N + 20, B * H * N - 2, B * H * N - 1])
+    sq, sk, sv = oracle.attention_backward_sampled(q, k, v, dout, scale, causal, rows, keys)
+    np.testing.assert_allclose(sq, dq[rows], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(sk, dk[keys], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(sv, dv[keys], rtol=1e-10, atol=1e-12)
