@@ -159,7 +159,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     // per ring slot: fq/eq for Q_i and its LSE/delta vectors, fg/eg for dO_i (dO_i is
     // freed by the earlier dV product and loaded second, so Q_i, needed first, lands sooner)
-    __shared__ __align__(8) uint64_t res_full, fq[C::NQS], eq[C::NQS], fg[C::NGS], eg[C::NGS], st_full, dp_full, p_ready, ds_ready, o_full,
+    __shared__ __align__(8) uint64_t res_full, fq[C::NQS], eq[C::NQS], fg[C::NGS], eg[C::NGS], st_full[2], dp_full, p_ready, ds_ready, o_full,
         drain;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
@@ -192,7 +192,8 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             mbar_init(smem_addr(&fg[s]), 1);
             mbar_init(smem_addr(&eg[s]), 1);
         }
-        mbar_init(smem_addr(&st_full), 1);
+        mbar_init(smem_addr(&st_full[0]), 1);
+        mbar_init(smem_addr(&st_full[1]), 1);
         mbar_init(smem_addr(&dp_full), 1);
         mbar_init(smem_addr(&p_ready), E::THREADS);
         mbar_init(smem_addr(&ds_ready), E::THREADS);
@@ -210,8 +211,16 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t tmem = tmem_base_s;
     const uint64_t limit = prm.limit;
     // tensor memory: S^T/P^T [0,128), dP^T/dS^T [128,256), dV [256,256+D), dK [256+D, 256+2D);
-    // the column half h of P^T (dS^T) is written over columns [64h, 64h + 32) of S^T (dP^T)
-    const uint32_t cS = 0, cP = 128, cV = 256, cK = 256 + D;
+    // the column half h of P^T (dS^T) is written over columns [64h, 64h + 32) of S^T (dP^T).
+    // At D = 64 the free columns [384, 512) hold a second S^T/P^T buffer: S^T(s) goes to
+    // buffer s % 2, so S^T(s+2) is issued as soon as dV(s) has been issued (it reads
+    // P^T(s) from that buffer first), two steps ahead, with a full barrier per buffer.
+    constexpr bool SB = D == 64;
+    constexpr int AHEAD = SB ? 2 : 1;  // S^T products issued ahead of the elementwise step
+    const uint32_t cP = 128, cV = 256, cK = 256 + D;
+    auto cS_of = [](int s) -> uint32_t { return (SB && (s & 1)) ? 256u + 2u * D : 0u; };
+    auto st_bar = [](int s) { return SB ? (s & 1) : 0; };
+    auto st_par = [](int s) -> uint32_t { return (uint32_t)((SB ? s >> 1 : s) & 1); };
 
     if (warp == TMA_WARP) {
         if (lane == 0) {
@@ -264,10 +273,11 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // S^T(s) = K Q_s^T into cS, dP^T(s) = V dO_s^T into cP
             auto mma_st = [&](int s) {
                 const uint64_t dQ = sdesc_sw128(sQr + (s % C::NQS) * C::TILE, 16, 1024);
+                const uint32_t d_s = tmem + cS_of(s);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
-                    mma_ss_w(tmem + cS, dK + off, dQ + off, id_s, kk > 0 ? 1u : 0u);
+                    mma_ss_w(d_s, dK + off, dQ + off, id_s, kk > 0 ? 1u : 0u);
                 }
                 issued = true;
             };
@@ -292,13 +302,19 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             };
             if (ok && (ok = wait_q(0))) {
                 mma_st(0);
-                mma_commit_w(smem_addr(&st_full));
+                mma_commit_w(smem_addr(&st_full[0]));
                 if ((ok = wait_g(0))) {
                     mma_dpt(0);
                     mma_commit_w(smem_addr(&dp_full));
                 }
+                for (int s = 1; ok && s < AHEAD && s < n_steps; ++s) {
+                    if ((ok = wait_q(s))) {
+                        mma_st(s);
+                        mma_commit_w(smem_addr(&st_full[st_bar(s)]));
+                    }
+                }
             }
-            // Per step: dV(s) once P^T(s) is written; then S^T(s+1) into the
+            // Per step: dV(s) once P^T(s) is written; then S^T(s+AHEAD) into the
             // columns dV(s) has just read (same-thread MMAs run in order), so
             // it overlaps the elementwise warps' dS^T(s); then dK(s) and dP^T(s+1).
             for (int s = 0; ok && s < n_steps; ++s) {
@@ -308,14 +324,14 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const uint64_t dQmn = sdesc_sw128(sQr + (s % C::NQS) * C::TILE, BOX, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts_w(tmem + cV, tmem + a_col<W>(cS, kk), dGmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                    mma_ts_w(tmem + cV, tmem + a_col<W>(cS_of(s), kk), dGmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
                            (s > 0 || kk > 0) ? 1u : 0u);
                 mma_commit_w(smem_addr(&eg[s % C::NGS]));  // dO_s read for the last time
                 const bool more = s + 1 < n_steps;
-                if (more) {
-                    if (!wait_q(s + 1)) { ok = false; break; }
-                    mma_st(s + 1);
-                    mma_commit_w(smem_addr(&st_full));
+                if (s + AHEAD < n_steps) {
+                    if (!wait_q(s + AHEAD)) { ok = false; break; }
+                    mma_st(s + AHEAD);
+                    mma_commit_w(smem_addr(&st_full[st_bar(s + AHEAD)]));
                 }
                 if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
@@ -346,12 +362,13 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int quarter = warp & 3, hf = warp >> 2;
         const int jr = quarter * 32 + lane, kj = k0 + jr;
         const uint32_t lb = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t cSh = cS + hf * W, cPh = cP + hf * W;
+        const uint32_t cPh = cP + hf * W;
         const float sl = prm.sl;
         bool ok = true;
         for (int s = 0; s < n_steps; ++s) {
             const int qs = s % C::NQS, q0 = (first + s) * BM + hf * W;
-            if (!wait_or_abort(smem_addr(&st_full), (uint32_t)(s & 1), limit, &abort_flag) ||
+            const uint32_t cSh = cS_of(s) + hf * W;
+            if (!wait_or_abort(smem_addr(&st_full[st_bar(s)]), st_par(s), limit, &abort_flag) ||
                 !wait_or_abort(smem_addr(&fq[qs]), (uint32_t)((s / C::NQS) & 1), limit, &abort_flag)) {
                 ok = false;
                 break;
