@@ -274,20 +274,26 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             auto mma_st = [&](int s) {
                 const uint64_t dQ = sdesc_sw128(sQr + (s % C::NQS) * C::TILE, 16, 1024);
                 const uint32_t d_s = tmem + cS_of(s);
+                uint64_t ka[D / 16], kb[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
-                    mma_ss_w(d_s, dK + off, dQ + off, id_s, kk > 0 ? 1u : 0u);
+                    ka[kk] = dK + off;
+                    kb[kk] = dQ + off;
                 }
+                mma_ss_k<D / 16>(d_s, ka, kb, id_s, 0u);
                 issued = true;
             };
             auto mma_dpt = [&](int s) {
                 const uint64_t dG = sdesc_sw128(sGr + (s % C::NGS) * C::TILE, 16, 1024);
+                uint64_t ka[D / 16], kb[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
-                    mma_ss_w(tmem + cP, dV + off, dG + off, id_s, kk > 0 ? 1u : 0u);
+                    ka[kk] = dV + off;
+                    kb[kk] = dG + off;
                 }
+                mma_ss_k<D / 16>(tmem + cP, ka, kb, id_s, 0u);
             };
             // Q_s in ring slot s % NQS, dO_s in slot s % NGS
             auto wait_q = [&](int s) -> bool {
@@ -322,10 +328,16 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tc_fence_after();
                 const uint64_t dGmn = sdesc_sw128(sGr + (s % C::NGS) * C::TILE, BOX, 1024);
                 const uint64_t dQmn = sdesc_sw128(sQr + (s % C::NQS) * C::TILE, BOX, 1024);
+                {
+                    uint32_t ta[BM / 16];
+                    uint64_t tb[BM / 16];
 #pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts_w(tmem + cV, tmem + a_col<W>(cS_of(s), kk), dGmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
-                           (s > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BM / 16; ++kk) {
+                        ta[kk] = tmem + a_col<W>(cS_of(s), kk);
+                        tb[kk] = dGmn + (uint64_t)((kk * 16 * 128) >> 4);
+                    }
+                    mma_ts_k<BM / 16>(tmem + cV, ta, tb, id_o, s > 0 ? 1u : 0u);
+                }
                 mma_commit_w(smem_addr(&eg[s % C::NGS]));  // dO_s read for the last time
                 const bool more = s + 1 < n_steps;
                 if (s + AHEAD < n_steps) {
@@ -335,10 +347,16 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
+                {
+                    uint32_t ta[BM / 16];
+                    uint64_t tb[BM / 16];
 #pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts_w(tmem + cK, tmem + a_col<W>(cP, kk), dQmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
-                           (s > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BM / 16; ++kk) {
+                        ta[kk] = tmem + a_col<W>(cP, kk);
+                        tb[kk] = dQmn + (uint64_t)((kk * 16 * 128) >> 4);
+                    }
+                    mma_ts_k<BM / 16>(tmem + cK, ta, tb, id_o, s > 0 ? 1u : 0u);
+                }
                 mma_commit_w(smem_addr(&eq[s % C::NQS]));  // Q_s read for the last time (its vectors by the elementwise warps before ds_ready)
                 if (more) {
                     if (!wait_g(s + 1)) { ok = false; break; }
@@ -601,20 +619,26 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             // S(s) = Q K_s^T into cS; dP(s) = dO V_s^T into cP
             auto mma_s = [&](int s) {
                 const uint64_t dK = sdesc_sw128(sKr + (s % C::NKS) * C::TILE, 16, 1024);
+                uint64_t ka[D / 16], kb[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
-                    mma_ss_w(tmem + cS, dQ + off, dK + off, id_s, kk > 0 ? 1u : 0u);
+                    ka[kk] = dQ + off;
+                    kb[kk] = dK + off;
                 }
+                mma_ss_k<D / 16>(tmem + cS, ka, kb, id_s, 0u);
                 issued = true;
             };
             auto mma_dp = [&](int s) {
                 const uint64_t dV = sdesc_sw128(sVr + (s % C::NVS) * C::TILE, 16, 1024);
+                uint64_t ka[D / 16], kb[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * BOX + (kk & 3) * 32) >> 4);
-                    mma_ss_w(tmem + cP, dG + off, dV + off, id_s, kk > 0 ? 1u : 0u);
+                    ka[kk] = dG + off;
+                    kb[kk] = dV + off;
                 }
+                mma_ss_k<D / 16>(tmem + cP, ka, kb, id_s, 0u);
             };
             if (ok && (ok = wait_k(0))) {
                 mma_s(0);
@@ -641,10 +665,16 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t dKmn = sdesc_sw128(sKr + (s % C::NKS) * C::TILE, BOX, 1024);
+                {
+                    uint32_t ta[BM / 16];
+                    uint64_t tb[BM / 16];
 #pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts_w(tmem + cQ, tmem + a_col<W>(cP, kk), dKmn + (uint64_t)((kk * 16 * 128) >> 4), id_o,
-                           (s > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BM / 16; ++kk) {
+                        ta[kk] = tmem + a_col<W>(cP, kk);
+                        tb[kk] = dKmn + (uint64_t)((kk * 16 * 128) >> 4);
+                    }
+                    mma_ts_k<BM / 16>(tmem + cQ, ta, tb, id_o, s > 0 ? 1u : 0u);
+                }
                 mma_commit_w(smem_addr(&ek[s % C::NKS]));  // K_s read for the last time
                 if (more) {
                     if (!wait_v(s + 1)) { ok = false; break; }

@@ -241,6 +241,84 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint6
         : "memory");
 }
 
+// A K loop of 4 or 8 MMAs into one accumulator, issued by one elected lane of
+// a converged warp under a single elect.sync: the first MMA accumulates when
+// `accumulate` is non-zero, the others always.  Same effect as the per-MMA
+// helpers above in a loop, with one election instead of one per MMA (the
+// issuing warp shares its sub-partition with busy elementwise warps, so every
+// instruction it saves shortens the issue).
+template <int NK>
+__device__ __forceinline__ void mma_ss_k(uint32_t d_tmem, const uint64_t (&a)[NK], const uint64_t (&b)[NK],
+                                         uint32_t idesc, uint32_t accumulate)
+{
+    static_assert(NK == 4 || NK == 8, "mma_ss_k: 4 or 8 MMAs");
+    if constexpr (NK == 4) {
+        asm volatile(
+            "{\n\t.reg .pred p, q, e;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "setp.ne.b32 p, %10, 0;\n\t"
+            "setp.eq.b32 q, %10, %10;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %9, p;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %9, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %9, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %9, q;\n\t}"
+            ::"r"(d_tmem), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p, q, e;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "setp.ne.b32 p, %18, 0;\n\t"
+            "setp.eq.b32 q, %18, %18;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %17, p;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %17, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %17, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %17, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %17, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %17, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %17, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %17, q;\n\t}"
+            ::"r"(d_tmem), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(accumulate)
+            : "memory");
+    }
+}
+
+template <int NK>
+__device__ __forceinline__ void mma_ts_k(uint32_t d_tmem, const uint32_t (&a)[NK], const uint64_t (&b)[NK],
+                                         uint32_t idesc, uint32_t accumulate)
+{
+    static_assert(NK == 4 || NK == 8, "mma_ts_k: 4 or 8 MMAs");
+    if constexpr (NK == 4) {
+        asm volatile(
+            "{\n\t.reg .pred p, q, e;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "setp.ne.b32 p, %10, 0;\n\t"
+            "setp.eq.b32 q, %10, %10;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %9, p;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %9, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %9, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %9, q;\n\t}"
+            ::"r"(d_tmem), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p, q, e;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "setp.ne.b32 p, %18, 0;\n\t"
+            "setp.eq.b32 q, %18, %18;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %17, p;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %17, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %17, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %17, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %17, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %17, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %17, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %17, q;\n\t}"
+            ::"r"(d_tmem), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(accumulate)
+            : "memory");
+    }
+}
+
 __device__ __forceinline__ void mma_commit_w(uint32_t bar)
 {
     asm volatile(
