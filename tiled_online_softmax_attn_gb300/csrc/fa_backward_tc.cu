@@ -9,11 +9,12 @@
 //   streams the query tiles that see them.  Per query tile:
 //     S^T  = K_j Q_i^T       (SS MMA)          -> TMEM
 //     dP^T = V_j dO_i^T      (SS MMA)          -> TMEM
-//     P^T  = exp2(S^T scale log2 e - LSE_i log2 e)   (softmax warps; written
-//            over S^T as bf16)
+//     P^T  = exp2(S^T scale log2 e - LSE_i log2 e)   (elementwise warps)
 //     dV  += P^T dO_i        (A = P^T from TMEM, B = dO_i MN-major)
-//     dS^T = P^T (dP^T - delta_i)   (written over dP^T as bf16)
+//     dS^T = P^T (dP^T - delta_i)
 //     dK  += dS^T Q_i        (A = dS^T from TMEM, B = Q_i MN-major)
+//   P^T and dS^T are written as bf16 over the dP^T columns once those are in
+//   registers, so S^T(i+1) is computed while the warps work on tile i.
 //   dQ kernel -- a CTA owns 128 queries and streams the key tiles they see:
 //     S = Q_i K_j^T, dP = dO_i V_j^T, dS = P (dP - delta), dQ += dS K_j.
 //
@@ -72,6 +73,18 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t BOX = 128 * 128;  // one 128-row x 64-column bf16 box
 constexpr uint32_t VEC_BYTES = 1024;  // lse2 and delta of 128 rows
 
+// Barriers and flags of the dK/dV kernel, kept at the end of its dynamic shared
+// memory: at d = 128 its tiles take all but a few hundred bytes of the 227 KB a
+// CTA may have, so nothing is left for static shared memory.
+struct KvBars {
+    uint64_t res_full, st_full, s_read, dp_full, p_ready, ds_ready, o_full, drain;
+    uint64_t fq[4], eq[4], fg[3], eg[3], fvec[2], evec[2];
+    uint32_t tmem_base;
+    int abort_flag;
+};
+constexpr uint32_t KV_BARS_BYTES = (sizeof(KvBars) + 255u) & ~255u;
+constexpr uint32_t SMEM_MAX = 227u * 1024u;  // dynamic + static shared memory of one CTA
+
 template <int D>
 struct BCfg {
     static constexpr int CH = D / 64;
@@ -80,13 +93,15 @@ struct BCfg {
     // Streamed tiles in rings of their own.  The score product of the next
     // tile (S^T(s+1) / S(s+1)) is issued early, but a ring slot is freed only
     // by the last product of the tile it held, so the operand of the score
-    // product gets one slot more than the other one where shared memory allows
-    // (at d = 128 the dK/dV kernel keeps two of each: three Q slots leave room
-    // for one dO slot, which measured slower).
-    // dK/dV kernel: Q ring (each slot with the LSE/delta vectors of its rows), dO ring
-    static constexpr int NQS = D == 64 ? 4 : 2;
+    // product gets one slot more than the other one.
+    // dK/dV kernel: Q ring, dO ring, a two-slot ring of the LSE/delta vectors of
+    // the Q tile in work, and the barriers (three Q slots at d = 128: the score
+    // product S^T(s+1) is issued while dK(s-1) still reads Q(s-1)).  The tiles
+    // start on a 1024-byte boundary; the kernel checks that its layout fits.
+    static constexpr int NQS = D == 64 ? 4 : 3;
     static constexpr int NGS = D == 64 ? 3 : 2;
-    static constexpr uint32_t SMEM_KV = RES + (NQS + NGS) * TILE + NQS * VEC_BYTES + 1024;
+    static constexpr uint32_t KV_NEED = RES + (NQS + NGS) * TILE + 2 * VEC_BYTES + KV_BARS_BYTES;
+    static constexpr uint32_t SMEM_KV = KV_NEED + 1024 <= SMEM_MAX ? KV_NEED + 1024 : SMEM_MAX;
     // dQ kernel: K ring, V ring
     static constexpr int NKS = D == 64 ? 4 : 3;
     static constexpr int NVS = D == 64 ? 3 : 2;
@@ -94,7 +109,8 @@ struct BCfg {
     // keep one CTA per SM (all 512 tensor-memory columns each)
     static constexpr uint32_t SMEM_KV_REQ = SMEM_KV < 120u * 1024u ? 120u * 1024u : SMEM_KV;
     static constexpr uint32_t SMEM_Q_REQ = SMEM_Q < 120u * 1024u ? 120u * 1024u : SMEM_Q;
-    static_assert(SMEM_KV <= 227u * 1024u && SMEM_Q <= 227u * 1024u, "backward rings exceed shared memory");
+    static_assert(KV_NEED <= SMEM_MAX && SMEM_Q <= SMEM_MAX, "backward rings exceed shared memory");
+    static_assert(NQS <= 4 && NGS <= 3, "ring depths exceed the barrier arrays");
 };
 
 struct BwdParams {
@@ -157,13 +173,6 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     using E = EW<D>;
     constexpr int W = E::W, TMA_WARP = E::TMA_WARP, MMA_WARP = E::MMA_WARP;
     extern __shared__ uint8_t smem_raw[];
-    // per ring slot: fq/eq for Q_i and its LSE/delta vectors, fg/eg for dO_i (dO_i is
-    // freed by the earlier dV product and loaded second, so Q_i, needed first, lands sooner)
-    __shared__ __align__(8) uint64_t res_full, fq[C::NQS], eq[C::NQS], fg[C::NGS], eg[C::NGS], st_full[2], dp_full, p_ready, ds_ready, o_full,
-        drain;
-    __shared__ uint32_t tmem_base_s;
-    __shared__ volatile int abort_flag;
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = prm.N;
     const int kt = (int)(blockIdx.x % prm.n_q), bh = (int)(blockIdx.x / prm.n_q);
@@ -173,13 +182,30 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     // 1024-byte aligned base, derived from smem_raw by an offset so the
     // compiler keeps the shared address space (plain shared loads for the
-    // per-query vectors)
-    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    // per-query vectors).  The layout must fit the allocation (it does when the
+    // allocation starts within a few hundred bytes of a 1024-byte boundary, as
+    // a CTA's shared memory does without static shared variables): checked here,
+    // with every thread leaving before any barrier or tensor memory is touched.
+    const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+    if (pad + C::KV_NEED > C::SMEM_KV_REQ) {
+        if (threadIdx.x == 0) atomicOr(&g_bwd_error_word, 128u);
+        return;
+    }
+    uint8_t *smem = smem_raw + pad;
     const uint32_t s_base = smem_addr(smem);
     const uint32_t sK = s_base, sV = s_base + C::TILE;
-    // Q ring, dO ring, then the LSE/delta vectors of each Q slot
+    // Q ring, dO ring, the vector ring (LSE * log2 e, then delta, of 128 queries
+    // per slot), the barriers
     const uint32_t sQr = s_base + C::RES, sGr = sQr + C::NQS * C::TILE;
     const uint32_t oVec = C::RES + (C::NQS + C::NGS) * C::TILE;
+    KvBars &bars = *reinterpret_cast<KvBars *>(smem + C::KV_NEED - KV_BARS_BYTES);
+    // per ring slot: fq/eq for Q_i, fg/eg for dO_i (dO_i is freed by the earlier dV
+    // product and loaded second, so Q_i, needed first, lands sooner), fvec/evec for
+    // the vectors of the step in work (freed by the elementwise warps)
+    uint64_t &res_full = bars.res_full, &st_full = bars.st_full, &s_read = bars.s_read, &dp_full = bars.dp_full,
+             &p_ready = bars.p_ready, &ds_ready = bars.ds_ready, &o_full = bars.o_full, &drain = bars.drain;
+    uint64_t *fq = bars.fq, *eq = bars.eq, *fg = bars.fg, *eg = bars.eg, *fvec = bars.fvec, *evec = bars.evec;
+    volatile int &abort_flag = *const_cast<volatile int *>(&bars.abort_flag);
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -192,8 +218,12 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             mbar_init(smem_addr(&fg[s]), 1);
             mbar_init(smem_addr(&eg[s]), 1);
         }
-        mbar_init(smem_addr(&st_full[0]), 1);
-        mbar_init(smem_addr(&st_full[1]), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_addr(&fvec[s]), 1);
+            mbar_init(smem_addr(&evec[s]), E::THREADS);
+        }
+        mbar_init(smem_addr(&st_full), 1);
+        mbar_init(smem_addr(&s_read), E::THREADS);
         mbar_init(smem_addr(&dp_full), 1);
         mbar_init(smem_addr(&p_ready), E::THREADS);
         mbar_init(smem_addr(&ds_ready), E::THREADS);
@@ -202,50 +232,52 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         fence_mbar_init();
     }
     if (warp == MMA_WARP) {
-        tmem_alloc(smem_addr(&tmem_base_s), TMEM_COLS);
+        tmem_alloc(smem_addr(&bars.tmem_base), TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = tmem_base_s;
+    const uint32_t tmem = bars.tmem_base;
     const uint64_t limit = prm.limit;
-    // tensor memory: S^T/P^T [0,128), dP^T/dS^T [128,256), dV [256,256+D), dK [256+D, 256+2D);
-    // the column half h of P^T (dS^T) is written over columns [64h, 64h + 32) of S^T (dP^T).
-    // At D = 64 the free columns [384, 512) hold a second S^T/P^T buffer: S^T(s) goes to
-    // buffer s % 2, so S^T(s+2) is issued as soon as dV(s) has been issued (it reads
-    // P^T(s) from that buffer first), two steps ahead, with a full barrier per buffer.
-    constexpr bool SB = D == 64;
-    constexpr int AHEAD = SB ? 2 : 1;  // S^T products issued ahead of the elementwise step
-    const uint32_t cP = 128, cV = 256, cK = 256 + D;
-    auto cS_of = [](int s) -> uint32_t { return (SB && (s & 1)) ? 256u + 2u * D : 0u; };
-    auto st_bar = [](int s) { return SB ? (s & 1) : 0; };
-    auto st_par = [](int s) -> uint32_t { return (uint32_t)((SB ? s >> 1 : s) & 1); };
+    // tensor memory: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D).
+    // Once the elementwise warps hold dP^T(s) in registers, the column half h
+    // of P^T(s) goes to columns [128 + 64h, +32) and of dS^T(s) to [128 + 64h + 32,
+    // +32), over the dP^T values that half has read: the S^T columns are free
+    // as soon as S^T(s) is in registers, so S^T(s+1) runs while they work on s.
+    const uint32_t cS = 0, cP = 128, cV = 256, cK = 256 + D;
 
     if (warp == TMA_WARP) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
             bool ok = true;
-            int issued_q = 0, issued_g = 0;
+            int issued_q = 0, issued_g = 0, issued_v = 0;
             mbar_arrive_expect_tx(smem_addr(&res_full), C::RES);
             for (int c = 0; c < C::CH; ++c) {
                 tma_load_3d(sK + c * BOX, &tm_k, smem_addr(&res_full), c * 64, k0, bh, pol);
                 tma_load_3d(sV + c * BOX, &tm_v, smem_addr(&res_full), c * 64, k0, bh, pol);
             }
             for (int s = 0; s < n_steps; ++s) {
-                const int qs = s % C::NQS, gs = s % C::NGS, q0 = (first + s) * BM;
+                const int qs = s % C::NQS, gs = s % C::NGS, vs = s & 1, q0 = (first + s) * BM;
                 if (!wait_or_abort(smem_addr(&eq[qs]), (uint32_t)(((s / C::NQS) & 1) ^ 1), limit, &abort_flag)) {
                     ok = false;
                     break;
                 }
                 const uint32_t bq = smem_addr(&fq[qs]);
-                mbar_arrive_expect_tx(bq, C::TILE + VEC_BYTES);
+                mbar_arrive_expect_tx(bq, C::TILE);
                 for (int c = 0; c < C::CH; ++c) tma_load_3d(sQr + qs * C::TILE + c * BOX, &tm_q, bq, c * 64, q0, bh, pol);
-                const size_t vrow = (size_t)bh * prm.pitch + q0;
-                const uint32_t dvec = s_base + oVec + qs * VEC_BYTES;
-                bulk_copy_g2s(dvec, prm.lse2 + vrow, 512, bq);
-                bulk_copy_g2s(dvec + 512, prm.delta + vrow, 512, bq);
                 issued_q = s + 1;
+                if (!wait_or_abort(smem_addr(&evec[vs]), (uint32_t)(((s >> 1) & 1) ^ 1), limit, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t bv = smem_addr(&fvec[vs]);
+                mbar_arrive_expect_tx(bv, VEC_BYTES);
+                const size_t vrow = (size_t)bh * prm.pitch + q0;
+                const uint32_t dvec = s_base + oVec + vs * VEC_BYTES;
+                bulk_copy_g2s(dvec, prm.lse2 + vrow, 512, bv);
+                bulk_copy_g2s(dvec + 512, prm.delta + vrow, 512, bv);
+                issued_v = s + 1;
                 if (!wait_or_abort(smem_addr(&eg[gs]), (uint32_t)(((s / C::NGS) & 1) ^ 1), limit, &abort_flag)) {
                     ok = false;
                     break;
@@ -259,6 +291,8 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (!abort_flag) fail_bwd(&abort_flag);
                 for (int s = (issued_q > C::NQS ? issued_q - C::NQS : 0); s < issued_q; ++s)
                     mbar_wait_bounded(smem_addr(&fq[s % C::NQS]), (uint32_t)((s / C::NQS) & 1), limit);
+                for (int s = (issued_v > 2 ? issued_v - 2 : 0); s < issued_v; ++s)
+                    mbar_wait_bounded(smem_addr(&fvec[s & 1]), (uint32_t)((s >> 1) & 1), limit);
                 for (int s = (issued_g > C::NGS ? issued_g - C::NGS : 0); s < issued_g; ++s)
                     mbar_wait_bounded(smem_addr(&fg[s % C::NGS]), (uint32_t)((s / C::NGS) & 1), limit);
                 mbar_wait_bounded(smem_addr(&res_full), 0, limit);
@@ -273,7 +307,6 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // S^T(s) = K Q_s^T into cS, dP^T(s) = V dO_s^T into cP
             auto mma_st = [&](int s) {
                 const uint64_t dQ = sdesc_sw128(sQr + (s % C::NQS) * C::TILE, 16, 1024);
-                const uint32_t d_s = tmem + cS_of(s);
                 uint64_t ka[D / 16], kb[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -281,7 +314,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     ka[kk] = dK + off;
                     kb[kk] = dQ + off;
                 }
-                mma_ss_k<D / 16>(d_s, ka, kb, id_s, 0u);
+                mma_ss_k<D / 16>(tmem + cS, ka, kb, id_s, 0u);
                 issued = true;
             };
             auto mma_dpt = [&](int s) {
@@ -294,6 +327,18 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     kb[kk] = dG + off;
                 }
                 mma_ss_k<D / 16>(tmem + cP, ka, kb, id_s, 0u);
+            };
+            // dV += P^T dO_s (A: the P^T columns of cP) or dK += dS^T Q_s (A: the
+            // dS^T columns, 32 further), B MN-major from its ring slot
+            auto mma_acc = [&](uint32_t d_col, uint32_t a_col0, uint64_t b_mn, int s) {
+                uint32_t ta[BM / 16];
+                uint64_t tb[BM / 16];
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk) {
+                    ta[kk] = tmem + a_col<W>(a_col0, kk);
+                    tb[kk] = b_mn + (uint64_t)((kk * 16 * 128) >> 4);
+                }
+                mma_ts_k<BM / 16>(tmem + d_col, ta, tb, id_o, s > 0 ? 1u : 0u);
             };
             // Q_s in ring slot s % NQS, dO_s in slot s % NGS
             auto wait_q = [&](int s) -> bool {
@@ -308,56 +353,33 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             };
             if (ok && (ok = wait_q(0))) {
                 mma_st(0);
-                mma_commit_w(smem_addr(&st_full[0]));
+                mma_commit_w(smem_addr(&st_full));
                 if ((ok = wait_g(0))) {
                     mma_dpt(0);
                     mma_commit_w(smem_addr(&dp_full));
                 }
-                for (int s = 1; ok && s < AHEAD && s < n_steps; ++s) {
-                    if ((ok = wait_q(s))) {
-                        mma_st(s);
-                        mma_commit_w(smem_addr(&st_full[st_bar(s)]));
-                    }
-                }
             }
-            // Per step: dV(s) once P^T(s) is written; then S^T(s+AHEAD) into the
-            // columns dV(s) has just read (same-thread MMAs run in order), so
-            // it overlaps the elementwise warps' dS^T(s); then dK(s) and dP^T(s+1).
+            // Per step: S^T(s+1) once the elementwise warps hold S^T(s) (it runs while
+            // they compute the weights of step s); dV(s) once P^T(s) is written; dK(s)
+            // once dS^T(s) is; then dP^T(s+1) over the columns those two have read.
             for (int s = 0; ok && s < n_steps; ++s) {
+                const bool more = s + 1 < n_steps;
+                if (more) {
+                    if (!wait_or_abort_w(smem_addr(&s_read), (uint32_t)(s & 1), limit, &abort_flag) || !wait_q(s + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mma_st(s + 1);
+                    mma_commit_w(smem_addr(&st_full));
+                }
                 if (!wait_or_abort_w(smem_addr(&p_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint64_t dGmn = sdesc_sw128(sGr + (s % C::NGS) * C::TILE, BOX, 1024);
-                const uint64_t dQmn = sdesc_sw128(sQr + (s % C::NQS) * C::TILE, BOX, 1024);
-                {
-                    uint32_t ta[BM / 16];
-                    uint64_t tb[BM / 16];
-#pragma unroll
-                    for (int kk = 0; kk < BM / 16; ++kk) {
-                        ta[kk] = tmem + a_col<W>(cS_of(s), kk);
-                        tb[kk] = dGmn + (uint64_t)((kk * 16 * 128) >> 4);
-                    }
-                    mma_ts_k<BM / 16>(tmem + cV, ta, tb, id_o, s > 0 ? 1u : 0u);
-                }
+                mma_acc(cV, cP, sdesc_sw128(sGr + (s % C::NGS) * C::TILE, BOX, 1024), s);
                 mma_commit_w(smem_addr(&eg[s % C::NGS]));  // dO_s read for the last time
-                const bool more = s + 1 < n_steps;
-                if (s + AHEAD < n_steps) {
-                    if (!wait_q(s + AHEAD)) { ok = false; break; }
-                    mma_st(s + AHEAD);
-                    mma_commit_w(smem_addr(&st_full[st_bar(s + AHEAD)]));
-                }
                 if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                {
-                    uint32_t ta[BM / 16];
-                    uint64_t tb[BM / 16];
-#pragma unroll
-                    for (int kk = 0; kk < BM / 16; ++kk) {
-                        ta[kk] = tmem + a_col<W>(cP, kk);
-                        tb[kk] = dQmn + (uint64_t)((kk * 16 * 128) >> 4);
-                    }
-                    mma_ts_k<BM / 16>(tmem + cK, ta, tb, id_o, s > 0 ? 1u : 0u);
-                }
-                mma_commit_w(smem_addr(&eq[s % C::NQS]));  // Q_s read for the last time (its vectors by the elementwise warps before ds_ready)
+                mma_acc(cK, cP + W / 2, sdesc_sw128(sQr + (s % C::NQS) * C::TILE, BOX, 1024), s);
+                mma_commit_w(smem_addr(&eq[s % C::NQS]));  // Q_s read for the last time
                 if (more) {
                     if (!wait_g(s + 1)) { ok = false; break; }
                     mma_dpt(s + 1);
@@ -380,30 +402,31 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int quarter = warp & 3, hf = warp >> 2;
         const int jr = quarter * 32 + lane, kj = k0 + jr;
         const uint32_t lb = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t cPh = cP + hf * W;
+        const uint32_t cSh = cS + hf * W, cPh = cP + hf * W;
         const float sl = prm.sl;
         bool ok = true;
         for (int s = 0; s < n_steps; ++s) {
-            const int qs = s % C::NQS, q0 = (first + s) * BM + hf * W;
-            const uint32_t cSh = cS_of(s) + hf * W;
-            if (!wait_or_abort(smem_addr(&st_full[st_bar(s)]), st_par(s), limit, &abort_flag) ||
-                !wait_or_abort(smem_addr(&fq[qs]), (uint32_t)((s / C::NQS) & 1), limit, &abort_flag)) {
+            const int vs = s & 1, q0 = (first + s) * BM + hf * W;
+            if (!wait_or_abort(smem_addr(&st_full), (uint32_t)(s & 1), limit, &abort_flag) ||
+                !wait_or_abort(smem_addr(&fvec[vs]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const float4 *vec = reinterpret_cast<const float4 *>(smem + oVec + qs * VEC_BYTES) + hf * (W / 4);
+            const float4 *vec = reinterpret_cast<const float4 *>(smem + oVec + vs * VEC_BYTES) + hf * (W / 4);
             // Tiles with no padded key or query and wholly below the diagonal
             // take the unmasked path (no per-element tests or selects).
             const int qt0 = (first + s) * BM;
             const bool masked = k0 + BM > N || qt0 + BM > N || (CAUSAL && qt0 < k0 + BM);
-            // P^T row: weights of this key for this half of the tile's queries,
-            // as bf16 pairs (kept in registers for dS^T and written to tensor
-            // memory for the dV product)
+            // P^T row: weights of this key for this half of the tile's queries, as
+            // bf16 pairs (kept in registers for dS^T, written to tensor memory for
+            // the dV product once dP^T(s) has been read)
             uint32_t pw[W / 2];
             {
                 uint32_t raw[W];
                 tmem_ld_cols(lb + cSh, raw);
+                tc_fence_before();
+                mbar_arrive(smem_addr(&s_read));  // S^T(s) is in registers: S^T(s+1) may overwrite it
                 const uint64_t sl2 = f2_pack(sl, sl);
                 auto weights = [&](auto mask) {
                     constexpr bool M = decltype(mask)::value;
@@ -428,12 +451,9 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 };
                 if (masked) weights(std::true_type{});
                 else weights(std::false_type{});
-                tmem_st_cols(lb + cSh, pw);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(smem_addr(&p_ready));
-            // dS^T row = P^T (dP^T - delta), with the bf16 weights the dV product uses
+            // dP^T(s) into registers; its columns then take P^T (for dV) and dS^T
+            // = P^T (dP^T - delta), with the bf16 weights the dV product uses
             if (!wait_or_abort(smem_addr(&dp_full), (uint32_t)(s & 1), limit, &abort_flag)) {
                 ok = false;
                 break;
@@ -442,6 +462,10 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             {
                 uint32_t raw[W];
                 tmem_ld_cols(lb + cPh, raw);
+                tmem_st_cols(lb + cPh, pw);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(smem_addr(&p_ready));
                 uint32_t pk[W / 2];
                 // a masked weight is exactly 0 and its dP may be anything, so the
                 // masked path selects 0 instead of multiplying
@@ -468,7 +492,8 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 };
                 if (masked) grads(std::true_type{});
                 else grads(std::false_type{});
-                tmem_st_cols(lb + cPh, pk);
+                mbar_arrive(smem_addr(&evec[vs]));  // this step's vectors are read
+                tmem_st_cols(lb + cPh + W / 2, pk);
             }
             tmem_wait_st();
             tc_fence_before();
