@@ -741,6 +741,8 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             {
                 uint32_t raw[W];
                 tmem_ld_cols(lb + cSh, raw);
+                tc_fence_before();
+                mbar_arrive(smem_addr(&s_read));  // S(s) is in registers: the MMA may overwrite it
                 const uint64_t sl2 = f2_pack(sl, sl), nl2 = f2_pack(-l2, -l2);
                 auto weights = [&](auto mask) {
                     constexpr bool M = decltype(mask)::value;
@@ -762,8 +764,6 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 if (masked) weights(std::true_type{});
                 else weights(std::false_type{});
             }
-            tc_fence_before();
-            mbar_arrive(smem_addr(&s_read));  // S(s) is in registers: the MMA may overwrite it
             if (!wait_or_abort(smem_addr(&dp_full), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
             tc_fence_after();
             {
