@@ -383,11 +383,14 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             auto mma_s = [&](int t, int slot) {
                 const uint64_t q = t ? dq1 : dq0, k = dk0 + (uint64_t)slot * K_STEP;
                 const uint32_t d_s = tmem + t * 128;
+                uint64_t qa[DK / 16], kb[DK / 16];
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4);
-                    mma_ss_w(d_s, q + off, k + off, idesc_s, kk > 0 ? 1u : 0u);
+                    qa[kk] = q + off;
+                    kb[kk] = k + off;
                 }
+                mma_ss_k<DK / 16>(d_s, qa, kb, idesc_s, 0u);  // the K loop under one election
                 issued_any = true;
             };
             // O_t += P_t V from ring slot `slot` (M = 128 rows, N = D, K = 128 keys in steps of 16);
@@ -398,10 +401,15 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 const uint64_t v = dv0 + (uint64_t)slot * V_STEP;
                 const uint32_t d_o = tmem + C::COL_O + t * DV, a_p = tmem + (C::SEP_P ? C::COL_P + t * 64 : t * 128);
                 constexpr int KS = BN / 16 / P_PARTS;  // K steps per slice
+                uint32_t pa[KS];
+                uint64_t vb[KS];
 #pragma unroll
-                for (int kk = KS * h; kk < KS * h + KS; ++kk)
-                    mma_ts_w(d_o, a_p + kk * 8, v + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
-                             (!first || kk > 0) ? 1u : 0u);
+                for (int x = 0; x < KS; ++x) {
+                    const int kk = KS * h + x;
+                    pa[x] = a_p + kk * 8;
+                    vb[x] = v + (uint64_t)((kk * 16 * 128) >> 4);
+                }
+                mma_ts_k<KS>(d_o, pa, vb, idesc_o, (!first || h > 0) ? 1u : 0u);
                 issued_any = true;
             };
             int slot = 0;            // ring slot of the current stage
