@@ -164,7 +164,9 @@ size_t fa_host_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d, int in
  * library creates once per device) form a pipeline, so copies in both
  * directions overlap the compute of other chunks.  The call is synchronous:
  * it returns once o_h and lse_h hold the result, or with the first error
- * (a device-side timeout included).
+ * (a device-side timeout included).  Concurrent calls on one device (from
+ * several host threads) take turns: the pipeline streams are one call's at a
+ * time.
  */
 fa_status fa_forward_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, float *lse_h,
                           int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,

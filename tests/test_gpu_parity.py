@@ -188,6 +188,42 @@ def test_host_buffer_entry_point_matches_device_path(B, H, N, d, dtype, causal):
     compare(oh.float().numpy(), lh.numpy(), o_ref, l_ref, dtype, dtype)
 
 
+def test_host_buffer_entry_point_from_two_threads():
+    """Two host threads call fa_forward_host at once on one device (the call
+    releases the interpreter lock): the shared pipeline streams are taken in
+    turn, and each result equals the device-buffer path bit for bit."""
+    import threading
+    cases = [synth.Workload("t", 2, 8, 2048, 128, "bf16", c, seed=3100 + c) for c in (0, 1)]
+    bufs, errors = [], []
+    for w in cases:
+        q, k, v = w.inputs()
+        qh, kh, vh = (torch.from_numpy(x).to(torch.bfloat16).pin_memory() for x in (q, k, v))
+        oh = torch.empty(w.shape, dtype=torch.bfloat16).pin_memory()
+        lh = torch.empty(w.shape[:3], dtype=torch.float32).pin_memory()
+        ws = torch.empty(fa.host_workspace_size(*w.shape, torch.bfloat16, torch.bfloat16),
+                         dtype=torch.uint8, device="cuda")
+        bufs.append((w, qh, kh, vh, oh, lh, ws))
+
+    def run(b):
+        w, qh, kh, vh, oh, lh, ws = b
+        try:
+            for _ in range(4):
+                fa.forward_host(qh, kh, vh, oh, lh, ws, scale=w.scale, causal=w.causal)
+        except Exception as e:  # reported by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(b,)) for b in bufs]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for w, qh, kh, vh, oh, lh, ws in bufs:
+        od, ld = fa.fa_forward(qh.cuda(), kh.cuda(), vh.cuda(), scale=w.scale, causal=w.causal)
+        torch.cuda.synchronize()
+        assert torch.equal(oh, od.cpu()) and torch.equal(lh, ld.cpu())
+
+
 def test_host_buffer_entry_point_rejects_small_workspace():
     x = torch.zeros((1, 1, 8, 64), dtype=torch.bfloat16)
     ws = torch.empty(256, dtype=torch.uint8, device="cuda")

@@ -102,17 +102,21 @@ HostLayout host_layout(const fa::Problem &p)
 }
 
 // Streams and events the host-buffer pipeline uses, created once per device.
+// One call uses them at a time: `in_use` is held for the whole (synchronous)
+// call, so concurrent callers on one device take turns instead of interleaving
+// their event records and waits on the same streams.
 constexpr int MAX_DEVICES = 64;
 constexpr int MAX_CHUNKS = 8;
 struct PipelineRes {
     bool ready = false;
     cudaStream_t compute = nullptr, d2h = nullptr;
     cudaEvent_t start = nullptr, copied[MAX_CHUNKS] = {}, computed[MAX_CHUNKS] = {};
+    std::mutex in_use;
 };
 PipelineRes g_pipes[MAX_DEVICES];
 std::mutex g_pipes_mu;
 
-cudaError_t pipeline_res(PipelineRes **out)
+cudaError_t pipeline_res(PipelineRes **out, std::unique_lock<std::mutex> *hold)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -131,6 +135,7 @@ cudaError_t pipeline_res(PipelineRes **out)
         }
         r.ready = true;
     }
+    *hold = std::unique_lock<std::mutex>(r.in_use);
     *out = &r;
     return cudaSuccess;
 }
@@ -523,7 +528,8 @@ fa_status fa_forward_host(const void *q_h, const void *k_h, const void *v_h, voi
     fa::Problem full{q_h, k_h, v_h, o_h, lse_h, B, H, N, d, scale, causal != 0, in_dtype, o_dtype};
     const HostLayout L = host_layout(full);
     PipelineRes *res = nullptr;
-    cudaError_t e = pipeline_res(&res);
+    std::unique_lock<std::mutex> hold;  // the pipeline is this call's until it returns
+    cudaError_t e = pipeline_res(&res, &hold);
     if (e != cudaSuccess) return cuda_fail(e, "creating the copy pipeline");
     cudaStream_t s_in = static_cast<cudaStream_t>(stream);
 
