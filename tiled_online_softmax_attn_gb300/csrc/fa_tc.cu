@@ -464,8 +464,9 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         mma_commit_w(smem_addr(&bars.kv_empty[slot]));
                     }
                     next_stage();
-                    // iteration j reads stage j + 1 (K_(j+1), V_j): S_t(j+1) as soon as
-                    // S_t(j) is read, then P_t(j) V_j
+                    // iteration j reads stage j + 1 (K_(j+1), V_j), tile by tile: S_t(j+1)
+                    // as soon as S_t(j) is read, then P_t(j) V_j.  Tile 0's products go
+                    // first, so they never wait behind tile 1's softmax.
                     for (int j = 0; ok && j < n1; ++j) {
                         if (!wait(&bars.kv_full[slot], phase)) break;
                         if (j + 1 < n0) {
@@ -474,17 +475,17 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                             mma_s(0, slot);
                             mma_commit_w(smem_addr(&bars.s_full[0]));
                         }
+                        if (j < n0) {
+                            if (!pv(0, slot, j == 0)) break;
+                            mma_commit_w(smem_addr(&bars.p_free[0]));
+                            if (j == n0 - 1) mma_commit_w(smem_addr(&bars.o_full[0]));
+                        }
                         if (j + 1 < n1) {
                             if (!s_free(1)) break;
                             tc_fence_after();
                             mma_s(1, slot);
                             mma_commit_w(smem_addr(&bars.s_full[1]));
                             if (PERSIST && j + 1 == n1 - 1) mma_commit_w(smem_addr(&bars.q_empty));
-                        }
-                        if (j < n0) {
-                            if (!pv(0, slot, j == 0)) break;
-                            mma_commit_w(smem_addr(&bars.p_free[0]));
-                            if (j == n0 - 1) mma_commit_w(smem_addr(&bars.o_full[0]));
                         }
                         if (!pv(1, slot, j == 0)) break;
                         mma_commit_w(smem_addr(&bars.p_free[1]));
