@@ -118,6 +118,7 @@ struct Params {
     int BH;            // batch * heads
     int n_qblocks;     // work items per head (256 query rows each)
     int n_items;       // n_qblocks * BH; see item_index for the CTA -> item order
+    int hgroup;        // causal: heads per group of the item order (see item_of)
     int n_kv;          // key tiles per head
     float scale_log2;  // scale * log2(e), > 0
     int causal;
@@ -173,9 +174,15 @@ __device__ __forceinline__ Item item_of(const Params &prm, int w)
         sp = w % prm.n_split;
         w /= prm.n_split;
     }
-    if (CAUSAL) {  // longest query blocks first
-        qb = prm.n_qblocks - 1 - w / prm.BH;
-        bh = w % prm.BH;
+    if (CAUSAL) {
+        // Heads in groups of hgroup whose keys and values fit in L2 together,
+        // one group after the other; within a group the longest query blocks
+        // first (the CTAs of short blocks fill in behind the long ones)
+        const int per = prm.hgroup * prm.n_qblocks;
+        const int g0 = (w / per) * prm.hgroup, x = w % per;
+        const int gh = min(prm.hgroup, prm.BH - g0);  // heads in this group
+        qb = prm.n_qblocks - 1 - x / gh;
+        bh = g0 + x % gh;
     } else {       // items of one head are adjacent: concurrent CTAs share its K/V in L2
         qb = w % prm.n_qblocks;
         bh = w / prm.n_qblocks;
@@ -850,6 +857,15 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     prm.BH = (int)BH;
     prm.n_qblocks = (int)((p.N + 2 * BM - 1) / (2 * BM));
     prm.n_items = (int)(prm.n_qblocks * BH);
+    {   // causal item order: as many heads per group as keep their K and V within
+        // half of L2 (a head's K/V stays there while its query blocks run)
+        int dev = 0, l2 = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+            l2 = 0;
+        const int64_t kv_head = Nk * (int64_t)(DK + DV) * 2;
+        const int64_t g = l2 > 0 ? (int64_t)l2 / 2 / std::max<int64_t>(kv_head, 1) : BH;
+        prm.hgroup = (int)std::max<int64_t>(1, std::min<int64_t>(g, BH));
+    }
     prm.n_kv = (int)((Nk + BN - 1) / BN);
     prm.scale_log2 = p.scale * 1.4426950408889634f;
     prm.causal = CAUSAL;
