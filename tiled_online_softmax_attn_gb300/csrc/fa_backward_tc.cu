@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -120,6 +121,7 @@ struct BwdParams {
     const float *lse2, *delta;  // [BH][pitch]
     void *dq, *dk, *dv;
     int g_fp32;
+    int hgroup;  // causal dQ order: heads per group (see fa_bwd_dq_tc)
 };
 
 __device__ __forceinline__ void store_row32(void *base, int fp32, size_t elem, const uint32_t (&raw)[32], float mul)
@@ -541,8 +543,19 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = prm.N;
-    const int qt = CAUSAL ? prm.n_q - 1 - (int)(blockIdx.x / prm.BH) : (int)(blockIdx.x % prm.n_q);
-    const int bh = CAUSAL ? (int)(blockIdx.x % prm.BH) : (int)(blockIdx.x / prm.n_q);
+    // causal: heads in groups of hgroup whose K and V fit in L2 together, one
+    // group after the other, the longest query tiles of a group first
+    int qt, bh;
+    if (CAUSAL) {
+        const int per = prm.hgroup * prm.n_q, w = (int)blockIdx.x;
+        const int g0 = (w / per) * prm.hgroup, x = w % per;
+        const int gh = min(prm.hgroup, prm.BH - g0);
+        qt = prm.n_q - 1 - x / gh;
+        bh = g0 + x % gh;
+    } else {
+        qt = (int)(blockIdx.x % prm.n_q);
+        bh = (int)(blockIdx.x / prm.n_q);
+    }
     const int q0 = qt * BM;
     const int n_steps = CAUSAL ? qt + 1 : prm.n_q;  // key tiles this query tile sees
 
@@ -859,6 +872,14 @@ cudaError_t launch_dims(const BackwardProblem &p, float *delta, float *lse2, int
     prm.N = (int)p.N;
     prm.BH = (int)BH;
     prm.n_q = (int)((p.N + BM - 1) / BM);
+    {   // causal dQ order: as many heads per group as keep their K and V within half of L2
+        int dev = 0, l2 = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+            l2 = 0;
+        const int64_t kv_head = p.N * (int64_t)D * 4;
+        const int64_t g = l2 > 0 ? (int64_t)l2 / 2 / std::max<int64_t>(kv_head, 1) : BH;
+        prm.hgroup = (int)std::max<int64_t>(1, std::min<int64_t>(g, BH));
+    }
     prm.pitch = pitch;
     prm.sl = p.scale * 1.4426950408889634f;
     prm.scale = p.scale;
