@@ -66,9 +66,41 @@ def workload_desc(w):
             f"{' causal' if w.causal else ''}{' QK x%g' % w.qk_mult if w.qk_mult != 1 else ''}")
 
 
+def source_code(text):
+    """The source without comments and blank lines, so that a comment edit
+    does not count as a change of the kernel (string literals kept as they are)."""
+    out, i, n, quote = [], 0, len(text), None
+    while i < n:
+        c = text[i]
+        if quote:
+            out.append(c)
+            if c == "\\" and i + 1 < n:
+                out.append(text[i + 1])
+                i += 2
+                continue
+            if c == quote:
+                quote = None
+            i += 1
+        elif c in "\"'":
+            quote = c
+            out.append(c)
+            i += 1
+        elif text.startswith("//", i):
+            while i < n and text[i] != "\n":
+                i += 1
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def source_digest(path):
-    with open(os.path.join(ROOT, path), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256 prefix of a kernel source's code (comments and blank lines left out)."""
+    with open(os.path.join(ROOT, path), encoding="utf-8") as f:
+        return hashlib.sha256(source_code(f.read()).encode()).hexdigest()[:16]
 
 
 def profiled_traffic(kernel_key, workload):

@@ -65,3 +65,15 @@ def test_reference_arm_prints_once_under_torchrun():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["unit"] == "TFLOP/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_source_digest_ignores_comments_only():
+    """The kernel-source digest that ties a profile to the code it was taken
+    on leaves comments and blank lines out, keeps string literals whole, and
+    changes with the code."""
+    a = 'int x = 1; // old note\n/* block */ const char *s = "p//q";\n\nx++;\n'
+    b = 'int x = 1; // new note\n\n/* another\n block */ const char *s = "p//q";\nx++;  // more\n'
+    c = 'int x = 2; // old note\n/* block */ const char *s = "p//q";\n\nx++;\n'
+    assert bench.source_code(a) == bench.source_code(b)
+    assert bench.source_code(a) != bench.source_code(c)
+    assert '"p//q"' in bench.source_code(a)

@@ -11,7 +11,9 @@
 //
 // A work item is two 128-row query tiles (Q0, Q1) of one (batch, head); a CTA
 // processes one item, or (short items) loops over items in rounds (item_index)
-// with one CTA per SM.  It streams the head's K/V tiles (128 keys) through a
+// with one CTA per SM.  Unmasked items of a head are adjacent; causal items
+// run longest first within groups of heads whose K/V fit in half of L2
+// (item_of).  A CTA streams the head's K/V tiles (128 keys) through a
 // shared-memory ring:
 //
 //   warp 8  (TMA)      loads Q0, Q1 once per item (after the previous item's
@@ -34,7 +36,8 @@
 // At D = 128, P_t (bf16, two per column) overwrites the first 64 columns of
 // S_t; the next S_t MMA is issued after the P_t V MMA, and MMAs from one
 // thread run in issue order.  At D = 64, P_t has columns of its own,
-// [384 + 64 t, ...), so the next S_t MMA waits only for S_t to be read.
+// [384 + 64 t, ...), so the next S_t MMA waits only for S_t to be read, and
+// the MMAs are issued tile by tile (S_0(j+1), P_0 V, then S_1(j+1), P_1 V).
 // Either way the softmax warps release P_t in two halves (keys 0-63, then
 // 64-127) and the P_t V product starts on the first.
 //
