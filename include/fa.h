@@ -275,7 +275,8 @@ fa_status fa_forward_noalloc(const void *q, const void *k, const void *v, void *
  * fa_check_device_error -- synchronise `stream`, then read and clear the
  * device-side error word the kernels set when a bounded pipeline wait gives
  * up.  Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if the stream itself
- * reports an error.  The error words are one per kernel family on the
+ * reports an error (or a backward kernel found its shared-memory allocation
+ * unusable for its layout and did nothing).  The error words are one per kernel family on the
  * current device, not per stream: a wait that gave up in work on another
  * stream is reported (and cleared) by whichever check reads the words
  * first once that work has run.

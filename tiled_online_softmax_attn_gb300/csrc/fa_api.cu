@@ -585,6 +585,8 @@ fa_status fa_check_device_error(void *stream)
     uint32_t word = 0;
     cudaError_t e = take_error_words(&word, s);
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize / reading the device error words");
+    if (word & 128u)  // the backward dK/dV kernel's layout check (see fa_backward_tc.cu)
+        return fail(FA_ERR_CUDA, "backward kernel: shared memory allocation not aligned as its layout needs (error word 0x%x)", word);
     if (word) return fail(FA_ERR_TIMEOUT, "a device pipeline wait gave up (error word 0x%x)", word);
     return FA_OK;
 }

@@ -159,9 +159,12 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t a, uint32_t (&r)[64]) { tm
 __device__ __forceinline__ void tmem_st_cols(uint32_t a, const uint32_t (&r)[16]) { tmem_st16(a, r); }
 __device__ __forceinline__ void tmem_st_cols(uint32_t a, const uint32_t (&r)[32]) { tmem_st32(a, r); }
 
+constexpr uint32_t ERR_BWD_WAIT = 64u;     // a backward wait gave up (bits distinct from the forward kernels')
+constexpr uint32_t ERR_BWD_LAYOUT = 128u;  // the dK/dV kernel's shared-memory layout did not fit its allocation
+
 __device__ __forceinline__ void fail_bwd(volatile int *abort_flag)
 {
-    atomicOr(&g_bwd_error_word, 64u);
+    atomicOr(&g_bwd_error_word, ERR_BWD_WAIT);
     *abort_flag = 1;
 }
 
@@ -190,7 +193,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // with every thread leaving before any barrier or tensor memory is touched.
     const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
     if (pad + C::KV_NEED > C::SMEM_KV_REQ) {
-        if (threadIdx.x == 0) atomicOr(&g_bwd_error_word, 128u);
+        if (threadIdx.x == 0) atomicOr(&g_bwd_error_word, ERR_BWD_LAYOUT);
         return;
     }
     uint8_t *smem = smem_raw + pad;
