@@ -8,7 +8,9 @@ workload.  Default workload: B=4, H=32, N=4096, d=128, bf16, non-causal --
 the multi-head shape the throughput target is quoted on.  Inputs are the
 seeded synthetic tensors of ``synth`` (i.i.d. N(0,1), rounded to bf16),
 resident in HBM before timing.  Q, K and V (403 MB) are larger than L2
-(129 MB), so no flush is needed between steps.
+(129 MB), so no flush is needed between steps; workloads whose inputs fit in
+L2 (tiny, large_d) write a buffer of twice L2 before each timed step, each
+step bracketed by its own events.
 
 Prints one JSON line (rank 0).  ``value`` is TFLOP/s = 4*B*H*N^2*d / time
 (halved under a causal mask) summed over ranks; ``e2e`` is the same metric
@@ -173,13 +175,18 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples_under_load": len(sm), "samples": len(self.lines)}
 
 
-def oracle_rows_rate(w, q, k, v, seconds, seed=0):
-    """Times the CPU oracle on a seeded row sample sized for about `seconds`;
-    returns (TFLOP/s, rows, threads, elapsed)."""
+def oracle_rows_rate(w, q, k, v, seconds, seed=0, threads=0):
+    """Times the CPU oracle on a seeded row sample sized for about `seconds`
+    on `threads` host threads (0: all of them); returns (TFLOP/s, rows,
+    threads, elapsed)."""
     import oracle
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     rng = np.random.default_rng(seed)
     total = w.B * w.H * w.N
+    # rows are drawn with replacement, so a workload smaller than the sample
+    # is simply covered several times; the fp64 outputs of one call are kept
+    # to about 256 MB
+    chunk = max(threads, (32 << 20) // v.shape[-1])
     # calibrate on a growing sample until it runs long enough to be representative
     n_cal = max(threads, 8)
     while True:
@@ -187,13 +194,14 @@ def oracle_rows_rate(w, q, k, v, seconds, seed=0):
         t0 = time.perf_counter()
         oracle.attention_rows(q, k, v, w.scale, w.causal, calib, threads)
         dt = max(time.perf_counter() - t0, 1e-6)
-        if dt >= min(0.5, seconds / 4) or n_cal >= total:
+        if dt >= min(0.5, seconds / 4) or n_cal >= chunk:
             break
-        n_cal = min(total, n_cal * 4)
-    nrows = int(max(threads, min(total, n_cal * seconds / dt)))
+        n_cal = min(chunk, n_cal * 4)
+    nrows = int(max(threads, n_cal * seconds / dt))
     rows = rng.integers(0, total, size=nrows)
     t0 = time.perf_counter()
-    oracle.attention_rows(q, k, v, w.scale, w.causal, rows, threads)
+    for c in range(0, nrows, chunk):
+        oracle.attention_rows(q, k, v, w.scale, w.causal, rows[c:c + chunk], threads)
     el = time.perf_counter() - t0
     i = rows % w.N
     keys = (i + 1) if w.causal else np.full(nrows, w.N)
@@ -207,10 +215,11 @@ def reference_arm(args, w, q, k, v, rank, world):
         return
     per_step = max(0.5, min(10.0, 90.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        oracle_rows_rate(w, q, k, v, per_step, seed=1)
+        oracle_rows_rate(w, q, k, v, per_step, seed=1, threads=args.cpu_threads)
     rates, rows_total, el_total, threads = [], 0, 0.0, 1
     for s in range(args.steps):
-        r, nrows, threads, el = oracle_rows_rate(w, q, k, v, per_step, seed=100 + s)
+        r, nrows, threads, el = oracle_rows_rate(w, q, k, v, per_step, seed=100 + s,
+                                                 threads=args.cpu_threads)
         rates.append(r)
         rows_total += nrows
         el_total += el
@@ -279,6 +288,53 @@ def aggregate_tflops(flops_per_rank: float, ms_max: float, world: int) -> float:
     return world * flops_per_rank / (ms_max * 1e-3) / 1e12
 
 
+def l2_plan(l2_bytes: int, input_bytes: int):
+    """How the timed steps keep L2 honest: inputs larger than L2 need nothing
+    (each step streams them from HBM again); smaller ones get a buffer of twice
+    L2 written before every timed step.  Returns (flush buffer bytes or 0, the
+    config text saying which)."""
+    if input_bytes > l2_bytes:
+        return 0, "no flush: inputs (%.1f MB) exceed L2 (%.0f MB)" % (input_bytes / 1e6, l2_bytes / 1e6)
+    return 2 * l2_bytes, ("flushed: a %.0f MB buffer written before each timed step, outside its "
+                          "events (inputs %.1f MB fit in L2 %.0f MB)" % (2 * l2_bytes / 1e6, input_bytes / 1e6,
+                                                                        l2_bytes / 1e6))
+
+
+def device_l2_bytes(torch, dev) -> int:
+    return int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or (129 << 20)
+
+
+def time_steps(torch, dev, stream, step, steps, flush):
+    """Device time of `steps` calls of `step` on `stream`.  Without a flush
+    buffer the calls run back to back with an event at every boundary (the
+    total is first to last event); with one, each call has its own event pair
+    and the buffer is written before it, outside the pair.  Returns (total ms,
+    sorted per-step ms)."""
+    if flush is None:
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        evs[0].record(stream)
+        for i in range(steps):
+            step()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        return evs[0].elapsed_time(evs[-1]), sorted(a.elapsed_time(b) for a, b in zip(evs, evs[1:]))
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in pairs:
+            flush.zero_()
+            a.record(stream)
+            step()
+            b.record(stream)
+    torch.cuda.synchronize(dev)
+    per = sorted(a.elapsed_time(b) for a, b in pairs)
+    return sum(per), per
+
+
+def step_spread(per):
+    """Minimum and median of the timed region's single steps."""
+    return {"min": per[0], "median": statistics.median(per), "steps": len(per)}
+
+
 def bench_backward(args, w, world, rank, local_rank):
     """fa_backward on the workload: one step = dQ, dK, dV from (Q, K, V, O, dO,
     LSE) by recomputation; FLOPs counted as the five products of 2 N^2 d each
@@ -309,18 +365,18 @@ def bench_backward(args, w, world, rank, local_rank):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # Q, K, V, O, dO and LSE are read
+    in_bytes = 5 * q.numel() * q.element_size() + lse.numel() * lse.element_size()
+    flush_bytes, l2_text = l2_plan(device_l2_bytes(torch, dev), in_bytes)
+    flush = torch.empty(flush_bytes, dtype=torch.uint8, device=dev) if flush_bytes else None
     if dist:
         dist.barrier()
     with ClockSampler(local_rank) as clocks:
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
+        ms_total, per = time_steps(torch, dev, stream, step, args.steps, flush)
     if fa.check_device_error(stream.cuda_stream) != fa.FA_OK:
         raise RuntimeError(fa.last_error())
-    ms = reduce_max(e0.elapsed_time(e1), dist, dev) / args.steps
+    ms = reduce_max(ms_total, dist, dev) / args.steps
+    spread = step_spread(per)
     flops = 2.5 * w.flops
     value = world * flops / (ms * 1e-3) / 1e12
     peaks, peak_kind = load_peaks()
@@ -332,11 +388,12 @@ def bench_backward(args, w, world, rank, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": workload_desc(w), "pass": "backward", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                   "causal": w.causal, "parallelism": "replicas"},
+                   "causal": w.causal, "parallelism": "replicas", "l2": l2_text},
         "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
                      "frac": value / world / peak, "peak_source": peak_kind,
                      "note": "5 products counted; the kernels form S and dP twice (7 products)"},
         "gpu_launches": args.steps * 3,  # delta, dK/dV, dQ
+        "per_step_ms": spread,
         "kernel": "tensor-core backward" if tc else "general backward",
         "clocks": clocks.summary(),
     }
@@ -357,6 +414,8 @@ def main():
     ap.add_argument("--heads", type=int, help="override H of the workload")
     ap.add_argument("--e2e-steps", type=int, default=20, help="0 skips the end-to-end measurement")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="host threads of the timed oracle (0: all host cores)")
     ap.add_argument("--pass", dest="which", choices=["forward", "backward"], default="forward",
                     help="backward times fa_backward (dQ, dK, dV by recomputation from LSE)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -418,21 +477,18 @@ def main():
     if fa.check_device_error(stream.cuda_stream) != fa.FA_OK:
         raise RuntimeError(fa.last_error())
 
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush_bytes, l2_text = l2_plan(device_l2_bytes(torch, dev), 3 * q.numel() * q.element_size())
+    flush = torch.empty(flush_bytes, dtype=torch.uint8, device=dev) if flush_bytes else None
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
     launches["n"] = 0
     with ClockSampler(local_rank) as clocks:
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
+        ms_total, per = time_steps(torch, dev, stream, step, args.steps, flush)
     if dist:
         dist.barrier()
-    ms_total = e0.elapsed_time(e1)
     timed_launches = launches["n"]
+    spread = step_spread(per)
     if fa.check_device_error(stream.cuda_stream) != fa.FA_OK:
         raise RuntimeError(fa.last_error())
     ms_total = reduce_max(ms_total, dist, dev)
@@ -475,21 +531,24 @@ def main():
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": workload_desc(w), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                    "causal": w.causal, "seed": w.seed, "parallelism": "replicas",
-                   "l2": "no flush: Q, K, V (%.0f MB) exceed L2 (129 MB)" % (3 * q.numel() * q.element_size() / 1e6)},
+                   "l2": l2_text},
         "pct_bf16_peak": 100.0 * (w.flops / (ms_step * 1e-3) / 1e12) / float(peaks["bf16_tflops"]),
         "pct_bf16_peak_sustained": 100.0 * (w.flops / (ms_step * 1e-3) / 1e12) / float(peaks["bf16_tflops_sustained"]),
         "roofline": roof,
         "e2e": line_e2e,
         "gpu_launches": timed_launches,
+        "per_step_ms": spread,
         "kernel": path,
         "workspace_bytes": ws_bytes,
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        rate, nrows, threads, el = oracle_rows_rate(w, q_np, k_np, v_np, args.cpu_seconds)
+        rate, nrows, threads, el = oracle_rows_rate(w, q_np, k_np, v_np, args.cpu_seconds,
+                                                    threads=args.cpu_threads)
         line["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                                "sample": f"{nrows} seeded query rows of the workload, full key range "
-                                          f"each, {el:.1f} s on {threads} host threads"}
+                                "sample": f"{nrows} seeded query rows of the workload (drawn with "
+                                          f"replacement), full key range each, {el:.1f} s on "
+                                          f"{threads} host threads"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:

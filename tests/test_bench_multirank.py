@@ -77,3 +77,22 @@ def test_source_digest_ignores_comments_only():
     assert bench.source_code(a) == bench.source_code(b)
     assert bench.source_code(a) != bench.source_code(c)
     assert '"p//q"' in bench.source_code(a)
+
+
+def test_l2_plan_flushes_only_inputs_that_fit():
+    l2 = 129 << 20
+    nbytes, text = bench.l2_plan(l2, 403 << 20)
+    assert nbytes == 0 and text.startswith("no flush")
+    nbytes, text = bench.l2_plan(l2, 264 * 1024)
+    assert nbytes == 2 * l2 and text.startswith("flushed")
+    # an input exactly the size of L2 still fits in it
+    assert bench.l2_plan(l2, l2)[0] == 2 * l2
+
+
+def test_reference_arm_honours_the_thread_count():
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
+           "--steps", "1", "--warmup", "3", "--cpu-threads", "1"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1])
+    assert d["cpu_baseline"]["cores"] == 1
