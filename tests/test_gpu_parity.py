@@ -14,6 +14,7 @@ import torch
 import oracle
 import synth
 import tiled_online_softmax_attn_gb300 as fa
+from conftest import read_golden
 from parity import compare, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -150,6 +151,37 @@ def test_uniform_scores_give_mean_of_values_on_gpu():
         ref = np.cumsum(v[0, 0].astype(np.float64), axis=0) / np.arange(1, N + 1)[:, None]
         assert np.abs(o[0, 0] - ref).max() < 1e-3
         assert np.abs(lse[0, 0] - np.log(np.arange(1, N + 1))).max() < 1e-4
+
+
+def test_worked_example_on_gpu():
+    """The 4x4 worked example of "Deep Learning - Flash Attention" ("An
+    Example"), zero-padded to d = 64 (the padding adds nothing to q . k and V's
+    padding columns are 0), with the page's scale passed explicitly: rows 1
+    and 2 of O are the probability rows the page prints to four decimals.  The
+    general kernel keeps fp32 weights, so it must agree to the printed digits;
+    the tensor-core kernel feeds bf16 weights to the P V product (each rounded
+    by up to 2^-8 of itself, and the normaliser, exact but for the top weight,
+    differs from their sum by up to 2^-8 of the other weights' share), so it is
+    allowed 2^-7 of each value more."""
+    g = read_golden("worked_example_4x4.txt")
+    Q = np.array([[1, 2, 3, 4], [2, 1, 0, -1], [4, 3, 2, 1], [-1, 0, 1, 2]], dtype=np.float32)
+    d = 64
+    q, k, v = (np.zeros((1, 1, 4, d), dtype=np.float32) for _ in range(3))
+    q[0, 0, :, :4] = Q
+    k[0, 0, :, :4] = 2.0 * np.eye(4)
+    v[0, 0, :, :4] = np.eye(4)
+    scale = g["scale"][0]
+    printed = np.array([g["O_row1"], g["O_row2"]])
+    half_digit = 0.5 * 10.0 ** -int(g["decimals"][0])
+    # S = scale Q (2 I) = Q, so the natural-log LSE of each row is logsumexp(Q_i)
+    lse_exact = np.log(np.exp(Q.astype(np.float64)).sum(axis=1))
+    for dtype, flags, rel in (("bf16", 0, 2.0 ** -7), ("bf16", fa.FA_FLAG_GENERAL_PATH, 0.0),
+                              ("fp32", 0, 0.0)):
+        o, lse = run(q, k, v, dtype, scale, False, "fp32", flags)
+        err = np.abs(o[0, 0, :2, :4] - printed)
+        assert np.all(err <= half_digit + rel * printed + 1e-5), (dtype, flags, err.max())
+        assert np.all(o[0, 0, :, 4:] == 0)
+        assert np.abs(lse[0, 0] - lse_exact).max() < 1e-4
 
 
 def test_invalid_arguments_are_rejected_before_launch():
