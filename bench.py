@@ -2,6 +2,8 @@
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload multihead|causal|peaked|tiny|large_d]
+                  [--batch B] [--heads H] [--seq N] [--pass forward|backward]
+                  [--layout bhnd|bnhd] [--nk NK] [--dv DV]
 
 One step = one forward pass (fa_forward, one kernel launch) over the whole
 workload.  Default workload: B=4, H=32, N=4096, d=128, bf16, non-causal --
@@ -22,6 +24,10 @@ peak; ``cpu_baseline`` times the CPU oracle on a bounded row sample.
 reference arm on the same workload, a bounded row sample per step.
 Under torchrun (N > 1) every rank runs the whole workload on its own GPU
 (independent replicas: the forward pass has no exchange step).
+
+``--layout``, ``--nk`` or ``--dv`` time the general entry point fa_attention
+instead: strided (batch, seq, heads, dim) storage, key counts other than the
+query count, value widths other than d; ``--pass backward`` times fa_backward.
 """
 from __future__ import annotations
 
@@ -335,6 +341,119 @@ def step_spread(per):
     return {"min": per[0], "median": statistics.median(per), "steps": len(per)}
 
 
+def attention_counts(B, H, Nq, Nk, dk, dv, causal, elt):
+    """(FLOPs, bytes) of one pass of the general entry point: two products of
+    2 d per (query, key) pair that the mask keeps (key <= query when causal),
+    Q, K, V read and O, LSE written once."""
+    if causal:
+        i = np.arange(Nq, dtype=np.float64)
+        pairs = float(np.minimum(i + 1, Nk).sum())
+    else:
+        pairs = float(Nq) * Nk
+    flops = 2.0 * B * H * pairs * (dk + dv)
+    nbytes = B * H * (elt * (Nq * dk + Nk * dk + Nk * dv + Nq * dv) + 4.0 * Nq)
+    return flops, nbytes
+
+
+def bench_attention(args, w, world, rank, local_rank):
+    """fa_attention (the strided, cross-shape entry point) on the workload with
+    Nk keys, value width dv and the chosen storage: "bhnd" is contiguous
+    [B, H, N, d], "bnhd" is (batch, seq, heads, dim) storage seen through a
+    transposed view, for Q, K, V and O alike.  One step = one call."""
+    import torch
+    import tiled_online_softmax_attn_gb300 as fa
+    from tiled_online_softmax_attn_gb300 import build as fa_build
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    fa_build.build()
+    B, H, Nq, dk = w.B, w.H, w.N, w.d
+    Nk, dv = args.nk or w.N, args.dv or w.d
+    s = w.seed
+    q_np = synth.tensor(3 * s, (B, H, Nq, dk), w.dtype, w.qk_mult)
+    k_np = synth.tensor(3 * s + 1, (B, H, Nk, dk), w.dtype, w.qk_mult)
+    v_np = synth.tensor(3 * s + 2, (B, H, Nk, dv), w.dtype)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def place(x):
+        t = torch.from_numpy(x).to(tdt)
+        if args.layout == "bhnd":
+            return t.to(dev)
+        return t.transpose(1, 2).contiguous().to(dev).transpose(1, 2)
+
+    q, k, v = place(q_np), place(k_np), place(v_np)
+    o = place(np.zeros((B, H, Nq, dv), dtype=np.float32))
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    ws_bytes = fa.attention_workspace_size(q, k, v, o=o, causal=w.causal)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+    per_call = 2 if ws_bytes else 1  # the key-range split adds its combine launch
+    stream = torch.cuda.current_stream(dev)
+    launches = {"n": 0}
+
+    def step():
+        fa.fa_attention(q, k, v, o=o, lse=lse, scale=1.0 / math.sqrt(dk), causal=w.causal,
+                        workspace=ws, stream=stream)
+        launches["n"] += per_call
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.check_device_error(stream.cuda_stream) != fa.FA_OK:
+        raise RuntimeError(fa.last_error())
+    elt = 2 if w.dtype == "bf16" else 4
+    flops, nbytes = attention_counts(B, H, Nq, Nk, dk, dv, w.causal, elt)
+    in_bytes = elt * B * H * (Nq * dk + Nk * dk + Nk * dv)
+    flush_bytes, l2_text = l2_plan(device_l2_bytes(torch, dev), in_bytes)
+    flush = torch.empty(flush_bytes, dtype=torch.uint8, device=dev) if flush_bytes else None
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches["n"] = 0
+    with ClockSampler(local_rank) as clocks:
+        ms_total, per = time_steps(torch, dev, stream, step, args.steps, flush)
+    if fa.check_device_error(stream.cuda_stream) != fa.FA_OK:
+        raise RuntimeError(fa.last_error())
+    ms = reduce_max(ms_total, dist, dev) / args.steps
+    value = world * flops / (ms * 1e-3) / 1e12
+    peaks, peak_kind = load_peaks()
+    t_tensor = flops / (float(peaks["bf16_tflops"]) * 1e12)
+    t_hbm = nbytes / (float(peaks["hbm_gbs"]) * 1e9)
+    if t_tensor >= t_hbm:
+        peak = float(peaks["bf16_tflops"])
+        achieved = flops / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}
+    else:
+        peak = float(peaks["hbm_gbs"])
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak}
+    roof.update({"peak_source": peak_kind, "traffic": None, "algorithmic_bytes": nbytes,
+                 "algorithmic_flops": flops, "launches_per_step": per_call})
+    line = {
+        "metric": "attention fwd TFLOP/s (2·B·H·Nq·Nk·(dk+dv)/time, masked pairs left out)", "value": value,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name} through fa_attention: B={B} H={H} Nq={Nq} Nk={Nk} dk={dk} dv={dv} "
+                               f"{w.dtype}{' causal' if w.causal else ''}, {args.layout} storage",
+                   "B": B, "H": H, "Nq": Nq, "Nk": Nk, "dk": dk, "dv": dv, "causal": w.causal,
+                   "layout": args.layout, "parallelism": "replicas", "l2": l2_text},
+        "roofline": roof,
+        "e2e": None,  # the host-buffer entry point takes the contiguous self-attention form only
+        "gpu_launches": launches["n"],
+        "per_step_ms": step_spread(per),
+        "kernel": "key-range split + combine" if ws_bytes else "one launch",
+        "workspace_bytes": ws_bytes,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
 def bench_backward(args, w, world, rank, local_rank):
     """fa_backward on the workload: one step = dQ, dK, dV from (Q, K, V, O, dO,
     LSE) by recomputation; FLOPs counted as the five products of 2 N^2 d each
@@ -412,6 +531,11 @@ def main():
     ap.add_argument("--workload", default="multihead", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--batch", type=int, help="override B of the workload (smaller profiling cases)")
     ap.add_argument("--heads", type=int, help="override H of the workload")
+    ap.add_argument("--seq", type=int, help="override N (the query count) of the workload")
+    ap.add_argument("--nk", type=int, help="key count for fa_attention (default: the query count)")
+    ap.add_argument("--dv", type=int, help="value width for fa_attention (default: d)")
+    ap.add_argument("--layout", choices=["bhnd", "bnhd"], help="time fa_attention on this storage "
+                    "(bnhd: (batch, seq, heads, dim) seen through a transposed view)")
     ap.add_argument("--e2e-steps", type=int, default=20, help="0 skips the end-to-end measurement")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-threads", type=int, default=0,
@@ -431,6 +555,8 @@ def main():
         w = w.scaled(B=args.batch)
     if args.heads:
         w = w.scaled(H=args.heads)
+    if args.seq:
+        w = w.scaled(N=args.seq)
 
     if args.impl == "reference":
         if rank == 0:
@@ -444,6 +570,9 @@ def main():
 
     if args.which == "backward":
         return bench_backward(args, w, world, rank, local_rank)
+    if args.layout or args.nk or args.dv:
+        args.layout = args.layout or "bhnd"
+        return bench_attention(args, w, world, rank, local_rank)
 
     dist = None
     if world > 1:

@@ -40,3 +40,12 @@ def test_small_backward_line_is_flushed():
     d = _line("--pass", "backward")
     assert d["config"]["l2"].startswith("flushed")
     assert d["per_step_ms"]["steps"] == 20 and d["value"] > 0
+
+
+def test_general_entry_point_line_on_strided_cross_shapes():
+    d = _line("--layout", "bnhd", "--nk", "300", "--dv", "64", "--cpu-seconds", "0")
+    c = d["config"]
+    assert c["layout"] == "bnhd" and c["Nk"] == 300 and c["dv"] == 64 and c["Nq"] == 256
+    # 2 * B * H * Nq * Nk * (dk + dv) for the tiny workload's B=1, H=2, dk=64
+    assert d["roofline"]["algorithmic_flops"] == 2.0 * 1 * 2 * 256 * 300 * (64 + 64)
+    assert d["gpu_launches"] >= 20 and d["value"] > 0
