@@ -184,6 +184,32 @@ def test_worked_example_on_gpu():
         assert np.abs(lse[0, 0] - lse_exact).max() < 1e-4
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("direction", ["rising", "falling"])
+def test_scores_ramping_across_key_tiles(d, causal, direction):
+    """Every query is one +-1 vector u and key j is t_j u, with t_j rising (or
+    falling) along the keys, so the scores climb by 14-20 (natural units) per
+    128-key tile.  Rising scores move every row's maximum on every tile, past
+    the lazy-rescale margin each time, so O is rescaled on each one; falling
+    scores keep the maximum in the first tile and drive the later weights to
+    exact zeros."""
+    N = 1024
+    u = np.where(synth.tensor(501, (d,), "bf16") < 0, -1.0, 1.0).astype(np.float32)
+    t = synth.round_to_bf16((14.0 * np.arange(N) / N).astype(np.float32))
+    if direction == "falling":
+        t = t[::-1].copy()
+    q = np.broadcast_to(u, (1, 2, N, d)).astype(np.float32)
+    # t_j is bf16 and u is +-1, so every key element is exact in bf16
+    k = np.broadcast_to(t[:, None] * u[None, :], (1, 2, N, d)).astype(np.float32)
+    v = synth.tensor(502, (1, 2, N, d), "bf16")
+    scale = 1.0 / np.sqrt(d)
+    o_ref, l_ref = oracle.attention(q, k, v, scale, causal)
+    for flags in PATHS.values():
+        o, lse = run(q, k, v, "bf16", scale, causal, None, flags)
+        compare(o, lse, o_ref, l_ref, "bf16", "bf16")
+
+
 def test_invalid_arguments_are_rejected_before_launch():
     q = torch.zeros((1, 1, 8, 64), dtype=torch.bfloat16, device="cuda")
     o = torch.empty_like(q)
