@@ -153,11 +153,22 @@ __device__ __forceinline__ uint32_t a_col(uint32_t col0, int kk)
     return col0 + (uint32_t)((e / W) * W + (e % W) / 2);
 }
 
-// Row slices of tensor memory by width (32 lanes; loads include the wait).
-__device__ __forceinline__ void tmem_ld_cols(uint32_t a, uint32_t (&r)[32]) { tmem_ld32(a, r); }
-__device__ __forceinline__ void tmem_ld_cols(uint32_t a, uint32_t (&r)[64]) { tmem_ld64(a, r); }
-__device__ __forceinline__ void tmem_st_cols(uint32_t a, const uint32_t (&r)[16]) { tmem_st16(a, r); }
-__device__ __forceinline__ void tmem_st_cols(uint32_t a, const uint32_t (&r)[32]) { tmem_st32(a, r); }
+// Row slices of tensor memory by width (32 lanes; loads include the wait):
+// W fp32 columns in, W / 2 packed bf16 columns out, for W = 32 or 64.
+template <int NC>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t a, uint32_t (&r)[NC])
+{
+    static_assert(NC == 32 || NC == 64, "tmem_ld_cols: 32 or 64 columns");
+    if constexpr (NC == 32) tmem_ld32(a, r);
+    else tmem_ld64(a, r);
+}
+template <int NC>
+__device__ __forceinline__ void tmem_st_cols(uint32_t a, const uint32_t (&r)[NC])
+{
+    static_assert(NC == 16 || NC == 32, "tmem_st_cols: 16 or 32 columns");
+    if constexpr (NC == 16) tmem_st16(a, r);
+    else tmem_st32(a, r);
+}
 
 constexpr uint32_t ERR_BWD_WAIT = 64u;     // a backward wait gave up (bits distinct from the forward kernels')
 constexpr uint32_t ERR_BWD_LAYOUT = 128u;  // the dK/dV kernel's shared-memory layout did not fit its allocation
