@@ -38,8 +38,9 @@
 // thread run in issue order.  At D = 64, P_t has columns of its own,
 // [384 + 64 t, ...), so the next S_t MMA waits only for S_t to be read, and
 // the MMAs are issued tile by tile (S_0(j+1), P_0 V, then S_1(j+1), P_1 V).
-// Either way the softmax warps release P_t in two halves (keys 0-63, then
-// 64-127) and the P_t V product starts on the first.
+// At D = 128 the softmax warps release P_t in two halves (keys 0-63, then
+// 64-127) and the P_t V product starts on the first; at D = 64 they release
+// it whole, which saves the MMA warp a wait per tile.
 //
 // With a caller workspace and too few items to fill the GPU, items are
 // further split over key ranges (SPLIT): each writes unnormalised O, m, l and
@@ -81,8 +82,7 @@ constexpr int MMA_WARP = 9;
 constexpr int NUM_THREADS = 320;  // 10 warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;  // lazy-rescale threshold, log2 units
-constexpr int P_PARTS = 2;            // P_t is released to the P V product in this many key slices
-                                      // (two halves: +3-5 %; four quarters measured 8 % slower than halves)
+constexpr int MAX_PARTS = 2;          // key slices P_t is released in, at most (Cfg::P_PARTS)
 
 // error word bits
 constexpr uint32_t ERR_WAIT_TMA = 1u;       // producer gave up waiting for a free slot
@@ -112,6 +112,12 @@ struct Cfg {
     // be issued as soon as the softmax warps have read S_t(j)
     static constexpr bool SEP_P = DV == 64;
     static constexpr uint32_t COL_P = 256 + 2 * DV;        // P0 at COL_P, P1 at COL_P + 64 (SEP_P)
+    // P_t is released to the P V product in this many key slices.  D = 128:
+    // two halves (+3-5 % over one; four quarters measured 8 % slower than
+    // halves).  D = 64: whole (+2.5 % on multi-head d = 64 over halves, every
+    // wait the MMA warp saves counting among its many N = 64 products;
+    // quarters -18 %).
+    static constexpr int P_PARTS = DV == 64 ? 1 : 2;
 };
 
 struct Params {
@@ -142,7 +148,7 @@ struct __align__(8) Barriers {
     uint64_t q_full[2], q_empty;      // query tiles of an item; free after its last S MMA
     uint64_t kv_full[3], kv_empty[3];
     uint64_t s_full[2];
-    uint64_t p_part[2][P_PARTS];      // P_t keys [0, (k + 1) BN / P_PARTS) written
+    uint64_t p_part[2][MAX_PARTS];    // P_t keys [0, (k + 1) BN / P_PARTS) written
     uint64_t s_read[2], p_free[2];    // SEP_P: S_t read by the softmax warps / P_t read by the P V product
     uint64_t o_full[2], o_empty[2];   // O_t complete / read by the epilogue
     uint64_t drain;
@@ -248,6 +254,8 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
              const __grid_constant__ CUtensorMap tm_v, const Params prm)
 {
     using C = Cfg<DK, DV>;
+    constexpr int P_PARTS = C::P_PARTS;
+    static_assert(P_PARTS <= MAX_PARTS && (BN / 32) % P_PARTS == 0, "P slices must be whole 32-key chunks");
     extern __shared__ uint8_t smem_raw[];
     __shared__ Barriers bars;
     __shared__ uint32_t tmem_base_s;
