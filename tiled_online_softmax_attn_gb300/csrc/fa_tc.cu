@@ -383,7 +383,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             auto wait = [&](uint64_t *b, uint32_t parity) -> bool {
                 if (!ok) return false;
                 const bool done = wait_or_abort(smem_addr(b), parity, limit, &abort_flag);
-                if (!__all_sync(0xffffffffu, done)) {  // reconverges the warp; one verdict for all lanes
+                if (!__all_sync(0xffffffffu, done)) {  // reconverges the warp; one outcome for all lanes
                     ok = false;
                     if (!abort_flag) raise_error(ERR_WAIT_MMA, &abort_flag);
                     return false;

@@ -26,7 +26,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
 }
 
 // The same wait made by a whole warp: every lane waits, and the warp leaves
-// converged with one verdict (true only if every lane saw the phase).
+// converged with one outcome (true only if every lane saw the phase).
 __device__ __forceinline__ bool wait_or_abort_w(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                                 volatile int *abort_flag)
 {
