@@ -96,3 +96,21 @@ def test_reference_arm_honours_the_thread_count():
     assert r.returncode == 0, r.stderr[-2000:]
     d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1])
     assert d["cpu_baseline"]["cores"] == 1
+
+
+def test_attention_counts_match_brute_force():
+    # pairs the mask keeps, counted one by one on a small ragged shape
+    B, H, Nq, Nk, dk, dv = 2, 3, 7, 5, 16, 8
+    for causal in (False, True):
+        pairs = sum(1 for i in range(Nq) for j in range(Nk) if not causal or j <= i)
+        flops, nbytes = bench.attention_counts(B, H, Nq, Nk, dk, dv, causal, 2)
+        assert flops == 2.0 * B * H * pairs * (dk + dv)
+        assert nbytes == B * H * (2 * (Nq * dk + Nk * dk + Nk * dv + Nq * dv) + 4 * Nq)
+    # the self-attention bench counts: 4 B H N^2 d unmasked
+    f, _ = bench.attention_counts(4, 32, 4096, 4096, 128, 128, False, 2)
+    assert f == 4.0 * 4 * 32 * 4096 ** 2 * 128
+
+
+def test_step_spread_reports_min_and_median():
+    s = bench.step_spread([0.5, 0.6, 0.7, 0.9])
+    assert s == {"min": 0.5, "median": 0.65, "steps": 4}
