@@ -31,8 +31,10 @@
  *     allocates no device memory and keeps no per-call state; it caches one
  *     driver entry point and, for fa_forward_host, two streams and some
  *     events per device.
- *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
- *     default stream).  Argument errors are reported before anything is
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void *;
+ *     NULL = the legacy default stream).  Streams travel as void * and dtypes
+ *     as int (fa_dtype values) so that this header includes no CUDA header and
+ *     a plain C program can use it.  Argument errors are reported before anything is
  *     launched; launch errors are reported on return; a device-side timeout
  *     (a pipeline wait that gave up) is reported by fa_check_device_error.
  *   - There is no CPU fallback: a shape or dtype no kernel covers returns
@@ -263,8 +265,12 @@ fa_status fa_backward(const void *q, const void *k, const void *v, const void *o
  *   - All calls on a device share the array and it keeps the last call's
  *     contents (nothing needs to start at zero).  Calls whose work can
  *     overlap on the GPU race on it: order them, e.g. on one stream.
+ *   - Arguments are checked by the rules of fa_forward_ws.
  *   - The first call on a device looks up the array's address with that
- *     device current; make it before any stream capture begins.
+ *     device current and keeps it with the identity of the device's context;
+ *     a later call that finds another context (after cudaDeviceReset, for
+ *     instance) looks it up again.  Make the first call, and the first call
+ *     after a reset, before any stream capture begins.
  */
 #define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
 fa_status fa_forward_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -283,9 +289,18 @@ fa_status fa_forward_noalloc(const void *q, const void *k, const void *v, void *
  */
 fa_status fa_check_device_error(void *stream);
 
-/* Text of the last failure on the calling host thread ("" if none).  The
- * pointer stays valid until the next fa_* call on that thread. */
-const char *fa_last_error(void);
+/*
+ * fa_last_error -- the status and text of the last fa_* call on the calling
+ * host thread that can fail.
+ *
+ *   buf, len  caller-owned host buffer of len bytes that receives the text,
+ *             NUL-terminated and cut to len - 1 characters ("" when that call
+ *             succeeded); NULL or len = 0 copies nothing.
+ * Returns the status that call returned (FA_OK when it succeeded).  Each
+ * thread keeps its own record; every entry point but fa_last_error,
+ * fa_version and the size queries replaces it.
+ */
+fa_status fa_last_error(char *buf, size_t len);
 
 /* Library version string, e.g. "0.1.0 sm_103a". */
 const char *fa_version(void);

@@ -99,14 +99,17 @@ static int run_case(int64_t B, int64_t H, int64_t N, int64_t d, int causal, uint
     CHECK_CUDA(cudaMemcpy(dk, hk, n * 2, cudaMemcpyHostToDevice));
     CHECK_CUDA(cudaMemcpy(dv, hv, n * 2, cudaMemcpyHostToDevice));
 
+    char msg[256];
     fa_status st = fa_forward(dq, dk, dv, dout, dlse, B, H, N, d, (float)scale, causal, FA_BF16, FA_FP32, NULL);
     if (st != FA_OK) {
-        fprintf(stderr, "fa_forward: status %d: %s\n", (int)st, fa_last_error());
+        fa_last_error(msg, sizeof(msg));
+        fprintf(stderr, "fa_forward: status %d: %s\n", (int)st, msg);
         return 1;
     }
     st = fa_check_device_error(NULL);
     if (st != FA_OK) {
-        fprintf(stderr, "fa_check_device_error: status %d: %s\n", (int)st, fa_last_error());
+        fa_last_error(msg, sizeof(msg));
+        fprintf(stderr, "fa_check_device_error: status %d: %s\n", (int)st, msg);
         return 1;
     }
     CHECK_CUDA(cudaMemcpy(ho, dout, n * 4, cudaMemcpyDeviceToHost));
@@ -152,9 +155,17 @@ int main(void)
 
     /* a rejected call: N = 0 never reaches the GPU and says why */
     const fa_status st = fa_forward(NULL, NULL, NULL, NULL, NULL, 1, 1, 0, 64, 0.125f, 0, FA_BF16, FA_BF16, NULL);
-    const char *msg = fa_last_error();
-    if (st != FA_ERR_INVALID_ARG || msg == NULL || msg[0] == '\0') {
-        fprintf(stderr, "invalid call: status %d, message \"%s\"\n", (int)st, msg ? msg : "(null)");
+    char msg[256];
+    const fa_status last = fa_last_error(msg, sizeof(msg));
+    if (st != FA_ERR_INVALID_ARG || last != st || msg[0] == '\0') {
+        fprintf(stderr, "invalid call: status %d (recorded %d), message \"%s\"\n", (int)st, (int)last, msg);
+        return 1;
+    }
+    /* a cut-down copy still ends in a NUL */
+    char small[8];
+    fa_last_error(small, sizeof(small));
+    if (strlen(small) != sizeof(small) - 1) {
+        fprintf(stderr, "truncated message has length %zu\n", strlen(small));
         return 1;
     }
     printf("rejected as expected: %s\n", msg);

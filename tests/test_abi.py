@@ -112,3 +112,32 @@ def test_attention_accepts_sequence_major_layout_on_the_host(lib):
                 v_stride=[Nk * H * dv, dv, H * dv], o_stride=[Nq * H * dv, dv, H * dv])
     st = lib.fa_attention(ctypes.byref(p), None, 0, None)
     assert st == fa.FA_ERR_CUDA, fa.last_error()
+
+
+def test_last_error_returns_the_status_and_cuts_the_text(lib):
+    import ctypes
+    assert fa.forward_raw(0, 16, 16, 16, 0, 1, 1, 8, 64, 1.0, 0, 0, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.last_status() == fa.FA_ERR_INVALID_ARG
+    small = ctypes.create_string_buffer(8)
+    assert lib.fa_last_error(small, len(small)) == fa.FA_ERR_INVALID_ARG
+    assert len(small.value) == 7 and fa.last_error().startswith(small.value.decode())
+    # a size query leaves the record alone; a later failure replaces it
+    lib.fa_workspace_size(1, 1, 8, 64, 0, 0, 0)
+    assert fa.last_status() == fa.FA_ERR_INVALID_ARG
+    assert fa.forward_raw(16, 32, 48, 1 << 30, 0, 1, 1, 8, 4096, 1.0, 0, 0, 0) == fa.FA_ERR_UNSUPPORTED
+    assert fa.last_status() == fa.FA_ERR_UNSUPPORTED and "1024" in fa.last_error()
+
+
+@pytest.mark.parametrize("lse,o,expect,text", [
+    ((5 << 40) + 2, 4 << 40, fa.FA_ERR_INVALID_ARG, "aligned"),     # LSE not 4-byte aligned
+    (None, (1 << 40) + 64, fa.FA_ERR_INVALID_ARG, "overlap"),       # O inside Q
+    (4 << 40, 4 << 40, fa.FA_ERR_INVALID_ARG, "overlap"),           # O on top of LSE
+])
+def test_noalloc_checks_arguments_like_the_workspace_entry_point(lib, lse, o, expect, text):
+    """fa_forward_noalloc applies the rules of fa_forward_ws before anything
+    else (placeholder addresses, never dereferenced: no GPU is touched)."""
+    q, k, v = 1 << 40, 2 << 40, 3 << 40
+    args = (q, k, v, o, lse, 1, 1, 64, 256, 0.0625, 0, fa.FA_FP32, fa.FA_FP32)
+    assert lib.fa_forward_noalloc(*args, None) == expect
+    assert text in fa.last_error()
+    assert lib.fa_forward_ws(*args, None, 0, None) == expect

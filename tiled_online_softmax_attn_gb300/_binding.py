@@ -61,7 +61,7 @@ SIGNATURES = {
     "fa_forward_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]),
     "fa_check_device_error": (ctypes.c_int, [_P]),
-    "fa_last_error": (ctypes.c_char_p, []),
+    "fa_last_error": (ctypes.c_int, [ctypes.c_char_p, ctypes.c_size_t]),
     "fa_version": (ctypes.c_char_p, []),
 }
 
@@ -96,7 +96,15 @@ def load(path: str | None = None):
 
 
 def last_error() -> str:
-    return load().fa_last_error().decode()
+    """Text of the last failure of an fa_* call on this host thread ("" if it succeeded)."""
+    buf = ctypes.create_string_buffer(1024)
+    load().fa_last_error(buf, len(buf))
+    return buf.value.decode()
+
+
+def last_status() -> int:
+    """fa_status the last fa_* call on this host thread returned."""
+    return int(load().fa_last_error(None, 0))
 
 
 def version() -> str:

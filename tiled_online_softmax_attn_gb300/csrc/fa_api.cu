@@ -15,7 +15,16 @@
 
 namespace {
 
+// Text and status of the last failure on this host thread; every entry
+// point that can fail clears both first.
 thread_local std::string g_last_error;
+thread_local fa_status g_last_status = FA_OK;
+
+void clear_error()
+{
+    g_last_error.clear();
+    g_last_status = FA_OK;
+}
 
 fa_status fail(fa_status s, const char *fmt, ...)
 {
@@ -25,6 +34,7 @@ fa_status fail(fa_status s, const char *fmt, ...)
     vsnprintf(buf, sizeof(buf), fmt, ap);
     va_end(ap);
     g_last_error = buf;
+    g_last_status = s;
     return s;
 }
 
@@ -393,7 +403,7 @@ size_t fa_attention_workspace_size(const fa_params *a)
     p.o = reinterpret_cast<void *>(base + 3 * gap);
     p.lse = nullptr;
     if (validate_general(p) != FA_OK) {
-        g_last_error.clear();
+        clear_error();
         return 0;
     }
     if (fa::tc_supported(p)) return fa::tc_split_plan(p).workspace_bytes;
@@ -403,7 +413,7 @@ size_t fa_attention_workspace_size(const fa_params *a)
 
 fa_status fa_attention(const fa_params *a, void *workspace, size_t workspace_bytes, void *stream)
 {
-    g_last_error.clear();
+    clear_error();
     if (!a) return fail(FA_ERR_INVALID_ARG, "params must be non-NULL");
     const fa::Problem p = problem_of(a);
     fa_status st = validate_general(p);
@@ -426,7 +436,7 @@ fa_status fa_backward(const void *q, const void *k, const void *v, const void *o
                       void *dq, void *dk, void *dv, int64_t B, int64_t H, int64_t N, int64_t d, float scale,
                       int causal, int in_dtype, int grad_dtype, void *workspace, size_t workspace_bytes, void *stream)
 {
-    g_last_error.clear();
+    clear_error();
     if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv)
         return fail(FA_ERR_INVALID_ARG, "q, k, v, o, dout, lse, dq, dk, dv must be non-NULL");
     fa::Problem fwd{q, k, v, const_cast<void *>(o), nullptr, B, H, N, d, scale, causal != 0, in_dtype, in_dtype};
@@ -472,7 +482,7 @@ fa_status fa_forward_ws(const void *q, const void *k, const void *v, void *o, fl
                         int64_t N, int64_t d, float scale, int causal, int in_dtype, int o_dtype, void *workspace,
                         size_t workspace_bytes, void *stream)
 {
-    g_last_error.clear();
+    clear_error();
     fa::Problem p{q, k, v, o, lse, B, H, N, d, scale, causal != 0, in_dtype, o_dtype};
     fa_status st = validate(p);
     if (st != FA_OK) return st;
@@ -483,7 +493,7 @@ fa_status fa_forward_ex(const void *q, const void *k, const void *v, void *o, fl
                         int64_t H, int64_t N, int64_t d, float scale, int causal, int in_dtype,
                         int o_dtype, void *stream, uint32_t flags)
 {
-    g_last_error.clear();
+    clear_error();
     fa::Problem p{q, k, v, o, lse, B, H, N, d, scale, causal != 0, in_dtype, o_dtype};
     fa_status st = validate(p);
     if (st != FA_OK) return st;
@@ -510,7 +520,7 @@ fa_status fa_forward_host(const void *q_h, const void *k_h, const void *v_h, voi
                           int in_dtype, int o_dtype, void *workspace, size_t workspace_bytes,
                           void *stream)
 {
-    g_last_error.clear();
+    clear_error();
     if (!q_h || !k_h || !v_h || !o_h) return fail(FA_ERR_INVALID_ARG, "q_h, k_h, v_h and o_h must be non-NULL");
     if (!workspace || !aligned(workspace, 256)) return fail(FA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
     const size_t need = fa_host_workspace_size(B, H, N, d, in_dtype, o_dtype);
@@ -580,7 +590,7 @@ fa_status fa_forward_host(const void *q_h, const void *k_h, const void *v_h, voi
 
 fa_status fa_check_device_error(void *stream)
 {
-    g_last_error.clear();
+    clear_error();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t word = 0;
     cudaError_t e = take_error_words(&word, s);
@@ -591,7 +601,15 @@ fa_status fa_check_device_error(void *stream)
     return FA_OK;
 }
 
-const char *fa_last_error(void) { return g_last_error.c_str(); }
+fa_status fa_last_error(char *buf, size_t len)
+{
+    if (buf && len) {
+        const size_t n = std::min(len - 1, g_last_error.size());
+        g_last_error.copy(buf, n);
+        buf[n] = '\0';
+    }
+    return g_last_status;
+}
 
 const char *fa_version(void) { return "0.1.0 sm_103a"; }
 
@@ -599,5 +617,11 @@ const char *fa_version(void) { return "0.1.0 sm_103a"; }
 
 namespace fa {
 // Lets other translation units of the library report through fa_last_error.
-void set_last_error(const char *msg) { g_last_error = msg ? msg : ""; }
+void set_last_error(fa_status status, const char *msg)
+{
+    g_last_error = msg ? msg : "";
+    g_last_status = status;
+}
+
+fa_status validate_forward(const Problem &p) { return validate(p); }
 }  // namespace fa

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "../../include/fa.h"
+
 namespace fa {
 
 // One forward problem, already validated by the C ABI.
@@ -131,7 +133,12 @@ bool backward_tc_supported(const BackwardProblem &p);
 cudaError_t launch_backward_tc(const BackwardProblem &p, void *workspace, cudaStream_t stream, const char **detail);
 cudaError_t bwd_error_word_ptr(uint32_t **ptr);
 
-// Sets the text fa_last_error returns on this host thread.
-void set_last_error(const char *msg);
+// Sets the status and text fa_last_error returns on this host thread.
+void set_last_error(fa_status status, const char *msg);
+
+// The argument rules of fa_forward / fa_forward_ws (pointers, alignment,
+// sizes, dtypes, scale, overlaps); FA_OK or the failure, reported through
+// fa_last_error.
+fa_status validate_forward(const Problem &p);
 
 }  // namespace fa

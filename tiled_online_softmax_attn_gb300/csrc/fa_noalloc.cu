@@ -13,6 +13,7 @@
 // Costs and rules:
 //   * every GPU that loads this library holds FA_NOALLOC_SCRATCH_BYTES of
 //     device memory for the array until the process exits;
+//   * arguments are checked by the same rules as fa_forward_ws;
 //   * problems whose scratch does not fit are rejected (FA_ERR_UNSUPPORTED,
 //     with the sizes in fa_last_error); nothing falls back to allocating;
 //   * all calls on a device share its one array, which keeps whatever the
@@ -23,11 +24,15 @@
 //     example by issuing them all on one stream.  Each device has its own
 //     copy of the array;
 //   * the first call on a device looks up the array's device address
-//     (cudaGetSymbolAddress, with that device current) and caches it; make
-//     that first call before any stream capture begins.
+//     (cudaGetSymbolAddress, with that device current) and caches it with the
+//     identity of the device's context.  A call that finds another context
+//     current (after cudaDeviceReset, for instance, the module is loaded
+//     again and the array may sit elsewhere) looks the address up again.
+//     Make the first call, and the first call after a reset, before any
+//     stream capture begins.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -43,7 +48,11 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int MAX_DEVICES = 64;
-void *g_scratch_ptr[MAX_DEVICES];
+struct ScratchEntry {
+    unsigned long long ctx_id;  // context the address belongs to (0: none yet)
+    void *ptr;
+};
+ScratchEntry g_scratch[MAX_DEVICES];
 std::mutex g_scratch_mu;
 
 fa_status report(fa_status st, const char *fmt, ...)
@@ -53,33 +62,63 @@ fa_status report(fa_status st, const char *fmt, ...)
     va_start(ap, fmt);
     vsnprintf(buf, sizeof(buf), fmt, ap);
     va_end(ap);
-    fa::set_last_error(buf);
+    fa::set_last_error(st, buf);
     return st;
 }
 
-// Device address of this device's scratch array, looked up once per device.
+// Unique id of the calling thread's current context (cuCtxGetId; ids are
+// never reused within a process), or 0 when no context is current yet.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+bool current_context_id(unsigned long long *id)
+{
+    static std::once_flag once;
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    if (!get_current || !get_id) return false;
+    CUcontext c = nullptr;
+    *id = 0;
+    if (get_current(&c) != CUDA_SUCCESS) return false;
+    if (!c) return true;
+    return get_id(c, id) == CUDA_SUCCESS;
+}
+
+// Device address of the current device's scratch array: looked up once per
+// device and context, then taken from the cache.
 fa_status scratch_address(void **out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return report(FA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= MAX_DEVICES) return report(FA_ERR_UNSUPPORTED, "device %d is beyond the %d supported", dev, MAX_DEVICES);
+    unsigned long long ctx = 0;
+    if (!current_context_id(&ctx)) return report(FA_ERR_CUDA, "cannot read the identity of the current context");
     std::lock_guard<std::mutex> g(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    ScratchEntry &s = g_scratch[dev];
+    if (ctx == 0 || s.ptr == nullptr || s.ctx_id != ctx) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // with no context yet, this creates it
         if (e != cudaSuccess || !p)
             return report(FA_ERR_CUDA, "cudaGetSymbolAddress of the scratch array: %s", cudaGetErrorString(e));
-        g_scratch_ptr[dev] = p;
+        if (!current_context_id(&ctx) || ctx == 0)
+            return report(FA_ERR_CUDA, "cannot read the identity of the current context");
+        s.ctx_id = ctx;
+        s.ptr = p;
     }
-    *out = g_scratch_ptr[dev];
+    *out = s.ptr;
     return FA_OK;
-}
-
-bool overlaps(const void *a, size_t na, const void *b, size_t nb)
-{
-    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-    return x < y + nb && y < x + na;
 }
 
 }  // namespace
@@ -88,18 +127,11 @@ extern "C" fa_status fa_forward_noalloc(const void *q, const void *k, const void
                                         int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
                                         int in_dtype, int o_dtype, void *stream)
 {
-    fa::set_last_error("");
-    if (!q || !k || !v || !o) return report(FA_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
-    if (!std::isfinite(scale)) return report(FA_ERR_INVALID_ARG, "scale must be finite");
-    const int launches = fa_plan(B, H, N, d, in_dtype, o_dtype, causal, 0, nullptr, 0);
-    if (launches < 0) return report(FA_ERR_INVALID_ARG, "invalid sizes or dtypes");
-    const size_t in_elt = in_dtype == FA_BF16 ? 2 : 4, o_elt = o_dtype == FA_BF16 ? 2 : 4;
-    const size_t n = (size_t)(B * H * N * d);
-    if (overlaps(o, n * o_elt, q, n * in_elt) || overlaps(o, n * o_elt, k, n * in_elt) ||
-        overlaps(o, n * o_elt, v, n * in_elt) || (lse && overlaps(o, n * o_elt, lse, (size_t)(B * H * N) * 4)))
-        return report(FA_ERR_INVALID_ARG, "o must not overlap q, k, v or lse");
-
+    fa::set_last_error(FA_OK, "");
     fa::Problem p{q, k, v, o, lse, B, H, N, d, scale, causal != 0, in_dtype, o_dtype};
+    const fa_status valid = fa::validate_forward(p);
+    if (valid != FA_OK) return valid;
+
     fa::WidePlan w = fa::wide_plan(p, 1 << 20);
     if (!w.ok)
         return report(FA_ERR_UNSUPPORTED,
