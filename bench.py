@@ -112,44 +112,126 @@ def source_digest(path):
 
 
 def profiled_traffic(kernel_key, workload):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source (matching digest) for this workload."""
+    """(DRAM bytes per launch, how they were counted) from a committed ncu
+    summary, if it was taken on the current kernel source (matching digest)
+    for this workload; (None, reason) otherwise."""
     path = os.path.join(ROOT, "profiles", f"ncu_{kernel_key}_{workload}.md")
     if not os.path.exists(path):
-        return None
+        return None, "no ncu summary for this kernel and workload"
     text = open(path).read()
     m_d = re.search(r"source_digest:\s*([0-9a-f]+)", text)
     m_t = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
-    if not m_d or not m_t or m_d.group(1) != source_digest(KERNEL_SOURCES[kernel_key]):
-        return None
-    return float(m_t.group(1))
+    m_n = re.search(r"traffic_note:\s*(.+)", text)
+    if not m_d or not m_t:
+        return None, "the ncu summary holds no traffic figure"
+    if m_d.group(1) != source_digest(KERNEL_SOURCES[kernel_key]):
+        return None, "the kernel source changed since the ncu capture"
+    return float(m_t.group(1)), (m_n.group(1).strip() if m_n else "ncu dram__bytes_read.sum + dram__bytes_write.sum")
+
+
+class _Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (ctypes; no
+    Python NVML package needed): SM clock, its maximum, power and the
+    active clock-event reasons of one device."""
+    SM = 1                                   # NVML_CLOCK_SM
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle for device %d" % index)
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _uint(self, fn, *args):
+        v = self.c.c_uint()
+        return v.value if fn(self.h, *args, self.c.byref(v)) == 0 else None
+
+    def sample(self):
+        mask = self.c.c_ulonglong()
+        ok = self.reasons_fn(self.h, self.c.byref(mask)) == 0
+        return (self._uint(self.lib.nvmlDeviceGetClockInfo, self.c.c_uint(self.SM)),
+                self._uint(self.lib.nvmlDeviceGetPowerUsage),
+                [n for b, n in self.REASONS.items() if ok and mask.value & b])
+
+    def max_sm(self):
+        return self._uint(self.lib.nvmlDeviceGetMaxClockInfo, self.c.c_uint(self.SM))
+
+    def close(self):
+        self.lib.nvmlShutdown()
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+    """SM clock and clock-event reasons sampled every 2 ms while the timed
+    region runs (NVML through ctypes; nvidia-smi every 100 ms where NVML
+    cannot be loaded).  Call ``mark_start()`` / ``mark_end()`` around the
+    timed region: samples taken between the two count as under load, so a
+    timed region of a dozen milliseconds still has its own clock record."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_S = 0.002
 
     def __init__(self, gpu_index):
-        self.gpu = gpu_index
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        self.gpu = int(ids[gpu_index]) if gpu_index < len(ids) and ids[gpu_index].isdigit() else gpu_index
         self.proc = None
-        self.out = None
+        self.nvml = None
+        self.samples = []          # (time, sm MHz, power mW, reasons)
+        self.window = [None, None]
+        self.lines = []
 
     def __enter__(self):
+        import threading
         try:
-            self.out = open(os.devnull, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
-        time.sleep(0.3)
+            self.nvml = _Nvml(self.gpu)
+        except (OSError, AttributeError):
+            self.nvml = None
+        if self.nvml is not None:
+            self.stop = threading.Event()
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+        else:
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self.proc = None
+        time.sleep(0.05)
         return self
 
+    def _run(self):
+        while not self.stop.is_set():
+            t = time.perf_counter()
+            try:
+                clk, pw, why = self.nvml.sample()
+            except OSError:
+                break
+            self.samples.append((t, clk, pw, why))
+            self.stop.wait(self.PERIOD_S)
+
+    def mark_start(self):
+        self.window[0] = time.perf_counter()
+
+    def mark_end(self):
+        self.window[1] = time.perf_counter()
+
     def __exit__(self, *exc):
-        self.lines = []
+        if self.nvml is not None:
+            time.sleep(0.01)
+            self.stop.set()
+            self.thread.join(timeout=5)
+            self.max_mhz = self.nvml.max_sm()
+            self.nvml.close()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -161,6 +243,14 @@ class ClockSampler:
         return False
 
     def summary(self):
+        if self.nvml is not None:
+            t0, t1 = self.window
+            load = [s for s in self.samples if t0 is not None and t1 is not None and t0 <= s[0] <= t1]
+            sm = [s[1] for s in load if s[1] is not None]
+            reasons = sorted({r for s in load for r in s[3]})
+            return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                    "reasons": reasons, "samples_under_load": len(sm), "samples": len(self.samples),
+                    "source": "NVML every %d ms, samples inside the timed region" % round(self.PERIOD_S * 1e3)}
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
@@ -178,7 +268,8 @@ class ClockSampler:
                 if val.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples_under_load": len(sm), "samples": len(self.lines)}
+                "reasons": sorted(reasons), "samples_under_load": len(sm), "samples": len(self.lines),
+                "source": "nvidia-smi every 100 ms, samples above 200 W"}
 
 
 def oracle_rows_rate(w, q, k, v, seconds, seed=0, threads=0):
@@ -413,7 +504,9 @@ def bench_attention(args, w, world, rank, local_rank):
     torch.cuda.synchronize(dev)
     launches["n"] = 0
     with ClockSampler(local_rank) as clocks:
+        clocks.mark_start()
         ms_total, per = time_steps(torch, dev, stream, step, args.steps, flush)
+        clocks.mark_end()
     if fa.check_device_error(stream.cuda_stream) != fa.FA_OK:
         raise RuntimeError(fa.last_error())
     ms = reduce_max(ms_total, dist, dev) / args.steps
@@ -491,7 +584,9 @@ def bench_backward(args, w, world, rank, local_rank):
     if dist:
         dist.barrier()
     with ClockSampler(local_rank) as clocks:
+        clocks.mark_start()
         ms_total, per = time_steps(torch, dev, stream, step, args.steps, flush)
+        clocks.mark_end()
     if fa.check_device_error(stream.cuda_stream) != fa.FA_OK:
         raise RuntimeError(fa.last_error())
     ms = reduce_max(ms_total, dist, dev) / args.steps
@@ -613,7 +708,9 @@ def main():
     torch.cuda.synchronize(dev)
     launches["n"] = 0
     with ClockSampler(local_rank) as clocks:
+        clocks.mark_start()
         ms_total, per = time_steps(torch, dev, stream, step, args.steps, flush)
+        clocks.mark_end()
     if dist:
         dist.barrier()
     timed_launches = launches["n"]
@@ -646,7 +743,7 @@ def main():
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak}
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json, burst)" if peak_kind == "measured" else "fallback"
-    roof["traffic"] = profiled_traffic(kernel_key, w.name)
+    roof["traffic"], roof["traffic_note"] = profiled_traffic(kernel_key, w.name)
     roof["algorithmic_bytes"] = w.bytes
     roof["algorithmic_flops"] = w.flops
     roof["launches_per_step"] = per_call

@@ -4,14 +4,22 @@ Tolerances (applied to |O_gpu - O_oracle| and |LSE_gpu - LSE_oracle|):
   bf16 inputs, fp32 accumulation:  O max-abs <= 1e-2, O mean-abs <= 1e-3
   fp32 inputs:                     O max-abs <= 2e-4
   LSE (any input type):            max-abs <= 1e-3
-When O is stored as bf16, rounding the exact O to bf16 alone costs up to
-half a bf16 ulp of |O| (0.0156 for |O| in [4, 8)); that floor is added to
-the bf16 max-abs bound elementwise, and the mean is then checked against
-bf16(oracle), as the very-long peaked-score shape needs (its one-hot rows
-carry |O| up to ~5).  The same shapes are also checked with fp32 O against
-the plain bounds.
+These plain bounds gate every comparison, except where rounding the exact
+O to the stored bf16 alone already breaks one of them (the "floor": |O| in
+[4, 8) has half a bf16 ulp of 0.0156, which the very-long peaked-score
+shape's one-hot rows reach; fp32 inputs with bf16 O break 2e-4 almost
+always).  Only then is half a bf16 ulp of |O| added to the max-abs bound
+elementwise, and the mean may be taken against bf16(oracle).  The plain
+statistics are computed and returned either way, and the same shapes are
+also checked with fp32 O, against the plain bounds.
+
+Setting FA_PARITY_LOG to a file name appends each comparison's statistics
+to it as one JSON line.
 """
 from __future__ import annotations
+
+import json
+import os
 
 import numpy as np
 
@@ -31,34 +39,50 @@ def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
     return 0.5 * 2.0 ** (e - 7)
 
 
-def compare(o_gpu, lse_gpu, o_ref, lse_ref, in_dtype: str, o_dtype: str):
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, in_dtype: str, o_dtype: str, label: str | None = None):
     """Returns a dict of error statistics and raises AssertionError past the bounds."""
     o_gpu = np.asarray(o_gpu, dtype=np.float64)
     o_ref = np.asarray(o_ref, dtype=np.float64)
     assert np.all(np.isfinite(o_gpu)), "non-finite values in O"
     err = np.abs(o_gpu - o_ref)
-    stats = {"o_max": float(err.max(initial=0.0)), "o_mean": float(err.mean()) if err.size else 0.0}
+    n = err.size
+    stats = {"o_max": float(err.max(initial=0.0)), "o_mean": float(err.mean()) if n else 0.0, "elements": n}
     if lse_gpu is not None:
         lerr = np.abs(np.asarray(lse_gpu, np.float64) - np.asarray(lse_ref, np.float64))
         assert np.all(np.isfinite(lse_gpu)), "non-finite values in LSE"
         stats["lse_max"] = float(lerr.max(initial=0.0))
-        assert stats["lse_max"] <= LSE_MAX, f"LSE max error {stats['lse_max']:.3e} > {LSE_MAX}"
-    if in_dtype == "fp32":
-        bound = O_MAX_FP32 + (half_ulp_bf16(o_ref) if o_dtype == "bf16" else 0.0)
-        bad = err > bound
-        assert not bad.any(), f"O error {stats['o_max']:.3e} above the fp32-input bound"
-        return stats
-    if o_dtype == "bf16":
-        bad = err > O_MAX_BF16 + half_ulp_bf16(o_ref)
+    max_bound = O_MAX_FP32 if in_dtype == "fp32" else O_MAX_BF16
+    widened = False
+    if o_dtype == "bf16" and n:
         q_ref = synth.round_to_bf16(o_ref.astype(np.float32)).astype(np.float64)
-        stats["o_mean_vs_bf16_oracle"] = float(np.abs(o_gpu - q_ref).mean()) if err.size else 0.0
-        mean_ok = stats["o_mean"] <= O_MEAN_BF16 or stats["o_mean_vs_bf16_oracle"] <= O_MEAN_BF16
+        floor = np.abs(q_ref - o_ref)
+        stats["floor_max"] = float(floor.max())
+        stats["floor_mean"] = float(floor.mean())
+        stats["o_mean_vs_bf16_oracle"] = float(np.abs(o_gpu - q_ref).mean())
+        widened = stats["floor_max"] > max_bound or (in_dtype != "fp32" and stats["floor_mean"] > O_MEAN_BF16)
+    stats["gate"] = "widened by the bf16 rounding floor" if widened else "plain"
+    if label is not None:
+        stats["label"] = label
+    _log(stats)
+    if lse_gpu is not None:
+        assert stats["lse_max"] <= LSE_MAX, f"LSE max error {stats['lse_max']:.3e} > {LSE_MAX}"
+    if widened:
+        bad = err > max_bound + half_ulp_bf16(o_ref)
+        mean_ok = in_dtype == "fp32" or stats["o_mean"] <= O_MEAN_BF16 or \
+            stats["o_mean_vs_bf16_oracle"] <= O_MEAN_BF16
     else:
-        bad = err > O_MAX_BF16
-        mean_ok = stats["o_mean"] <= O_MEAN_BF16
-    assert not bad.any(), f"O max error {stats['o_max']:.3e} above the bound"
+        bad = err > max_bound
+        mean_ok = in_dtype == "fp32" or stats["o_mean"] <= O_MEAN_BF16
+    assert not bad.any(), f"O max error {stats['o_max']:.3e} above the {stats['gate']} bound"
     assert mean_ok, f"O mean error {stats['o_mean']:.3e} > {O_MEAN_BF16}"
     return stats
+
+
+def _log(stats):
+    path = os.environ.get("FA_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(stats) + "\n")
 
 
 def sample_rows(B, H, N, n, seed=0):

@@ -1,11 +1,12 @@
 """GPU parity: the CUDA kernels (through the C ABI) against the CPU fp64 oracle.
 
-Small shapes are compared element by element on every output; the five
-workload shapes at full size are compared on sampled rows (every head's
-first and last rows and tile edges, plus a seeded draw) against the full
-key range.  Both kernels are covered: the tensor-core kernel (bf16, d of 64
-or 128) through the default dispatch and the general-d kernel through
-FA_FLAG_GENERAL_PATH.
+Small shapes are compared element by element on every output.  At full
+size the multi-head (4x32x4096x128) and causal (1x32x16384x128) workloads
+are compared on every row, and the very-long peaked one (1x8x65536x64) on
+16384 seeded rows plus the first, second, 128th, 129th, middle and last two
+rows of every head, each against the full key range.  Both kernels are
+covered: the tensor-core kernel (bf16, d of 64 or 128) through the default
+dispatch and the general-d kernel through FA_FLAG_GENERAL_PATH.
 """
 import numpy as np
 import pytest
@@ -40,7 +41,9 @@ def full_check(w, path, o_dtype=None):
     q, k, v = w.inputs()
     o, lse = run(q, k, v, w.dtype, w.scale, w.causal, o_dtype, PATHS[path])
     o_ref, lse_ref = oracle.attention(q, k, v, w.scale, w.causal)
-    return compare(o, lse, o_ref, lse_ref, w.dtype, o_dtype or w.dtype)
+    return compare(o, lse, o_ref, lse_ref, w.dtype, o_dtype or w.dtype,
+                   label=f"{w.name} {w.B}x{w.H}x{w.N}x{w.d} {w.dtype}{' causal' if w.causal else ''} {path} "
+                         f"O {o_dtype or w.dtype}")
 
 
 SMALL = [
@@ -91,12 +94,26 @@ def _sampled(w, o_dtype=None, flags=0, nrows=384):
     rows = sample_rows(w.B, w.H, w.N, nrows, seed=w.seed)
     o_ref, lse_ref = oracle.attention_rows(q, k, v, w.scale, w.causal, rows)
     return compare(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref,
-                   w.dtype, o_dtype or w.dtype)
+                   w.dtype, o_dtype or w.dtype, label=f"{w.name} {rows.size} rows O {o_dtype or w.dtype}")
 
 
-@pytest.mark.parametrize("name", ["multihead", "causal", "peaked"])
-def test_full_size_workloads_sampled(name):
-    _sampled(synth.WORKLOADS[name])
+@pytest.mark.parametrize("name", ["multihead", "causal"])
+def test_full_size_workloads_every_row(name):
+    """Every element of O and LSE of the full-size workload against the
+    oracle's three passes over the full key range."""
+    w = synth.WORKLOADS[name]
+    q, k, v = w.inputs()
+    o, lse = run(q, k, v, w.dtype, w.scale, w.causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, w.scale, w.causal)
+    del q, k, v
+    compare(o, lse, o_ref, lse_ref, w.dtype, w.dtype, label=f"{w.name} every row O {w.dtype}")
+
+
+@pytest.mark.parametrize("o_dtype", ["bf16", "fp32"])
+def test_peaked_workload_rows(o_dtype):
+    """The 1x8x65536x64 peaked workload on 16384 seeded rows plus each head's
+    edge rows; with fp32 O the plain bounds hold without the bf16 floor."""
+    _sampled(synth.WORKLOADS["peaked"], o_dtype=o_dtype, nrows=16384)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -112,11 +129,6 @@ def test_persistent_ctas_with_ragged_rows(d):
                                      np.arange(w.N - 232, w.N, dtype=np.int64) + (w.B * w.H - 1) * w.N]))
     o_ref, lse_ref = oracle.attention_rows(q, k, v, w.scale, w.causal, rows)
     compare(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, w.dtype, w.dtype)
-
-
-def test_peaked_workload_fp32_output():
-    """With fp32 O the plain bounds hold without the bf16 rounding floor."""
-    _sampled(synth.WORKLOADS["peaked"], o_dtype="fp32")
 
 
 def test_repeat_runs_are_bitwise_identical():

@@ -6,13 +6,15 @@ scratch in a fixed array inside the library.
 Runs last (file name) so that a failure here cannot hide another test's.
 Each case calls the allocation-free entry point through the C ABI and checks
 its output against fa_forward_ws, the entry point that takes a caller
-workspace, within the parity tolerances of the other GPU tests, for two calls
-in a row: the second call reuses the array the first one left behind.
+workspace, and against the CPU oracle, within the parity tolerances of the
+other GPU tests, for two calls in a row: the second call reuses the array
+the first one left behind.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 import tiled_online_softmax_attn_gb300 as fa
 from parity import compare
@@ -37,16 +39,20 @@ def with_workspace(q, k, v, w):
 
 
 def one_call(w):
-    q, k, v = (torch.from_numpy(x).cuda().to(TORCH_DT[w.dtype]) for x in w.inputs())
+    q_np, k_np, v_np = w.inputs()
+    q, k, v = (torch.from_numpy(x).cuda().to(TORCH_DT[w.dtype]) for x in (q_np, k_np, v_np))
     o = torch.empty_like(q)
     lse = torch.empty(w.shape[:3], dtype=torch.float32, device="cuda")
     st = noalloc(q, k, v, o, lse, w)
     assert st == fa.FA_OK, fa.last_error()
-    o_ref, lse_ref = with_workspace(q, k, v, w)
+    o_ws, lse_ws = with_workspace(q, k, v, w)
     torch.cuda.synchronize()
     assert fa.check_device_error() == fa.FA_OK, fa.last_error()
-    compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref.float().cpu().numpy().astype(np.float64),
-            lse_ref.cpu().numpy().astype(np.float64), w.dtype, w.dtype)
+    got_o, got_l = o.float().cpu().numpy(), lse.cpu().numpy()
+    compare(got_o, got_l, o_ws.float().cpu().numpy().astype(np.float64),
+            lse_ws.cpu().numpy().astype(np.float64), w.dtype, w.dtype)
+    o_ref, lse_ref = oracle.attention(q_np, k_np, v_np, w.scale, w.causal)
+    compare(got_o, got_l, o_ref, lse_ref, w.dtype, w.dtype)
 
 
 def test_two_calls_in_a_row_match_the_workspace_entry_point():
@@ -60,6 +66,19 @@ def test_the_same_problem_twice():
     w = synth.Workload("t", 1, 2, 513, 512, "fp32", False, seed=6002)
     one_call(w)
     one_call(w.scaled(seed=6003))
+
+
+def test_problem_that_fits_only_without_key_splits():
+    """fp32, d = 1024, N = 2048: the bf16 hi/lo copies take 24 MB, and the
+    partials of a key split would push the scratch past its 32 MB, so the
+    call plans a single key range; fa_forward_ws with a full workspace splits
+    the keys, so the two agree to rounding, and both match the oracle."""
+    w = synth.Workload("t", 1, 1, 2048, 1024, "fp32", False, seed=6004)
+    full = fa.workspace_size(w.B, w.H, w.N, w.d, fa.FA_FP32, fa.FA_FP32, False)
+    assert full > (32 << 20)
+    assert "splits=1" in fa.plan(w.B, w.H, w.N, w.d, fa.FA_FP32, fa.FA_FP32, False, 32 << 20)[1]
+    one_call(w)
+    one_call(w.scaled(seed=6005))
 
 
 def test_problems_beyond_the_scratch_are_rejected():
