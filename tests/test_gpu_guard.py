@@ -12,7 +12,8 @@ tiles past the end of each head, where the kernels mask their stores.
 
 Paths: the 64/128 tensor-core kernel (one work item per CTA, persistent
 CTAs over many items, the key-range split with a workspace), the general-d
-kernel, the wide-head path (bf16 d = 256, fp32 d = 128 with key splits),
+kernel, the wide-head path (bf16 d = 256, fp32 d = 128 with key splits, and the
+cluster form for d = 512 and 1024),
 fa_attention with a padded O, fa_forward_host on host buffers and
 fa_forward_noalloc.
 """
@@ -140,6 +141,14 @@ def test_wide_head_bf16(N, causal):
 def test_wide_head_fp32_with_key_splits(N):
     device_case(synth.Workload("guard", 1, 1, N, 128, "fp32", False, seed=8500 + N), workspace=True,
                 o_dtype="fp32", expect_plan="wide-head")
+
+
+@pytest.mark.parametrize("N", [129, 1000])
+@pytest.mark.parametrize("d,dtype", [(512, "fp32"), (1024, "bf16")])
+def test_wide_head_clusters(N, d, dtype):
+    """d = 512 and 1024: the CTAs of a query tile form S once as a cluster."""
+    device_case(synth.Workload("guard", 1, 2, N, d, dtype, dtype == "bf16", seed=8550 + N + d),
+                workspace=dtype == "fp32", expect_plan="cluster=%d" % (d // 256))
 
 
 @pytest.mark.parametrize("N", [77, 300])

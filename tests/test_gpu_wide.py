@@ -23,6 +23,12 @@ WIDE = [
     (1, 1, 500, 256, "bf16", True),
     (1, 1, 129, 1024, "bf16", True),
     (1, 1, 1, 1024, "fp32", False),
+    # d = 512 and 1024 run as clusters sharing one formation of S
+    (1, 3, 300, 512, "fp32", True),
+    (2, 1, 1000, 1024, "fp32", False),
+    (1, 2, 700, 1024, "fp32", True),
+    (1, 1, 1000, 1024, "bf16", False),
+    (2, 2, 77, 512, "bf16", True),
 ]
 
 
@@ -50,6 +56,7 @@ def test_wide_path(B, H, N, d, dtype, causal, ws_mode):
     desc, _ = run(w, ws_mode)
     if dtype == "bf16" or ws_mode == "full":
         assert desc.startswith("wide-head"), desc
+        assert ("cluster=%d" % (d // 256)) in desc if d in (512, 1024) else "cluster=1" in desc
 
 
 def test_large_d_workload_on_tensor_cores():

@@ -362,8 +362,8 @@ int fa_plan(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int o_dtyp
         if (w.ok && workspace_bytes && workspace_bytes < w.workspace_bytes) w = fa::wide_plan(p, 1);
         if (w.ok && (w.workspace_bytes == 0 || workspace_bytes >= w.workspace_bytes)) {
             launches = (w.nprod == 3 ? 1 : 0) + 1 + (w.n_split > 1 ? 1 : 0);
-            snprintf(buf, sizeof(buf), "wide-head %s dv=%d splits=%d", w.nprod == 3 ? "fp32 as bf16 hi+lo" : "bf16",
-                     w.dv, w.n_split);
+            snprintf(buf, sizeof(buf), "wide-head %s dv=%d splits=%d cluster=%d",
+                     w.nprod == 3 ? "fp32 as bf16 hi+lo" : "bf16", w.dv, w.n_split, w.cluster);
         } else {
             launches = 1;
             snprintf(buf, sizeof(buf), "general-d");

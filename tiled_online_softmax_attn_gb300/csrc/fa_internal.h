@@ -84,6 +84,7 @@ struct WidePlan {
     bool ok;             // the path applies to this problem
     int nprod;           // 3: fp32 inputs as bf16 hi + lo pairs; 1: bf16 inputs
     int dv;              // width of the O slice a CTA owns (256 or 128)
+    int cluster;         // CTAs per cluster sharing one formation of S (d / 256 for d = 512, 1024), else 1
     int n_q, n_kv, n_dv; // query tiles, key tiles, O slices
     int n_split, tiles_per_split;
     size_t off_split[6]; // workspace offsets of Q/K/V hi and lo copies (fp32 inputs)

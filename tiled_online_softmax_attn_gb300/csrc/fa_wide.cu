@@ -407,6 +407,574 @@ fa_wide_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_constant_
     }
 }
 
+// ---------------------------------------------------------------------------
+// Cluster form of the wide-head kernel, for head dimensions of 512 and 1024
+// (R = d / 256 CTAs per cluster).  The R CTAs of a cluster share one query
+// tile and one key range; CTA x owns the O slice of columns [256 x, 256 x +
+// 256) and forms the partial scores S_x = Q[:, 256 x ...] K[:, 256 x ...]^T
+// over its part of the head dimension, so S = sum_x S_x is formed once per
+// cluster instead of once per O slice.  The partials meet in distributed
+// shared memory, one 32-row quarter of the tile at a time:
+//
+//   * quarter w (tensor-memory lanes 32 w ...) is owned by CTA w % R.  Every
+//     other CTA's warp w stages its 32 partial rows in its own shared memory
+//     and one lane copies them (bulk copy engine) into the owner's receive
+//     slot, completing the bytes on the owner's `recv_full`;
+//   * the owner's warp w adds the R partials (its own first, then the others
+//     in rank order), runs the online softmax of "Tiling the Loop" for the 32
+//     rows (running maximum, weights, row sums; lazy rescaling as in the
+//     single-CTA kernel), writes the weights (bf16 hi, and lo for fp32 inputs)
+//     into its own tensor memory, and copies them, with each row's reference
+//     maximum m and normaliser l + dq, into every other CTA's staging slot;
+//   * each CTA's warp w takes the weights of its lanes from the staging slot
+//     into tensor memory, rescales its O rows by alpha = 2^(m_old - m) (the
+//     same instruction on the same values as the owner's), and the MMA warp
+//     forms O_x += P V[:, 256 x ...] from there.
+//
+// No slot needs a "free" signal: a sender stages partial(j + 1) in its staging
+// slot only after it has read the weights of tile j that arrived there, and
+// the owner writes those only after every partial(j) has landed; the owner
+// stages the copy of tile j for CTA y in y's own receive slot, which y
+// refills with partial(j + 1) only after that copy has reached it.
+//
+// The CTAs of a cluster synchronise once after setup (nobody arrives on a
+// barrier that is not initialised yet) and once before exit (nobody writes
+// into the shared memory of a CTA that has left).  Every wait is bounded as
+// in the rest of the library.
+//
+// Tensor memory: S partial [0, 128), P_hi [128, 192), P_lo [192, 256), O slice
+// [256, 512).  Shared memory (all dynamic, 1024-byte aligned base checked at
+// run time): a two-slot ring of 64 KB (the S chunks of the CTA's part of Q and
+// K, then the V slice), the receive slots (32 rows x 128 fp32), the staging
+// slots (32 rows x 128 bf16 hi + 128 lo) and 8-byte row records {m, l + dq},
+// slots stored chunk-major (slot_chunk).  The epilogue stages the O slice in
+// the ring, idle by then, and writes it row by row with the lanes of a warp on
+// consecutive addresses.
+
+template <int R>
+struct ClLayout {
+    static constexpr int OWNED = 4 / R;                  // row quarters a CTA owns
+    static constexpr int FOREIGN = 4 - OWNED;            // quarters other CTAs own
+    static constexpr uint32_t SLOT = 32 * 512;           // 32 rows x 512 bytes
+    static constexpr uint32_t REC = 32 * 8;              // 32 row records {m, l + dq}
+    static constexpr uint32_t OFF_RECV = 2 * STAGE_BYTES;                // [OWNED][R - 1] slots
+    static constexpr uint32_t OFF_PST = OFF_RECV + OWNED * (R - 1) * SLOT;  // [FOREIGN] slots
+    static constexpr uint32_t OFF_PREC = OFF_PST + FOREIGN * SLOT;         // [FOREIGN] incoming records
+    static constexpr uint32_t OFF_OREC = OFF_PREC + FOREIGN * REC;         // [OWNED][R - 1] outgoing records
+    static constexpr uint32_t OFF_BARS = OFF_OREC + OWNED * (R - 1) * REC;
+    // barriers: full[2], empty[2], s_full, s_read, p_full, p_free, o_full, drain,
+    // recv_full[2], pst_full[3]; then tensor-memory base and abort flag
+    static constexpr uint32_t BAR_BYTES = 18 * 8 + 16;
+    static constexpr uint32_t NEED = OFF_BARS + BAR_BYTES;
+    static constexpr uint32_t SMEM_MAX = 232448;
+    static constexpr uint32_t SMEM = NEED + 1024 <= SMEM_MAX ? NEED + 1024 : SMEM_MAX;
+};
+static_assert(ClLayout<4>::NEED <= ClLayout<4>::SMEM_MAX && ClLayout<2>::NEED <= ClLayout<2>::SMEM_MAX,
+              "cluster kernel: shared memory above the 227 KB a CTA may use");
+
+// Byte offset of 16-byte chunk c of row `row` in an exchange slot: chunk-major,
+// so that the 32 lanes of a warp (one row each) touch 512 contiguous bytes.
+__device__ __forceinline__ uint32_t slot_chunk(int row, int c) { return (uint32_t)(c * 512 + row * 16); }
+
+constexpr uint32_t ERR_CL_LAYOUT = 64u;  // the cluster kernel's shared-memory layout did not fit its allocation
+
+template <int NPROD, int R, bool CAUSAL>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+fa_wide_cluster_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_constant__ CUtensorMap tm_ql,
+                       const __grid_constant__ CUtensorMap tm_kh, const __grid_constant__ CUtensorMap tm_kl,
+                       const __grid_constant__ CUtensorMap tm_vh, const __grid_constant__ CUtensorMap tm_vl,
+                       const WideParams prm)
+{
+    using L = ClLayout<R>;
+    constexpr int DVC = 256;                       // O columns per CTA
+    constexpr uint32_t P_BYTES = NPROD == 3 ? L::SLOT : L::SLOT / 2;  // chunk-major: hi chunks first
+    extern __shared__ uint8_t smem_raw[];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N = prm.N, D = prm.D;
+    const int x = (int)(blockIdx.x % R);           // rank in the cluster = O slice = part of d
+    const int cl = (int)(blockIdx.x / R);
+    const int qt = CAUSAL ? prm.n_q - 1 - cl / prm.n_split : cl / prm.n_split;
+    const int sp = cl % prm.n_split;
+    const int bh = (int)blockIdx.y;
+    const int q0 = qt * BM, dv0 = x * DVC, dk0 = x * DVC;
+    const int kv_need = CAUSAL ? min(prm.n_kv, qt + 1) : prm.n_kv;
+    const int kv_lo = sp * prm.tiles_per_split;
+    const int n_j = min(kv_lo + prm.tiles_per_split, kv_need) - kv_lo;
+    const size_t part_row = ((size_t)sp * prm.BH + bh) * N;
+
+    if (n_j <= 0) {  // every CTA of the cluster takes this branch: an empty partial
+        if (!prm.direct && x == 0 && warp < 4) {
+            const int grow = q0 + (int)threadIdx.x;
+            if (grow < N) {
+                prm.m_part[part_row + grow] = -INFINITY;
+                prm.l_part[part_row + grow] = 0.f;
+                prm.d_part[part_row + grow] = 0.f;
+            }
+        }
+        return;
+    }
+    // 1024-byte aligned base (every CTA of the cluster gets the same offset, so
+    // all of them leave here together if the layout does not fit)
+    const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+    if (pad + L::NEED > L::SMEM) {
+        if (threadIdx.x == 0) atomicOr(&g_wide_error_word, ERR_CL_LAYOUT);
+        return;
+    }
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t s_base = smem_addr(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BARS);
+    uint64_t *full_b = bars, *empty_b = bars + 2;
+    uint64_t &s_full = bars[4], &s_read = bars[5], &p_full = bars[6], &p_free = bars[7], &o_full = bars[8],
+             &drain = bars[9];
+    uint64_t *recv_full = bars + 10, *pst_full = bars + 12;
+    uint32_t &tmem_base_s = *reinterpret_cast<uint32_t *>(smem + L::OFF_BARS + 18 * 8);
+    volatile int &abort_flag = *reinterpret_cast<volatile int *>(smem + L::OFF_BARS + 18 * 8 + 4);
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_addr(&full_b[s]), 1);
+            mbar_init(smem_addr(&empty_b[s]), 1);
+        }
+        mbar_init(smem_addr(&s_full), 1);
+        mbar_init(smem_addr(&s_read), 128);
+        mbar_init(smem_addr(&p_full), 128);
+        mbar_init(smem_addr(&p_free), 1);
+        mbar_init(smem_addr(&o_full), 1);
+        mbar_init(smem_addr(&drain), 1);
+        for (int i = 0; i < 2; ++i) mbar_init(smem_addr(&recv_full[i]), 1);  // the owner's expect_tx
+        for (int i = 0; i < 3; ++i) mbar_init(smem_addr(&pst_full[i]), 1);   // the receiver's expect_tx
+        fence_mbar_init();
+    }
+    if (warp == MMA_WARP) {
+        tmem_alloc(smem_addr(&tmem_base_s), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // the peers' barriers are initialised before anyone arrives on them
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    const uint64_t limit = prm.wait_limit_ns;
+
+    if (warp == TMA_WARP) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_last();
+            int it = 0;
+            bool ok = true;
+            auto acquire = [&](uint32_t bytes) -> int {
+                const int st = it & 1;
+                if (!wait_or_abort(smem_addr(&empty_b[st]), (uint32_t)(((it >> 1) & 1) ^ 1), limit, &abort_flag))
+                    return -1;
+                mbar_arrive_expect_tx(smem_addr(&full_b[st]), bytes);
+                return st;
+            };
+            auto load_s = [&](int jj) {
+                const int k0 = (kv_lo + jj) * BN;
+                for (int c = 0; ok && c < DVC / 64; ++c) {
+                    const int st = acquire(NPROD == 3 ? 4 * BOX_BYTES : 2 * BOX_BYTES);
+                    if (st < 0) { ok = false; break; }
+                    const uint32_t dst = s_base + st * STAGE_BYTES, fb = smem_addr(&full_b[st]);
+                    tma_load_3d(dst, &tm_qh, fb, dk0 + c * 64, q0, bh, pol);
+                    tma_load_3d(dst + 2 * BOX_BYTES, &tm_kh, fb, dk0 + c * 64, k0, bh, pol);
+                    if (NPROD == 3) {
+                        tma_load_3d(dst + BOX_BYTES, &tm_ql, fb, dk0 + c * 64, q0, bh, pol);
+                        tma_load_3d(dst + 3 * BOX_BYTES, &tm_kl, fb, dk0 + c * 64, k0, bh, pol);
+                    }
+                    ++it;
+                }
+            };
+            auto load_v = [&](int jj) {
+                const int k0 = (kv_lo + jj) * BN;
+                for (int part = 0; ok && part < (NPROD == 3 ? 2 : 1); ++part) {
+                    const int st = acquire((DVC / 64) * BOX_BYTES);
+                    if (st < 0) { ok = false; break; }
+                    const uint32_t dst = s_base + st * STAGE_BYTES, fb = smem_addr(&full_b[st]);
+                    for (int a = 0; a < DVC / 64; ++a)
+                        tma_load_3d(dst + a * BOX_BYTES, part ? &tm_vl : &tm_vh, fb, dv0 + a * 64, k0, bh, pol);
+                    ++it;
+                }
+            };
+            // the order the MMA warp consumes: S(0), then S(j), V(j - 1) ..., then V(last)
+            for (int jj = 0; ok && jj < n_j; ++jj) {
+                load_s(jj);
+                if (jj > 0) load_v(jj - 1);
+            }
+            if (ok) load_v(n_j - 1);
+            if (!ok) {
+                if (!abort_flag) raise_wide(ERR_WAIT, &abort_flag);
+                for (int j = max(0, it - 2); j < it; ++j)
+                    if (!mbar_wait_bounded(smem_addr(&full_b[j & 1]), (uint32_t)((j >> 1) & 1), limit))
+                        atomicOr(&g_wide_error_word, ERR_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        // ================================================================ MMA issuer
+        {
+            const uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
+            const uint32_t idesc_o = idesc_bf16_f32(BM, DVC, 0, 1);
+            const uint32_t tS = tmem, tPh = tmem + 128, tPl = tmem + 192, tO = tmem + COL_O;
+            int it = 0;
+            bool ok = true, issued = false;
+            auto wait_full = [&]() -> int {
+                const int st = it & 1;
+                if (!wait_or_abort_w(smem_addr(&full_b[st]), (uint32_t)((it >> 1) & 1), limit, &abort_flag))
+                    return -1;
+                tc_fence_after();
+                return st;
+            };
+            auto mma_s = [&](int jj) -> bool {
+                if (jj > 0 && !wait_or_abort_w(smem_addr(&s_read), (uint32_t)((jj - 1) & 1), limit, &abort_flag))
+                    return false;
+                tc_fence_after();
+                for (int c = 0; c < DVC / 64; ++c) {
+                    const int st = wait_full();
+                    if (st < 0) return false;
+                    const uint32_t base = s_base + st * STAGE_BYTES;
+                    const uint64_t dqh = sdesc_sw128(base, 16, 1024), dql = sdesc_sw128(base + BOX_BYTES, 16, 1024);
+                    const uint64_t dkh = sdesc_sw128(base + 2 * BOX_BYTES, 16, 1024),
+                                   dkl = sdesc_sw128(base + 3 * BOX_BYTES, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t off = (uint64_t)(kk * 2);
+                        mma_ss_w(tS, dqh + off, dkh + off, idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
+                        if (NPROD == 3) {
+                            mma_ss_w(tS, dqh + off, dkl + off, idesc_s, 1u);
+                            mma_ss_w(tS, dql + off, dkh + off, idesc_s, 1u);
+                        }
+                    }
+                    issued = true;
+                    mma_commit_w(smem_addr(&empty_b[st]));
+                    ++it;
+                }
+                mma_commit_w(smem_addr(&s_full));
+                return true;
+            };
+            auto mma_pv = [&](int jj) -> bool {
+                if (!wait_or_abort_w(smem_addr(&p_full), (uint32_t)(jj & 1), limit, &abort_flag)) return false;
+                tc_fence_after();
+                for (int part = 0; part < (NPROD == 3 ? 2 : 1); ++part) {
+                    const int st = wait_full();
+                    if (st < 0) return false;
+                    const uint64_t dv = sdesc_sw128(s_base + st * STAGE_BYTES, BOX_BYTES, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        const uint64_t voff = (uint64_t)((kk * 16 * 128) >> 4);
+                        if (part == 0) {
+                            mma_ts_w(tO, tPh + kk * 8, dv + voff, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                            if (NPROD == 3) mma_ts_w(tO, tPl + kk * 8, dv + voff, idesc_o, 1u);
+                        } else {
+                            mma_ts_w(tO, tPh + kk * 8, dv + voff, idesc_o, 1u);
+                        }
+                    }
+                    issued = true;
+                    mma_commit_w(smem_addr(&empty_b[st]));
+                    ++it;
+                }
+                mma_commit_w(smem_addr(&p_free));
+                return true;
+            };
+            for (int jj = 0; ok && jj < n_j; ++jj) {
+                if (!mma_s(jj)) { ok = false; break; }
+                if (jj > 0 && !mma_pv(jj - 1)) { ok = false; break; }
+            }
+            if (ok && !mma_pv(n_j - 1)) ok = false;
+            if (ok) {
+                mma_commit_w(smem_addr(&o_full));
+            } else {
+                if (!abort_flag) raise_wide(ERR_WAIT, &abort_flag);
+                if (issued) {
+                    mma_commit_w(smem_addr(&drain));
+                    if (!mbar_wait_bounded(smem_addr(&drain), 0, limit)) atomicOr(&g_wide_error_word, ERR_DRAIN);
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================================================================ score exchange, softmax, epilogue
+        const int w = warp;                          // row quarter: tensor-memory lanes 32 w ...
+        const int r = w * 32 + lane;
+        const int grow = q0 + r;
+        const uint32_t lane_base = tmem + ((uint32_t)(w * 32) << 16);
+        const uint32_t tS = lane_base, tPh = lane_base + 128, tPl = lane_base + 192, tO = lane_base + COL_O;
+        const float sl = prm.scale_log2;
+        const int owner = w % R;
+        const bool is_owner = owner == x;
+        const int oi = w / R;                        // index of quarter w among its owner's quarters
+        // index of quarter w among CTA y's foreign quarters (w not owned by y)
+        auto foreign_index = [](int y, int ww) { int f = 0; for (int v = 0; v < ww; ++v) f += (v % R != y); return f; };
+        auto other_index = [](int y, int o) { return y < o ? y : y - 1; };  // rank y among the CTAs other than o
+        float m = -INFINITY, l = 0.f, dq = 0.f;     // owner: running statistics; others: m and l + dq
+        bool ok = true;
+        auto fail = [&]() {
+            ok = false;
+            if (!abort_flag) raise_wide(ERR_WAIT, &abort_flag);
+            else atomicOr(&g_wide_error_word, ERR_WAIT);
+        };
+        // Bounded waits with one outcome for the whole warp, so that the
+        // warp-collective tensor-memory accesses after them stay converged.
+        auto uwait = [&](const uint64_t *bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, wait_or_abort(smem_addr(bar), parity, limit, &abort_flag));
+        };
+        auto uwait_cl = [&](const uint64_t *bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, wait_or_abort_cluster(smem_addr(bar), parity, limit, &abort_flag));
+        };
+        const int fi = is_owner ? 0 : foreign_index(x, w);
+        for (int jj = 0; ok && jj < n_j; ++jj) {
+            if (!uwait(&s_full, (uint32_t)(jj & 1))) { fail(); break; }
+            tc_fence_after();
+            float s[BN];
+            {
+                uint32_t raw[BN];
+                tmem_ld128(tS, raw);
+#pragma unroll
+                for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(raw[c]);
+            }
+            tc_fence_before();
+            mbar_arrive(smem_addr(&s_read));          // the next S partial may overwrite tensor memory
+            uint32_t ph[64], pl[64];                  // this row's weights, bf16 pairs
+            float alpha = 1.f;
+            if (is_owner) {
+                // ---- sum the partials of the other CTAs into this row
+                if (lane == 0)
+                    mbar_arrive_expect_tx(smem_addr(&recv_full[oi]), (uint32_t)(R - 1) * L::SLOT);
+                if (!uwait_cl(&recv_full[oi], (uint32_t)(jj & 1))) { fail(); break; }
+                for (int y = 0; y < R; ++y) {
+                    if (y == x) continue;
+                    const uint8_t *slot = smem + L::OFF_RECV + (oi * (R - 1) + other_index(y, x)) * L::SLOT;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const float4 v = *reinterpret_cast<const float4 *>(slot + slot_chunk(lane, c));
+                        s[4 * c] += v.x;
+                        s[4 * c + 1] += v.y;
+                        s[4 * c + 2] += v.z;
+                        s[4 * c + 3] += v.w;
+                    }
+                }
+                // ---- online softmax of the row
+                const int kc0 = (kv_lo + jj) * BN;
+                int lim = N - kc0;
+                if (CAUSAL) lim = min(lim, grow - kc0 + 1);
+                if (lim < BN) {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c)
+                        if (c >= lim) s[c] = -INFINITY;
+                }
+                const float mx = row_max_128(s);
+                const float m_tile = mx * sl;
+                if (m_tile > m + RESCALE_LOG2) {
+                    alpha = ex2(m - m_tile);
+                    m = m_tile;
+                }
+                const float base = (m == -INFINITY) ? 0.f : m;
+                const uint64_t sl2 = f2_pack(sl, sl), nb2 = f2_pack(-base, -base);
+                uint64_t rs2[2] = {0ull, 0ull};
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    float a0, a1;
+                    f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2, nb2), a0, a1);
+                    const float p0 = ex2(a0), p1 = ex2(a1);
+                    rs2[c & 1] = f2_add(rs2[c & 1], f2_pack(p0, p1));
+                    ph[c] = pack_bf16x2(p0, p1);
+                    pl[c] = NPROD == 3 ? pack_bf16x2(p0 - __uint_as_float(ph[c] << 16),
+                                                     p1 - __uint_as_float(ph[c] & 0xFFFF0000u))
+                                       : 0u;
+                }
+                float r0, r1;
+                f2_unpack(f2_add(rs2[0], rs2[1]), r0, r1);
+                l = l * alpha + (r0 + r1);
+                if (NPROD == 1) {
+                    const float p_top = ex2(fmaf(mx, sl, -base));
+                    dq = dq * alpha + (__uint_as_float(pack_bf16x2(p_top, 0.f) << 16) - p_top);
+                }
+                // ---- the weights and {m, l + dq} to every other CTA: staged in that
+                // CTA's own receive slot (its partial has been read), one bulk copy each
+                for (int y = 0; y < R; ++y) {
+                    if (y == x) continue;
+                    const int k = oi * (R - 1) + other_index(y, x);
+                    uint8_t *stg = smem + L::OFF_RECV + k * L::SLOT;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        *reinterpret_cast<uint4 *>(stg + slot_chunk(lane, c)) =
+                            make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
+                    if (NPROD == 3) {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            *reinterpret_cast<uint4 *>(stg + slot_chunk(lane, 16 + c)) =
+                                make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
+                    }
+                    *reinterpret_cast<float2 *>(smem + L::OFF_OREC + k * L::REC + lane * 8) = make_float2(m, l + dq);
+                }
+                fence_proxy_async_smem();            // the staged bytes are visible to the bulk copies
+                __syncwarp();
+                if (lane == 0) {
+                    for (int y = 0; y < R; ++y) {
+                        if (y == x) continue;
+                        const int k = oi * (R - 1) + other_index(y, x);
+                        const int fy = foreign_index(y, w);
+                        const uint32_t bar = mapa_shared(smem_addr(&pst_full[fy]), (uint32_t)y);
+                        bulk_copy_s2cluster(mapa_shared(s_base + L::OFF_PST + fy * L::SLOT, (uint32_t)y),
+                                            s_base + L::OFF_RECV + k * L::SLOT, P_BYTES, bar);
+                        bulk_copy_s2cluster(mapa_shared(s_base + L::OFF_PREC + fy * L::REC, (uint32_t)y),
+                                            s_base + L::OFF_OREC + k * L::REC, L::REC, bar);
+                    }
+                }
+            } else {
+                // ---- send this row's partial to the owner, take the weights back
+                uint8_t *stg = smem + L::OFF_PST + fi * L::SLOT;  // free: its last weights were read
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    *reinterpret_cast<float4 *>(stg + slot_chunk(lane, c)) =
+                        make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    // arm the slot for the weights of this tile before they can arrive
+                    mbar_arrive_expect_tx(smem_addr(&pst_full[fi]), P_BYTES + L::REC);
+                    const int k = oi * (R - 1) + other_index(x, owner);
+                    bulk_copy_s2cluster(mapa_shared(s_base + L::OFF_RECV + k * L::SLOT, (uint32_t)owner),
+                                        s_base + L::OFF_PST + fi * L::SLOT, L::SLOT,
+                                        mapa_shared(smem_addr(&recv_full[oi]), (uint32_t)owner));
+                }
+                if (!uwait_cl(&pst_full[fi], (uint32_t)(jj & 1))) { fail(); break; }
+                const uint8_t *pslot = smem + L::OFF_PST + fi * L::SLOT;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(pslot + slot_chunk(lane, c));
+                    ph[4 * c] = v.x;
+                    ph[4 * c + 1] = v.y;
+                    ph[4 * c + 2] = v.z;
+                    ph[4 * c + 3] = v.w;
+                }
+                if (NPROD == 3) {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(pslot + slot_chunk(lane, 16 + c));
+                        pl[4 * c] = v.x;
+                        pl[4 * c + 1] = v.y;
+                        pl[4 * c + 2] = v.z;
+                        pl[4 * c + 3] = v.w;
+                    }
+                }
+                const float2 rec = *reinterpret_cast<const float2 *>(smem + L::OFF_PREC + fi * L::REC + lane * 8);
+                if (rec.x != m) alpha = ex2(m - rec.x);  // the owner's alpha: same instruction, same inputs
+                m = rec.x;
+                l = rec.y;                            // l + dq
+            }
+            // ---- this CTA's copy of the weights; O rows rescaled once the previous P V is done
+            if (jj > 0 && !uwait(&p_free, (uint32_t)((jj - 1) & 1))) { fail(); break; }
+            tc_fence_after();
+            if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+                for (int c = 0; c < DVC / 32; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(tO + c * 32, raw);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float o0, o1;
+                        f2_unpack(f2_mul(f2_pack(__uint_as_float(raw[2 * e]), __uint_as_float(raw[2 * e + 1])), a2), o0, o1);
+                        raw[2 * e] = __float_as_uint(o0);
+                        raw[2 * e + 1] = __float_as_uint(o1);
+                    }
+                    tmem_st32(tO + c * 32, raw);
+                }
+            }
+            {
+                uint32_t h32[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) h32[c] = ph[c];
+                tmem_st32(tPh, h32);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) h32[c] = ph[32 + c];
+                tmem_st32(tPh + 32, h32);
+                if (NPROD == 3) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) h32[c] = pl[c];
+                    tmem_st32(tPl, h32);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) h32[c] = pl[32 + c];
+                    tmem_st32(tPl + 32, h32);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_addr(&p_full));
+        }
+        if (ok && uwait(&o_full, 0)) {
+            tc_fence_after();
+            // O rows through shared memory: thread r writes its row (256 fp32,
+            // chunks rotated by the row so the warp's stores spread over the
+            // banks), then the warp writes each of its 32 rows with its lanes on
+            // consecutive addresses.  Warp w uses its own 32 KB of the ring.
+            const float inv = prm.direct ? 1.f / (is_owner ? l + dq : l) : 1.f;
+            uint8_t *stage = smem + (uint32_t)w * 32 * (DVC * 4);
+            fence_proxy_async_smem();
+#pragma unroll 1
+            for (int c = 0; c < DVC / 32; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(tO + c * 32, raw);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int ch = c * 8 + q;  // float4 chunk of the row, 0..63
+                    *reinterpret_cast<float4 *>(stage + lane * (DVC * 4) + (((ch ^ lane) & 63) << 4)) =
+                        make_float4(__uint_as_float(raw[4 * q]) * inv, __uint_as_float(raw[4 * q + 1]) * inv,
+                                    __uint_as_float(raw[4 * q + 2]) * inv, __uint_as_float(raw[4 * q + 3]) * inv);
+                }
+            }
+            __syncwarp();
+            for (int rr = 0; rr < 32; ++rr) {
+                const int g = q0 + w * 32 + rr;
+                if (g >= N) break;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int ch = h * 32 + lane;
+                    const float4 v = *reinterpret_cast<const float4 *>(stage + rr * (DVC * 4) + (((ch ^ rr) & 63) << 4));
+                    if (!prm.direct) {
+                        reinterpret_cast<float4 *>(prm.o_part + (part_row + g) * D + dv0)[ch] = v;
+                    } else if (prm.o_fp32) {
+                        reinterpret_cast<float4 *>(static_cast<float *>(prm.o) + ((size_t)bh * N + g) * D + dv0)[ch] = v;
+                    } else {
+                        reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(prm.o) + ((size_t)bh * N + g) * D + dv0)[ch] =
+                            make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+                    }
+                }
+            }
+            if (grow < N && is_owner) {  // the row statistics, from the CTA that computed them
+                if (prm.direct) {
+                    if (prm.lse) prm.lse[(size_t)bh * N + grow] = (m + log2f(l)) * 0.69314718055994530942f;
+                } else {
+                    prm.m_part[part_row + grow] = m;
+                    prm.l_part[part_row + grow] = l;
+                    prm.d_part[part_row + grow] = dq;
+                }
+            }
+        } else if (ok) {
+            if (!abort_flag) raise_wide(ERR_WAIT, &abort_flag);
+            else atomicOr(&g_wide_error_word, ERR_WAIT);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+    if (abort_flag) {
+        // After a wait gave up, a peer's bulk copy toward this CTA may still be
+        // in flight (nobody waits for it any more): give it time to land before
+        // the shared memory is released.
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 20000ull) {
+        }
+    }
+    cluster_sync_all();  // no peer writes into this CTA's shared memory after it exits
+}
+
 // x = hi + lo with hi = bf16(x), lo = bf16(x - hi), for Q, K and V in one
 // launch (blockIdx.y picks the tensor); four elements per thread.
 struct SplitArgs {
@@ -539,6 +1107,8 @@ WidePlan wide_plan(const Problem &p, int max_splits)
     const int64_t BH = p.B * p.H;
     w.nprod = fp32_in ? 3 : 1;
     w.dv = (p.d % 256 == 0) ? 256 : 128;
+    // d = 512 and 1024: the CTAs of one query tile form S once as a cluster
+    w.cluster = (p.d == 512 || p.d == 1024) ? (int)(p.d / 256) : 1;
     w.n_q = (int)((p.N + BM - 1) / BM);
     w.n_kv = (int)((p.N + BN - 1) / BN);
     w.n_dv = (int)(p.d / w.dv);
@@ -620,6 +1190,39 @@ cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cu
     }
     (void)flags;
     dim3 grid((unsigned)(w.n_q * w.n_dv * w.n_split), (unsigned)BH);
+    if (w.cluster > 1) {
+        // grid.x = (query tile, split) clusters of R CTAs, one O slice each
+        auto go_cl = [&](auto kern, int smem) -> cudaError_t {
+            cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (err != cudaSuccess) return err;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = grid;
+            cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+            cfg.dynamicSmemBytes = (size_t)smem;
+            cfg.stream = stream;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = (unsigned)w.cluster;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            return cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], m[3], m[4], m[5], prm);
+        };
+        constexpr int S4 = (int)ClLayout<4>::SMEM, S2 = (int)ClLayout<2>::SMEM;
+        if (w.nprod == 3) {
+            if (w.cluster == 4) e = p.causal ? go_cl(fa_wide_cluster_kernel<3, 4, true>, S4) : go_cl(fa_wide_cluster_kernel<3, 4, false>, S4);
+            else e = p.causal ? go_cl(fa_wide_cluster_kernel<3, 2, true>, S2) : go_cl(fa_wide_cluster_kernel<3, 2, false>, S2);
+        } else {
+            if (w.cluster == 4) e = p.causal ? go_cl(fa_wide_cluster_kernel<1, 4, true>, S4) : go_cl(fa_wide_cluster_kernel<1, 4, false>, S4);
+            else e = p.causal ? go_cl(fa_wide_cluster_kernel<1, 2, true>, S2) : go_cl(fa_wide_cluster_kernel<1, 2, false>, S2);
+        }
+        if (e != cudaSuccess) return e;
+        if (!prm.direct)
+            e = launch_combine(prm.o_part, prm.m_part, prm.l_part, prm.d_part, p.o, p.o_dtype == 1, p.lse, BH, p.N,
+                               (int)p.d, w.n_split, stream);
+        return e;
+    }
     auto go = [&](auto kern) -> cudaError_t {
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (err != cudaSuccess) return err;

@@ -34,6 +34,22 @@ __device__ __forceinline__ bool wait_or_abort_w(uint32_t bar, uint32_t parity, u
     return __all_sync(0xffffffffu, done);
 }
 
+// wait_or_abort with cluster-scope acquire, for barriers other CTAs of the
+// cluster arrive on; polls without suspending.
+__device__ __forceinline__ bool wait_or_abort_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                      volatile int *abort_flag)
+{
+    if (mbar_test_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_test_wait_cluster(bar, parity)) return true;
+        if ((spin & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+
 // Maximum of NV scores (NV a multiple of 8): eight independent chains of
 // three-input maxima, then a short combine (depth about NV / 16 + 3 instead
 // of an NV-long dependency chain).
