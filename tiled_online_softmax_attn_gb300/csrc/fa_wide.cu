@@ -555,6 +555,8 @@ fa_wide_cluster_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_c
     __syncthreads();
     cluster_sync_all();  // the peers' barriers are initialised before anyone arrives on them
     tc_fence_after();
+    pdl_launch_dependents();  // the merge kernel may be scheduled; it waits for this one
+    pdl_wait_prior();         // the split pass's bf16 copies are complete and visible
     const uint32_t tmem = tmem_base_s;
     const uint64_t limit = prm.wait_limit_ns;
 
@@ -976,30 +978,45 @@ fa_wide_cluster_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_c
 }
 
 // x = hi + lo with hi = bf16(x), lo = bf16(x - hi), for Q, K and V in one
-// launch (blockIdx.y picks the tensor); four elements per thread.
+// launch (blockIdx.y picks the tensor).  A block converts SPLIT_PER_BLOCK
+// float4 groups, four per thread, all four loads issued before any store (the
+// fp32 inputs are read once: streaming loads).
 struct SplitArgs {
     const float4 *x[3];
     uint2 *hi[3];
     uint2 *lo[3];
 };
+constexpr int SPLIT_THREADS = 256, SPLIT_UNROLL = 4, SPLIT_PER_BLOCK = SPLIT_THREADS * SPLIT_UNROLL;
 
-__global__ void fa_split_kernel(const SplitArgs a, size_t n4)
+__global__ void __launch_bounds__(SPLIT_THREADS) fa_split_kernel(const SplitArgs a, size_t n4)
 {
     const float4 *__restrict__ x = a.x[blockIdx.y];
     uint2 *__restrict__ hi = a.hi[blockIdx.y];
     uint2 *__restrict__ lo = a.lo[blockIdx.y];
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-        const float4 v = x[i];
-        const uint32_t h01 = pack_bf16x2(v.x, v.y), h23 = pack_bf16x2(v.z, v.w);
-        const uint32_t l01 = pack_bf16x2(v.x - __uint_as_float(h01 << 16), v.y - __uint_as_float(h01 & 0xFFFF0000u));
-        const uint32_t l23 = pack_bf16x2(v.z - __uint_as_float(h23 << 16), v.w - __uint_as_float(h23 & 0xFFFF0000u));
+    const size_t i0 = (size_t)blockIdx.x * SPLIT_PER_BLOCK + threadIdx.x;
+    float4 v[SPLIT_UNROLL];
+#pragma unroll
+    for (int u = 0; u < SPLIT_UNROLL; ++u) {
+        const size_t i = i0 + (size_t)u * SPLIT_THREADS;
+        if (i < n4) v[u] = __ldcs(x + i);
+    }
+    pdl_launch_dependents();  // the attention kernel's prologue may overlap the stores
+#pragma unroll
+    for (int u = 0; u < SPLIT_UNROLL; ++u) {
+        const size_t i = i0 + (size_t)u * SPLIT_THREADS;
+        if (i >= n4) break;
+        const uint32_t h01 = pack_bf16x2(v[u].x, v[u].y), h23 = pack_bf16x2(v[u].z, v[u].w);
+        const uint32_t l01 = pack_bf16x2(v[u].x - __uint_as_float(h01 << 16), v[u].y - __uint_as_float(h01 & 0xFFFF0000u));
+        const uint32_t l23 = pack_bf16x2(v[u].z - __uint_as_float(h23 << 16), v[u].w - __uint_as_float(h23 & 0xFFFF0000u));
         hi[i] = make_uint2(h01, h23);
         lo[i] = make_uint2(l01, l23);
     }
 }
 
 // Merge of the per-split partial results, one CTA per query row and one
-// float4 of the row per thread, every split's load in flight together.
+// float4 of the row per thread.  Each thread's loads of its partial rows are
+// issued before warp 0 has the split weights, so the two round trips to
+// memory overlap.
 template <typename Tout>
 __global__ void __launch_bounds__(256)
 fa_combine_kernel(const float *__restrict__ o_part, const float *__restrict__ m_part,
@@ -1010,6 +1027,15 @@ fa_combine_kernel(const float *__restrict__ o_part, const float *__restrict__ m_
     __shared__ float inv_s;
     const size_t row = blockIdx.x;
     const size_t stride = (size_t)BH * N;
+    pdl_wait_prior();  // the partials come from the kernel before this one
+    constexpr int HOLD = 4;  // partial rows held in registers per thread (more splits: loaded as used)
+    const int c0 = threadIdx.x * 4;
+    float4 held[HOLD];
+    if (c0 < D) {
+#pragma unroll
+        for (int s = 0; s < HOLD; ++s)
+            if (s < n_split) held[s] = __ldcs(reinterpret_cast<const float4 *>(o_part + (s * stride + row) * D + c0));
+    }
     if (threadIdx.x < 32) {
         // warp 0: reference maximum, weights 2^(m_s - m), denominators
         const int s = threadIdx.x;
@@ -1033,13 +1059,13 @@ fa_combine_kernel(const float *__restrict__ o_part, const float *__restrict__ m_
     }
     __syncthreads();
     const float inv = inv_s;
-    for (int c = threadIdx.x * 4; c < D; c += blockDim.x * 4) {
+    for (int c = c0; c < D; c += blockDim.x * 4) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
         for (int s = 0; s < n_split; ++s) {
             const float wt = w_s[s];
             if (wt == 0.f) continue;  // empty splits hold no partial O
-            const float4 v = __ldcs(reinterpret_cast<const float4 *>(o_part + (s * stride + row) * D + c));
+            const float4 v = (c == c0 && s < HOLD) ? held[s]
+                                                   : __ldcs(reinterpret_cast<const float4 *>(o_part + (s * stride + row) * D + c));
             acc.x = fmaf(wt, v.x, acc.x);
             acc.y = fmaf(wt, v.y, acc.y);
             acc.z = fmaf(wt, v.z, acc.z);
@@ -1155,8 +1181,8 @@ cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cu
             sa.lo[t] = static_cast<uint2 *>(buf[2 * t + 1]);
         }
         const size_t n4 = n / 4;
-        const unsigned blocks = (unsigned)std::min<size_t>((n4 + 255) / 256, (size_t)sm_count() * 4);
-        fa_split_kernel<<<dim3(blocks, 3), 256, 0, stream>>>(sa, n4);
+        const unsigned blocks = (unsigned)((n4 + SPLIT_PER_BLOCK - 1) / SPLIT_PER_BLOCK);
+        fa_split_kernel<<<dim3(blocks, 3), SPLIT_THREADS, 0, stream>>>(sa, n4);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         qh = buf[0]; ql = buf[1]; kh = buf[2]; kl = buf[3]; vh = buf[4]; vl = buf[5];
     }
@@ -1200,13 +1226,17 @@ cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cu
             cfg.blockDim = dim3(NUM_THREADS, 1, 1);
             cfg.dynamicSmemBytes = (size_t)smem;
             cfg.stream = stream;
-            cudaLaunchAttribute at[1];
+            cudaLaunchAttribute at[2];
             at[0].id = cudaLaunchAttributeClusterDimension;
             at[0].val.clusterDim.x = (unsigned)w.cluster;
             at[0].val.clusterDim.y = 1;
             at[0].val.clusterDim.z = 1;
+            // the prologue may overlap the split pass's tail (the kernel waits for it
+            // before its first global access)
+            at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            at[1].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = at;
-            cfg.numAttrs = 1;
+            cfg.numAttrs = w.nprod == 3 ? 2 : 1;
             return cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], m[3], m[4], m[5], prm);
         };
         constexpr int S4 = (int)ClLayout<4>::SMEM, S2 = (int)ClLayout<2>::SMEM;
@@ -1249,13 +1279,23 @@ cudaError_t launch_combine(const float *o_part, const float *m_part, const float
     if (n_split < 1 || n_split > MAX_SPLITS || D % 4 != 0) return cudaErrorInvalidValue;
     const unsigned rows = (unsigned)(BH * N);
     const int threads = (int)std::min<int64_t>(256, std::max<int64_t>(32, D / 4));
+    // programmatic dependent launch: the merge's blocks may be scheduled while
+    // the attention kernel finishes; they wait for it before reading (pdl_wait_prior)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rows, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
     if (o_fp32)
-        fa_combine_kernel<float><<<rows, threads, 0, stream>>>(o_part, m_part, l_part, d_part, static_cast<float *>(o),
-                                                               lse, (int)BH, (int)N, D, n_split);
-    else
-        fa_combine_kernel<__nv_bfloat16><<<rows, threads, 0, stream>>>(
-            o_part, m_part, l_part, d_part, static_cast<__nv_bfloat16 *>(o), lse, (int)BH, (int)N, D, n_split);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, fa_combine_kernel<float>, o_part, m_part, l_part, d_part, static_cast<float *>(o),
+                                  lse, (int)BH, (int)N, D, n_split);
+    return cudaLaunchKernelEx(&cfg, fa_combine_kernel<__nv_bfloat16>, o_part, m_part, l_part, d_part,
+                              static_cast<__nv_bfloat16 *>(o), lse, (int)BH, (int)N, D, n_split);
 }
 
 cudaError_t wide_error_word_ptr(uint32_t **ptr)

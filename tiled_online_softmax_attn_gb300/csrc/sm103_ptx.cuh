@@ -584,6 +584,13 @@ __device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst, uint32_t src, 
                  : "memory");
 }
 
+// Programmatic dependent launch: the next kernel in the stream may start
+// (its prologue overlapping this kernel's tail); and, in that next kernel,
+// wait until the kernels it depends on have finished and their writes are
+// visible.  Both are no-ops when the launch did not ask for the overlap.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Every thread of every CTA of the cluster arrives, then waits for all.
 __device__ __forceinline__ void cluster_sync_all()
 {
