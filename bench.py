@@ -567,7 +567,9 @@ def bench_backward(args, w, world, rank, local_rank):
     q, k, v, g = (torch.from_numpy(x).to(tdt).to(dev) for x in (q_np, k_np, v_np, g_np))
     o, lse = fa.fa_forward(q, k, v, scale=w.scale, causal=w.causal)
     dq, dk, dv = (torch.empty_like(q) for _ in range(3))
-    ws = torch.empty(fa.load().fa_backward_workspace_size(*w.shape), dtype=torch.uint8, device=dev)
+    ws_bytes = fa.backward_workspace_size(*w.shape, tdt)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    n_launch, path = fa.backward_plan(*w.shape, tdt, w.causal, ws_bytes)
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -595,7 +597,6 @@ def bench_backward(args, w, world, rank, local_rank):
     value = world * flops / (ms * 1e-3) / 1e12
     peaks, peak_kind = load_peaks()
     peak = float(peaks["bf16_tflops"])
-    tc = w.dtype == "bf16" and w.d in (64, 128)
     line = {
         "metric": "attention bwd TFLOP/s (10·B·H·N²·d/time, halved for causal)", "value": value,
         "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -606,9 +607,9 @@ def bench_backward(args, w, world, rank, local_rank):
         "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
                      "frac": value / world / peak, "peak_source": peak_kind,
                      "note": "5 products counted; the kernels form S and dP twice (7 products)"},
-        "gpu_launches": args.steps * 3,  # delta, dK/dV, dQ
+        "gpu_launches": args.steps * n_launch,  # delta, (hi/lo split,) dK/dV, dQ
         "per_step_ms": spread,
-        "kernel": "tensor-core backward" if tc else "general backward",
+        "kernel": path + " backward",
         "clocks": clocks.summary(),
     }
     if rank == 0:

@@ -244,6 +244,35 @@ fa_status fa_backward(const void *q, const void *k, const void *v, const void *o
                       void *stream);
 
 /*
+ * fa_backward_workspace_size_ex -- the workspace fa_backward needs to run this
+ * problem on the tensor cores.  fp32 inputs with d a multiple of 128 (up to
+ * 1024) take the wide-head tensor-core backward, which carries them as bf16
+ * hi + lo pairs (as the wide forward does) and needs room for those copies of
+ * Q, K, V and dO; with only fa_backward_workspace_size bytes they run on the
+ * CUDA cores.  For every other problem it equals fa_backward_workspace_size.
+ * 0 for invalid sizes or dtypes.
+ *
+ * The tensor-core backward covers bf16 inputs with d of 64 or 128, and, for
+ * head dimensions too wide for one tile's gradients to fit tensor memory, bf16
+ * inputs with d a multiple of 128 in 256..1024 and fp32 inputs with d a
+ * multiple of 128 in 128..1024: a CTA owns a slice of the gradient columns
+ * and forms the score products S and dP over the whole head dimension
+ * itself.  Everything else runs on the CUDA cores.  All of them need
+ * scale > 0 and 16-byte aligned pointers for the tensor cores.
+ */
+size_t fa_backward_workspace_size_ex(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype);
+
+/*
+ * fa_backward_plan -- the path fa_backward would take for this problem with
+ * `workspace_bytes` of workspace: returns the number of kernel launches one
+ * call enqueues (-1 for invalid sizes) and writes a short description
+ * ("tensor-core", "wide-head tensor-core ...", "general") into desc (may be
+ * NULL).  Pointer alignment and scale > 0 are assumed.
+ */
+int fa_backward_plan(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int causal, size_t workspace_bytes,
+                     char *desc, size_t desc_len);
+
+/*
  * fa_forward_noalloc -- the wide-head path of fa_forward_ws for callers that
  * cannot allocate device memory.  The pages have no counterpart: it exists
  * for code that must not call cudaMalloc while it runs (a plugin inside a

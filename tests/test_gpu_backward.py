@@ -22,16 +22,24 @@ pytestmark = pytest.mark.gpu
 
 TORCH_DT = {"bf16": torch.bfloat16, "fp32": torch.float32}
 REL = {"bf16": 2e-2, "fp32": 1e-5}
+# fp32 inputs on the tensor cores travel as bf16 hi + lo pairs (16 significant
+# bits of each operand, the lo*lo term dropped: about 2^-16 of each product),
+# for the weights and dS as well: ten such units of the gradient's scale.
+REL_FP32_TC = 1.5e-4
 
 
-def _check(grads, ref, dtype, grad_dtype):
+def _rel(dtype, path):
+    return REL_FP32_TC if dtype == "fp32" and "tensor-core" in path else REL[dtype]
+
+
+def _check(grads, ref, dtype, grad_dtype, path="general"):
     stats = {}
     for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
         if np.size(r) == 0:
             continue
         g = np.asarray(g, dtype=np.float64)
         err = np.abs(g - r)
-        bound = REL[dtype] * np.abs(r).max()
+        bound = _rel(dtype, path) * np.abs(r).max()
         if grad_dtype == "bf16":
             bound = bound + half_ulp_bf16(r)
         stats[name] = (float(err.max()), float(np.abs(r).max()))
@@ -54,9 +62,10 @@ def run_backward(B, H, N, d, dtype, causal, grad_dtype=None, seed=0):
     w = synth.Workload("t", B, H, N, d, dtype, causal, seed=seed)
     q, k, v = w.inputs()
     dout = synth.tensor(3 * seed + 9, w.shape, dtype)
+    path = fa.backward_plan(B, H, N, d, TORCH_DT[dtype], causal)[1]
     grads = _gpu_backward(w, q, k, v, dout, grad_dtype)
     ref = oracle.attention_backward(q, k, v, dout, w.scale, causal)
-    return _check([g.float().cpu().numpy() for g in grads], ref, dtype, grad_dtype or dtype)
+    return _check([g.float().cpu().numpy() for g in grads], ref, dtype, grad_dtype or dtype, path), path
 
 
 SHAPES = [
@@ -75,6 +84,38 @@ SHAPES = [
 @pytest.mark.parametrize("B,H,N,d,dtype", SHAPES)
 def test_backward_matches_oracle(B, H, N, d, dtype, causal):
     run_backward(B, H, N, d, dtype, causal, seed=8000 + N + d)
+
+
+WIDE = [
+    # (B, H, N, d, dtype): heads too wide for one tile's gradients in tensor memory
+    (1, 2, 300, 256, "bf16"),
+    (1, 1, 200, 512, "bf16"),
+    (1, 1, 129, 1024, "bf16"),
+    (1, 2, 150, 128, "fp32"),
+    (1, 1, 257, 256, "fp32"),
+    (2, 1, 64, 384, "fp32"),
+    (1, 1, 130, 1024, "fp32"),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N,d,dtype", WIDE)
+def test_wide_head_backward_on_tensor_cores(B, H, N, d, dtype, causal):
+    """The wide-head tensor-core backward (a CTA per gradient column slice,
+    the score products over the whole head dimension) against the oracle."""
+    stats, path = run_backward(B, H, N, d, dtype, causal, seed=8300 + N + d)
+    assert path.startswith("wide-head tensor-core"), path
+    if dtype == "fp32":
+        print(f"wide fp32 d={d} causal={causal}: " +
+              ", ".join(f"{k} {e / m:.2e}" for k, (e, m) in stats.items()))
+
+
+def test_wide_fp32_backward_without_room_for_copies_runs_on_cuda_cores():
+    B, H, N, d = 1, 1, 100, 256
+    base = fa.load().fa_backward_workspace_size(B, H, N, d)
+    assert fa.backward_workspace_size(B, H, N, d, torch.float32) > base
+    assert fa.backward_plan(B, H, N, d, torch.float32, False, base)[1] == "general"
+    assert fa.backward_plan(B, H, N, d, torch.bfloat16, False, base)[1].startswith("wide-head")
 
 
 def test_backward_fp32_gradients_from_bf16_inputs():

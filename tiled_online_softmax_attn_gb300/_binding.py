@@ -56,6 +56,9 @@ SIGNATURES = {
     "fa_attention": (ctypes.c_int, [ctypes.POINTER(FaParams), _P, ctypes.c_size_t, _P]),
     "fa_attention_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(FaParams)]),
     "fa_backward_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
+    "fa_backward_workspace_size_ex": (ctypes.c_size_t, [_I64, _I64, _I64, _I64, ctypes.c_int]),
+    "fa_backward_plan": (ctypes.c_int, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_size_t,
+                                        ctypes.c_char_p, ctypes.c_size_t]),
     "fa_backward": (ctypes.c_int, [_P] * 9 + [_I64, _I64, _I64, _I64, ctypes.c_float, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "fa_forward_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
@@ -311,8 +314,7 @@ def fa_backward(q, k, v, o, dout, lse, scale=None, causal=False, grad_dtype=None
     dk = torch.empty(q.shape, dtype=gdt, device=q.device) if dk is None else dk
     dv = torch.empty(q.shape, dtype=gdt, device=q.device) if dv is None else dv
     if workspace is None:
-        workspace = torch.empty(load().fa_backward_workspace_size(B, H, N, d), dtype=torch.uint8,
-                                device=q.device)
+        workspace = torch.empty(backward_workspace_size(B, H, N, d, q.dtype), dtype=torch.uint8, device=q.device)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if stream is None:
@@ -325,3 +327,21 @@ def fa_backward(q, k, v, o, dout, lse, scale=None, causal=False, grad_dtype=None
                             workspace.data_ptr(), workspace.numel() * workspace.element_size(), stream)
     check(st)
     return dq, dk, dv
+
+
+def backward_workspace_size(B, H, N, d, in_dtype) -> int:
+    """Workspace bytes that let fa_backward run on the tensor cores where it can
+    (dtype: a torch dtype or an FA_* code)."""
+    ic = in_dtype if isinstance(in_dtype, int) else _dtype_code(in_dtype)
+    return int(load().fa_backward_workspace_size_ex(B, H, N, d, ic))
+
+
+def backward_plan(B, H, N, d, in_dtype, causal=False, workspace_bytes=None):
+    """(kernel launches per call, description) of the path fa_backward takes
+    (workspace_bytes defaults to backward_workspace_size)."""
+    ic = in_dtype if isinstance(in_dtype, int) else _dtype_code(in_dtype)
+    if workspace_bytes is None:
+        workspace_bytes = backward_workspace_size(B, H, N, d, ic)
+    buf = ctypes.create_string_buffer(96)
+    n = load().fa_backward_plan(B, H, N, d, ic, int(bool(causal)), workspace_bytes, buf, len(buf))
+    return int(n), buf.value.decode()

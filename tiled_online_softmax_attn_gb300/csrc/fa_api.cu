@@ -230,22 +230,24 @@ fa_status validate_general(const fa::Problem &p)
 // this host thread, and cleared where set.
 cudaError_t take_error_words(uint32_t *word, cudaStream_t s)
 {
-    thread_local uint32_t *host = nullptr;  // pinned, 3 words, one block per host thread
+    constexpr int NW = 4;
+    thread_local uint32_t *host = nullptr;  // pinned, NW words, one block per host thread
     if (!host) {
-        cudaError_t e = cudaHostAlloc(reinterpret_cast<void **>(&host), 4 * sizeof(uint32_t), cudaHostAllocDefault);
+        cudaError_t e = cudaHostAlloc(reinterpret_cast<void **>(&host), NW * sizeof(uint32_t), cudaHostAllocDefault);
         if (e != cudaSuccess) return e;
     }
-    uint32_t *dev[3] = {nullptr, nullptr, nullptr};
+    uint32_t *dev[NW] = {nullptr, nullptr, nullptr, nullptr};
     cudaError_t e = fa::tc_error_word_ptr(&dev[0]);
     if (e == cudaSuccess) e = fa::wide_error_word_ptr(&dev[1]);
     if (e == cudaSuccess) e = fa::bwd_error_word_ptr(&dev[2]);
-    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+    if (e == cudaSuccess) e = fa::bwdw_error_word_ptr(&dev[3]);
+    for (int i = 0; i < NW && e == cudaSuccess; ++i)
         e = cudaMemcpyAsync(&host[i], dev[i], sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return e;
-    *word = host[0] | host[1] | host[2];
+    *word = host[0] | host[1] | host[2] | host[3];
     if (*word == 0) return cudaSuccess;
-    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+    for (int i = 0; i < NW && e == cudaSuccess; ++i)
         if (host[i]) e = cudaMemsetAsync(dev[i], 0, sizeof(uint32_t), s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     return e;
@@ -432,6 +434,49 @@ size_t fa_backward_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d)
     return fa::backward_workspace_bytes(p);
 }
 
+namespace {
+// A backward problem with aligned placeholder pointers and scale 1, for the
+// size and plan queries (which read no pointer).
+fa::BackwardProblem planning_problem(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int causal)
+{
+    const void *a = reinterpret_cast<const void *>(uintptr_t(256));
+    void *b = reinterpret_cast<void *>(uintptr_t(256));
+    return fa::BackwardProblem{a, a, a, a, a, static_cast<const float *>(a), b, b, b, B, H, N, d, 1.0f,
+                               causal != 0, in_dtype, in_dtype};
+}
+}  // namespace
+
+size_t fa_backward_workspace_size_ex(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype)
+{
+    if (B < 1 || H < 1 || N < 1 || d < 1 || (in_dtype != FA_BF16 && in_dtype != FA_FP32)) return 0;
+    const fa::BackwardProblem p = planning_problem(B, H, N, d, in_dtype, 0);
+    size_t n = fa::backward_workspace_bytes(p);
+    if (!fa::backward_tc_supported(p) && fa::backward_wide_supported(p)) n += fa::backward_wide_copy_bytes(p);
+    return n;
+}
+
+int fa_backward_plan(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int causal, size_t workspace_bytes,
+                     char *desc, size_t desc_len)
+{
+    if (B < 1 || H < 1 || N < 1 || d < 1 || d > 1024 || (in_dtype != FA_BF16 && in_dtype != FA_FP32)) return -1;
+    const fa::BackwardProblem p = planning_problem(B, H, N, d, in_dtype, causal);
+    const size_t base = fa::backward_workspace_bytes(p);
+    int launches;
+    const char *what;
+    if (fa::backward_tc_supported(p)) {
+        launches = 3;
+        what = "tensor-core";
+    } else if (fa::backward_wide_supported(p) && workspace_bytes >= base + fa::backward_wide_copy_bytes(p)) {
+        launches = in_dtype == FA_FP32 ? 4 : 3;
+        what = in_dtype == FA_FP32 ? "wide-head tensor-core fp32 as bf16 hi+lo" : "wide-head tensor-core bf16";
+    } else {
+        launches = 3;
+        what = "general";
+    }
+    if (desc && desc_len) snprintf(desc, desc_len, "%s", what);
+    return launches;
+}
+
 fa_status fa_backward(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
                       void *dq, void *dk, void *dv, int64_t B, int64_t H, int64_t N, int64_t d, float scale,
                       int causal, int in_dtype, int grad_dtype, void *workspace, size_t workspace_bytes, void *stream)
@@ -471,6 +516,14 @@ fa_status fa_backward(const void *q, const void *k, const void *v, const void *o
         cudaError_t e = fa::launch_backward_tc(p, workspace, static_cast<cudaStream_t>(stream), &detail);
         if (e != cudaSuccess)
             return detail ? fail(FA_ERR_CUDA, "tensor-core backward: %s", detail) : cuda_fail(e, "tensor-core backward");
+        return FA_OK;
+    }
+    if (fa::backward_wide_supported(p) && workspace_bytes >= need + fa::backward_wide_copy_bytes(p)) {
+        const char *detail = nullptr;
+        cudaError_t e = fa::launch_backward_wide(p, workspace, static_cast<cudaStream_t>(stream), &detail);
+        if (e != cudaSuccess)
+            return detail ? fail(FA_ERR_CUDA, "wide-head tensor-core backward: %s", detail)
+                          : cuda_fail(e, "wide-head tensor-core backward");
         return FA_OK;
     }
     cudaError_t e = fa::launch_backward_general(p, workspace, static_cast<cudaStream_t>(stream));
@@ -595,8 +648,8 @@ fa_status fa_check_device_error(void *stream)
     uint32_t word = 0;
     cudaError_t e = take_error_words(&word, s);
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize / reading the device error words");
-    if (word & 128u)  // the backward dK/dV kernel's layout check (see fa_backward_tc.cu)
-        return fail(FA_ERR_CUDA, "backward kernel: shared memory allocation not aligned as its layout needs (error word 0x%x)", word);
+    if (word & (128u | 256u))  // the layout checks of the backward dK/dV and wide cluster kernels
+        return fail(FA_ERR_CUDA, "a kernel's shared memory allocation is not aligned as its layout needs (error word 0x%x)", word);
     if (word) return fail(FA_ERR_TIMEOUT, "a device pipeline wait gave up (error word 0x%x)", word);
     return FA_OK;
 }

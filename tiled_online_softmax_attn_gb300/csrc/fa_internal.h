@@ -133,6 +133,18 @@ cudaError_t launch_backward_delta(const BackwardProblem &p, void *workspace, cud
 bool backward_tc_supported(const BackwardProblem &p);
 cudaError_t launch_backward_tc(const BackwardProblem &p, void *workspace, cudaStream_t stream, const char **detail);
 cudaError_t bwd_error_word_ptr(uint32_t **ptr);
+// Wide-head tensor-core backward (fa_backward_wide.cu): d % 128 == 0, d <= 1024,
+// bf16 inputs with d >= 256, fp32 inputs (as bf16 hi + lo) with d >= 128.
+// fp32 inputs need backward_wide_copy_bytes more workspace after the
+// backward_workspace_bytes of the row vectors.
+bool backward_wide_supported(const BackwardProblem &p);
+size_t backward_wide_copy_bytes(const BackwardProblem &p);
+cudaError_t launch_backward_wide(const BackwardProblem &p, void *workspace, cudaStream_t stream, const char **detail);
+cudaError_t bwdw_error_word_ptr(uint32_t **ptr);
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi) for `count` (<= 4) fp32
+// arrays of n elements each (n % 4 == 0, 16-byte aligned), one launch.
+cudaError_t launch_split_hilo(const float *const *x, void *const *hi, void *const *lo, int count, size_t n,
+                              cudaStream_t stream);
 
 // Sets the status and text fa_last_error returns on this host thread.
 void set_last_error(fa_status status, const char *msg);

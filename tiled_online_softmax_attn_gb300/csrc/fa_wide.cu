@@ -476,7 +476,7 @@ static_assert(ClLayout<4>::NEED <= ClLayout<4>::SMEM_MAX && ClLayout<2>::NEED <=
 // so that the 32 lanes of a warp (one row each) touch 512 contiguous bytes.
 __device__ __forceinline__ uint32_t slot_chunk(int row, int c) { return (uint32_t)(c * 512 + row * 16); }
 
-constexpr uint32_t ERR_CL_LAYOUT = 64u;  // the cluster kernel's shared-memory layout did not fit its allocation
+constexpr uint32_t ERR_CL_LAYOUT = 256u;  // the cluster kernel's shared-memory layout did not fit its allocation
 
 template <int NPROD, int R, bool CAUSAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -982,9 +982,9 @@ fa_wide_cluster_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_c
 // float4 groups, four per thread, all four loads issued before any store (the
 // fp32 inputs are read once: streaming loads).
 struct SplitArgs {
-    const float4 *x[3];
-    uint2 *hi[3];
-    uint2 *lo[3];
+    const float4 *x[4];
+    uint2 *hi[4];
+    uint2 *lo[4];
 };
 constexpr int SPLIT_THREADS = 256, SPLIT_UNROLL = 4, SPLIT_PER_BLOCK = SPLIT_THREADS * SPLIT_UNROLL;
 
@@ -1271,6 +1271,22 @@ cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cu
         e = launch_combine(prm.o_part, prm.m_part, prm.l_part, prm.d_part, p.o, p.o_dtype == 1, p.lse, BH, p.N,
                            (int)p.d, w.n_split, stream);
     return e;
+}
+
+cudaError_t launch_split_hilo(const float *const *x, void *const *hi, void *const *lo, int count, size_t n,
+                              cudaStream_t stream)
+{
+    if (count < 1 || count > 4 || n % 4 != 0) return cudaErrorInvalidValue;
+    SplitArgs sa{};
+    for (int t = 0; t < count; ++t) {
+        sa.x[t] = reinterpret_cast<const float4 *>(x[t]);
+        sa.hi[t] = static_cast<uint2 *>(hi[t]);
+        sa.lo[t] = static_cast<uint2 *>(lo[t]);
+    }
+    const size_t n4 = n / 4;
+    const unsigned blocks = (unsigned)((n4 + SPLIT_PER_BLOCK - 1) / SPLIT_PER_BLOCK);
+    fa_split_kernel<<<dim3(blocks, (unsigned)count), SPLIT_THREADS, 0, stream>>>(sa, n4);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const float *o_part, const float *m_part, const float *l_part, const float *d_part, void *o,
