@@ -13,14 +13,18 @@
 // products over the whole head dimension itself, 64 columns at a time through
 // a three-slot ring (as the single-CTA wide forward does):
 //
-//   dK/dV kernel -- 128 keys (one per tensor-memory lane) and a 128-column
+// One launch, two kinds of CTA (the first n_t * d/128 of each head take the
+// dK/dV role, the rest the dQ role: the two are independent, and on problems
+// with few tiles neither fills the GPU alone):
+//
+//   dK/dV role -- 128 keys (one per tensor-memory lane) and a 128-column
 //   slice of dK and dV.  Per query tile i that sees the keys:
 //     S^T = K Q_i^T, dP^T = V dO_i^T              -> [0, 128), [128, 256)
 //     P^T, dS^T by the elementwise warps, as bf16 (hi, lo) over their own
 //       columns of S^T and dP^T
 //     dV[:, slice] += P^T dO_i[:, slice]          -> [256, 384)
 //     dK[:, slice] += dS^T Q_i[:, slice]          -> [384, 512)
-//   dQ kernel -- 128 queries and a 256- (or 128-) column slice of dQ.  Per
+//   dQ role -- 128 queries and a 256- (or 128-) column slice of dQ.  Per
 //   key tile j the query tile sees:
 //     S = Q K_j^T, dP = dO V_j^T                  -> [0, 128), [128, 256)
 //     dS as bf16 (hi, lo) over the S columns
@@ -71,7 +75,8 @@ constexpr uint32_t ERR_WAIT = 1u, ERR_DRAIN = 2u;
 
 struct WbParams {
     int N, BH, D, n_t;     // n_t: 128-row tiles along the sequence
-    int n_sl;              // output slices per tile
+    int n_sl_kv;           // dK/dV slices per key tile (d / 128)
+    int n_sl_q;            // dQ slices per query tile (d / dsq)
     int dsq;               // dQ slice width (256 or 128)
     float sl, scale;       // scale * log2 e, scale
     const float *lse2, *delta;  // [BH][pitch]: LSE * log2 e and delta per row
@@ -119,12 +124,6 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t 
     lo = pack_bf16x2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
 }
 
-// The ring of 64 KB stages shared by both kernels' producer and MMA warps.
-struct Ring {
-    uint64_t *full, *empty;
-    int it = 0;
-};
-
 // ---------------------------------------------------------------- dK / dV
 //
 // Stage order per query tile (the order the MMA warp consumes): D/64 stages
@@ -133,11 +132,10 @@ struct Ring {
 // B_hi, B_lo] boxes (A the 128-key operand), a slice stage [hi atom 0, hi
 // atom 1, lo atom 0, lo atom 1] of the 128 slice columns.
 template <int NPROD, bool CAUSAL>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-fa_bwdw_dkdv(const __grid_constant__ CUtensorMap tm_qh, const __grid_constant__ CUtensorMap tm_ql,
-             const __grid_constant__ CUtensorMap tm_kh, const __grid_constant__ CUtensorMap tm_kl,
-             const __grid_constant__ CUtensorMap tm_vh, const __grid_constant__ CUtensorMap tm_vl,
-             const __grid_constant__ CUtensorMap tm_gh, const __grid_constant__ CUtensorMap tm_gl, const WbParams prm)
+__device__ __forceinline__ void dkdv_role(const CUtensorMap &tm_qh, const CUtensorMap &tm_ql, const CUtensorMap &tm_kh,
+                                          const CUtensorMap &tm_kl, const CUtensorMap &tm_vh, const CUtensorMap &tm_vl,
+                                          const CUtensorMap &tm_gh, const CUtensorMap &tm_gl, const WbParams &prm,
+                                          int cta)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_b[STAGES], empty_b[STAGES], st_full, dpt_full, p_ready, ds_ready, tm_free,
@@ -147,7 +145,7 @@ fa_bwdw_dkdv(const __grid_constant__ CUtensorMap tm_qh, const __grid_constant__ 
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = prm.N, D = prm.D;
-    const int kt = (int)(blockIdx.x / prm.n_sl), sl = (int)(blockIdx.x % prm.n_sl);
+    const int kt = cta / prm.n_sl_kv, sl = cta % prm.n_sl_kv;  // longest first when causal
     const int bh = (int)blockIdx.y;
     const int k0 = kt * BM, c0 = sl * DS_KV;
     const int first = CAUSAL ? kt : 0;          // query tiles before the key tile see none of its keys
@@ -445,11 +443,9 @@ fa_bwdw_dkdv(const __grid_constant__ CUtensorMap tm_qh, const __grid_constant__ 
 // (dO, V) for dP, then the K slice: DSQ / 64 atoms of hi in one stage and of
 // lo in the next (fp32 inputs).
 template <int NPROD, int DSQ, bool CAUSAL>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-fa_bwdw_dq(const __grid_constant__ CUtensorMap tm_qh, const __grid_constant__ CUtensorMap tm_ql,
-           const __grid_constant__ CUtensorMap tm_kh, const __grid_constant__ CUtensorMap tm_kl,
-           const __grid_constant__ CUtensorMap tm_vh, const __grid_constant__ CUtensorMap tm_vl,
-           const __grid_constant__ CUtensorMap tm_gh, const __grid_constant__ CUtensorMap tm_gl, const WbParams prm)
+__device__ __forceinline__ void dq_role(const CUtensorMap &tm_qh, const CUtensorMap &tm_ql, const CUtensorMap &tm_kh,
+                                        const CUtensorMap &tm_kl, const CUtensorMap &tm_vh, const CUtensorMap &tm_vl,
+                                        const CUtensorMap &tm_gh, const CUtensorMap &tm_gl, const WbParams &prm, int cta)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_b[STAGES], empty_b[STAGES], s_full, dp_full, ds_ready, tm_free, o_full, drain;
@@ -458,7 +454,8 @@ fa_bwdw_dq(const __grid_constant__ CUtensorMap tm_qh, const __grid_constant__ CU
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = prm.N, D = prm.D;
-    const int qt = (int)(blockIdx.x / prm.n_sl), sl = (int)(blockIdx.x % prm.n_sl);
+    const int qi = cta / prm.n_sl_q, sl = cta % prm.n_sl_q;
+    const int qt = CAUSAL ? prm.n_t - 1 - qi : qi;  // longest first when causal
     const int bh = (int)blockIdx.y;
     const int q0 = qt * BM, c0 = sl * DSQ;
     const int n_steps = CAUSAL ? qt + 1 : prm.n_t;  // key tiles this query tile sees
@@ -707,6 +704,23 @@ fa_bwdw_dq(const __grid_constant__ CUtensorMap tm_qh, const __grid_constant__ CU
     }
 }
 
+// One launch for both: the first n_t * n_sl_kv CTAs (of each head) take the
+// dK/dV role, the rest the dQ role.  The two are independent, and on problems
+// with few tiles neither fills the GPU alone.
+template <int NPROD, int DSQ, bool CAUSAL>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+fa_bwdw_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_constant__ CUtensorMap tm_ql,
+               const __grid_constant__ CUtensorMap tm_kh, const __grid_constant__ CUtensorMap tm_kl,
+               const __grid_constant__ CUtensorMap tm_vh, const __grid_constant__ CUtensorMap tm_vl,
+               const __grid_constant__ CUtensorMap tm_gh, const __grid_constant__ CUtensorMap tm_gl, const WbParams prm)
+{
+    const int n_kv = prm.n_t * prm.n_sl_kv;
+    if ((int)blockIdx.x < n_kv)
+        dkdv_role<NPROD, CAUSAL>(tm_qh, tm_ql, tm_kh, tm_kl, tm_vh, tm_vl, tm_gh, tm_gl, prm, (int)blockIdx.x);
+    else
+        dq_role<NPROD, DSQ, CAUSAL>(tm_qh, tm_ql, tm_kh, tm_kl, tm_vh, tm_vl, tm_gh, tm_gl, prm, (int)blockIdx.x - n_kv);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -799,31 +813,25 @@ cudaError_t launch_backward_wide(const BackwardProblem &p, void *workspace, cuda
     prm.dv = p.dv;
     prm.g_fp32 = p.grad_dtype == 1;
     prm.wait_limit_ns = 2000000000ull;
-    // maps: Q, K, V, dO (hi, lo each) as the kernels take them
-    auto go = [&](auto kern, unsigned gx) -> cudaError_t {
+    // maps: Q, K, V, dO (hi, lo each) as the kernel takes them
+    const bool wide_q = p.d % 256 == 0;
+    prm.dsq = wide_q ? 256 : 128;
+    prm.n_sl_kv = (int)(p.d / DS_KV);
+    prm.n_sl_q = (int)(p.d / prm.dsq);
+    const unsigned gx = (unsigned)(prm.n_t * (prm.n_sl_kv + prm.n_sl_q));
+    auto go = [&](auto kern) -> cudaError_t {
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (err != cudaSuccess) return err;
         kern<<<dim3(gx, (unsigned)BH), NUM_THREADS, SMEM_BYTES, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7],
                                                                           prm);
         return cudaGetLastError();
     };
-    prm.n_sl = (int)(p.d / DS_KV);
-    const unsigned gkv = (unsigned)(prm.n_t * prm.n_sl);
-    if (nprod == 3) e = p.causal ? go(fa_bwdw_dkdv<3, true>, gkv) : go(fa_bwdw_dkdv<3, false>, gkv);
-    else e = p.causal ? go(fa_bwdw_dkdv<1, true>, gkv) : go(fa_bwdw_dkdv<1, false>, gkv);
-    if (e != cudaSuccess) return e;
-    const bool wide_q = p.d % 256 == 0;
-    prm.dsq = wide_q ? 256 : 128;
-    prm.n_sl = (int)(p.d / prm.dsq);
-    const unsigned gq = (unsigned)(prm.n_t * prm.n_sl);
     if (nprod == 3) {
-        if (wide_q) e = p.causal ? go(fa_bwdw_dq<3, 256, true>, gq) : go(fa_bwdw_dq<3, 256, false>, gq);
-        else e = p.causal ? go(fa_bwdw_dq<3, 128, true>, gq) : go(fa_bwdw_dq<3, 128, false>, gq);
-    } else {
-        if (wide_q) e = p.causal ? go(fa_bwdw_dq<1, 256, true>, gq) : go(fa_bwdw_dq<1, 256, false>, gq);
-        else e = p.causal ? go(fa_bwdw_dq<1, 128, true>, gq) : go(fa_bwdw_dq<1, 128, false>, gq);
+        if (wide_q) return p.causal ? go(fa_bwdw_kernel<3, 256, true>) : go(fa_bwdw_kernel<3, 256, false>);
+        return p.causal ? go(fa_bwdw_kernel<3, 128, true>) : go(fa_bwdw_kernel<3, 128, false>);
     }
-    return e;
+    if (wide_q) return p.causal ? go(fa_bwdw_kernel<1, 256, true>) : go(fa_bwdw_kernel<1, 256, false>);
+    return p.causal ? go(fa_bwdw_kernel<1, 128, true>) : go(fa_bwdw_kernel<1, 128, false>);
 }
 
 cudaError_t bwdw_error_word_ptr(uint32_t **ptr)

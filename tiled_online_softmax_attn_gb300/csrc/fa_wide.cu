@@ -1218,6 +1218,7 @@ cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cu
     dim3 grid((unsigned)(w.n_q * w.n_dv * w.n_split), (unsigned)BH);
     if (w.cluster > 1) {
         // grid.x = (query tile, split) clusters of R CTAs, one O slice each
+        bool no_room = false;  // set when the GPU cannot hold even one cluster of this size
         auto go_cl = [&](auto kern, int smem) -> cudaError_t {
             cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (err != cudaSuccess) return err;
@@ -1237,6 +1238,23 @@ cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cu
             at[1].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = at;
             cfg.numAttrs = w.nprod == 3 ? 2 : 1;
+            // a GPU partition may have too few SMs per cluster slot: asked once per
+            // device and cluster size
+            static int fits[64][5];  // 0 unknown, 1 fits, 2 does not
+            int dev = 0;
+            if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+            int &f = fits[dev & 63][w.cluster];
+            if (f == 0) {
+                int n = 0;
+                cudaLaunchConfig_t one = cfg;
+                one.numAttrs = 1;
+                f = (cudaOccupancyMaxActiveClusters(&n, kern, &one) == cudaSuccess && n > 0) ? 1 : 2;
+                (void)cudaGetLastError();
+            }
+            if (f == 2) {
+                no_room = true;
+                return cudaSuccess;
+            }
             return cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], m[3], m[4], m[5], prm);
         };
         constexpr int S4 = (int)ClLayout<4>::SMEM, S2 = (int)ClLayout<2>::SMEM;
@@ -1247,11 +1265,16 @@ cudaError_t launch_wide(const Problem &p, const WidePlan &w, void *workspace, cu
             if (w.cluster == 4) e = p.causal ? go_cl(fa_wide_cluster_kernel<1, 4, true>, S4) : go_cl(fa_wide_cluster_kernel<1, 4, false>, S4);
             else e = p.causal ? go_cl(fa_wide_cluster_kernel<1, 2, true>, S2) : go_cl(fa_wide_cluster_kernel<1, 2, false>, S2);
         }
-        if (e != cudaSuccess) return e;
-        if (!prm.direct)
-            e = launch_combine(prm.o_part, prm.m_part, prm.l_part, prm.d_part, p.o, p.o_dtype == 1, p.lse, BH, p.N,
-                               (int)p.d, w.n_split, stream);
-        return e;
+        if (no_room) {
+            // no room for a cluster of this size: the single-CTA kernel below
+            // computes the same result
+        } else {
+            if (e != cudaSuccess) return e;
+            if (!prm.direct)
+                e = launch_combine(prm.o_part, prm.m_part, prm.l_part, prm.d_part, p.o, p.o_dtype == 1, p.lse, BH, p.N,
+                                   (int)p.d, w.n_split, stream);
+            return e;
+        }
     }
     auto go = [&](auto kern) -> cudaError_t {
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
