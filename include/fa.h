@@ -87,9 +87,11 @@ typedef enum fa_dtype {
  *   stream    cudaStream_t to enqueue on.
  *
  * Pointers must be aligned to their element size.  The tensor-core kernel is
- * used when in_dtype = FA_BF16, d is 64 or 128, scale > 0 and q, k, v, o are
- * 16-byte aligned; bf16 inputs with d a multiple of 128 in 256..1024 take the
- * wide-head tensor-core path; everything else the general-d kernel.  Outputs are undefined if the
+ * used when in_dtype = FA_BF16, d is a multiple of 8 up to 128 (64 and 128
+ * natively, other widths padded inside the kernel to 64 or 128 with zero
+ * columns), scale > 0 and q, k, v, o are 16-byte aligned; bf16 inputs with d a
+ * multiple of 128 in 256..1024 take the wide-head tensor-core path; everything
+ * else the general-d kernel.  Outputs are undefined if the
  * call does not return FA_OK.  O must not overlap Q, K, V or LSE.
  */
 fa_status fa_forward(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -190,9 +192,9 @@ fa_status fa_forward_host(const void *q_h, const void *k_h, const void *v_h, voi
  *   causal masks key j > query i (the same rule as for Nq = Nk).
  *   workspace as for fa_forward_ws (may be NULL).
  *
- * The 64/128 tensor-core kernel covers bf16 inputs with dk and dv each 64
- * or 128, scale > 0, 16-byte aligned pointers and every stride a non-zero
- * multiple of 16 bytes; the wide-head path covers the contiguous Nq = Nk,
+ * The tensor-core kernel covers bf16 inputs with dk and dv each a multiple
+ * of 8 up to 128, scale > 0, 16-byte aligned pointers and every stride a
+ * non-zero multiple of 16 bytes; the wide-head path covers the contiguous Nq = Nk,
  * dk = dv layouts of fa_forward_ws; the general-d kernel covers the rest
  * (dk, dv <= 1024, any strides).
  */

@@ -59,7 +59,9 @@ CROSS = [
     (1, 2, 129, 257, 128, 64, "bf16"),
     (1, 1, 1, 500, 128, 128, "bf16"),
     (1, 1, 500, 1, 64, 64, "bf16"),
-    (1, 2, 100, 333, 40, 72, "bf16"),
+    (1, 2, 100, 333, 40, 72, "bf16"),     # padded to 64 / 128 on the tensor cores
+    (2, 2, 190, 260, 96, 40, "bf16"),
+    (1, 1, 77, 300, 120, 8, "bf16"),
     (2, 1, 150, 90, 96, 200, "fp32"),
 ]
 

@@ -77,6 +77,18 @@ def test_general_head_dims(d, dtype, causal):
     full_check(w, "general")
 
 
+@pytest.mark.parametrize("d", [8, 16, 24, 40, 56, 72, 80, 96, 112, 120])
+@pytest.mark.parametrize("causal", [False, True])
+def test_narrow_head_dims_on_tensor_cores(d, causal):
+    """Head dimensions below 128 that are multiples of 8 run on the tensor-core
+    kernel padded to 64 or 128: the tensor maps keep the real width, so the
+    missing columns load as zeros (no effect on S) and O's padding columns are
+    not stored."""
+    w = synth.Workload("t", 1, 3, 200, d, "bf16", causal, seed=2500 + d)
+    assert fa.plan(w.B, w.H, w.N, d, torch.bfloat16, torch.bfloat16, causal)[1] == f"tensor-core d={d}"
+    full_check(w, "auto")
+
+
 @pytest.mark.parametrize("path", ["auto", "general"])
 @pytest.mark.parametrize("o_dtype", ["bf16", "fp32"])
 def test_tiny_workload(path, o_dtype):

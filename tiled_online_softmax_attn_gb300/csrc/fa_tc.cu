@@ -138,6 +138,7 @@ struct Params {
     int qperm, kperm, vperm;   // which of (sequence, head, batch) each outer map dimension holds
     float *lse;
     int o_fp32;
+    int dv_real;       // O columns stored (<= DV: narrower heads are padded with zeros)
     // key-range split (n_split > 1): each item covers key tiles [kv_per sp, kv_per (sp + 1))
     // and writes unnormalised partials instead of O and LSE
     int n_split, kv_per;
@@ -225,6 +226,8 @@ __device__ __forceinline__ void raise_error(uint32_t bit, volatile int *abort_fl
     *abort_flag = 1;
 }
 
+// Columns col0 .. col0 + ncols - 1 of an O row (ncols <= 32, a multiple of 8:
+// a head dimension padded up to the kernel's stores only its own columns).
 __device__ __forceinline__ void store_o_row(void *o, int o_fp32, size_t row_elem, const float *vals,
                                             int col0, int ncols)
 {
@@ -238,6 +241,7 @@ __device__ __forceinline__ void store_o_row(void *o, int o_fp32, size_t row_elem
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o) + row_elem + col0);
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
+            if (8 * x >= ncols) break;
             uint4 w;
             w.x = pack_bf16x2(vals[8 * x + 0], vals[8 * x + 1]);
             w.y = pack_bf16x2(vals[8 * x + 2], vals[8 * x + 3]);
@@ -746,7 +750,8 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     float vals[32];
 #pragma unroll
                     for (int x = 0; x < 32; ++x) vals[x] = __uint_as_float(ov[c * 32 + x]) * inv_l;
-                    if (grow < N) store_o_row(prm.o, prm.o_fp32, row_elem, vals, c * 32, 32);
+                    const int nc = min(32, prm.dv_real - c * 32);
+                    if (grow < N && nc > 0) store_o_row(prm.o, prm.o_fp32, row_elem, vals, c * 32, nc);
                 }
             } else {  // the only item of the CTA: no one waits for O
 #pragma unroll
@@ -756,7 +761,8 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     float vals[32];
 #pragma unroll
                     for (int x = 0; x < 32; ++x) vals[x] = __uint_as_float(raw[x]) * inv_l;
-                    if (grow < N) store_o_row(prm.o, prm.o_fp32, row_elem, vals, c * 32, 32);
+                    const int nc = min(32, prm.dv_real - c * 32);
+                    if (grow < N && nc > 0) store_o_row(prm.o, prm.o_fp32, row_elem, vals, c * 32, nc);
                 }
             }
             if (prm.lse && grow < N) prm.lse[(size_t)wi.bh * N + grow] = (m + log2f(l)) * 0.69314718055994530942f;
@@ -857,8 +863,10 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     strides_of(p, 2, sv);
     strides_of(p, 3, so);
     Params prm;
-    if (!make_map(&mq, p.q, DK, p.N, p.H, p.B, sq, &prm.qperm) || !make_map(&mk, p.k, DK, Nk, p.H, p.B, sk, &prm.kperm) ||
-        !make_map(&mv, p.v, DV, Nk, p.H, p.B, sv, &prm.vperm)) {
+    // maps of the real widths: the columns a padded head lacks read as zeros,
+    // which add nothing to S and leave O's padding columns (never stored) at zero
+    if (!make_map(&mq, p.q, p.d, p.N, p.H, p.B, sq, &prm.qperm) || !make_map(&mk, p.k, p.d, Nk, p.H, p.B, sk, &prm.kperm) ||
+        !make_map(&mv, p.v, dv_of(p), Nk, p.H, p.B, sv, &prm.vperm)) {
         *detail = "cuTensorMapEncodeTiled failed or is unavailable";
         return cudaErrorInvalidValue;
     }
@@ -890,6 +898,7 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     prm.os_n = so[2];
     prm.lse = p.lse;
     prm.o_fp32 = p.o_dtype == 1;
+    prm.dv_real = (int)dv_of(p);
     prm.n_split = 1;
     prm.kv_per = prm.n_kv;
     prm.o_part = prm.m_part = prm.l_part = prm.d_part = nullptr;
@@ -939,10 +948,15 @@ cudaError_t launch_dims(const Problem &p, cudaStream_t stream, uint32_t flags, c
 
 }  // namespace
 
+// Head widths the kernel covers: 64 and 128, and any narrower multiple of 8
+// (16-byte rows for TMA), padded up to 64 or 128 with zero columns.
+inline bool tc_width(int64_t w) { return w >= 8 && w <= 128 && w % 8 == 0; }
+inline int tc_padded(int64_t w) { return w <= 64 ? 64 : 128; }
+
 bool tc_supported(const Problem &p)
 {
     const int64_t dv = dv_of(p);
-    if (p.in_dtype != 0 || !(p.d == 64 || p.d == 128) || !(dv == 64 || dv == 128) || !(p.scale > 0.f)) return false;
+    if (p.in_dtype != 0 || !tc_width(p.d) || !tc_width(dv) || !(p.scale > 0.f)) return false;
     auto al16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
     if (!(al16(p.q) && al16(p.k) && al16(p.v) && al16(p.o))) return false;
     // TMA: every stride a non-zero multiple of 16 bytes; O rows start 16-byte aligned
@@ -959,9 +973,9 @@ bool tc_supported(const Problem &p)
 
 cudaError_t launch_tc(const Problem &p, cudaStream_t stream, uint32_t flags, const char **detail)
 {
-    const int64_t dv = dv_of(p);
-    if (p.d == 128) return dv == 128 ? launch_dims<128, 128>(p, stream, flags, detail)
-                                     : launch_dims<128, 64>(p, stream, flags, detail);
+    const int dk = tc_padded(p.d), dv = tc_padded(dv_of(p));
+    if (dk == 128) return dv == 128 ? launch_dims<128, 128>(p, stream, flags, detail)
+                                    : launch_dims<128, 64>(p, stream, flags, detail);
     return dv == 128 ? launch_dims<64, 128>(p, stream, flags, detail) : launch_dims<64, 64>(p, stream, flags, detail);
 }
 
@@ -973,6 +987,7 @@ TcSplit tc_split_plan(const Problem &p)
     TcSplit sp{1, 0, 0};
     if (p.causal || !tc_supported(p)) return sp;
     const int64_t dv = dv_of(p);
+    if (tc_padded(p.d) != p.d || tc_padded(dv) != dv) return sp;  // the merge writes whole 64/128-column rows
     int64_t os[3];
     strides_of(p, 3, os);
     if (os[2] != dv || os[1] != p.N * dv || os[0] != p.H * p.N * dv) return sp;  // combine writes contiguous O
@@ -995,7 +1010,7 @@ TcSplit tc_split_plan(const Problem &p)
 
 cudaError_t launch_tc_split(const Problem &p, const TcSplit &sp, void *workspace, cudaStream_t stream, const char **detail)
 {
-    const int64_t dv = dv_of(p);
+    const int64_t dv = dv_of(p);  // not padded: tc_split_plan splits only 64 and 128
     if (p.d == 128) return dv == 128 ? launch_dims<128, 128>(p, stream, 0, detail, &sp, workspace)
                                      : launch_dims<128, 64>(p, stream, 0, detail, &sp, workspace);
     return dv == 128 ? launch_dims<64, 128>(p, stream, 0, detail, &sp, workspace)
