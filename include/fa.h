@@ -254,7 +254,9 @@ fa_status fa_backward(const void *q, const void *k, const void *v, const void *o
  * CUDA cores.  For every other problem it equals fa_backward_workspace_size.
  * 0 for invalid sizes or dtypes.
  *
- * The tensor-core backward covers bf16 inputs with d of 64 or 128, and, for
+ * The tensor-core backward covers bf16 inputs with d a multiple of 8 up to
+ * 128 (64 and 128 natively; a narrower head is padded with zero columns up to
+ * the next of them, and only its own columns are written), and, for
  * head dimensions too wide for one tile's gradients to fit tensor memory, bf16
  * inputs with d a multiple of 128 in 256..1024 and fp32 inputs with d a
  * multiple of 128 in 128..1024: a CTA owns a slice of the gradient columns

@@ -141,3 +141,16 @@ def test_noalloc_checks_arguments_like_the_workspace_entry_point(lib, lse, o, ex
     assert lib.fa_forward_noalloc(*args, None) == expect
     assert text in fa.last_error()
     assert lib.fa_forward_ws(*args, None, 0, None) == expect
+
+
+@pytest.mark.parametrize("d,dtype,path", [
+    (64, fa.FA_BF16, "tensor-core"), (128, fa.FA_BF16, "tensor-core"), (8, fa.FA_BF16, "tensor-core"),
+    (40, fa.FA_BF16, "tensor-core"), (120, fa.FA_BF16, "tensor-core"), (44, fa.FA_BF16, "general"),
+    (136, fa.FA_BF16, "general"), (40, fa.FA_FP32, "general"), (256, fa.FA_BF16, "wide-head tensor-core bf16"),
+    (128, fa.FA_FP32, "wide-head tensor-core fp32 as bf16 hi+lo")])
+def test_backward_plan_picks_the_path_by_head_width(lib, d, dtype, path):
+    """Host-side choice of the backward kernel: bf16 heads of a multiple of 8
+    up to 128 on the tensor cores (padded below 64 and between 64 and 128),
+    wider ones on the wide-head kernel, the rest on the CUDA cores."""
+    n, desc = fa.backward_plan(1, 2, 300, d, dtype, True)
+    assert desc == path and n >= 3

@@ -110,6 +110,37 @@ def test_wide_head_backward_on_tensor_cores(B, H, N, d, dtype, causal):
               ", ".join(f"{k} {e / m:.2e}" for k, (e, m) in stats.items()))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,d", [(300, 8), (200, 40), (257, 80), (130, 96), (513, 120)])
+def test_narrow_head_backward_on_tensor_cores(N, d, causal):
+    """bf16 heads narrower than 64 or between 64 and 128 (multiples of 8):
+    the tensor-core backward loads them padded with zero columns and writes
+    only their own columns of dQ, dK and dV."""
+    stats, path = run_backward(1, 2, N, d, "bf16", causal, seed=8400 + N + d)
+    assert path == "tensor-core", path
+
+
+def test_narrow_head_backward_leaves_neighbouring_memory_alone():
+    """dQ, dK and dV of a d = 40 head sit inside sentinel-filled buffers; the
+    padded columns the kernel computes must not reach memory."""
+    B, H, N, d = 1, 2, 300, 40
+    w = synth.Workload("t", B, H, N, d, "bf16", True, seed=8450)
+    q, k, v = w.inputs()
+    dout = synth.tensor(3 * 8450 + 9, w.shape, "bf16")
+    qt, kt, vt, gt = (torch.from_numpy(x).to(torch.bfloat16).cuda() for x in (q, k, v, dout))
+    o, lse = fa.fa_forward(qt, kt, vt, scale=w.scale, causal=True)
+    n, guard = B * H * N * d, 256
+    bufs = [torch.full((n + 2 * guard,), 0x5A5A, dtype=torch.int16, device="cuda") for _ in range(3)]
+    grads = [b[guard:guard + n].view(torch.bfloat16).view(w.shape) for b in bufs]
+    fa.fa_backward(qt, kt, vt, o, gt, lse, scale=w.scale, causal=True, dq=grads[0], dk=grads[1], dv=grads[2])
+    torch.cuda.synchronize()
+    for b in bufs:
+        h = b.cpu()
+        assert bool((h[:guard] == 0x5A5A).all()) and bool((h[guard + n:] == 0x5A5A).all())
+    ref = oracle.attention_backward(q, k, v, dout, w.scale, True)
+    _check([g.float().cpu().numpy() for g in grads], ref, "bf16", "bf16", "tensor-core")
+
+
 def test_wide_fp32_backward_without_room_for_copies_runs_on_cuda_cores():
     B, H, N, d = 1, 1, 100, 256
     base = fa.load().fa_backward_workspace_size(B, H, N, d)

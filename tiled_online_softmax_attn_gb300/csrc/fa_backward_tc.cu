@@ -116,6 +116,7 @@ struct BCfg {
 
 struct BwdParams {
     int N, BH, n_q, pitch;
+    int dreal;   // head width of the tensors (<= D: narrower heads are padded with zeros)
     float sl, scale;
     uint64_t limit;
     const float *lse2, *delta;  // [BH][pitch]
@@ -124,19 +125,22 @@ struct BwdParams {
     int hgroup;  // causal dQ order: heads per group (see fa_bwd_dq_tc)
 };
 
-__device__ __forceinline__ void store_row32(void *base, int fp32, size_t elem, const uint32_t (&raw)[32], float mul)
+// Columns 0 .. ncols - 1 of a 32-column chunk (ncols a multiple of 8, <= 32),
+// times `mul`.
+__device__ __forceinline__ void store_row32(void *base, int fp32, size_t elem, const uint32_t (&raw)[32], float mul,
+                                            int ncols = 32)
 {
     if (fp32) {
         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(base) + elem);
 #pragma unroll
         for (int x = 0; x < 8; ++x)
-            dst[x] = make_float4(__uint_as_float(raw[4 * x]) * mul, __uint_as_float(raw[4 * x + 1]) * mul,
+            if (4 * x < ncols) dst[x] = make_float4(__uint_as_float(raw[4 * x]) * mul, __uint_as_float(raw[4 * x + 1]) * mul,
                                  __uint_as_float(raw[4 * x + 2]) * mul, __uint_as_float(raw[4 * x + 3]) * mul);
     } else {
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(base) + elem);
 #pragma unroll
         for (int x = 0; x < 4; ++x)
-            dst[x] = make_uint4(pack_bf16x2(__uint_as_float(raw[8 * x]) * mul, __uint_as_float(raw[8 * x + 1]) * mul),
+            if (8 * x < ncols) dst[x] = make_uint4(pack_bf16x2(__uint_as_float(raw[8 * x]) * mul, __uint_as_float(raw[8 * x + 1]) * mul),
                                 pack_bf16x2(__uint_as_float(raw[8 * x + 2]) * mul, __uint_as_float(raw[8 * x + 3]) * mul),
                                 pack_bf16x2(__uint_as_float(raw[8 * x + 4]) * mul, __uint_as_float(raw[8 * x + 5]) * mul),
                                 pack_bf16x2(__uint_as_float(raw[8 * x + 6]) * mul, __uint_as_float(raw[8 * x + 7]) * mul));
@@ -517,14 +521,15 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         if (ok && wait_or_abort(smem_addr(&o_full), 0, limit, &abort_flag)) {
             tc_fence_after();
-            const size_t row = ((size_t)bh * N + kj) * D;
+            const size_t row = ((size_t)bh * N + kj) * prm.dreal;
 #pragma unroll 1
             for (int c = hf; c < D / 32; c += E::NH) {  // this warp's 32-column chunks
                 uint32_t raw[32];
+                const int nc = min(32, prm.dreal - c * 32);  // a padded head stores its own columns only
                 tmem_ld32(lb + cV + c * 32, raw);
-                if (kj < N) store_row32(prm.dv, prm.g_fp32, row + c * 32, raw, 1.f);
+                if (kj < N && nc > 0) store_row32(prm.dv, prm.g_fp32, row + c * 32, raw, 1.f, nc);
                 tmem_ld32(lb + cK + c * 32, raw);
-                if (kj < N) store_row32(prm.dk, prm.g_fp32, row + c * 32, raw, prm.scale);
+                if (kj < N && nc > 0) store_row32(prm.dk, prm.g_fp32, row + c * 32, raw, prm.scale, nc);
             }
         } else if (!abort_flag) {
             fail_bwd(&abort_flag);
@@ -823,12 +828,13 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         if (ok && wait_or_abort(smem_addr(&o_full), 0, limit, &abort_flag)) {
             tc_fence_after();
-            const size_t row = ((size_t)bh * N + qi) * D;
+            const size_t row = ((size_t)bh * N + qi) * prm.dreal;
 #pragma unroll 1
             for (int c = hf; c < D / 32; c += E::NH) {  // this warp's 32-column chunks
                 uint32_t raw[32];
+                const int nc = min(32, prm.dreal - c * 32);
                 tmem_ld32(lb + cQ + c * 32, raw);
-                if (qi < N) store_row32(prm.dq, prm.g_fp32, row + c * 32, raw, prm.scale);
+                if (qi < N && nc > 0) store_row32(prm.dq, prm.g_fp32, row + c * 32, raw, prm.scale, nc);
             }
         } else if (!abort_flag) {
             fail_bwd(&abort_flag);
@@ -877,8 +883,9 @@ cudaError_t launch_dims(const BackwardProblem &p, float *delta, float *lse2, int
     using C = BCfg<D>;
     const int64_t BH = p.B * p.H;
     CUtensorMap mq, mk, mv, mg;
-    if (!make_map(&mq, p.q, BH, p.N, D) || !make_map(&mk, p.k, BH, p.N, D) || !make_map(&mv, p.v, BH, p.N, D) ||
-        !make_map(&mg, p.dout, BH, p.N, D)) {
+    // maps of the real width: a padded head's missing columns load as zeros
+    if (!make_map(&mq, p.q, BH, p.N, p.d) || !make_map(&mk, p.k, BH, p.N, p.d) || !make_map(&mv, p.v, BH, p.N, p.d) ||
+        !make_map(&mg, p.dout, BH, p.N, p.d)) {
         *detail = "cuTensorMapEncodeTiled failed or is unavailable";
         return cudaErrorInvalidValue;
     }
@@ -890,11 +897,12 @@ cudaError_t launch_dims(const BackwardProblem &p, float *delta, float *lse2, int
         int dev = 0, l2 = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
             l2 = 0;
-        const int64_t kv_head = p.N * (int64_t)D * 4;
+        const int64_t kv_head = p.N * p.d * 4;
         const int64_t g = l2 > 0 ? (int64_t)l2 / 2 / std::max<int64_t>(kv_head, 1) : BH;
         prm.hgroup = (int)std::max<int64_t>(1, std::min<int64_t>(g, BH));
     }
     prm.pitch = pitch;
+    prm.dreal = (int)p.d;
     prm.sl = p.scale * 1.4426950408889634f;
     prm.scale = p.scale;
     prm.limit = 2000000000ull;
@@ -918,9 +926,10 @@ cudaError_t launch_dims(const BackwardProblem &p, float *delta, float *lse2, int
 
 }  // namespace
 
+// bf16 heads of width 64 or 128, and narrower multiples of 8 padded up to them.
 bool backward_tc_supported(const BackwardProblem &p)
 {
-    if (p.in_dtype != 0 || !(p.d == 64 || p.d == 128) || !(p.scale > 0.f)) return false;
+    if (p.in_dtype != 0 || p.d < 8 || p.d > 128 || p.d % 8 != 0 || !(p.scale > 0.f)) return false;
     auto al16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
     return al16(p.q) && al16(p.k) && al16(p.v) && al16(p.dout) && al16(p.dq) && al16(p.dk) && al16(p.dv);
 }
@@ -931,7 +940,7 @@ cudaError_t launch_backward_tc(const BackwardProblem &p, void *workspace, cudaSt
     float *delta = nullptr, *lse2 = nullptr;
     cudaError_t e = launch_backward_delta(p, workspace, stream, pitch, &delta, &lse2);
     if (e != cudaSuccess) return e;
-    if (p.d == 128)
+    if (p.d > 64)
         return p.causal ? launch_dims<128, true>(p, delta, lse2, pitch, stream, detail)
                         : launch_dims<128, false>(p, delta, lse2, pitch, stream, detail);
     return p.causal ? launch_dims<64, true>(p, delta, lse2, pitch, stream, detail)
