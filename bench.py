@@ -427,6 +427,21 @@ def time_steps(torch, dev, stream, step, steps, flush):
     return sum(per), per
 
 
+EX2_PER_CLOCK_PER_SM = 32  # GB300's exponential units (twice B200's 16)
+
+
+def exp_roofline(w, ms_step, sms, sm_max_mhz):
+    """The exponential unit's roofline, reported beside the tensor one: one
+    ex2 per (query, key) pair the mask keeps, against EX2_PER_CLOCK_PER_SM
+    x SMs x the maximum SM clock."""
+    pairs = w.B * w.H * (w.N * (w.N + 1) / 2 if w.causal else float(w.N) ** 2)
+    mhz = sm_max_mhz or 2070
+    peak = EX2_PER_CLOCK_PER_SM * sms * mhz * 1e6 / 1e12
+    achieved = pairs / (ms_step * 1e-3) / 1e12
+    return {"exps": pairs, "achieved": achieved, "peak": peak, "unit": "Tex2/s", "frac": achieved / peak,
+            "peak_source": f"derived: {EX2_PER_CLOCK_PER_SM} ex2 per clock per SM x {sms} SMs x {mhz} MHz"}
+
+
 def step_spread(per):
     """Minimum and median of the timed region's single steps."""
     return {"min": per[0], "median": statistics.median(per), "steps": len(per)}
@@ -751,6 +766,7 @@ def main():
     if per_call > 1:
         roof["note"] = "achieved over the whole step (%d launches)" % per_call
 
+    clock_summary = clocks.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -762,12 +778,14 @@ def main():
         "pct_bf16_peak": 100.0 * (w.flops / (ms_step * 1e-3) / 1e12) / float(peaks["bf16_tflops"]),
         "pct_bf16_peak_sustained": 100.0 * (w.flops / (ms_step * 1e-3) / 1e12) / float(peaks["bf16_tflops_sustained"]),
         "roofline": roof,
+        "exp_roofline": exp_roofline(w, ms_step, torch.cuda.get_device_properties(dev).multi_processor_count,
+                                     clock_summary.get("sm_max_mhz")),
         "e2e": line_e2e,
         "gpu_launches": timed_launches,
         "per_step_ms": spread,
         "kernel": path,
         "workspace_bytes": ws_bytes,
-        "clocks": clocks.summary(),
+        "clocks": clock_summary,
     }
     if rank == 0 and not args.no_cpu_baseline:
         rate, nrows, threads, el = oracle_rows_rate(w, q_np, k_np, v_np, args.cpu_seconds,

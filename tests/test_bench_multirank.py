@@ -114,3 +114,17 @@ def test_attention_counts_match_brute_force():
 def test_step_spread_reports_min_and_median():
     s = bench.step_spread([0.5, 0.6, 0.7, 0.9])
     assert s["min"] == 0.5 and s["steps"] == 4 and s["median"] == pytest.approx(0.65)
+
+
+def test_exp_roofline_counts_the_kept_pairs():
+    """One exponential per (query, key) pair the mask keeps: N^2 per head, or
+    N (N + 1) / 2 with the causal mask, against 32 per clock per SM."""
+    import synth
+    w = synth.Workload("t", 2, 3, 5, 64, "bf16", False, seed=1)
+    r = bench.exp_roofline(w, 1.0, 152, 2000)
+    assert r["exps"] == 2 * 3 * 25
+    assert r["peak"] == pytest.approx(32 * 152 * 2000e6 / 1e12)
+    assert r["achieved"] == pytest.approx(150 / 1e-3 / 1e12)
+    assert r["frac"] == pytest.approx(r["achieved"] / r["peak"])
+    wc = synth.Workload("t", 2, 3, 5, 64, "bf16", True, seed=1)
+    assert bench.exp_roofline(wc, 1.0, 152, None)["exps"] == 2 * 3 * 15

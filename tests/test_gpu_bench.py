@@ -32,6 +32,7 @@ def test_small_workload_line_is_flushed_and_complete():
     # the mean of the flushed steps is the reported time
     assert spread["min"] <= d["ms_per_step"]
     assert d["roofline"]["frac"] > 0 and d["roofline"]["achieved"] > 0
+    assert 0 < d["exp_roofline"]["frac"] < 1.5 and d["exp_roofline"]["exps"] == 2 * 256 * 256
     assert d["cpu_baseline"]["cores"] == 1 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
 
