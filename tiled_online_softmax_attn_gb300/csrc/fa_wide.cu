@@ -988,7 +988,7 @@ struct SplitArgs {
 };
 constexpr int SPLIT_THREADS = 256, SPLIT_UNROLL = 4, SPLIT_PER_BLOCK = SPLIT_THREADS * SPLIT_UNROLL;
 
-__global__ void __launch_bounds__(SPLIT_THREADS) fa_split_kernel(const SplitArgs a, size_t n4)
+__global__ void __launch_bounds__(SPLIT_THREADS) fa_split_kernel(const __grid_constant__ SplitArgs a, size_t n4)
 {
     const float4 *__restrict__ x = a.x[blockIdx.y];
     uint2 *__restrict__ hi = a.hi[blockIdx.y];
@@ -1013,72 +1013,85 @@ __global__ void __launch_bounds__(SPLIT_THREADS) fa_split_kernel(const SplitArgs
     }
 }
 
-// Merge of the per-split partial results, one CTA per query row and one
-// float4 of the row per thread.  Each thread's loads of its partial rows are
-// issued before warp 0 has the split weights, so the two round trips to
-// memory overlap.
+// Merge of the per-split partial results ("Core FlashAttention Mechanics",
+// item 3: rescale each partial by 2^(m_s - M) and divide by the rescaled sum).
+// COMBINE_COLS columns of a row per thread, D / COMBINE_COLS threads per row,
+// as many rows as fit in 256 threads per block (two blocks per SM: one wave
+// for the d = 1024 rows of a 1024-row head).  Every thread loads the maxima,
+// sums and partial rows of the first HOLD splits itself (one round trip to
+// memory, no block barrier); further splits are loaded as they are used.
+constexpr int COMBINE_THREADS = 256, COMBINE_COLS = 16;
+
 template <typename Tout>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(COMBINE_THREADS, 2)
 fa_combine_kernel(const float *__restrict__ o_part, const float *__restrict__ m_part,
                   const float *__restrict__ l_part, const float *__restrict__ d_part,
                   Tout *__restrict__ o, float *__restrict__ lse, int BH, int N, int D, int n_split)
 {
-    __shared__ float w_s[MAX_SPLITS];
-    __shared__ float inv_s;
-    const size_t row = blockIdx.x;
-    const size_t stride = (size_t)BH * N;
+    constexpr int V = COMBINE_COLS / 4;  // float4 per thread and split
+    const int tpr = D / COMBINE_COLS, per_block = COMBINE_THREADS / tpr;  // threads per row, rows per block
+    const size_t rows = (size_t)BH * N;
+    const int r = (int)threadIdx.x / tpr;
+    const size_t row = (size_t)blockIdx.x * per_block + r;
+    const int c0 = (int)(threadIdx.x % tpr) * COMBINE_COLS;
     pdl_wait_prior();  // the partials come from the kernel before this one
-    constexpr int HOLD = 4;  // partial rows held in registers per thread (more splits: loaded as used)
-    const int c0 = threadIdx.x * 4;
-    float4 held[HOLD];
-    if (c0 < D) {
+    if (r >= per_block || row >= rows) return;
+    constexpr int HOLD = 4;
+    const size_t ostep = rows * (size_t)D;  // elements between two splits' partial O
+    const float *op = o_part + row * D + c0, *mp = m_part + row, *lp = l_part + row, *dp = d_part + row;
+    float4 x[HOLD][V];
+    float ms[HOLD], ls[HOLD], ds[HOLD];
 #pragma unroll
-        for (int s = 0; s < HOLD; ++s)
-            if (s < n_split) held[s] = __ldcs(reinterpret_cast<const float4 *>(o_part + (s * stride + row) * D + c0));
-    }
-    if (threadIdx.x < 32) {
-        // warp 0: reference maximum, weights 2^(m_s - m), denominators
-        const int s = threadIdx.x;
-        const float ms = s < n_split ? m_part[s * stride + row] : -INFINITY;
-        float M = ms;
+    for (int s = 0; s < HOLD; ++s) {
+        ms[s] = -INFINITY;
+        if (s < n_split) {
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        const float wt = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-        float L = wt != 0.f ? wt * l_part[s * stride + row] : 0.f;
-        float Lq = wt != 0.f ? wt * (l_part[s * stride + row] + d_part[s * stride + row]) : 0.f;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            L += __shfl_xor_sync(0xffffffffu, L, off);
-            Lq += __shfl_xor_sync(0xffffffffu, Lq, off);
-        }
-        if (s < n_split) w_s[s] = wt;
-        if (s == 0) {
-            inv_s = 1.f / Lq;
-            if (lse) lse[row] = (M + log2f(L)) * 0.69314718055994530942f;
+            for (int v = 0; v < V; ++v) x[s][v] = __ldcs(reinterpret_cast<const float4 *>(op + s * ostep) + v);
+            ms[s] = mp[s * rows];
+            ls[s] = lp[s * rows];
+            ds[s] = dp[s * rows];
         }
     }
-    __syncthreads();
-    const float inv = inv_s;
-    for (int c = c0; c < D; c += blockDim.x * 4) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < n_split; ++s) {
-            const float wt = w_s[s];
-            if (wt == 0.f) continue;  // empty splits hold no partial O
-            const float4 v = (c == c0 && s < HOLD) ? held[s]
-                                                   : __ldcs(reinterpret_cast<const float4 *>(o_part + (s * stride + row) * D + c));
-            acc.x = fmaf(wt, v.x, acc.x);
-            acc.y = fmaf(wt, v.y, acc.y);
-            acc.z = fmaf(wt, v.z, acc.z);
-            acc.w = fmaf(wt, v.w, acc.w);
-        }
-        Tout *dst = o + row * D + c;
-        if constexpr (sizeof(Tout) == 4) {
-            *reinterpret_cast<float4 *>(dst) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        } else {
-            *reinterpret_cast<uint2 *>(dst) =
-                make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-        }
+    float M = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < HOLD; ++s) M = fmaxf(M, ms[s]);
+#pragma unroll 1
+    for (int s = HOLD; s < n_split; ++s) M = fmaxf(M, mp[s * rows]);
+    float L = 0.f, Lq = 0.f;
+    float4 acc[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](float m_s, float l_s, float d_s, const float4 (&y)[V]) {
+        if (m_s == -INFINITY) return;  // an empty split holds no partial O
+        const float wt = exp2f(m_s - M);
+        L = fmaf(wt, l_s, L);
+        Lq = fmaf(wt, l_s + d_s, Lq);
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+            acc[v] = make_float4(fmaf(wt, y[v].x, acc[v].x), fmaf(wt, y[v].y, acc[v].y), fmaf(wt, y[v].z, acc[v].z),
+                                 fmaf(wt, y[v].w, acc[v].w));
+    };
+#pragma unroll
+    for (int s = 0; s < HOLD; ++s)
+        if (s < n_split) add(ms[s], ls[s], ds[s], x[s]);
+#pragma unroll 1
+    for (int s = HOLD; s < n_split; ++s) {
+        float4 y[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) y[v] = __ldcs(reinterpret_cast<const float4 *>(op + s * ostep) + v);
+        add(mp[s * rows], lp[s * rows], dp[s * rows], y);
     }
+    const float inv = 1.f / Lq;
+    Tout *dst = o + row * D + c0;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const float4 a = acc[v];
+        if constexpr (sizeof(Tout) == 4)
+            reinterpret_cast<float4 *>(dst)[v] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+        else
+            reinterpret_cast<uint2 *>(dst)[v] = make_uint2(pack_bf16x2(a.x * inv, a.y * inv), pack_bf16x2(a.z * inv, a.w * inv));
+    }
+    if (lse && c0 == 0) lse[row] = (M + log2f(L)) * 0.69314718055994530942f;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -1315,14 +1328,15 @@ cudaError_t launch_split_hilo(const float *const *x, void *const *hi, void *cons
 cudaError_t launch_combine(const float *o_part, const float *m_part, const float *l_part, const float *d_part, void *o,
                            bool o_fp32, float *lse, int64_t BH, int64_t N, int D, int n_split, cudaStream_t stream)
 {
-    if (n_split < 1 || n_split > MAX_SPLITS || D % 4 != 0) return cudaErrorInvalidValue;
-    const unsigned rows = (unsigned)(BH * N);
-    const int threads = (int)std::min<int64_t>(256, std::max<int64_t>(32, D / 4));
+    if (n_split < 1 || n_split > MAX_SPLITS || D % COMBINE_COLS != 0 || D > COMBINE_COLS * COMBINE_THREADS)
+        return cudaErrorInvalidValue;
+    const int64_t per_block = COMBINE_THREADS / (D / COMBINE_COLS);
+    const unsigned blocks = (unsigned)((BH * N + per_block - 1) / per_block);
     // programmatic dependent launch: the merge's blocks may be scheduled while
     // the attention kernel finishes; they wait for it before reading (pdl_wait_prior)
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(rows, 1, 1);
-    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.gridDim = dim3(blocks, 1, 1);
+    cfg.blockDim = dim3(COMBINE_THREADS, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute at[1];
