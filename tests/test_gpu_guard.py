@@ -11,7 +11,8 @@ oracle.  Ragged N (1, 77, 129, 300, 513, 1000) puts the last query and key
 tiles past the end of each head, where the kernels mask their stores.
 
 Paths: the 64/128 tensor-core kernel (one work item per CTA, persistent
-CTAs over many items, the key-range split with a workspace), the general-d
+CTAs over many items, unmasked and causal, the key-range split with a
+workspace), the general-d
 kernel, the wide-head path (bf16 d = 256, fp32 d = 128 with key splits, and the
 cluster form for d = 512 and 1024),
 fa_attention with a padded O, fa_forward_host on host buffers and
@@ -115,6 +116,13 @@ def test_tensor_core_kernel(N, d, causal):
 def test_tensor_core_kernel_persistent_ctas(d):
     # 2 x 80 heads of three 256-row blocks: 480 items, several per CTA
     device_case(synth.Workload("guard", 2, 80, 513, d, "bf16", False, seed=8100 + d))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_tensor_core_kernel_persistent_causal_ctas(d):
+    # 2 x 80 causal heads of two 256-row blocks (the second ragged): 320 short
+    # items of unequal length on persistent CTAs
+    device_case(synth.Workload("guard", 2, 80, 300, d, "bf16", True, seed=8150 + d))
 
 
 @pytest.mark.parametrize("N", [513, 1000])

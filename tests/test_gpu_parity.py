@@ -143,6 +143,19 @@ def test_persistent_ctas_with_ragged_rows(d):
     compare(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, w.dtype, w.dtype)
 
 
+@pytest.mark.parametrize("d,N", [(64, 1000), (128, 300), (128, 2048)])
+def test_persistent_ctas_causal_short_items(d, N):
+    """Causal items short enough to run on persistent CTAs (at most 2048
+    key-tile columns, more items than SMs): every CTA loops over items of
+    unequal length, longest first in rounds of alternating direction.  Every
+    row against the oracle."""
+    w = synth.Workload("persistent causal", 2, 80 if N < 2048 else 40, N, d, "bf16", True, seed=7200 + d + N)
+    q, k, v = w.inputs()
+    o, lse = run(q, k, v, w.dtype, w.scale, w.causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, w.scale, w.causal)
+    compare(o, lse, o_ref, lse_ref, w.dtype, w.dtype, label=f"persistent causal {w.B}x{w.H}x{N}x{d}")
+
+
 def test_repeat_runs_are_bitwise_identical():
     w = synth.WORKLOADS["tiny"].scaled(N=333, causal=True)
     q, k, v = w.inputs()

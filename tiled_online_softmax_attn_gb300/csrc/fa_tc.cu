@@ -916,22 +916,25 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     // Short unmasked items (64 key tiles or fewer): one persistent CTA per SM
     // loops over them, so an item's prologue (query loads, first S MMA) and
     // epilogue overlap its neighbours' work (multi-head workload +2.5 %).  Long
-    // items gain nothing from that, and items of unequal cost (causal) balance
-    // best one per CTA, handed out by the hardware as SMs free up (measured:
-    // persistence with alternating-direction rounds gave the causal workload
-    // -1 %, the peaked one -2 %).
-    const bool persist = !CAUSAL && prm.n_kv <= 64 && prm.n_split == 1;
+    // items gain nothing from that, and long items of unequal cost (causal)
+    // balance best one per CTA, handed out by the hardware as SMs free up
+    // (measured: persistence with alternating-direction rounds gave the causal
+    // workload -1 %, the peaked one -2 %).  Short causal items, when there are
+    // more of them than SMs, gain more from the overlap than they lose in
+    // balance: at most 2048 key-tile columns (16 key tiles at d = 128, 32 at
+    // d = 64) measured +4 to +31 % on 512-4096-key problems.
+    cudaError_t e = cudaSuccess;
+    const int sms = sm_count(&e);
+    if (e != cudaSuccess) return e;
+    const bool persist = prm.n_split == 1 && (CAUSAL ? prm.n_items > sms && prm.n_kv * std::max(DK, DV) <= 2048
+                                                     : prm.n_kv <= 64);
     auto kern = prm.n_split > 1 ? fa_tc_kernel<DK, DV, CAUSAL, false, !CAUSAL>
                 : persist       ? fa_tc_kernel<DK, DV, CAUSAL, true, false>
                                 : fa_tc_kernel<DK, DV, CAUSAL, false, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM_BYTES);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     int grid = prm.n_items;
-    if (persist) {
-        const int sms = sm_count(&e);
-        if (e != cudaSuccess) return e;
-        grid = std::min(prm.n_items, sms);
-    }
+    if (persist) grid = std::min(prm.n_items, sms);
     kern<<<(unsigned)grid, NUM_THREADS, Cf::SMEM_BYTES, stream>>>(mq, mk, mv, prm);
     if ((e = cudaGetLastError()) != cudaSuccess || prm.n_split == 1) return e;
     return launch_combine(prm.o_part, prm.m_part, prm.l_part, prm.d_part, p.o, p.o_dtype == 1, p.lse, BH, p.N, DV,
