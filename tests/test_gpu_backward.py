@@ -120,6 +120,39 @@ def test_narrow_head_backward_on_tensor_cores(N, d, causal):
     assert path == "tensor-core", path
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N,d", [(2, 80, 300, 64), (2, 80, 300, 128), (1, 80, 2000, 128), (2, 40, 513, 40)])
+def test_persistent_backward_ctas(B, H, N, d, causal):
+    """More items (128-row tiles x heads) than SMs, each of at most 16 tiles:
+    the dK/dV and dQ kernels run on persistent CTAs that loop over items,
+    handing the resident tiles and the accumulators over between them.  Every
+    gradient element against the oracle."""
+    assert (N + 127) // 128 <= 16 and (N + 127) // 128 * B * H > 152
+    stats, path = run_backward(B, H, N, d, "bf16", causal, seed=8600 + N + d)
+    assert path == "tensor-core", path
+
+
+def test_persistent_backward_leaves_neighbouring_memory_alone():
+    """dQ, dK and dV of 480 persistent items inside sentinel-filled buffers."""
+    B, H, N, d = 2, 80, 300, 64
+    w = synth.Workload("t", B, H, N, d, "bf16", False, seed=8650)
+    q, k, v = w.inputs()
+    dout = synth.tensor(3 * 8650 + 9, w.shape, "bf16")
+    qt, kt, vt, gt = (torch.from_numpy(x).to(torch.bfloat16).cuda() for x in (q, k, v, dout))
+    o, lse = fa.fa_forward(qt, kt, vt, scale=w.scale)
+    n, guard = B * H * N * d, 256
+    bufs = [torch.full((n + 2 * guard,), 0x5A5A, dtype=torch.int16, device="cuda") for _ in range(3)]
+    grads = [b[guard:guard + n].view(torch.bfloat16).view(w.shape) for b in bufs]
+    fa.fa_backward(qt, kt, vt, o, gt, lse, scale=w.scale, dq=grads[0], dk=grads[1], dv=grads[2])
+    torch.cuda.synchronize()
+    assert fa.check_device_error() == fa.FA_OK, fa.last_error()
+    for b in bufs:
+        h = b.cpu()
+        assert bool((h[:guard] == 0x5A5A).all()) and bool((h[guard + n:] == 0x5A5A).all())
+    ref = oracle.attention_backward(q, k, v, dout, w.scale, False)
+    _check([g.float().cpu().numpy() for g in grads], ref, "bf16", "bf16", "tensor-core")
+
+
 def test_narrow_head_backward_leaves_neighbouring_memory_alone():
     """dQ, dK and dV of a d = 40 head sit inside sentinel-filled buffers; the
     padded columns the kernel computes must not reach memory."""

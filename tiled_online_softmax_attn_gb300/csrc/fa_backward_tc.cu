@@ -35,6 +35,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -71,6 +72,7 @@ struct EW {
     static constexpr int MMA_WARP = WARPS + 1;
 };
 constexpr uint32_t TMEM_COLS = 512;
+constexpr int PERSIST_MAX_TILES = 16;  // persistent CTAs for items of at most this many steps
 constexpr uint32_t BOX = 128 * 128;  // one 128-row x 64-column bf16 box
 constexpr uint32_t VEC_BYTES = 1024;  // lse2 and delta of 128 rows
 
@@ -78,7 +80,7 @@ constexpr uint32_t VEC_BYTES = 1024;  // lse2 and delta of 128 rows
 // memory: at d = 128 its tiles take all but a few hundred bytes of the 227 KB a
 // CTA may have, so nothing is left for static shared memory.
 struct KvBars {
-    uint64_t res_full, st_full, s_read, dp_full, p_ready, ds_ready, o_full, drain;
+    uint64_t res_full, res_empty, st_full, s_read, dp_full, p_ready, ds_ready, o_full, acc_empty, drain;
     uint64_t fq[4], eq[4], fg[3], eg[3], fvec[2], evec[2];
     uint32_t tmem_base;
     int abort_flag;
@@ -183,8 +185,25 @@ __device__ __forceinline__ void fail_bwd(volatile int *abort_flag)
     *abort_flag = 1;
 }
 
+// Work item `it` of this CTA: its block index, or (persistent CTAs, short
+// items) rounds of alternating direction over the CTAs, so that items of
+// unequal length (causal) even out per CTA.
+template <bool PERSIST>
+__device__ __forceinline__ int bwd_item_index(int it)
+{
+    if (!PERSIST) return it == 0 ? (int)blockIdx.x : INT_MAX;
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    return it * G + ((it & 1) ? G - 1 - c : c);
+}
+
 // ---------------------------------------------------------------- dK / dV
-template <int D, bool CAUSAL>
+// A work item is one 128-key tile of one head.  With PERSIST a CTA loops over
+// several: the steps (query tiles) of all its items are numbered globally, so
+// the rings and the per-step barriers run on across items; the resident K and
+// V of the next item load once the last score products of the current one
+// have read theirs (res_empty), and its first dV product waits until the
+// epilogue has read the current dV and dK from tensor memory (acc_empty).
+template <int D, bool CAUSAL, bool PERSIST>
 __global__ void __launch_bounds__(EW<D>::NUM_THREADS, 1)
 fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g, const BwdParams prm)
@@ -195,10 +214,18 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = prm.N;
-    const int kt = (int)(blockIdx.x % prm.n_q), bh = (int)(blockIdx.x / prm.n_q);
-    const int k0 = kt * BM;
-    const int first = CAUSAL ? kt : 0;  // query tiles before the key tile see none of its keys
-    const int n_steps = prm.n_q - first;
+    const int n_items = prm.n_q * prm.BH;
+    // item it: key tile kt of head bh, query tiles first .. n_q - 1
+    auto item = [&](int it, int &k0, int &bh, int &first, int &n_steps) -> bool {
+        const int w = bwd_item_index<PERSIST>(it);
+        if (w >= n_items) return false;
+        const int kt = w % prm.n_q;
+        bh = w / prm.n_q;
+        k0 = kt * BM;
+        first = CAUSAL ? kt : 0;  // query tiles before the key tile see none of its keys
+        n_steps = prm.n_q - first;
+        return true;
+    };
 
     // 1024-byte aligned base, derived from smem_raw by an offset so the
     // compiler keeps the shared address space (plain shared loads for the
@@ -222,14 +249,16 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // per ring slot: fq/eq for Q_i, fg/eg for dO_i (dO_i is freed by the earlier dV
     // product and loaded second, so Q_i, needed first, lands sooner), fvec/evec for
     // the vectors of the step in work (freed by the elementwise warps)
-    uint64_t &res_full = bars.res_full, &st_full = bars.st_full, &s_read = bars.s_read, &dp_full = bars.dp_full,
-             &p_ready = bars.p_ready, &ds_ready = bars.ds_ready, &o_full = bars.o_full, &drain = bars.drain;
+    uint64_t &res_full = bars.res_full, &res_empty = bars.res_empty, &st_full = bars.st_full, &s_read = bars.s_read,
+             &dp_full = bars.dp_full, &p_ready = bars.p_ready, &ds_ready = bars.ds_ready, &o_full = bars.o_full,
+             &acc_empty = bars.acc_empty, &drain = bars.drain;
     uint64_t *fq = bars.fq, *eq = bars.eq, *fg = bars.fg, *eg = bars.eg, *fvec = bars.fvec, *evec = bars.evec;
     volatile int &abort_flag = *const_cast<volatile int *>(&bars.abort_flag);
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(smem_addr(&res_full), 1);
+        mbar_init(smem_addr(&res_empty), 1);
         for (int s = 0; s < C::NQS; ++s) {
             mbar_init(smem_addr(&fq[s]), 1);
             mbar_init(smem_addr(&eq[s]), 1);
@@ -248,6 +277,7 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_init(smem_addr(&p_ready), E::THREADS);
         mbar_init(smem_addr(&ds_ready), E::THREADS);
         mbar_init(smem_addr(&o_full), 1);
+        mbar_init(smem_addr(&acc_empty), E::THREADS);
         mbar_init(smem_addr(&drain), 1);
         fence_mbar_init();
     }
@@ -271,51 +301,71 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
             bool ok = true;
-            int issued_q = 0, issued_g = 0, issued_v = 0;
-            mbar_arrive_expect_tx(smem_addr(&res_full), C::RES);
-            for (int c = 0; c < C::CH; ++c) {
-                tma_load_3d(sK + c * BOX, &tm_k, smem_addr(&res_full), c * 64, k0, bh, pol);
-                tma_load_3d(sV + c * BOX, &tm_v, smem_addr(&res_full), c * 64, k0, bh, pol);
-            }
-            for (int s = 0; s < n_steps; ++s) {
-                const int qs = s % C::NQS, gs = s % C::NGS, vs = s & 1, q0 = (first + s) * BM;
-                if (!wait_or_abort(smem_addr(&eq[qs]), (uint32_t)(((s / C::NQS) & 1) ^ 1), limit, &abort_flag)) {
-                    ok = false;
-                    break;
+            int g = 0;  // global step: ring positions run on across items
+            int issued_q = 0, issued_g = 0, issued_v = 0, res_items = 0;
+            int k0, bh, first, n_steps;
+            bool have = item(0, k0, bh, first, n_steps);
+            for (int it = 0; ok && have; ++it) {
+                // the item's resident K and V, once the previous item's are read: the
+                // first item's before anything else, a later one's after the first
+                // step's Q and vectors (which need not wait for them)
+                auto load_res = [&]() -> bool {
+                    if (it > 0 && !wait_or_abort(smem_addr(&res_empty), (uint32_t)((it - 1) & 1), limit, &abort_flag))
+                        return false;
+                    mbar_arrive_expect_tx(smem_addr(&res_full), C::RES);
+                    for (int c = 0; c < C::CH; ++c) {
+                        tma_load_3d(sK + c * BOX, &tm_k, smem_addr(&res_full), c * 64, k0, bh, pol);
+                        tma_load_3d(sV + c * BOX, &tm_v, smem_addr(&res_full), c * 64, k0, bh, pol);
+                    }
+                    res_items = it + 1;
+                    return true;
+                };
+                if (it == 0 && !(ok = load_res())) break;
+                for (int s = 0; s < n_steps; ++s, ++g) {
+                    const int qs = g % C::NQS, gs = g % C::NGS, vs = g & 1, q0 = (first + s) * BM;
+                    if (!wait_or_abort(smem_addr(&eq[qs]), (uint32_t)(((g / C::NQS) & 1) ^ 1), limit, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bq = smem_addr(&fq[qs]);
+                    mbar_arrive_expect_tx(bq, C::TILE);
+                    for (int c = 0; c < C::CH; ++c)
+                        tma_load_3d(sQr + qs * C::TILE + c * BOX, &tm_q, bq, c * 64, q0, bh, pol);
+                    issued_q = g + 1;
+                    if (!wait_or_abort(smem_addr(&evec[vs]), (uint32_t)(((g >> 1) & 1) ^ 1), limit, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bv = smem_addr(&fvec[vs]);
+                    mbar_arrive_expect_tx(bv, VEC_BYTES);
+                    const size_t vrow = (size_t)bh * prm.pitch + q0;
+                    const uint32_t dvec = s_base + oVec + vs * VEC_BYTES;
+                    bulk_copy_g2s(dvec, prm.lse2 + vrow, 512, bv);
+                    bulk_copy_g2s(dvec + 512, prm.delta + vrow, 512, bv);
+                    issued_v = g + 1;
+                    if (s == 0 && it > 0 && !(ok = load_res())) break;
+                    if (!wait_or_abort(smem_addr(&eg[gs]), (uint32_t)(((g / C::NGS) & 1) ^ 1), limit, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bg = smem_addr(&fg[gs]);
+                    mbar_arrive_expect_tx(bg, C::TILE);
+                    for (int c = 0; c < C::CH; ++c)
+                        tma_load_3d(sGr + gs * C::TILE + c * BOX, &tm_g, bg, c * 64, q0, bh, pol);
+                    issued_g = g + 1;
                 }
-                const uint32_t bq = smem_addr(&fq[qs]);
-                mbar_arrive_expect_tx(bq, C::TILE);
-                for (int c = 0; c < C::CH; ++c) tma_load_3d(sQr + qs * C::TILE + c * BOX, &tm_q, bq, c * 64, q0, bh, pol);
-                issued_q = s + 1;
-                if (!wait_or_abort(smem_addr(&evec[vs]), (uint32_t)(((s >> 1) & 1) ^ 1), limit, &abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t bv = smem_addr(&fvec[vs]);
-                mbar_arrive_expect_tx(bv, VEC_BYTES);
-                const size_t vrow = (size_t)bh * prm.pitch + q0;
-                const uint32_t dvec = s_base + oVec + vs * VEC_BYTES;
-                bulk_copy_g2s(dvec, prm.lse2 + vrow, 512, bv);
-                bulk_copy_g2s(dvec + 512, prm.delta + vrow, 512, bv);
-                issued_v = s + 1;
-                if (!wait_or_abort(smem_addr(&eg[gs]), (uint32_t)(((s / C::NGS) & 1) ^ 1), limit, &abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t bg = smem_addr(&fg[gs]);
-                mbar_arrive_expect_tx(bg, C::TILE);
-                for (int c = 0; c < C::CH; ++c) tma_load_3d(sGr + gs * C::TILE + c * BOX, &tm_g, bg, c * 64, q0, bh, pol);
-                issued_g = s + 1;
+                if constexpr (!PERSIST) break;  // one item per CTA
+                have = item(it + 1, k0, bh, first, n_steps);
             }
             if (!ok) {
                 if (!abort_flag) fail_bwd(&abort_flag);
-                for (int s = (issued_q > C::NQS ? issued_q - C::NQS : 0); s < issued_q; ++s)
-                    mbar_wait_bounded(smem_addr(&fq[s % C::NQS]), (uint32_t)((s / C::NQS) & 1), limit);
-                for (int s = (issued_v > 2 ? issued_v - 2 : 0); s < issued_v; ++s)
-                    mbar_wait_bounded(smem_addr(&fvec[s & 1]), (uint32_t)((s >> 1) & 1), limit);
-                for (int s = (issued_g > C::NGS ? issued_g - C::NGS : 0); s < issued_g; ++s)
-                    mbar_wait_bounded(smem_addr(&fg[s % C::NGS]), (uint32_t)((s / C::NGS) & 1), limit);
-                mbar_wait_bounded(smem_addr(&res_full), 0, limit);
+                for (int x = (issued_q > C::NQS ? issued_q - C::NQS : 0); x < issued_q; ++x)
+                    mbar_wait_bounded(smem_addr(&fq[x % C::NQS]), (uint32_t)((x / C::NQS) & 1), limit);
+                for (int x = (issued_v > 2 ? issued_v - 2 : 0); x < issued_v; ++x)
+                    mbar_wait_bounded(smem_addr(&fvec[x & 1]), (uint32_t)((x >> 1) & 1), limit);
+                for (int x = (issued_g > C::NGS ? issued_g - C::NGS : 0); x < issued_g; ++x)
+                    mbar_wait_bounded(smem_addr(&fg[x % C::NGS]), (uint32_t)((x / C::NGS) & 1), limit);
+                if (res_items > 0) mbar_wait_bounded(smem_addr(&res_full), (uint32_t)((res_items - 1) & 1), limit);
             }
         }
         __syncwarp();
@@ -323,10 +373,10 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         {  // whole warp, converged; elect.sync picks the issuing lane
             const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0), id_o = idesc_bf16_f32(BM, D, 0, 1);
             const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
-            bool ok = wait_or_abort_w(smem_addr(&res_full), 0, limit, &abort_flag), issued = false;
-            // S^T(s) = K Q_s^T into cS, dP^T(s) = V dO_s^T into cP
-            auto mma_st = [&](int s) {
-                const uint64_t dQ = sdesc_sw128(sQr + (s % C::NQS) * C::TILE, 16, 1024);
+            bool ok = true, issued = false;
+            // S^T(g) = K Q_g^T into cS, dP^T(g) = V dO_g^T into cP (g a global step)
+            auto mma_st = [&](int g) {
+                const uint64_t dQ = sdesc_sw128(sQr + (g % C::NQS) * C::TILE, 16, 1024);
                 uint64_t ka[D / 16], kb[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -337,8 +387,8 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 mma_ss_k<D / 16>(tmem + cS, ka, kb, id_s, 0u);
                 issued = true;
             };
-            auto mma_dpt = [&](int s) {
-                const uint64_t dG = sdesc_sw128(sGr + (s % C::NGS) * C::TILE, 16, 1024);
+            auto mma_dpt = [&](int g) {
+                const uint64_t dG = sdesc_sw128(sGr + (g % C::NGS) * C::TILE, 16, 1024);
                 uint64_t ka[D / 16], kb[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -348,8 +398,9 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 mma_ss_k<D / 16>(tmem + cP, ka, kb, id_s, 0u);
             };
-            // dV += P^T dO_s (A: the P^T columns of cP) or dK += dS^T Q_s (A: the
-            // dS^T columns, 32 further), B MN-major from its ring slot
+            // dV += P^T dO_g (A: the P^T columns of cP) or dK += dS^T Q_g (A: the
+            // dS^T columns, 32 further), B MN-major from its ring slot; the first
+            // step of an item overwrites
             auto mma_acc = [&](uint32_t d_col, uint32_t a_col0, uint64_t b_mn, int s) {
                 uint32_t ta[BM / 16];
                 uint64_t tb[BM / 16];
@@ -360,55 +411,116 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 mma_ts_k<BM / 16>(tmem + d_col, ta, tb, id_o, s > 0 ? 1u : 0u);
             };
-            // Q_s in ring slot s % NQS, dO_s in slot s % NGS
-            auto wait_q = [&](int s) -> bool {
-                if (!wait_or_abort_w(smem_addr(&fq[s % C::NQS]), (uint32_t)((s / C::NQS) & 1), limit, &abort_flag)) return false;
+            // Q_g in ring slot g % NQS, dO_g in slot g % NGS
+            auto wait_q = [&](int g) -> bool {
+                if (!wait_or_abort_w(smem_addr(&fq[g % C::NQS]), (uint32_t)((g / C::NQS) & 1), limit, &abort_flag)) return false;
                 tc_fence_after();
                 return true;
             };
-            auto wait_g = [&](int s) -> bool {
-                if (!wait_or_abort_w(smem_addr(&fg[s % C::NGS]), (uint32_t)((s / C::NGS) & 1), limit, &abort_flag)) return false;
+            auto wait_g = [&](int g) -> bool {
+                if (!wait_or_abort_w(smem_addr(&fg[g % C::NGS]), (uint32_t)((g / C::NGS) & 1), limit, &abort_flag)) return false;
                 tc_fence_after();
                 return true;
             };
-            if (ok && (ok = wait_q(0))) {
-                mma_st(0);
-                mma_commit_w(smem_addr(&st_full));
-                if ((ok = wait_g(0))) {
-                    mma_dpt(0);
-                    mma_commit_w(smem_addr(&dp_full));
+            if constexpr (!PERSIST) {
+                // One item.  (The item loop below, run for one item, measured 4 %
+                // slower on long sequences than this plain loop.)
+                int k0, bh, first, n_steps;
+                item(0, k0, bh, first, n_steps);
+                ok = wait_or_abort_w(smem_addr(&res_full), 0, limit, &abort_flag);
+                if (ok && (ok = wait_q(0))) {
+                    mma_st(0);
+                    mma_commit_w(smem_addr(&st_full));
+                    if ((ok = wait_g(0))) {
+                        mma_dpt(0);
+                        mma_commit_w(smem_addr(&dp_full));
+                    }
                 }
-            }
-            // Per step: S^T(s+1) once the elementwise warps hold S^T(s) (it runs while
-            // they compute the weights of step s); dV(s) once P^T(s) is written; dK(s)
-            // once dS^T(s) is; then dP^T(s+1) over the columns those two have read.
-            for (int s = 0; ok && s < n_steps; ++s) {
-                const bool more = s + 1 < n_steps;
-                if (more) {
-                    if (!wait_or_abort_w(smem_addr(&s_read), (uint32_t)(s & 1), limit, &abort_flag) || !wait_q(s + 1)) {
+                // Per step: S^T(s+1) once the elementwise warps hold S^T(s) (it runs while
+                // they compute the weights of step s); dV(s) once P^T(s) is written; dK(s)
+                // once dS^T(s) is; then dP^T(s+1) over the columns those two have read.
+                for (int s = 0; ok && s < n_steps; ++s) {
+                    const bool more = s + 1 < n_steps;
+                    if (more) {
+                        if (!wait_or_abort_w(smem_addr(&s_read), (uint32_t)(s & 1), limit, &abort_flag) || !wait_q(s + 1)) {
+                            ok = false;
+                            break;
+                        }
+                        mma_st(s + 1);
+                        mma_commit_w(smem_addr(&st_full));
+                    }
+                    if (!wait_or_abort_w(smem_addr(&p_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    mma_acc(cV, cP, sdesc_sw128(sGr + (s % C::NGS) * C::TILE, BOX, 1024), s);
+                    mma_commit_w(smem_addr(&eg[s % C::NGS]));  // dO_s read for the last time
+                    if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    mma_acc(cK, cP + W / 2, sdesc_sw128(sQr + (s % C::NQS) * C::TILE, BOX, 1024), s);
+                    mma_commit_w(smem_addr(&eq[s % C::NQS]));  // Q_s read for the last time
+                    if (more) {
+                        if (!wait_g(s + 1)) { ok = false; break; }
+                        mma_dpt(s + 1);
+                        mma_commit_w(smem_addr(&dp_full));
+                    }
+                }
+                if (ok) mma_commit_w(smem_addr(&o_full));
+            } else {
+                // Items one after the other, steps numbered globally.  An item's first
+                // two score products wait for its resident K and V (and for the
+                // previous S^T to be in registers); its first dV product waits until
+                // the previous item's dV and dK have left tensor memory.
+                int g = 0;
+                int k0, bh, first, n_steps;
+                bool have = item(0, k0, bh, first, n_steps);
+                for (int it = 0; ok && have; ++it) {
+                    if (!wait_or_abort_w(smem_addr(&res_full), (uint32_t)(it & 1), limit, &abort_flag) ||
+                        (g > 0 && !wait_or_abort_w(smem_addr(&s_read), (uint32_t)((g - 1) & 1), limit, &abort_flag)) ||
+                        !wait_q(g)) {
                         ok = false;
                         break;
                     }
-                    mma_st(s + 1);
+                    mma_st(g);
                     mma_commit_w(smem_addr(&st_full));
-                }
-                if (!wait_or_abort_w(smem_addr(&p_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                mma_acc(cV, cP, sdesc_sw128(sGr + (s % C::NGS) * C::TILE, BOX, 1024), s);
-                mma_commit_w(smem_addr(&eg[s % C::NGS]));  // dO_s read for the last time
-                if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                mma_acc(cK, cP + W / 2, sdesc_sw128(sQr + (s % C::NQS) * C::TILE, BOX, 1024), s);
-                mma_commit_w(smem_addr(&eq[s % C::NQS]));  // Q_s read for the last time
-                if (more) {
-                    if (!wait_g(s + 1)) { ok = false; break; }
-                    mma_dpt(s + 1);
+                    if (!wait_g(g)) { ok = false; break; }
+                    mma_dpt(g);
                     mma_commit_w(smem_addr(&dp_full));
+                    if (n_steps == 1) mma_commit_w(smem_addr(&res_empty));  // K and V read for the last time
+                    for (int s = 0; s < n_steps; ++s, ++g) {
+                        const bool more = s + 1 < n_steps;
+                        if (more) {
+                            if (!wait_or_abort_w(smem_addr(&s_read), (uint32_t)(g & 1), limit, &abort_flag) || !wait_q(g + 1)) {
+                                ok = false;
+                                break;
+                            }
+                            mma_st(g + 1);
+                            mma_commit_w(smem_addr(&st_full));
+                        }
+                        if (!wait_or_abort_w(smem_addr(&p_ready), (uint32_t)(g & 1), limit, &abort_flag) ||
+                            (s == 0 && it > 0 &&
+                             !wait_or_abort_w(smem_addr(&acc_empty), (uint32_t)((it - 1) & 1), limit, &abort_flag))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        mma_acc(cV, cP, sdesc_sw128(sGr + (g % C::NGS) * C::TILE, BOX, 1024), s);
+                        mma_commit_w(smem_addr(&eg[g % C::NGS]));  // dO_g read for the last time
+                        if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(g & 1), limit, &abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+                        mma_acc(cK, cP + W / 2, sdesc_sw128(sQr + (g % C::NQS) * C::TILE, BOX, 1024), s);
+                        mma_commit_w(smem_addr(&eq[g % C::NQS]));  // Q_g read for the last time
+                        if (more) {
+                            if (!wait_g(g + 1)) { ok = false; break; }
+                            mma_dpt(g + 1);
+                            mma_commit_w(smem_addr(&dp_full));
+                            if (s + 2 == n_steps) mma_commit_w(smem_addr(&res_empty));  // K and V read for the last time
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit_w(smem_addr(&o_full));  // this item's dV and dK are complete
+                    have = item(it + 1, k0, bh, first, n_steps);
                 }
             }
-            if (ok) {
-                mma_commit_w(smem_addr(&o_full));
-            } else {
+            if (!ok) {
                 if (!abort_flag) fail_bwd(&abort_flag);
                 if (issued) {
                     mma_commit_w(smem_addr(&drain));
@@ -420,106 +532,114 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     } else {
         // one key per thread (tensor-memory lane), queries [W hf, W hf + W) of each tile
         const int quarter = warp & 3, hf = warp >> 2;
-        const int jr = quarter * 32 + lane, kj = k0 + jr;
+        const int jr = quarter * 32 + lane;
         const uint32_t lb = tmem + ((uint32_t)(quarter * 32) << 16);
         const uint32_t cSh = cS + hf * W, cPh = cP + hf * W;
         const float sl = prm.sl;
         bool ok = true;
-        for (int s = 0; s < n_steps; ++s) {
-            const int vs = s & 1, q0 = (first + s) * BM + hf * W;
-            if (!wait_or_abort(smem_addr(&st_full), (uint32_t)(s & 1), limit, &abort_flag) ||
-                !wait_or_abort(smem_addr(&fvec[vs]), (uint32_t)((s >> 1) & 1), limit, &abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const float4 *vec = reinterpret_cast<const float4 *>(smem + oVec + vs * VEC_BYTES) + hf * (W / 4);
-            // Tiles with no padded key or query and wholly below the diagonal
-            // take the unmasked path (no per-element tests or selects).
-            const int qt0 = (first + s) * BM;
-            const bool masked = k0 + BM > N || qt0 + BM > N || (CAUSAL && qt0 < k0 + BM);
-            // P^T row: weights of this key for this half of the tile's queries, as
-            // bf16 pairs (kept in registers for dS^T, written to tensor memory for
-            // the dV product once dP^T(s) has been read)
-            uint32_t pw[W / 2];
-            {
-                uint32_t raw[W];
-                tmem_ld_cols(lb + cSh, raw);
-                tc_fence_before();
-                mbar_arrive(smem_addr(&s_read));  // S^T(s) is in registers: S^T(s+1) may overwrite it
-                const uint64_t sl2 = f2_pack(sl, sl);
-                auto weights = [&](auto mask) {
-                    constexpr bool M = decltype(mask)::value;
+        int g = 0;
+        int k0, bh, first, n_steps;
+        bool have = item(0, k0, bh, first, n_steps);
+        for (int it = 0; ok && have; ++it) {
+            const int kj = k0 + jr;
+            for (int s = 0; s < n_steps; ++s, ++g) {
+                const int vs = g & 1, q0 = (first + s) * BM + hf * W;
+                if (!wait_or_abort(smem_addr(&st_full), (uint32_t)(g & 1), limit, &abort_flag) ||
+                    !wait_or_abort(smem_addr(&fvec[vs]), (uint32_t)((g >> 1) & 1), limit, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float4 *vec = reinterpret_cast<const float4 *>(smem + oVec + vs * VEC_BYTES) + hf * (W / 4);
+                // Tiles with no padded key or query and wholly below the diagonal
+                // take the unmasked path (no per-element tests or selects).
+                const int qt0 = (first + s) * BM;
+                const bool masked = k0 + BM > N || qt0 + BM > N || (CAUSAL && qt0 < k0 + BM);
+                // P^T row: weights of this key for this half of the tile's queries, as
+                // bf16 pairs (kept in registers for dS^T, written to tensor memory for
+                // the dV product once dP^T(s) has been read)
+                uint32_t pw[W / 2];
+                {
+                    uint32_t raw[W];
+                    tmem_ld_cols(lb + cSh, raw);
+                    tc_fence_before();
+                    mbar_arrive(smem_addr(&s_read));  // S^T(s) is in registers: S^T(s+1) may overwrite it
+                    const uint64_t sl2 = f2_pack(sl, sl);
+                    auto weights = [&](auto mask) {
+                        constexpr bool M = decltype(mask)::value;
 #pragma unroll
-                    for (int c4 = 0; c4 < W / 4; ++c4) {
-                        const float4 l4 = vec[c4];  // LSE * log2 e of queries q0 + 4 c4 ...
+                        for (int c4 = 0; c4 < W / 4; ++c4) {
+                            const float4 l4 = vec[c4];  // LSE * log2 e of queries q0 + 4 c4 ...
 #pragma unroll
-                        for (int e = 0; e < 4; e += 2) {
-                            const int c = 4 * c4 + e;
-                            const uint64_t nl = e ? f2_pack(-l4.z, -l4.w) : f2_pack(-l4.x, -l4.y);
-                            float a0, a1;
-                            f2_unpack(f2_fma(f2_pack(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1])), sl2, nl), a0, a1);
-                            float w0 = ex2(a0), w1 = ex2(a1);
-                            if (M) {
-                                const int q = q0 + c;
-                                w0 = (kj < N && q < N && (!CAUSAL || kj <= q)) ? w0 : 0.f;
-                                w1 = (kj < N && q + 1 < N && (!CAUSAL || kj <= q + 1)) ? w1 : 0.f;
+                            for (int e = 0; e < 4; e += 2) {
+                                const int c = 4 * c4 + e;
+                                const uint64_t nl = e ? f2_pack(-l4.z, -l4.w) : f2_pack(-l4.x, -l4.y);
+                                float a0, a1;
+                                f2_unpack(f2_fma(f2_pack(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1])), sl2, nl), a0, a1);
+                                float w0 = ex2(a0), w1 = ex2(a1);
+                                if (M) {
+                                    const int q = q0 + c;
+                                    w0 = (kj < N && q < N && (!CAUSAL || kj <= q)) ? w0 : 0.f;
+                                    w1 = (kj < N && q + 1 < N && (!CAUSAL || kj <= q + 1)) ? w1 : 0.f;
+                                }
+                                pw[c / 2] = pack_bf16x2(w0, w1);
                             }
-                            pw[c / 2] = pack_bf16x2(w0, w1);
                         }
-                    }
-                };
-                if (masked) weights(std::true_type{});
-                else weights(std::false_type{});
-            }
-            // dP^T(s) into registers; its columns then take P^T (for dV) and dS^T
-            // = P^T (dP^T - delta), with the bf16 weights the dV product uses
-            if (!wait_or_abort(smem_addr(&dp_full), (uint32_t)(s & 1), limit, &abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            {
-                uint32_t raw[W];
-                tmem_ld_cols(lb + cPh, raw);
-                tmem_st_cols(lb + cPh, pw);
+                    };
+                    if (masked) weights(std::true_type{});
+                    else weights(std::false_type{});
+                }
+                // dP^T(s) into registers; its columns then take P^T (for dV) and dS^T
+                // = P^T (dP^T - delta), with the bf16 weights the dV product uses
+                if (!wait_or_abort(smem_addr(&dp_full), (uint32_t)(g & 1), limit, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                {
+                    uint32_t raw[W];
+                    tmem_ld_cols(lb + cPh, raw);
+                    tmem_st_cols(lb + cPh, pw);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(smem_addr(&p_ready));
+                    uint32_t pk[W / 2];
+                    // a masked weight is exactly 0 and its dP may be anything, so the
+                    // masked path selects 0 instead of multiplying
+                    auto grads = [&](auto mask) {
+                        constexpr bool M = decltype(mask)::value;
+#pragma unroll
+                        for (int c4 = 0; c4 < W / 4; ++c4) {
+                            const float4 d4 = vec[BM / 4 + c4];  // delta of queries q0 + 4 c4 ...
+#pragma unroll
+                            for (int e = 0; e < 4; e += 2) {
+                                const int c = 4 * c4 + e;
+                                const uint64_t nd = e ? f2_pack(-d4.z, -d4.w) : f2_pack(-d4.x, -d4.y);
+                                const float p0 = __uint_as_float(pw[c / 2] << 16), p1 = __uint_as_float(pw[c / 2] & 0xffff0000u);
+                                const uint64_t t = f2_add(f2_pack(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1])), nd);
+                                float d0, d1;
+                                f2_unpack(f2_mul(f2_pack(p0, p1), t), d0, d1);
+                                if (M) {
+                                    d0 = p0 != 0.f ? d0 : 0.f;
+                                    d1 = p1 != 0.f ? d1 : 0.f;
+                                }
+                                pk[c / 2] = pack_bf16x2(d0, d1);
+                            }
+                        }
+                    };
+                    if (masked) grads(std::true_type{});
+                    else grads(std::false_type{});
+                    mbar_arrive(smem_addr(&evec[vs]));  // this step's vectors are read
+                    tmem_st_cols(lb + cPh + W / 2, pk);
+                }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(smem_addr(&p_ready));
-                uint32_t pk[W / 2];
-                // a masked weight is exactly 0 and its dP may be anything, so the
-                // masked path selects 0 instead of multiplying
-                auto grads = [&](auto mask) {
-                    constexpr bool M = decltype(mask)::value;
-#pragma unroll
-                    for (int c4 = 0; c4 < W / 4; ++c4) {
-                        const float4 d4 = vec[BM / 4 + c4];  // delta of queries q0 + 4 c4 ...
-#pragma unroll
-                        for (int e = 0; e < 4; e += 2) {
-                            const int c = 4 * c4 + e;
-                            const uint64_t nd = e ? f2_pack(-d4.z, -d4.w) : f2_pack(-d4.x, -d4.y);
-                            const float p0 = __uint_as_float(pw[c / 2] << 16), p1 = __uint_as_float(pw[c / 2] & 0xffff0000u);
-                            const uint64_t t = f2_add(f2_pack(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1])), nd);
-                            float d0, d1;
-                            f2_unpack(f2_mul(f2_pack(p0, p1), t), d0, d1);
-                            if (M) {
-                                d0 = p0 != 0.f ? d0 : 0.f;
-                                d1 = p1 != 0.f ? d1 : 0.f;
-                            }
-                            pk[c / 2] = pack_bf16x2(d0, d1);
-                        }
-                    }
-                };
-                if (masked) grads(std::true_type{});
-                else grads(std::false_type{});
-                mbar_arrive(smem_addr(&evec[vs]));  // this step's vectors are read
-                tmem_st_cols(lb + cPh + W / 2, pk);
+                mbar_arrive(smem_addr(&ds_ready));
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(smem_addr(&ds_ready));
-        }
-        if (ok && wait_or_abort(smem_addr(&o_full), 0, limit, &abort_flag)) {
+            if (!ok || !wait_or_abort(smem_addr(&o_full), (uint32_t)(it & 1), limit, &abort_flag)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             const size_t row = ((size_t)bh * N + kj) * prm.dreal;
 #pragma unroll 1
@@ -531,9 +651,12 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tmem_ld32(lb + cK + c * 32, raw);
                 if (kj < N && nc > 0) store_row32(prm.dk, prm.g_fp32, row + c * 32, raw, prm.scale, nc);
             }
-        } else if (!abort_flag) {
-            fail_bwd(&abort_flag);
+            tc_fence_before();
+            mbar_arrive(smem_addr(&acc_empty));  // dV and dK read: the next item may overwrite them
+            if constexpr (!PERSIST) break;  // one item per CTA
+            have = item(it + 1, k0, bh, first, n_steps);
         }
+        if (!ok && !abort_flag) fail_bwd(&abort_flag);
     }
     tc_fence_before();
     __syncthreads();
@@ -544,7 +667,10 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 }
 
 // ---------------------------------------------------------------- dQ
-template <int D, bool CAUSAL>
+// A work item is one 128-query tile of one head; PERSIST as in the dK/dV
+// kernel, with the resident Q and dO and the accumulator dQ handed over
+// between items by res_empty and acc_empty.
+template <int D, bool CAUSAL, bool PERSIST>
 __global__ void __launch_bounds__(EW<D>::NUM_THREADS, 1)
 fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g, const BwdParams prm)
@@ -555,28 +681,35 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     extern __shared__ uint8_t smem_raw[];
     // per ring slot: fk/ek for K_j, fv/ev for V_j (V_j is freed by the earlier dP
     // product and loaded second, so K_j, needed first, lands sooner)
-    __shared__ __align__(8) uint64_t res_full, fk[C::NKS], ek[C::NKS], fv[C::NVS], ev[C::NVS], s_full, dp_full, s_read, ds_ready, o_full,
-        drain;
+    __shared__ __align__(8) uint64_t res_full, res_empty, fk[C::NKS], ek[C::NKS], fv[C::NVS], ev[C::NVS], s_full,
+        dp_full, s_read, ds_ready, o_full, acc_empty, drain;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = prm.N;
-    // causal: heads in groups of hgroup whose K and V fit in L2 together, one
-    // group after the other, the longest query tiles of a group first
-    int qt, bh;
-    if (CAUSAL) {
-        const int per = prm.hgroup * prm.n_q, w = (int)blockIdx.x;
-        const int g0 = (w / per) * prm.hgroup, x = w % per;
-        const int gh = min(prm.hgroup, prm.BH - g0);
-        qt = prm.n_q - 1 - x / gh;
-        bh = g0 + x % gh;
-    } else {
-        qt = (int)(blockIdx.x % prm.n_q);
-        bh = (int)(blockIdx.x / prm.n_q);
-    }
-    const int q0 = qt * BM;
-    const int n_steps = CAUSAL ? qt + 1 : prm.n_q;  // key tiles this query tile sees
+    const int n_items = prm.n_q * prm.BH;
+    // item it: query tile qt of head bh, key tiles 0 .. n_steps - 1.  Causal:
+    // heads in groups of hgroup whose K and V fit in L2 together, one group
+    // after the other, the longest query tiles of a group first
+    auto item = [&](int it, int &q0, int &bh, int &n_steps) -> bool {
+        const int w = bwd_item_index<PERSIST>(it);
+        if (w >= n_items) return false;
+        int qt;
+        if (CAUSAL) {
+            const int per = prm.hgroup * prm.n_q;
+            const int g0 = (w / per) * prm.hgroup, x = w % per;
+            const int gh = min(prm.hgroup, prm.BH - g0);
+            qt = prm.n_q - 1 - x / gh;
+            bh = g0 + x % gh;
+        } else {
+            qt = w % prm.n_q;
+            bh = w / prm.n_q;
+        }
+        q0 = qt * BM;
+        n_steps = CAUSAL ? qt + 1 : prm.n_q;  // key tiles this query tile sees
+        return true;
+    };
 
     // 1024-byte aligned base, derived from smem_raw by an offset so the
     // compiler keeps the shared address space (plain shared loads for the
@@ -589,6 +722,7 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(smem_addr(&res_full), 1);
+        mbar_init(smem_addr(&res_empty), 1);
         for (int s = 0; s < C::NKS; ++s) {
             mbar_init(smem_addr(&fk[s]), 1);
             mbar_init(smem_addr(&ek[s]), 1);
@@ -602,6 +736,7 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         mbar_init(smem_addr(&s_read), E::THREADS);
         mbar_init(smem_addr(&ds_ready), E::THREADS);
         mbar_init(smem_addr(&o_full), 1);
+        mbar_init(smem_addr(&acc_empty), E::THREADS);
         mbar_init(smem_addr(&drain), 1);
         fence_mbar_init();
     }
@@ -622,38 +757,58 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
             bool ok = true;
-            int issued_k = 0, issued_v = 0;
-            mbar_arrive_expect_tx(smem_addr(&res_full), C::RES);
-            for (int c = 0; c < C::CH; ++c) {
-                tma_load_3d(sQ + c * BOX, &tm_q, smem_addr(&res_full), c * 64, q0, bh, pol);
-                tma_load_3d(sG + c * BOX, &tm_g, smem_addr(&res_full), c * 64, q0, bh, pol);
-            }
-            for (int s = 0; s < n_steps; ++s) {
-                const int ks = s % C::NKS, vs = s % C::NVS, k0 = s * BM;
-                if (!wait_or_abort(smem_addr(&ek[ks]), (uint32_t)(((s / C::NKS) & 1) ^ 1), limit, &abort_flag)) {
-                    ok = false;
-                    break;
+            int g = 0;  // global step: ring positions run on across items
+            int issued_k = 0, issued_v = 0, res_items = 0;
+            int q0, bh, n_steps;
+            bool have = item(0, q0, bh, n_steps);
+            for (int it = 0; ok && have; ++it) {
+                // the item's resident Q and dO, once the previous item's are read: the
+                // first item's before anything else, a later one's after the first
+                // step's K (which need not wait for them)
+                auto load_res = [&]() -> bool {
+                    if (it > 0 && !wait_or_abort(smem_addr(&res_empty), (uint32_t)((it - 1) & 1), limit, &abort_flag))
+                        return false;
+                    mbar_arrive_expect_tx(smem_addr(&res_full), C::RES);
+                    for (int c = 0; c < C::CH; ++c) {
+                        tma_load_3d(sQ + c * BOX, &tm_q, smem_addr(&res_full), c * 64, q0, bh, pol);
+                        tma_load_3d(sG + c * BOX, &tm_g, smem_addr(&res_full), c * 64, q0, bh, pol);
+                    }
+                    res_items = it + 1;
+                    return true;
+                };
+                if (it == 0 && !(ok = load_res())) break;
+                for (int s = 0; s < n_steps; ++s, ++g) {
+                    const int ks = g % C::NKS, vs = g % C::NVS, k0 = s * BM;
+                    if (!wait_or_abort(smem_addr(&ek[ks]), (uint32_t)(((g / C::NKS) & 1) ^ 1), limit, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bk = smem_addr(&fk[ks]);
+                    mbar_arrive_expect_tx(bk, C::TILE);
+                    for (int c = 0; c < C::CH; ++c)
+                        tma_load_3d(sKr + ks * C::TILE + c * BOX, &tm_k, bk, c * 64, k0, bh, pol);
+                    issued_k = g + 1;
+                    if (s == 0 && it > 0 && !(ok = load_res())) break;
+                    if (!wait_or_abort(smem_addr(&ev[vs]), (uint32_t)(((g / C::NVS) & 1) ^ 1), limit, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bv = smem_addr(&fv[vs]);
+                    mbar_arrive_expect_tx(bv, C::TILE);
+                    for (int c = 0; c < C::CH; ++c)
+                        tma_load_3d(sVr + vs * C::TILE + c * BOX, &tm_v, bv, c * 64, k0, bh, pol);
+                    issued_v = g + 1;
                 }
-                const uint32_t bk = smem_addr(&fk[ks]);
-                mbar_arrive_expect_tx(bk, C::TILE);
-                for (int c = 0; c < C::CH; ++c) tma_load_3d(sKr + ks * C::TILE + c * BOX, &tm_k, bk, c * 64, k0, bh, pol);
-                issued_k = s + 1;
-                if (!wait_or_abort(smem_addr(&ev[vs]), (uint32_t)(((s / C::NVS) & 1) ^ 1), limit, &abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t bv = smem_addr(&fv[vs]);
-                mbar_arrive_expect_tx(bv, C::TILE);
-                for (int c = 0; c < C::CH; ++c) tma_load_3d(sVr + vs * C::TILE + c * BOX, &tm_v, bv, c * 64, k0, bh, pol);
-                issued_v = s + 1;
+                if constexpr (!PERSIST) break;  // one item per CTA
+                have = item(it + 1, q0, bh, n_steps);
             }
             if (!ok) {
                 if (!abort_flag) fail_bwd(&abort_flag);
-                for (int s = (issued_k > C::NKS ? issued_k - C::NKS : 0); s < issued_k; ++s)
-                    mbar_wait_bounded(smem_addr(&fk[s % C::NKS]), (uint32_t)((s / C::NKS) & 1), limit);
-                for (int s = (issued_v > C::NVS ? issued_v - C::NVS : 0); s < issued_v; ++s)
-                    mbar_wait_bounded(smem_addr(&fv[s % C::NVS]), (uint32_t)((s / C::NVS) & 1), limit);
-                mbar_wait_bounded(smem_addr(&res_full), 0, limit);
+                for (int x = (issued_k > C::NKS ? issued_k - C::NKS : 0); x < issued_k; ++x)
+                    mbar_wait_bounded(smem_addr(&fk[x % C::NKS]), (uint32_t)((x / C::NKS) & 1), limit);
+                for (int x = (issued_v > C::NVS ? issued_v - C::NVS : 0); x < issued_v; ++x)
+                    mbar_wait_bounded(smem_addr(&fv[x % C::NVS]), (uint32_t)((x / C::NVS) & 1), limit);
+                if (res_items > 0) mbar_wait_bounded(smem_addr(&res_full), (uint32_t)((res_items - 1) & 1), limit);
             }
         }
         __syncwarp();
@@ -661,21 +816,21 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         {  // whole warp, converged; elect.sync picks the issuing lane
             const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0), id_o = idesc_bf16_f32(BM, D, 0, 1);
             const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), dG = sdesc_sw128(sG, 16, 1024);
-            bool ok = wait_or_abort_w(smem_addr(&res_full), 0, limit, &abort_flag), issued = false;
-            // K_s in ring slot s % KQ, V_s in slot s % 2
-            auto wait_k = [&](int s) -> bool {
-                if (!wait_or_abort_w(smem_addr(&fk[s % C::NKS]), (uint32_t)((s / C::NKS) & 1), limit, &abort_flag)) return false;
+            bool ok = true, issued = false;
+            // K_g in ring slot g % NKS, V_g in slot g % NVS (g a global step)
+            auto wait_k = [&](int g) -> bool {
+                if (!wait_or_abort_w(smem_addr(&fk[g % C::NKS]), (uint32_t)((g / C::NKS) & 1), limit, &abort_flag)) return false;
                 tc_fence_after();
                 return true;
             };
-            auto wait_v = [&](int s) -> bool {
-                if (!wait_or_abort_w(smem_addr(&fv[s % C::NVS]), (uint32_t)((s / C::NVS) & 1), limit, &abort_flag)) return false;
+            auto wait_v = [&](int g) -> bool {
+                if (!wait_or_abort_w(smem_addr(&fv[g % C::NVS]), (uint32_t)((g / C::NVS) & 1), limit, &abort_flag)) return false;
                 tc_fence_after();
                 return true;
             };
-            // S(s) = Q K_s^T into cS; dP(s) = dO V_s^T into cP
-            auto mma_s = [&](int s) {
-                const uint64_t dK = sdesc_sw128(sKr + (s % C::NKS) * C::TILE, 16, 1024);
+            // S(g) = Q K_g^T into cS; dP(g) = dO V_g^T into cP
+            auto mma_s = [&](int g) {
+                const uint64_t dK = sdesc_sw128(sKr + (g % C::NKS) * C::TILE, 16, 1024);
                 uint64_t ka[D / 16], kb[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -686,8 +841,8 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 mma_ss_k<D / 16>(tmem + cS, ka, kb, id_s, 0u);
                 issued = true;
             };
-            auto mma_dp = [&](int s) {
-                const uint64_t dV = sdesc_sw128(sVr + (s % C::NVS) * C::TILE, 16, 1024);
+            auto mma_dp = [&](int g) {
+                const uint64_t dV = sdesc_sw128(sVr + (g % C::NVS) * C::TILE, 16, 1024);
                 uint64_t ka[D / 16], kb[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -697,52 +852,112 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 }
                 mma_ss_k<D / 16>(tmem + cP, ka, kb, id_s, 0u);
             };
-            if (ok && (ok = wait_k(0))) {
-                mma_s(0);
-                mma_commit_w(smem_addr(&s_full));
-                if ((ok = wait_v(0))) {
-                    mma_dp(0);
-                    mma_commit_w(smem_addr(&dp_full));
-                    mma_commit_w(smem_addr(&ev[0]));  // V_0 read for the last time
+            // dQ += dS K_g (A: dS over the dP columns, B: K_g MN-major); the first
+            // step of an item overwrites
+            auto mma_dq = [&](int g, int s) {
+                const uint64_t dKmn = sdesc_sw128(sKr + (g % C::NKS) * C::TILE, BOX, 1024);
+                uint32_t ta[BM / 16];
+                uint64_t tb[BM / 16];
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk) {
+                    ta[kk] = tmem + a_col<W>(cP, kk);
+                    tb[kk] = dKmn + (uint64_t)((kk * 16 * 128) >> 4);
                 }
-            }
-            // Per step: S(s+1) as soon as the softmax warps have read S(s) (it
-            // overlaps their dS(s)); dQ(s) once dS(s) is written over dP(s);
-            // then dP(s+1) into the columns dQ(s) has just read.
-            for (int s = 0; ok && s < n_steps; ++s) {
-                const bool more = s + 1 < n_steps;
-                if (more) {
-                    if (!wait_or_abort_w(smem_addr(&s_read), (uint32_t)(s & 1), limit, &abort_flag) || !wait_k(s + 1)) {
+                mma_ts_k<BM / 16>(tmem + cQ, ta, tb, id_o, s > 0 ? 1u : 0u);
+            };
+            if constexpr (!PERSIST) {
+                // One item.  (The item loop below, run for one item, measured 4 %
+                // slower on long sequences than this plain loop.)
+                int q0, bh, n_steps;
+                item(0, q0, bh, n_steps);
+                ok = wait_or_abort_w(smem_addr(&res_full), 0, limit, &abort_flag);
+                if (ok && (ok = wait_k(0))) {
+                    mma_s(0);
+                    mma_commit_w(smem_addr(&s_full));
+                    if ((ok = wait_v(0))) {
+                        mma_dp(0);
+                        mma_commit_w(smem_addr(&dp_full));
+                        mma_commit_w(smem_addr(&ev[0]));  // V_0 read for the last time
+                    }
+                }
+                // Per step: S(s+1) as soon as the softmax warps have read S(s) (it
+                // overlaps their dS(s)); dQ(s) once dS(s) is written over dP(s);
+                // then dP(s+1) into the columns dQ(s) has just read.
+                for (int s = 0; ok && s < n_steps; ++s) {
+                    const bool more = s + 1 < n_steps;
+                    if (more) {
+                        if (!wait_or_abort_w(smem_addr(&s_read), (uint32_t)(s & 1), limit, &abort_flag) || !wait_k(s + 1)) {
+                            ok = false;
+                            break;
+                        }
+                        mma_s(s + 1);
+                        mma_commit_w(smem_addr(&s_full));
+                    }
+                    if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    mma_dq(s, s);
+                    mma_commit_w(smem_addr(&ek[s % C::NKS]));  // K_s read for the last time
+                    if (more) {
+                        if (!wait_v(s + 1)) { ok = false; break; }
+                        mma_dp(s + 1);
+                        mma_commit_w(smem_addr(&dp_full));
+                        mma_commit_w(smem_addr(&ev[(s + 1) % C::NVS]));  // V_(s+1) read for the last time
+                    }
+                }
+                if (ok) mma_commit_w(smem_addr(&o_full));
+            } else {
+                // Items one after the other, steps numbered globally, handed over as
+                // in the dK/dV kernel (res_full / res_empty, acc_empty).
+                int g = 0;
+                int q0, bh, n_steps;
+                bool have = item(0, q0, bh, n_steps);
+                for (int it = 0; ok && have; ++it) {
+                    if (!wait_or_abort_w(smem_addr(&res_full), (uint32_t)(it & 1), limit, &abort_flag) ||
+                        (g > 0 && !wait_or_abort_w(smem_addr(&s_read), (uint32_t)((g - 1) & 1), limit, &abort_flag)) ||
+                        !wait_k(g)) {
                         ok = false;
                         break;
                     }
-                    mma_s(s + 1);
+                    mma_s(g);
                     mma_commit_w(smem_addr(&s_full));
-                }
-                if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                const uint64_t dKmn = sdesc_sw128(sKr + (s % C::NKS) * C::TILE, BOX, 1024);
-                {
-                    uint32_t ta[BM / 16];
-                    uint64_t tb[BM / 16];
-#pragma unroll
-                    for (int kk = 0; kk < BM / 16; ++kk) {
-                        ta[kk] = tmem + a_col<W>(cP, kk);
-                        tb[kk] = dKmn + (uint64_t)((kk * 16 * 128) >> 4);
-                    }
-                    mma_ts_k<BM / 16>(tmem + cQ, ta, tb, id_o, s > 0 ? 1u : 0u);
-                }
-                mma_commit_w(smem_addr(&ek[s % C::NKS]));  // K_s read for the last time
-                if (more) {
-                    if (!wait_v(s + 1)) { ok = false; break; }
-                    mma_dp(s + 1);
+                    if (!wait_v(g)) { ok = false; break; }
+                    mma_dp(g);
                     mma_commit_w(smem_addr(&dp_full));
-                    mma_commit_w(smem_addr(&ev[(s + 1) % C::NVS]));  // V_(s+1) read for the last time
+                    mma_commit_w(smem_addr(&ev[g % C::NVS]));  // V_g read for the last time
+                    if (n_steps == 1) mma_commit_w(smem_addr(&res_empty));  // Q and dO read for the last time
+                    for (int s = 0; s < n_steps; ++s, ++g) {
+                        const bool more = s + 1 < n_steps;
+                        if (more) {
+                            if (!wait_or_abort_w(smem_addr(&s_read), (uint32_t)(g & 1), limit, &abort_flag) || !wait_k(g + 1)) {
+                                ok = false;
+                                break;
+                            }
+                            mma_s(g + 1);
+                            mma_commit_w(smem_addr(&s_full));
+                        }
+                        if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(g & 1), limit, &abort_flag) ||
+                            (s == 0 && it > 0 &&
+                             !wait_or_abort_w(smem_addr(&acc_empty), (uint32_t)((it - 1) & 1), limit, &abort_flag))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        mma_dq(g, s);
+                        mma_commit_w(smem_addr(&ek[g % C::NKS]));  // K_g read for the last time
+                        if (more) {
+                            if (!wait_v(g + 1)) { ok = false; break; }
+                            mma_dp(g + 1);
+                            mma_commit_w(smem_addr(&dp_full));
+                            mma_commit_w(smem_addr(&ev[(g + 1) % C::NVS]));  // V_(g+1) read for the last time
+                            if (s + 2 == n_steps) mma_commit_w(smem_addr(&res_empty));  // Q and dO read for the last time
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit_w(smem_addr(&o_full));  // this item's dQ is complete
+                    have = item(it + 1, q0, bh, n_steps);
                 }
             }
-            if (ok) {
-                mma_commit_w(smem_addr(&o_full));
-            } else {
+            if (!ok) {
                 if (!abort_flag) fail_bwd(&abort_flag);
                 if (issued) {
                     mma_commit_w(smem_addr(&drain));
@@ -754,79 +969,87 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     } else {
         // one query per thread (tensor-memory lane), keys [W hf, W hf + W) of each tile
         const int quarter = warp & 3, hf = warp >> 2;
-        const int r = quarter * 32 + lane, qi = q0 + r;
+        const int r = quarter * 32 + lane;
         const uint32_t lb = tmem + ((uint32_t)(quarter * 32) << 16);
         const uint32_t cSh = cS + hf * W, cPh = cP + hf * W;
         const float sl = prm.sl;
-        const float l2 = qi < N ? prm.lse2[(size_t)bh * prm.pitch + qi] : 0.f;
-        const float de = qi < N ? prm.delta[(size_t)bh * prm.pitch + qi] : 0.f;
         bool ok = true;
-        for (int s = 0; s < n_steps; ++s) {
-            const int k0 = s * BM + hf * W;
-            if (!wait_or_abort(smem_addr(&s_full), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            // Tiles with no padded key or query and wholly below the diagonal
-            // take the unmasked path (no per-element tests or selects).
-            const int kt0 = s * BM;
-            const bool masked = kt0 + BM > N || q0 + BM > N || (CAUSAL && kt0 + BM > q0);
-            float p[W];
-            {
-                uint32_t raw[W];
-                tmem_ld_cols(lb + cSh, raw);
+        int g = 0;
+        int q0, bh, n_steps;
+        bool have = item(0, q0, bh, n_steps);
+        for (int it = 0; ok && have; ++it) {
+            const int qi = q0 + r;
+            const float l2 = qi < N ? prm.lse2[(size_t)bh * prm.pitch + qi] : 0.f;
+            const float de = qi < N ? prm.delta[(size_t)bh * prm.pitch + qi] : 0.f;
+            for (int s = 0; s < n_steps; ++s, ++g) {
+                const int k0 = s * BM + hf * W;
+                if (!wait_or_abort(smem_addr(&s_full), (uint32_t)(g & 1), limit, &abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                // Tiles with no padded key or query and wholly below the diagonal
+                // take the unmasked path (no per-element tests or selects).
+                const int kt0 = s * BM;
+                const bool masked = kt0 + BM > N || q0 + BM > N || (CAUSAL && kt0 + BM > q0);
+                float p[W];
+                {
+                    uint32_t raw[W];
+                    tmem_ld_cols(lb + cSh, raw);
+                    tc_fence_before();
+                    mbar_arrive(smem_addr(&s_read));  // S(s) is in registers: the MMA may overwrite it
+                    const uint64_t sl2 = f2_pack(sl, sl), nl2 = f2_pack(-l2, -l2);
+                    auto weights = [&](auto mask) {
+                        constexpr bool M = decltype(mask)::value;
+#pragma unroll
+                        for (int c = 0; c < W; c += 2) {
+                            float a0, a1;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1])), sl2, nl2), a0, a1);
+                            const float w0 = ex2(a0), w1 = ex2(a1);
+                            if (M) {
+                                const int kj = k0 + c;
+                                p[c] = (qi < N && kj < N && (!CAUSAL || kj <= qi)) ? w0 : 0.f;
+                                p[c + 1] = (qi < N && kj + 1 < N && (!CAUSAL || kj + 1 <= qi)) ? w1 : 0.f;
+                            } else {
+                                p[c] = w0;
+                                p[c + 1] = w1;
+                            }
+                        }
+                    };
+                    if (masked) weights(std::true_type{});
+                    else weights(std::false_type{});
+                }
+                if (!wait_or_abort(smem_addr(&dp_full), (uint32_t)(g & 1), limit, &abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                {
+                    uint32_t raw[W];
+                    tmem_ld_cols(lb + cPh, raw);
+                    uint32_t pk[W / 2];
+                    const uint64_t nd2 = f2_pack(-de, -de);
+                    auto grads = [&](auto mask) {
+                        constexpr bool M = decltype(mask)::value;
+#pragma unroll
+                        for (int x = 0; x < W / 2; ++x) {
+                            const int c = 2 * x;
+                            const uint64_t t = f2_add(f2_pack(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1])), nd2);
+                            float d0, d1;
+                            f2_unpack(f2_mul(f2_pack(p[c], p[c + 1]), t), d0, d1);
+                            if (M) {
+                                d0 = p[c] != 0.f ? d0 : 0.f;
+                                d1 = p[c + 1] != 0.f ? d1 : 0.f;
+                            }
+                            pk[x] = pack_bf16x2(d0, d1);
+                        }
+                    };
+                    if (masked) grads(std::true_type{});
+                    else grads(std::false_type{});
+                    tmem_st_cols(lb + cPh, pk);  // dS over the dP columns already read
+                }
+                tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(smem_addr(&s_read));  // S(s) is in registers: the MMA may overwrite it
-                const uint64_t sl2 = f2_pack(sl, sl), nl2 = f2_pack(-l2, -l2);
-                auto weights = [&](auto mask) {
-                    constexpr bool M = decltype(mask)::value;
-#pragma unroll
-                    for (int c = 0; c < W; c += 2) {
-                        float a0, a1;
-                        f2_unpack(f2_fma(f2_pack(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1])), sl2, nl2), a0, a1);
-                        const float w0 = ex2(a0), w1 = ex2(a1);
-                        if (M) {
-                            const int kj = k0 + c;
-                            p[c] = (qi < N && kj < N && (!CAUSAL || kj <= qi)) ? w0 : 0.f;
-                            p[c + 1] = (qi < N && kj + 1 < N && (!CAUSAL || kj + 1 <= qi)) ? w1 : 0.f;
-                        } else {
-                            p[c] = w0;
-                            p[c + 1] = w1;
-                        }
-                    }
-                };
-                if (masked) weights(std::true_type{});
-                else weights(std::false_type{});
+                mbar_arrive(smem_addr(&ds_ready));
             }
-            if (!wait_or_abort(smem_addr(&dp_full), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            {
-                uint32_t raw[W];
-                tmem_ld_cols(lb + cPh, raw);
-                uint32_t pk[W / 2];
-                const uint64_t nd2 = f2_pack(-de, -de);
-                auto grads = [&](auto mask) {
-                    constexpr bool M = decltype(mask)::value;
-#pragma unroll
-                    for (int x = 0; x < W / 2; ++x) {
-                        const int c = 2 * x;
-                        const uint64_t t = f2_add(f2_pack(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1])), nd2);
-                        float d0, d1;
-                        f2_unpack(f2_mul(f2_pack(p[c], p[c + 1]), t), d0, d1);
-                        if (M) {
-                            d0 = p[c] != 0.f ? d0 : 0.f;
-                            d1 = p[c + 1] != 0.f ? d1 : 0.f;
-                        }
-                        pk[x] = pack_bf16x2(d0, d1);
-                    }
-                };
-                if (masked) grads(std::true_type{});
-                else grads(std::false_type{});
-                tmem_st_cols(lb + cPh, pk);  // dS over the dP columns already read
+            if (!ok || !wait_or_abort(smem_addr(&o_full), (uint32_t)(it & 1), limit, &abort_flag)) {
+                ok = false;
+                break;
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(smem_addr(&ds_ready));
-        }
-        if (ok && wait_or_abort(smem_addr(&o_full), 0, limit, &abort_flag)) {
             tc_fence_after();
             const size_t row = ((size_t)bh * N + qi) * prm.dreal;
 #pragma unroll 1
@@ -836,9 +1059,12 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 tmem_ld32(lb + cQ + c * 32, raw);
                 if (qi < N && nc > 0) store_row32(prm.dq, prm.g_fp32, row + c * 32, raw, prm.scale, nc);
             }
-        } else if (!abort_flag) {
-            fail_bwd(&abort_flag);
+            tc_fence_before();
+            mbar_arrive(smem_addr(&acc_empty));  // dQ read: the next item may overwrite it
+            if constexpr (!PERSIST) break;  // one item per CTA
+            have = item(it + 1, q0, bh, n_steps);
         }
+        if (!ok && !abort_flag) fail_bwd(&abort_flag);
     }
     tc_fence_before();
     __syncthreads();
@@ -912,12 +1138,21 @@ cudaError_t launch_dims(const BackwardProblem &p, float *delta, float *lse2, int
     prm.dk = p.dk;
     prm.dv = p.dv;
     prm.g_fp32 = p.grad_dtype == 1;
-    auto kv = fa_bwd_dkdv_tc<D, CAUSAL>;
-    auto kq = fa_bwd_dq_tc<D, CAUSAL>;
-    cudaError_t e;
+    // Short items (at most PERSIST_MAX_TILES streamed tiles each) on persistent
+    // CTAs, one per SM, when there are more of them than SMs: each item's
+    // prologue (resident loads, first score products) and epilogue then overlap
+    // its neighbours' steps.  Longer items run one per CTA.
+    cudaError_t e = cudaSuccess;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int64_t items = (int64_t)prm.n_q * BH;
+    const bool persist = prm.n_q <= PERSIST_MAX_TILES && items > sms;
+    auto kv = persist ? fa_bwd_dkdv_tc<D, CAUSAL, true> : fa_bwd_dkdv_tc<D, CAUSAL, false>;
+    auto kq = persist ? fa_bwd_dq_tc<D, CAUSAL, true> : fa_bwd_dq_tc<D, CAUSAL, false>;
     if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_KV_REQ)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_Q_REQ)) != cudaSuccess) return e;
-    const unsigned grid = (unsigned)((int64_t)prm.n_q * BH);
+    const unsigned grid = (unsigned)(persist ? std::min<int64_t>(items, sms) : items);
     kv<<<grid, EW<D>::NUM_THREADS, C::SMEM_KV_REQ, stream>>>(mq, mk, mv, mg, prm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     kq<<<grid, EW<D>::NUM_THREADS, C::SMEM_Q_REQ, stream>>>(mq, mk, mv, mg, prm);
