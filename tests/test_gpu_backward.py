@@ -121,13 +121,16 @@ def test_narrow_head_backward_on_tensor_cores(N, d, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("B,H,N,d", [(2, 80, 300, 64), (2, 80, 300, 128), (1, 80, 2000, 128), (2, 40, 513, 40)])
+@pytest.mark.parametrize("B,H,N,d", [(2, 80, 300, 64), (2, 80, 300, 128), (1, 80, 2000, 128), (2, 40, 513, 40),
+                                     (1, 8, 3000, 64)])
 def test_persistent_backward_ctas(B, H, N, d, causal):
-    """More items (128-row tiles x heads) than SMs, each of at most 16 tiles:
-    the dK/dV and dQ kernels run on persistent CTAs that loop over items,
-    handing the resident tiles and the accumulators over between them.  Every
-    gradient element against the oracle."""
-    assert (N + 127) // 128 <= 16 and (N + 127) // 128 * B * H > 152
+    """More items (128-row tiles x heads) than SMs, each of at most 2048
+    tile-columns (16 tiles at d = 128, 32 at d = 64): the dK/dV and dQ kernels
+    run on persistent CTAs that loop over items, handing the resident tiles and
+    the accumulators over between them.  Every gradient element against the
+    oracle."""
+    n_t, width = (N + 127) // 128, 64 if d <= 64 else 128
+    assert n_t * width <= 2048 and n_t * B * H > 152
     stats, path = run_backward(B, H, N, d, "bf16", causal, seed=8600 + N + d)
     assert path == "tensor-core", path
 

@@ -72,7 +72,7 @@ struct EW {
     static constexpr int MMA_WARP = WARPS + 1;
 };
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int PERSIST_MAX_TILES = 16;  // persistent CTAs for items of at most this many steps
+constexpr int PERSIST_MAX_COLS = 2048;  // persistent CTAs for items of at most this many tiles x d
 constexpr uint32_t BOX = 128 * 128;  // one 128-row x 64-column bf16 box
 constexpr uint32_t VEC_BYTES = 1024;  // lse2 and delta of 128 rows
 
@@ -1138,16 +1138,17 @@ cudaError_t launch_dims(const BackwardProblem &p, float *delta, float *lse2, int
     prm.dk = p.dk;
     prm.dv = p.dv;
     prm.g_fp32 = p.grad_dtype == 1;
-    // Short items (at most PERSIST_MAX_TILES streamed tiles each) on persistent
-    // CTAs, one per SM, when there are more of them than SMs: each item's
-    // prologue (resident loads, first score products) and epilogue then overlap
-    // its neighbours' steps.  Longer items run one per CTA.
+    // Short items (at most PERSIST_MAX_COLS streamed tiles x d: 16 tiles at
+    // d = 128, 32 at d = 64) on persistent CTAs, one per SM, when there are more
+    // of them than SMs: each item's prologue (resident loads, first score
+    // products) and epilogue then overlap its neighbours' steps.  Longer items
+    // run one per CTA (persistent, they measured -1 to -7 % at d = 128).
     cudaError_t e = cudaSuccess;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int64_t items = (int64_t)prm.n_q * BH;
-    const bool persist = prm.n_q <= PERSIST_MAX_TILES && items > sms;
+    const bool persist = prm.n_q * D <= PERSIST_MAX_COLS && items > sms;
     auto kv = persist ? fa_bwd_dkdv_tc<D, CAUSAL, true> : fa_bwd_dkdv_tc<D, CAUSAL, false>;
     auto kq = persist ? fa_bwd_dq_tc<D, CAUSAL, true> : fa_bwd_dq_tc<D, CAUSAL, false>;
     if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_KV_REQ)) != cudaSuccess) return e;
