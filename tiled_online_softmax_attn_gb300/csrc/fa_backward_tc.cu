@@ -196,6 +196,18 @@ __device__ __forceinline__ int bwd_item_index(int it)
     return it * G + ((it & 1) ? G - 1 - c : c);
 }
 
+// Slot and phase parity of a ring of N slots at some step, advanced one step
+// at a time (no division by N in the issue loops).
+struct RingPos {
+    int slot;
+    uint32_t phase;
+};
+template <int N>
+__device__ __forceinline__ RingPos ring_next(RingPos p)
+{
+    return p.slot + 1 == N ? RingPos{0, p.phase ^ 1u} : RingPos{p.slot + 1, p.phase};
+}
+
 // ---------------------------------------------------------------- dK / dV
 // A work item is one 128-key tile of one head.  With PERSIST a CTA loops over
 // several: the steps (query tiles) of all its items are numbered globally, so
@@ -374,9 +386,10 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0), id_o = idesc_bf16_f32(BM, D, 0, 1);
             const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
             bool ok = true, issued = false;
-            // S^T(g) = K Q_g^T into cS, dP^T(g) = V dO_g^T into cP (g a global step)
-            auto mma_st = [&](int g) {
-                const uint64_t dQ = sdesc_sw128(sQr + (g % C::NQS) * C::TILE, 16, 1024);
+            // S^T(g) = K Q_g^T into cS, dP^T(g) = V dO_g^T into cP (g a global step;
+            // the _at forms take the ring slot)
+            auto mma_st_at = [&](int slot) {
+                const uint64_t dQ = sdesc_sw128(sQr + slot * C::TILE, 16, 1024);
                 uint64_t ka[D / 16], kb[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -387,8 +400,8 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 mma_ss_k<D / 16>(tmem + cS, ka, kb, id_s, 0u);
                 issued = true;
             };
-            auto mma_dpt = [&](int g) {
-                const uint64_t dG = sdesc_sw128(sGr + (g % C::NGS) * C::TILE, 16, 1024);
+            auto mma_dpt_at = [&](int slot) {
+                const uint64_t dG = sdesc_sw128(sGr + slot * C::TILE, 16, 1024);
                 uint64_t ka[D / 16], kb[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -398,6 +411,8 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 mma_ss_k<D / 16>(tmem + cP, ka, kb, id_s, 0u);
             };
+            auto mma_st = [&](int g) { mma_st_at(g % C::NQS); };
+            auto mma_dpt = [&](int g) { mma_dpt_at(g % C::NGS); };
             // dV += P^T dO_g (A: the P^T columns of cP) or dK += dS^T Q_g (A: the
             // dS^T columns, 32 further), B MN-major from its ring slot; the first
             // step of an item overwrites
@@ -412,16 +427,13 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 mma_ts_k<BM / 16>(tmem + d_col, ta, tb, id_o, s > 0 ? 1u : 0u);
             };
             // Q_g in ring slot g % NQS, dO_g in slot g % NGS
-            auto wait_q = [&](int g) -> bool {
-                if (!wait_or_abort_w(smem_addr(&fq[g % C::NQS]), (uint32_t)((g / C::NQS) & 1), limit, &abort_flag)) return false;
+            auto wait_at = [&](uint64_t *full, RingPos p) -> bool {
+                if (!wait_or_abort_w(smem_addr(&full[p.slot]), p.phase, limit, &abort_flag)) return false;
                 tc_fence_after();
                 return true;
             };
-            auto wait_g = [&](int g) -> bool {
-                if (!wait_or_abort_w(smem_addr(&fg[g % C::NGS]), (uint32_t)((g / C::NGS) & 1), limit, &abort_flag)) return false;
-                tc_fence_after();
-                return true;
-            };
+            auto wait_q = [&](int g) { return wait_at(fq, RingPos{g % C::NQS, (uint32_t)((g / C::NQS) & 1)}); };
+            auto wait_g = [&](int g) { return wait_at(fg, RingPos{g % C::NGS, (uint32_t)((g / C::NGS) & 1)}); };
             if constexpr (!PERSIST) {
                 // One item.  (The item loop below, run for one item, measured 4 %
                 // slower on long sequences than this plain loop.)
@@ -469,51 +481,56 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 // two score products wait for its resident K and V (and for the
                 // previous S^T to be in registers); its first dV product waits until
                 // the previous item's dV and dK have left tensor memory.
-                int g = 0;
+                RingPos q{0, 0u}, gq{0, 0u};  // Q and dO ring positions of the step in work
+                uint32_t par = 0;              // parity of the step in work (per-step barriers)
                 int k0, bh, first, n_steps;
                 bool have = item(0, k0, bh, first, n_steps);
                 for (int it = 0; ok && have; ++it) {
                     if (!wait_or_abort_w(smem_addr(&res_full), (uint32_t)(it & 1), limit, &abort_flag) ||
-                        (g > 0 && !wait_or_abort_w(smem_addr(&s_read), (uint32_t)((g - 1) & 1), limit, &abort_flag)) ||
-                        !wait_q(g)) {
+                        (it > 0 && !wait_or_abort_w(smem_addr(&s_read), par ^ 1u, limit, &abort_flag)) ||
+                        !wait_at(fq, q)) {
                         ok = false;
                         break;
                     }
-                    mma_st(g);
+                    mma_st_at(q.slot);
                     mma_commit_w(smem_addr(&st_full));
-                    if (!wait_g(g)) { ok = false; break; }
-                    mma_dpt(g);
+                    if (!wait_at(fg, gq)) { ok = false; break; }
+                    mma_dpt_at(gq.slot);
                     mma_commit_w(smem_addr(&dp_full));
                     if (n_steps == 1) mma_commit_w(smem_addr(&res_empty));  // K and V read for the last time
-                    for (int s = 0; s < n_steps; ++s, ++g) {
+                    for (int s = 0; s < n_steps; ++s) {
                         const bool more = s + 1 < n_steps;
+                        const RingPos q1 = ring_next<C::NQS>(q), gq1 = ring_next<C::NGS>(gq);
                         if (more) {
-                            if (!wait_or_abort_w(smem_addr(&s_read), (uint32_t)(g & 1), limit, &abort_flag) || !wait_q(g + 1)) {
+                            if (!wait_or_abort_w(smem_addr(&s_read), par, limit, &abort_flag) || !wait_at(fq, q1)) {
                                 ok = false;
                                 break;
                             }
-                            mma_st(g + 1);
+                            mma_st_at(q1.slot);
                             mma_commit_w(smem_addr(&st_full));
                         }
-                        if (!wait_or_abort_w(smem_addr(&p_ready), (uint32_t)(g & 1), limit, &abort_flag) ||
+                        if (!wait_or_abort_w(smem_addr(&p_ready), par, limit, &abort_flag) ||
                             (s == 0 && it > 0 &&
                              !wait_or_abort_w(smem_addr(&acc_empty), (uint32_t)((it - 1) & 1), limit, &abort_flag))) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        mma_acc(cV, cP, sdesc_sw128(sGr + (g % C::NGS) * C::TILE, BOX, 1024), s);
-                        mma_commit_w(smem_addr(&eg[g % C::NGS]));  // dO_g read for the last time
-                        if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(g & 1), limit, &abort_flag)) { ok = false; break; }
+                        mma_acc(cV, cP, sdesc_sw128(sGr + gq.slot * C::TILE, BOX, 1024), s);
+                        mma_commit_w(smem_addr(&eg[gq.slot]));  // dO of this step read for the last time
+                        if (!wait_or_abort_w(smem_addr(&ds_ready), par, limit, &abort_flag)) { ok = false; break; }
                         tc_fence_after();
-                        mma_acc(cK, cP + W / 2, sdesc_sw128(sQr + (g % C::NQS) * C::TILE, BOX, 1024), s);
-                        mma_commit_w(smem_addr(&eq[g % C::NQS]));  // Q_g read for the last time
+                        mma_acc(cK, cP + W / 2, sdesc_sw128(sQr + q.slot * C::TILE, BOX, 1024), s);
+                        mma_commit_w(smem_addr(&eq[q.slot]));  // Q of this step read for the last time
                         if (more) {
-                            if (!wait_g(g + 1)) { ok = false; break; }
-                            mma_dpt(g + 1);
+                            if (!wait_at(fg, gq1)) { ok = false; break; }
+                            mma_dpt_at(gq1.slot);
                             mma_commit_w(smem_addr(&dp_full));
                             if (s + 2 == n_steps) mma_commit_w(smem_addr(&res_empty));  // K and V read for the last time
                         }
+                        q = q1;
+                        gq = gq1;
+                        par ^= 1u;
                     }
                     if (!ok) break;
                     mma_commit_w(smem_addr(&o_full));  // this item's dV and dK are complete
@@ -817,20 +834,18 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0), id_o = idesc_bf16_f32(BM, D, 0, 1);
             const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), dG = sdesc_sw128(sG, 16, 1024);
             bool ok = true, issued = false;
-            // K_g in ring slot g % NKS, V_g in slot g % NVS (g a global step)
-            auto wait_k = [&](int g) -> bool {
-                if (!wait_or_abort_w(smem_addr(&fk[g % C::NKS]), (uint32_t)((g / C::NKS) & 1), limit, &abort_flag)) return false;
+            // K_g in ring slot g % NKS, V_g in slot g % NVS (g a global step; the _at
+            // forms take the ring slot)
+            auto wait_at = [&](uint64_t *full, RingPos p) -> bool {
+                if (!wait_or_abort_w(smem_addr(&full[p.slot]), p.phase, limit, &abort_flag)) return false;
                 tc_fence_after();
                 return true;
             };
-            auto wait_v = [&](int g) -> bool {
-                if (!wait_or_abort_w(smem_addr(&fv[g % C::NVS]), (uint32_t)((g / C::NVS) & 1), limit, &abort_flag)) return false;
-                tc_fence_after();
-                return true;
-            };
+            auto wait_k = [&](int g) { return wait_at(fk, RingPos{g % C::NKS, (uint32_t)((g / C::NKS) & 1)}); };
+            auto wait_v = [&](int g) { return wait_at(fv, RingPos{g % C::NVS, (uint32_t)((g / C::NVS) & 1)}); };
             // S(g) = Q K_g^T into cS; dP(g) = dO V_g^T into cP
-            auto mma_s = [&](int g) {
-                const uint64_t dK = sdesc_sw128(sKr + (g % C::NKS) * C::TILE, 16, 1024);
+            auto mma_s_at = [&](int slot) {
+                const uint64_t dK = sdesc_sw128(sKr + slot * C::TILE, 16, 1024);
                 uint64_t ka[D / 16], kb[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -841,8 +856,8 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 mma_ss_k<D / 16>(tmem + cS, ka, kb, id_s, 0u);
                 issued = true;
             };
-            auto mma_dp = [&](int g) {
-                const uint64_t dV = sdesc_sw128(sVr + (g % C::NVS) * C::TILE, 16, 1024);
+            auto mma_dp_at = [&](int slot) {
+                const uint64_t dV = sdesc_sw128(sVr + slot * C::TILE, 16, 1024);
                 uint64_t ka[D / 16], kb[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -852,10 +867,12 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 }
                 mma_ss_k<D / 16>(tmem + cP, ka, kb, id_s, 0u);
             };
-            // dQ += dS K_g (A: dS over the dP columns, B: K_g MN-major); the first
-            // step of an item overwrites
-            auto mma_dq = [&](int g, int s) {
-                const uint64_t dKmn = sdesc_sw128(sKr + (g % C::NKS) * C::TILE, BOX, 1024);
+            auto mma_s = [&](int g) { mma_s_at(g % C::NKS); };
+            auto mma_dp = [&](int g) { mma_dp_at(g % C::NVS); };
+            // dQ += dS K (A: dS over the dP columns, B: the K tile of ring slot
+            // `slot`, MN-major); the first step of an item overwrites
+            auto mma_dq = [&](int slot, int s) {
+                const uint64_t dKmn = sdesc_sw128(sKr + slot * C::TILE, BOX, 1024);
                 uint32_t ta[BM / 16];
                 uint64_t tb[BM / 16];
 #pragma unroll
@@ -895,7 +912,7 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     }
                     if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(s & 1), limit, &abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    mma_dq(s, s);
+                    mma_dq(s % C::NKS, s);
                     mma_commit_w(smem_addr(&ek[s % C::NKS]));  // K_s read for the last time
                     if (more) {
                         if (!wait_v(s + 1)) { ok = false; break; }
@@ -908,49 +925,54 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             } else {
                 // Items one after the other, steps numbered globally, handed over as
                 // in the dK/dV kernel (res_full / res_empty, acc_empty).
-                int g = 0;
+                RingPos kq{0, 0u}, vq{0, 0u};  // K and V ring positions of the step in work
+                uint32_t par = 0;              // parity of the step in work (per-step barriers)
                 int q0, bh, n_steps;
                 bool have = item(0, q0, bh, n_steps);
                 for (int it = 0; ok && have; ++it) {
                     if (!wait_or_abort_w(smem_addr(&res_full), (uint32_t)(it & 1), limit, &abort_flag) ||
-                        (g > 0 && !wait_or_abort_w(smem_addr(&s_read), (uint32_t)((g - 1) & 1), limit, &abort_flag)) ||
-                        !wait_k(g)) {
+                        (it > 0 && !wait_or_abort_w(smem_addr(&s_read), par ^ 1u, limit, &abort_flag)) ||
+                        !wait_at(fk, kq)) {
                         ok = false;
                         break;
                     }
-                    mma_s(g);
+                    mma_s_at(kq.slot);
                     mma_commit_w(smem_addr(&s_full));
-                    if (!wait_v(g)) { ok = false; break; }
-                    mma_dp(g);
+                    if (!wait_at(fv, vq)) { ok = false; break; }
+                    mma_dp_at(vq.slot);
                     mma_commit_w(smem_addr(&dp_full));
-                    mma_commit_w(smem_addr(&ev[g % C::NVS]));  // V_g read for the last time
+                    mma_commit_w(smem_addr(&ev[vq.slot]));  // this V tile read for the last time
                     if (n_steps == 1) mma_commit_w(smem_addr(&res_empty));  // Q and dO read for the last time
-                    for (int s = 0; s < n_steps; ++s, ++g) {
+                    for (int s = 0; s < n_steps; ++s) {
                         const bool more = s + 1 < n_steps;
+                        const RingPos kq1 = ring_next<C::NKS>(kq), vq1 = ring_next<C::NVS>(vq);
                         if (more) {
-                            if (!wait_or_abort_w(smem_addr(&s_read), (uint32_t)(g & 1), limit, &abort_flag) || !wait_k(g + 1)) {
+                            if (!wait_or_abort_w(smem_addr(&s_read), par, limit, &abort_flag) || !wait_at(fk, kq1)) {
                                 ok = false;
                                 break;
                             }
-                            mma_s(g + 1);
+                            mma_s_at(kq1.slot);
                             mma_commit_w(smem_addr(&s_full));
                         }
-                        if (!wait_or_abort_w(smem_addr(&ds_ready), (uint32_t)(g & 1), limit, &abort_flag) ||
+                        if (!wait_or_abort_w(smem_addr(&ds_ready), par, limit, &abort_flag) ||
                             (s == 0 && it > 0 &&
                              !wait_or_abort_w(smem_addr(&acc_empty), (uint32_t)((it - 1) & 1), limit, &abort_flag))) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        mma_dq(g, s);
-                        mma_commit_w(smem_addr(&ek[g % C::NKS]));  // K_g read for the last time
+                        mma_dq(kq.slot, s);
+                        mma_commit_w(smem_addr(&ek[kq.slot]));  // this K tile read for the last time
                         if (more) {
-                            if (!wait_v(g + 1)) { ok = false; break; }
-                            mma_dp(g + 1);
+                            if (!wait_at(fv, vq1)) { ok = false; break; }
+                            mma_dp_at(vq1.slot);
                             mma_commit_w(smem_addr(&dp_full));
-                            mma_commit_w(smem_addr(&ev[(g + 1) % C::NVS]));  // V_(g+1) read for the last time
+                            mma_commit_w(smem_addr(&ev[vq1.slot]));  // the next V tile read for the last time
                             if (s + 2 == n_steps) mma_commit_w(smem_addr(&res_empty));  // Q and dO read for the last time
                         }
+                        kq = kq1;
+                        vq = vq1;
+                        par ^= 1u;
                     }
                     if (!ok) break;
                     mma_commit_w(smem_addr(&o_full));  // this item's dQ is complete
