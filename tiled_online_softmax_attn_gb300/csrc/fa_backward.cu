@@ -63,6 +63,48 @@ __global__ void fa_bwd_delta_kernel(const T *__restrict__ o, const T *__restrict
     }
 }
 
+// The same with 16-byte loads, for rows whose length in bytes is a multiple
+// of 16: 2^tpr_log2 lanes share a row (the smallest power of two that covers
+// its 16-byte chunks, at most 32), so a warp reads several short rows at once.
+__device__ __forceinline__ float dot16(uint4 a, uint4 b, const float *)
+{
+    return __uint_as_float(a.x) * __uint_as_float(b.x) + __uint_as_float(a.y) * __uint_as_float(b.y) +
+           __uint_as_float(a.z) * __uint_as_float(b.z) + __uint_as_float(a.w) * __uint_as_float(b.w);
+}
+__device__ __forceinline__ float dot16(uint4 a, uint4 b, const __nv_bfloat16 *)
+{
+    const uint32_t x[4] = {a.x, a.y, a.z, a.w}, y[4] = {b.x, b.y, b.z, b.w};
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc = fmaf(__uint_as_float(x[i] << 16), __uint_as_float(y[i] << 16), acc);
+        acc = fmaf(__uint_as_float(x[i] & 0xffff0000u), __uint_as_float(y[i] & 0xffff0000u), acc);
+    }
+    return acc;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+fa_bwd_delta_vec_kernel(const T *__restrict__ o, const T *__restrict__ dout, const float *__restrict__ lse,
+                        float *__restrict__ delta, float *__restrict__ lse2, int64_t rows, int d, int N, int pitch,
+                        int tpr_log2)
+{
+    const int tpr = 1 << tpr_log2, chunks = d * (int)sizeof(T) / 16;
+    const int sub = (int)(threadIdx.x & (uint32_t)(tpr - 1));
+    const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> tpr_log2;
+    float acc = 0.f;
+    if (row < rows) {
+        const uint4 *po = reinterpret_cast<const uint4 *>(o + row * d), *pg = reinterpret_cast<const uint4 *>(dout + row * d);
+        for (int c = sub; c < chunks; c += tpr) acc += dot16(__ldg(po + c), __ldg(pg + c), o);
+    }
+    for (int off = tpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && sub == 0) {
+        const int64_t idx = (row / N) * pitch + row % N;
+        delta[idx] = acc;
+        lse2[idx] = lse[row] * 1.4426950408889634f;
+    }
+}
+
 // KV = true: dK, dV for one block of BC keys and one DCH-column slice.
 // KV = false: dQ for one block of BR queries and one DCH-column slice.
 template <typename Tin, typename Tout, bool KV>
@@ -261,6 +303,22 @@ cudaError_t launch_backward_delta(const BackwardProblem &p, void *workspace, cud
     *delta_out = delta;
     *lse2_out = lse2;
     const int64_t rows = p.B * p.H * p.N;
+    const int64_t row_bytes = p.d * (p.in_dtype == 0 ? 2 : 4);
+    auto al16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
+    if (row_bytes % 16 == 0 && al16(p.o) && al16(p.dout)) {
+        int tpr_log2 = 0;
+        while ((1 << tpr_log2) < 32 && (int64_t)(1 << tpr_log2) * 16 < row_bytes) ++tpr_log2;
+        const unsigned blocks = (unsigned)((rows * (1 << tpr_log2) + 255) / 256);
+        if (p.in_dtype == 0)
+            fa_bwd_delta_vec_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+                static_cast<const __nv_bfloat16 *>(p.o), static_cast<const __nv_bfloat16 *>(p.dout), p.lse, delta, lse2,
+                rows, (int)p.d, (int)p.N, pitch, tpr_log2);
+        else
+            fa_bwd_delta_vec_kernel<float><<<blocks, 256, 0, stream>>>(static_cast<const float *>(p.o),
+                                                                        static_cast<const float *>(p.dout), p.lse, delta,
+                                                                        lse2, rows, (int)p.d, (int)p.N, pitch, tpr_log2);
+        return cudaGetLastError();
+    }
     if (p.in_dtype == 0)
         fa_bwd_delta_kernel<__nv_bfloat16><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
             static_cast<const __nv_bfloat16 *>(p.o), static_cast<const __nv_bfloat16 *>(p.dout), p.lse, delta, lse2,
