@@ -300,6 +300,9 @@ fa_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the dQ kernel (independent of this one) may take SMs as this grid's last
+    // CTAs leave them
+    pdl_launch_dependents();
     const uint32_t tmem = bars.tmem_base;
     const uint64_t limit = prm.limit;
     // tensor memory: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D).
@@ -1088,6 +1091,9 @@ fa_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         if (!ok && !abort_flag) fail_bwd(&abort_flag);
     }
+    // launched as a programmatic dependent of the dK/dV kernel: finish only
+    // after it has, so that work after this kernel sees both
+    pdl_wait_prior();
     tc_fence_before();
     __syncthreads();
     if (warp == MMA_WARP) {
@@ -1178,8 +1184,19 @@ cudaError_t launch_dims(const BackwardProblem &p, float *delta, float *lse2, int
     const unsigned grid = (unsigned)(persist ? std::min<int64_t>(items, sms) : items);
     kv<<<grid, EW<D>::NUM_THREADS, C::SMEM_KV_REQ, stream>>>(mq, mk, mv, mg, prm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    kq<<<grid, EW<D>::NUM_THREADS, C::SMEM_Q_REQ, stream>>>(mq, mk, mv, mg, prm);
-    return cudaGetLastError();
+    // programmatic dependent launch: the dQ CTAs (which read nothing the dK/dV
+    // kernel writes) start on the SMs its last wave leaves idle
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(EW<D>::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_Q_REQ;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kq, mq, mk, mv, mg, prm);
 }
 
 }  // namespace
