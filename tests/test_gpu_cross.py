@@ -103,3 +103,83 @@ def test_sequence_major_matches_contiguous_bitwise():
     o3, l3 = fa.fa_forward(*a, causal=True)
     torch.cuda.synchronize()
     assert torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
+
+SINGLE_TILE = [
+    # (B, H, Nq, Nk, dk, dv, o_dtype): at most 128 query rows, so every item is
+    # one query tile; Nk up to 64 key tiles runs persistent CTAs, beyond that one
+    # CTA per item
+    (1, 3, 1, 700, 128, 128, "bf16"),
+    (2, 2, 100, 129, 64, 64, "bf16"),
+    (1, 2, 128, 8192, 64, 128, "bf16"),
+    (1, 2, 77, 9000, 128, 64, "bf16"),
+    (3, 1, 128, 1, 64, 64, "fp32"),        # one key tile: no odd tiles to merge
+    (1, 1, 33, 8321, 64, 64, "fp32"),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,dk,dv,o_dtype", SINGLE_TILE)
+def test_single_query_tile_items(B, H, Nq, Nk, dk, dv, o_dtype):
+    """Queries that fit one 128-row tile: the two softmax warpgroups take the
+    even and the odd key tiles and their partial results are merged in the CTA.
+    Checked against the oracle, with and without a workspace (key-range split
+    where the plan picks one)."""
+    q, k, v = draw(7500 + Nq + Nk, B, H, Nq, Nk, dk, dv, "bf16")
+    qd, kd, vd = (torch.from_numpy(x).to(torch.bfloat16).cuda() for x in (q, k, v))
+    odt = TORCH_DT[o_dtype]
+    scale = 1.0 / np.sqrt(dk)
+    o, lse = fa.fa_attention(qd, kd, vd, scale=scale, o_dtype=odt)
+    ws = torch.empty(max(1, fa.attention_workspace_size(qd, kd, vd, o_dtype=odt)), dtype=torch.uint8, device="cuda")
+    o2, lse2 = fa.fa_attention(qd, kd, vd, scale=scale, o_dtype=odt, workspace=ws)
+    torch.cuda.synchronize()
+    assert fa.check_device_error() == fa.FA_OK, fa.last_error()
+    o_ref, l_ref = oracle.attention(q, k, v, scale, False)
+    compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "bf16", o_dtype)
+    compare(o2.float().cpu().numpy(), lse2.cpu().numpy(), o_ref, l_ref, "bf16", o_dtype)
+
+
+@pytest.mark.parametrize("Nq,Nk,dk,dv", [(1, 800, 128, 128), (77, 800, 64, 64), (128, 640, 64, 128)])
+def test_single_query_tile_key_range_split(Nq, Nk, dk, dv):
+    """Key-range splits of single-tile items, uneven ones included: 800 keys
+    are 7 key tiles, split 3 + 3 + 1 (the last range has no odd tile); 640 keys
+    are 5, split 3 + 2."""
+    q, k, v = draw(7600 + Nq + dk, 1, 1, Nq, Nk, dk, dv, "bf16")
+    qd, kd, vd = (torch.from_numpy(x).to(torch.bfloat16).cuda() for x in (q, k, v))
+    ws_bytes = fa.attention_workspace_size(qd, kd, vd)
+    assert ws_bytes > 0, "the problem should plan a key-range split"
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    scale = 1.0 / np.sqrt(dk)
+    o, lse = fa.fa_attention(qd, kd, vd, scale=scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert fa.check_device_error() == fa.FA_OK, fa.last_error()
+    o_ref, l_ref = oracle.attention(q, k, v, scale, False)
+    compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "bf16", "bf16")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("hot", [3, 200, 300, 1000])
+def test_single_query_tile_hot_key(d, hot):
+    """One key whose score is about 40 above every other: in an even key tile
+    (keys 3 and 300: tiles 0 and 2), an odd one (key 200: tile 1) or the ragged
+    last one (key 1000 of 1001: tile 7).  The merge then weighs one warpgroup's partial result by about
+    2^-58 against the other's, and O must be that key's V row."""
+    B, H, Nq, Nk = 1, 2, 9, 1001
+    q, k, v = draw(7700 + hot + d, B, H, Nq, Nk, d, d, "bf16")
+    k = (k * 0.25).astype(np.float32)          # ordinary scores about 0.25 sigma
+    u = np.zeros(d, np.float32)
+    u[:8] = 4.0
+    q[..., :8] = 4.0                            # every query row shares the direction u
+    k[:, :, hot, :] = 0.0
+    k[:, :, hot, :8] = u[:8] * (np.sqrt(d) * 40.0 / (8 * 16.0 * 4.0) * 4.0)
+    q, k, v = (torch.from_numpy(x).to(torch.bfloat16).float().numpy() for x in (q, k, v))
+    qd, kd, vd = (torch.from_numpy(x).to(torch.bfloat16).cuda() for x in (q, k, v))
+    scale = 1.0 / np.sqrt(d)
+    o, lse = fa.fa_attention(qd, kd, vd, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.check_device_error() == fa.FA_OK, fa.last_error()
+    o_ref, l_ref = oracle.attention(q, k, v, scale, False)
+    s_hot = scale * (q[0, 0, 0] @ k[0, 0, hot])
+    assert s_hot > 30.0                         # the hot key dominates the row
+    compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "bf16", "bf16")
+    assert np.abs(o_ref[:, :, :, :] - v[:, :, hot:hot + 1, :]).max() < 1e-6

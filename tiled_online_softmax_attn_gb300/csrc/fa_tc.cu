@@ -90,19 +90,28 @@ constexpr uint32_t ERR_WAIT_MMA = 2u;       // MMA thread gave up waiting for da
 constexpr uint32_t ERR_WAIT_SOFTMAX = 4u;   // softmax gave up waiting for S or O
 constexpr uint32_t ERR_DRAIN = 8u;          // teardown could not confirm in-flight work
 
-template <int DK, int DV>
+constexpr int MAX_KVS = 6;            // key/value ring stages, at most
+
+template <int DK, int DV, bool ONE = false>
 struct Cfg {
     static constexpr int QCH = DK / 64;                    // 128-byte swizzle chunks of a Q/K row
     static constexpr int VCH = DV / 64;                    // ... of a V row
     static constexpr uint32_t Q_BYTES = BM * DK * 2;       // one 128 x DK bf16 tile
     static constexpr uint32_t K_BYTES = BN * DK * 2;
     static constexpr uint32_t V_BYTES = BN * DV * 2;
+    static constexpr int Q_TILES = ONE ? 1 : 2;            // query tiles of an item
     // Ring of key/value stages: stage j holds K_j and V_(j-1), the two tiles
-    // that iteration j of the MMA loop reads.  Three stages when they fit in
-    // shared memory, else two.
-    static constexpr int KVS = (2 * Q_BYTES + 3 * (K_BYTES + V_BYTES) + 1024 <= 227u * 1024u) ? 3 : 2;
+    // that iteration j of the MMA loop reads.  Two query tiles: three stages
+    // when they fit in shared memory, else two.  One query tile (a short query
+    // against a long key range: loading is most of the time): as many as fit
+    // beside 2 KB of static shared memory, up to MAX_KVS, so each SM keeps more
+    // bytes in flight (d = 128: 3, d = 64: 6).
+    static constexpr int KVS_FIT = (int)((227u * 1024u - 1024u - 2048u - Q_BYTES) / (K_BYTES + V_BYTES));
+    static constexpr int KVS = ONE ? (KVS_FIT < MAX_KVS ? KVS_FIT : MAX_KVS)
+                                   : ((2 * Q_BYTES + 3 * (K_BYTES + V_BYTES) + 1024 <= 227u * 1024u) ? 3 : 2);
+    static_assert(KVS >= 2 && KVS <= MAX_KVS, "key/value ring size");
     static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = 2 * Q_BYTES;
+    static constexpr uint32_t OFF_K = Q_TILES * Q_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + KVS * K_BYTES;
     static constexpr uint32_t SMEM_TILES = OFF_V + KVS * V_BYTES;
     static constexpr uint32_t SMEM_BYTES = SMEM_TILES + 1024;  // + alignment slack
@@ -147,11 +156,12 @@ struct Params {
 
 struct __align__(8) Barriers {
     uint64_t q_full[2], q_empty;      // query tiles of an item; free after its last S MMA
-    uint64_t kv_full[3], kv_empty[3];
+    uint64_t kv_full[MAX_KVS], kv_empty[MAX_KVS];
     uint64_t s_full[2];
     uint64_t p_part[2][MAX_PARTS];    // P_t keys [0, (k + 1) BN / P_PARTS) written
     uint64_t s_read[2], p_free[2];    // SEP_P: S_t read by the softmax warps / P_t read by the P V product
     uint64_t o_full[2], o_empty[2];   // O_t complete / read by the epilogue
+    uint64_t part_full, part_empty;   // single-tile items: the odd key tiles' m, l, dq written / read
     uint64_t drain;
 };
 
@@ -252,18 +262,24 @@ __device__ __forceinline__ void store_o_row(void *o, int o_fp32, size_t row_elem
     }
 }
 
-template <int DK, int DV, bool CAUSAL, bool PERSIST, bool SPLIT>
+// ONE: every item has a single query tile (at most 128 query rows per head,
+// unmasked).  The two softmax warpgroups then share that tile's key tiles,
+// even ones to warps 0-3 and odd ones to warps 4-7, each with its own running
+// maximum, sum and O accumulator in the tile slots of S, P and O; warps 0-3
+// merge the two partial results by the log-sum-exp rule before the epilogue.
+template <int DK, int DV, bool CAUSAL, bool PERSIST, bool SPLIT, bool ONE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const Params prm)
 {
-    using C = Cfg<DK, DV>;
+    using C = Cfg<DK, DV, ONE>;
     constexpr int P_PARTS = C::P_PARTS;
     static_assert(P_PARTS <= MAX_PARTS && (BN / 32) % P_PARTS == 0, "P slices must be whole 32-key chunks");
     extern __shared__ uint8_t smem_raw[];
     __shared__ Barriers bars;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
+    __shared__ float part_mld[ONE ? 3 : 1][ONE ? BM : 1];  // ONE: m, l, dq of the odd key tiles, per row
 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_base = smem_addr(smem);
@@ -284,7 +300,9 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             mbar_init(smem_addr(&bars.o_empty[t]), 128);
         }
         mbar_init(smem_addr(&bars.q_empty), 1);
-        for (int s = 0; s < 3; ++s) {
+        mbar_init(smem_addr(&bars.part_full), 128);
+        mbar_init(smem_addr(&bars.part_empty), 128);
+        for (int s = 0; s < C::KVS; ++s) {
             mbar_init(smem_addr(&bars.kv_full[s]), 1);
             mbar_init(smem_addr(&bars.kv_empty[s]), 1);
         }
@@ -300,6 +318,10 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
     const uint64_t limit = prm.wait_limit_ns;
+    // The merge of the key-range partials may be scheduled now (it waits for this
+    // grid to finish before reading); a split grid never has more CTAs than SMs,
+    // so its blocks take only SMs this grid leaves idle.
+    if constexpr (SPLIT) pdl_launch_dependents();
 
     if (warp == TMA_WARP) {
         // ================================================================ TMA producer
@@ -346,7 +368,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 if (ok && it > 0 && !wait_or_abort(smem_addr(&bars.q_empty), (uint32_t)((it - 1) & 1), limit, &abort_flag))
                     ok = false;
                 if (ok) {
-                    for (int t = 0; t < 2; ++t) {
+                    for (int t = 0; t < (ONE ? 1 : 2); ++t) {
                         const uint32_t bar = smem_addr(&bars.q_full[t]);
                         mbar_arrive_expect_tx(bar, C::Q_BYTES);
                         for (int c = 0; c < C::QCH; ++c)
@@ -368,7 +390,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     if (!mbar_wait_bounded(full, (uint32_t)((p / C::KVS) & 1), limit)) atomicOr(&g_tc_error_word, ERR_DRAIN);
                 }
                 if (q_items > 0)
-                    for (int t = 0; t < 2; ++t)
+                    for (int t = 0; t < (ONE ? 1 : 2); ++t)
                         if (!mbar_wait_bounded(smem_addr(&bars.q_full[t]), (uint32_t)((q_items - 1) & 1), limit))
                             atomicOr(&g_tc_error_word, ERR_DRAIN);
             }
@@ -403,7 +425,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             constexpr uint64_t K_STEP = C::K_BYTES >> 4, V_STEP = C::V_BYTES >> 4;  // one ring slot, descriptor units
             // S_t = Q_t K^T from ring slot `slot` (M = 128 rows, N = 128 keys, K = D in steps of 16)
             auto mma_s = [&](int t, int slot) {
-                const uint64_t q = t ? dq1 : dq0, k = dk0 + (uint64_t)slot * K_STEP;
+                const uint64_t q = (t && !ONE) ? dq1 : dq0, k = dk0 + (uint64_t)slot * K_STEP;
                 const uint32_t d_s = tmem + t * 128;
                 uint64_t qa[DK / 16], kb[DK / 16];
 #pragma unroll
@@ -464,14 +486,101 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     }
                     return true;
                 };
-                if constexpr (C::SEP_P) {
-                    // Before S_t is overwritten the softmax warps must have read the
-                    // previous S_t (ns[t] S_t products so far over all items).
-                    auto s_free = [&](int t) -> bool {
-                        const bool r = ns[t] == 0 || wait(&bars.s_read[t], (ns[t] - 1) & 1u);
-                        ++ns[t];
-                        return r;
+                // Before S_t is overwritten the softmax warps must have read the
+                // previous S_t (ns[t] S_t products so far over all items).
+                auto s_free = [&](int t) -> bool {
+                    const bool r = ns[t] == 0 || wait(&bars.s_read[t], (ns[t] - 1) & 1u);
+                    ++ns[t];
+                    return r;
+                };
+                if constexpr (ONE && C::SEP_P) {
+                    // Key tile k goes to slot k mod 2.  P has columns of its own, so
+                    // S(k + 2) is issued as soon as the slot's softmax warps have read
+                    // S(k), ahead of P(k) V: they find their next scores ready when they
+                    // finish a tile.  Two ring positions: `ws` is the next stage to wait
+                    // for (its K feeds an S product), `slot` the next to release (its V
+                    // feeds P V); stage j is released after P(j - 1) V, stage 0 after S(0).
+                    int ws = slot;
+                    uint32_t wph = phase;
+                    auto next_w = [&]() {
+                        if (++ws == C::KVS) {
+                            ws = 0;
+                            wph ^= 1u;
+                        }
                     };
+                    auto s_at = [&](int t) -> bool {  // S_t = Q K from stage ws
+                        if (!s_free(t)) return false;
+                        tc_fence_after();
+                        mma_s(t, ws);
+                        mma_commit_w(smem_addr(&bars.s_full[t]));
+                        return true;
+                    };
+                    auto pv_stage = [&](int u, bool first, bool last) -> bool {
+                        if (!pv(u, slot, first)) return false;
+                        mma_commit_w(smem_addr(&bars.p_free[u]));
+                        if (last) mma_commit_w(smem_addr(&bars.o_full[u]));
+                        return true;
+                    };
+                    if (!wait(&bars.q_full[0], (uint32_t)(it & 1))) break;
+                    for (int k = 0; ok && k < 2 && k < n0; ++k) {
+                        if (!wait(&bars.kv_full[ws], wph) || !(k ? s_at(1) : s_at(0))) break;
+                        if (PERSIST && k == n0 - 1) mma_commit_w(smem_addr(&bars.q_empty));
+                        next_w();
+                    }
+                    if (!ok) break;
+                    mma_commit_w(smem_addr(&bars.kv_empty[slot]));  // stage 0: K_0 only
+                    next_stage();
+                    for (int k = 0; ok && k < n0; ++k) {
+                        if (k + 2 < n0) {
+                            if (!wait(&bars.kv_full[ws], wph) || !((k & 1) ? s_at(1) : s_at(0))) break;
+                            if (PERSIST && k + 2 == n0 - 1) mma_commit_w(smem_addr(&bars.q_empty));
+                            next_w();
+                        }
+                        // stage k + 1 (K_(k+1), V_k) was waited for when S(k + 1) was
+                        // issued; the last stage holds V only
+                        if (k + 1 == n0 && !wait(&bars.kv_full[slot], phase)) break;
+                        const bool first = k < 2, last = k + 2 >= n0;  // slot's first / last key tile
+                        if (!((k & 1) ? pv_stage(1, first, last) : pv_stage(0, first, last))) break;
+                        mma_commit_w(smem_addr(&bars.kv_empty[slot]));
+                        next_stage();
+                    }
+                } else if constexpr (ONE) {
+                    // Stage s holds K_s and V_(s-1).  Key tile s goes to slot t = s mod 2
+                    // (S_t = Q K_s), and P_u V_(s-1) for u = 1 - t completes key tile
+                    // s - 1.  S_t is issued first: slot t's previous P_t V product was
+                    // issued a stage earlier, so it is ordered before the overwrite.
+                    // (the slot is passed as a literal at each call, so the per-slot
+                    // counters stay in registers)
+                    auto s_stage = [&](int t) -> bool {
+                        if (C::SEP_P && !s_free(t)) return false;
+                        tc_fence_after();
+                        mma_s(t, slot);
+                        mma_commit_w(smem_addr(&bars.s_full[t]));
+                        return true;
+                    };
+                    auto pv_stage = [&](int u, bool first, bool last) -> bool {
+                        if (!pv(u, slot, first)) return false;
+                        if (C::SEP_P) mma_commit_w(smem_addr(&bars.p_free[u]));
+                        if (last) mma_commit_w(smem_addr(&bars.o_full[u]));
+                        return true;
+                    };
+                    for (int s = 0; ok && s <= n0; ++s) {
+                        if (!wait(&bars.kv_full[slot], phase)) break;
+                        if (s == 0 && !wait(&bars.q_full[0], (uint32_t)(it & 1))) break;
+                        if (s < n0) {
+                            if (!((s & 1) ? s_stage(1) : s_stage(0))) break;
+                            if (PERSIST && s == n0 - 1) mma_commit_w(smem_addr(&bars.q_empty));
+                        }
+                        if (s >= 1) {
+                            // key tiles 0 and 1 start O_0 and O_1; slot u's last key tile is s - 1
+                            // when no key tile s + 1 follows
+                            const bool first = s - 1 < 2, last = s + 1 >= n0;
+                            if (!((s & 1) ? pv_stage(0, first, last) : pv_stage(1, first, last))) break;
+                        }
+                        mma_commit_w(smem_addr(&bars.kv_empty[slot]));
+                        next_stage();
+                    }
+                } else if constexpr (C::SEP_P) {
                     // stage 0: K_0
                     if (wait(&bars.q_full[0], (uint32_t)(it & 1)) && wait(&bars.kv_full[slot], phase) && s_free(0)) {
                         tc_fence_after();
@@ -595,8 +704,9 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const int w = item_index<PERSIST>(it);
             if (w >= prm.n_items) break;
             const Item wi = item_of<CAUSAL, SPLIT>(prm, w);
-            const int grow = wi.qrow0 + t * BM + r;  // global query row of this thread
-            const int n_t = t == 0 ? wi.n0 : wi.n1;
+            const int grow = wi.qrow0 + (ONE ? 0 : t * BM) + r;  // global query row of this thread
+            // key tiles of this warpgroup (ONE: every other one, from key tile t)
+            const int n_t = ONE ? (wi.n0 + 1 - t) >> 1 : (t == 0 ? wi.n0 : wi.n1);
             float m = -INFINITY;  // running maximum, log2 units
             float l = 0.f;        // running denominator (exact weights): LSE
             float dq = 0.f;       // bf16 rounding of each tile's largest weight: O / (l + dq)
@@ -618,7 +728,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     tc_fence_before();
                     mbar_arrive(smem_addr(&bars.s_read[t]));
                 }
-                const int kv0 = (wi.kv_lo + j) * BN;
+                const int kv0 = (wi.kv_lo + (ONE ? 2 * j + t : j)) * BN;
                 int lim = Nk - kv0;                         // keys >= Nk are padding
                 if (CAUSAL) lim = min(lim, grow - kv0 + 1);  // keys after this query
                 if (lim < BN) {
@@ -700,6 +810,22 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 mbar_arrive(smem_addr(&bars.p_part[t][P_PARTS - 1]));
             }
             if (!ok) break;
+            // ONE: warps 4-7 hand their rows' m, l, dq to warps 0-3 and are done
+            // with the item; warps 0-3 merge O_1 into O_0 as they read it.  (Every
+            // item of a persistent grid has the same key tiles, so the barriers
+            // below change phase once per item, or never when there is one key tile.)
+            if (ONE && t == 1) {
+                if (n_t == 0) continue;
+                if (it > 0 && !wait_or_abort(smem_addr(&bars.part_empty), (uint32_t)((it - 1) & 1), limit, &abort_flag)) {
+                    fail();
+                    break;
+                }
+                part_mld[0][r] = m;
+                part_mld[1][r] = l;
+                part_mld[2][r] = dq;
+                mbar_arrive(smem_addr(&bars.part_full));
+                continue;
+            }
             // ---- epilogue: O / l, LSE.  O_t is read whole, then released to the
             // next item's first P V product before the stores.
             if (!wait_or_abort(smem_addr(&bars.o_full[t]), (uint32_t)(it & 1), limit, &abort_flag)) {
@@ -707,12 +833,49 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 break;
             }
             tc_fence_after();
+            const bool has1 = ONE && wi.n0 >= 2;  // ONE: O_1 holds the odd key tiles
+            float w0 = 1.f, w1 = 0.f;             // their weights in the merged O
+            if (has1) {
+                if (!wait_or_abort(smem_addr(&bars.part_full), (uint32_t)(it & 1), limit, &abort_flag) ||
+                    !wait_or_abort(smem_addr(&bars.o_full[1]), (uint32_t)(it & 1), limit, &abort_flag)) {
+                    fail();
+                    break;
+                }
+                tc_fence_after();
+                const float m1 = part_mld[0][r], l1 = part_mld[1][r], d1 = part_mld[2][r];
+                mbar_arrive(smem_addr(&bars.part_empty));
+                // the log-sum-exp merge of two key ranges: both sums and O move to
+                // the larger reference maximum
+                const float mm = fmaxf(m, m1);
+                w0 = m == -INFINITY ? 0.f : ex2(m - mm);
+                w1 = m1 == -INFINITY ? 0.f : ex2(m1 - mm);
+                m = mm;
+                l = w0 * l + w1 * l1;
+                dq = w0 * dq + w1 * d1;
+            }
+            // 32 columns of O from column c * 32: O_t, or under ONE w0 O_0 + w1 O_1
+            auto load_o = [&](int c, uint32_t (&raw)[32]) {
+                tmem_ld32(tO + c * 32, raw);
+                if (ONE && has1) {
+                    uint32_t raw1[32];
+                    tmem_ld32(tO + DV + c * 32, raw1);
+#pragma unroll
+                    for (int x = 0; x < 32; ++x)
+                        raw[x] = __float_as_uint(fmaf(w0, __uint_as_float(raw[x]), w1 * __uint_as_float(raw1[x])));
+                }
+            };
+            // releases the O columns this epilogue read (persistent grids)
+            auto release_o = [&]() {
+                tc_fence_before();
+                mbar_arrive(smem_addr(&bars.o_empty[t]));
+                if (has1) mbar_arrive(smem_addr(&bars.o_empty[1]));
+            };
             if constexpr (SPLIT) {  // key-range partials: unnormalised O, m, l, dq
                 const size_t prow = ((size_t)wi.sp * prm.BH + wi.bh) * N + grow;
 #pragma unroll
                 for (int c = 0; c < DV / 32; ++c) {
                     uint32_t raw[32];
-                    tmem_ld32(tO + c * 32, raw);
+                    load_o(c, raw);
                     if (grow < N) {
                         float4 *dst = reinterpret_cast<float4 *>(prm.o_part + prow * DV + c * 32);
 #pragma unroll
@@ -721,10 +884,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                                                  __uint_as_float(raw[4 * x + 2]), __uint_as_float(raw[4 * x + 3]));
                     }
                 }
-                if (PERSIST) {
-                    tc_fence_before();
-                    mbar_arrive(smem_addr(&bars.o_empty[t]));
-                }
+                if (PERSIST) release_o();
                 if (grow < N) {
                     prm.m_part[prow] = m;
                     prm.l_part[prow] = l;
@@ -734,7 +894,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
             const float inv_l = 1.f / (l + dq);
             const size_t row_elem = (size_t)(wi.b * prm.os_b + wi.h * prm.os_h + (int64_t)grow * prm.os_n);
-            if (PERSIST) {
+            if (PERSIST && !ONE) {
                 uint32_t ov[DV];
 #pragma unroll
                 for (int c = 0; c < DV / 32; ++c) {
@@ -753,17 +913,18 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     const int nc = min(32, prm.dv_real - c * 32);
                     if (grow < N && nc > 0) store_o_row(prm.o, prm.o_fp32, row_elem, vals, c * 32, nc);
                 }
-            } else {  // the only item of the CTA: no one waits for O
+            } else {  // the only item of the CTA, or ONE: O released after the stores
 #pragma unroll
                 for (int c = 0; c < DV / 32; ++c) {
                     uint32_t raw[32];
-                    tmem_ld32(tO + c * 32, raw);
+                    load_o(c, raw);
                     float vals[32];
 #pragma unroll
                     for (int x = 0; x < 32; ++x) vals[x] = __uint_as_float(raw[x]) * inv_l;
                     const int nc = min(32, prm.dv_real - c * 32);
                     if (grow < N && nc > 0) store_o_row(prm.o, prm.o_fp32, row_elem, vals, c * 32, nc);
                 }
+                if (PERSIST) release_o();
             }
             if (prm.lse && grow < N) prm.lse[(size_t)wi.bh * N + grow] = (m + log2f(l)) * 0.69314718055994530942f;
         }
@@ -854,7 +1015,6 @@ template <int DK, int DV, bool CAUSAL>
 cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, const char **detail,
                          const TcSplit *split = nullptr, void *workspace = nullptr)
 {
-    using Cf = Cfg<DK, DV>;
     CUtensorMap mq, mk, mv;
     const int64_t BH = p.B * p.H, Nk = keys_of(p);
     int64_t sq[3], sk[3], sv[3], so[3];
@@ -928,14 +1088,20 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     if (e != cudaSuccess) return e;
     const bool persist = prm.n_split == 1 && (CAUSAL ? prm.n_items > sms && prm.n_kv * std::max(DK, DV) <= 2048
                                                      : prm.n_kv <= 64);
-    auto kern = prm.n_split > 1 ? fa_tc_kernel<DK, DV, CAUSAL, false, !CAUSAL>
-                : persist       ? fa_tc_kernel<DK, DV, CAUSAL, true, false>
-                                : fa_tc_kernel<DK, DV, CAUSAL, false, false>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM_BYTES);
+    // at most 128 query rows, unmasked: items of a single query tile
+    const bool one = !CAUSAL && p.N <= BM;
+    auto kern = prm.n_split > 1 ? (one ? fa_tc_kernel<DK, DV, CAUSAL, false, !CAUSAL, !CAUSAL>
+                                       : fa_tc_kernel<DK, DV, CAUSAL, false, !CAUSAL, false>)
+                : persist       ? (one ? fa_tc_kernel<DK, DV, CAUSAL, true, false, !CAUSAL>
+                                       : fa_tc_kernel<DK, DV, CAUSAL, true, false, false>)
+                                : (one ? fa_tc_kernel<DK, DV, CAUSAL, false, false, !CAUSAL>
+                                       : fa_tc_kernel<DK, DV, CAUSAL, false, false, false>);
+    const uint32_t smem_bytes = one ? Cfg<DK, DV, true>::SMEM_BYTES : Cfg<DK, DV>::SMEM_BYTES;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
     if (e != cudaSuccess) return e;
     int grid = prm.n_items;
     if (persist) grid = std::min(prm.n_items, sms);
-    kern<<<(unsigned)grid, NUM_THREADS, Cf::SMEM_BYTES, stream>>>(mq, mk, mv, prm);
+    kern<<<(unsigned)grid, NUM_THREADS, smem_bytes, stream>>>(mq, mk, mv, prm);
     if ((e = cudaGetLastError()) != cudaSuccess || prm.n_split == 1) return e;
     return launch_combine(prm.o_part, prm.m_part, prm.l_part, prm.d_part, p.o, p.o_dtype == 1, p.lse, BH, p.N, DV,
                           prm.n_split, stream);
