@@ -129,6 +129,15 @@ def profiled_traffic(kernel_key, workload):
     return float(m_t.group(1)), (m_n.group(1).strip() if m_n else "ncu dram__bytes_read.sum + dram__bytes_write.sum")
 
 
+def traffic_for(kernel_key, w):
+    """profiled_traffic for a workload as named; a resized one (--batch,
+    --heads, --seq) has no figure, since the summaries hold the named
+    workload's traffic."""
+    if w != synth.WORKLOADS.get(w.name):
+        return None, "workload resized from the named one: no ncu figure for it"
+    return profiled_traffic(kernel_key, w.name)
+
+
 class _Nvml:
     """Read-only NVML queries through the driver's libnvidia-ml (ctypes; no
     Python NVML package needed): SM clock, its maximum, power and the
@@ -759,7 +768,7 @@ def main():
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak}
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json, burst)" if peak_kind == "measured" else "fallback"
-    roof["traffic"], roof["traffic_note"] = profiled_traffic(kernel_key, w.name)
+    roof["traffic"], roof["traffic_note"] = traffic_for(kernel_key, w)
     roof["algorithmic_bytes"] = w.bytes
     roof["algorithmic_flops"] = w.flops
     roof["launches_per_step"] = per_call

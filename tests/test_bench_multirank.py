@@ -128,3 +128,14 @@ def test_exp_roofline_counts_the_kept_pairs():
     assert r["frac"] == pytest.approx(r["achieved"] / r["peak"])
     wc = synth.Workload("t", 2, 3, 5, 64, "bf16", True, seed=1)
     assert bench.exp_roofline(wc, 1.0, 152, None)["exps"] == 2 * 3 * 15
+
+
+def test_traffic_only_for_the_named_workload():
+    """A resized workload (--batch, --heads, --seq) gets no ncu traffic figure:
+    the committed summaries hold the named workload's bytes per launch."""
+    import synth
+    w = synth.WORKLOADS["multihead"]
+    assert bench.traffic_for("tc", w) == bench.profiled_traffic("tc", "multihead")
+    for small in (w.scaled(B=1), w.scaled(H=64), w.scaled(N=1024)):
+        traffic, note = bench.traffic_for("tc", small)
+        assert traffic is None and "resized" in note
