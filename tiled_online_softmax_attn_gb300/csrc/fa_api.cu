@@ -352,12 +352,13 @@ int fa_plan(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int o_dtyp
     int launches;
     if (fa::tc_supported(p)) {
         const fa::TcSplit sp = fa::tc_split_plan(p);
+        const char *rows = fa::tc_item_rows(p) == 128 ? ", one query tile per item" : "";
         if (sp.n_split > 1 && workspace_bytes >= sp.workspace_bytes) {
             launches = 2;
-            snprintf(buf, sizeof(buf), "tensor-core d=%lld key splits=%d", (long long)d, sp.n_split);
+            snprintf(buf, sizeof(buf), "tensor-core d=%lld key splits=%d%s", (long long)d, sp.n_split, rows);
         } else {
             launches = 1;
-            snprintf(buf, sizeof(buf), "tensor-core d=%lld", (long long)d);
+            snprintf(buf, sizeof(buf), "tensor-core d=%lld%s", (long long)d, rows);
         }
     } else {
         fa::WidePlan w = fa::wide_plan(p, workspace_bytes ? 1 << 20 : 1);
@@ -531,15 +532,30 @@ fa_status fa_backward(const void *q, const void *k, const void *v, const void *o
     return FA_OK;
 }
 
+namespace {
+
+// fa_forward_ws with the tensor-core kernel's query rows per work item fixed
+// (0: chosen from the problem's fill)
+fa_status forward_ws_rows(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B, int64_t H,
+                          int64_t N, int64_t d, float scale, int causal, int in_dtype, int o_dtype, void *workspace,
+                          size_t workspace_bytes, void *stream, int item_rows)
+{
+    fa::Problem p{q, k, v, o, lse, B, H, N, d, scale, causal != 0, in_dtype, o_dtype};
+    p.item_rows = item_rows;
+    fa_status st = validate(p);
+    if (st != FA_OK) return st;
+    return dispatch(p, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), 0u);
+}
+
+}  // namespace
+
 fa_status fa_forward_ws(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B, int64_t H,
                         int64_t N, int64_t d, float scale, int causal, int in_dtype, int o_dtype, void *workspace,
                         size_t workspace_bytes, void *stream)
 {
     clear_error();
-    fa::Problem p{q, k, v, o, lse, B, H, N, d, scale, causal != 0, in_dtype, o_dtype};
-    fa_status st = validate(p);
-    if (st != FA_OK) return st;
-    return dispatch(p, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), 0u);
+    return forward_ws_rows(q, k, v, o, lse, B, H, N, d, scale, causal, in_dtype, o_dtype, workspace, workspace_bytes,
+                           stream, 0);
 }
 
 fa_status fa_forward_ex(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
@@ -600,6 +616,9 @@ fa_status fa_forward_host(const void *q_h, const void *k_h, const void *v_h, voi
     const size_t ei = dtype_size(in_dtype), eo = dtype_size(o_dtype);
     const size_t head_elems = (size_t)(N * d);
     const int chunks = host_chunks(full);
+    // every chunk runs the work items the whole problem would, so the result is
+    // the device-buffer call's, bit for bit
+    const int item_rows = fa::tc_item_rows(full);
     uint8_t *kernel_ws = ws + L.total;             // scratch of the wide-head path, shared by the chunks
     const size_t kernel_ws_bytes = workspace_bytes - L.total;  // (they run in order on one stream)
 
@@ -622,10 +641,10 @@ fa_status fa_forward_host(const void *q_h, const void *k_h, const void *v_h, voi
             (e = cudaEventRecord(res->copied[c], s_in)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(res->compute, res->copied[c], 0)) != cudaSuccess)
             return cuda_fail(e, "host-to-device copy");
-        fa_status st = fa_forward_ws(ws + L.q + off_in, ws + L.k + off_in, ws + L.v + off_in, ws + L.o + off_o,
-                                     lse_h ? reinterpret_cast<float *>(ws + L.lse + off_l) : nullptr, 1, nh, N, d,
-                                     scale, causal, in_dtype, o_dtype, kernel_ws_bytes ? kernel_ws : nullptr,
-                                     kernel_ws_bytes, res->compute);
+        fa_status st = forward_ws_rows(ws + L.q + off_in, ws + L.k + off_in, ws + L.v + off_in, ws + L.o + off_o,
+                                       lse_h ? reinterpret_cast<float *>(ws + L.lse + off_l) : nullptr, 1, nh, N, d,
+                                       scale, causal, in_dtype, o_dtype, kernel_ws_bytes ? kernel_ws : nullptr,
+                                       kernel_ws_bytes, res->compute, item_rows);
         if (st != FA_OK) return st;
         if ((e = cudaEventRecord(res->computed[c], res->compute)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(res->d2h, res->computed[c], 0)) != cudaSuccess ||

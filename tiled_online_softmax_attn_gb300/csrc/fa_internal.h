@@ -24,6 +24,10 @@ struct Problem {
     int o_dtype;           // fa_dtype
     int64_t Nk = 0, dv = 0;
     int64_t qs[3] = {0, 0, 0}, ks[3] = {0, 0, 0}, vs[3] = {0, 0, 0}, os[3] = {0, 0, 0};
+    // tensor-core kernel: query rows per work item, 128 or 256; 0 = chosen from
+    // the problem's own fill (tc_item_rows).  A caller that runs a problem in
+    // pieces fixes it so that every piece computes as the whole would.
+    int item_rows = 0;
 };
 
 inline int64_t keys_of(const Problem &p) { return p.Nk ? p.Nk : p.N; }
@@ -111,6 +115,10 @@ struct TcSplit {
     size_t workspace_bytes;
 };
 TcSplit tc_split_plan(const Problem &p);
+// Query rows per work item of the tensor-core kernel: 256 (two query tiles),
+// or 128 (one tile, its key tiles shared by both softmax warpgroups) for
+// unmasked problems of at most 128 query rows or too few items to fill the GPU.
+int tc_item_rows(const Problem &p);
 cudaError_t launch_tc_split(const Problem &p, const TcSplit &sp, void *workspace, cudaStream_t stream, const char **detail);
 
 // Backward problem: contiguous [B, H, N, d] Q, K, V, O, dO of in_dtype,

@@ -134,7 +134,7 @@ struct Params {
     int Nk;            // key sequence length
     int H;             // heads
     int BH;            // batch * heads
-    int n_qblocks;     // work items per head (256 query rows each)
+    int n_qblocks;     // work items per head (256 query rows each; 128 for single-tile items)
     int n_items;       // n_qblocks * BH; see item_index for the CTA -> item order
     int hgroup;        // causal: heads per group of the item order (see item_of)
     int n_kv;          // key tiles per head
@@ -186,7 +186,7 @@ __device__ __forceinline__ int item_index(int it)
     return it * G + ((it & 1) ? G - 1 - c : c);
 }
 
-template <bool CAUSAL, bool SPLIT>
+template <bool CAUSAL, bool SPLIT, bool ONE>
 __device__ __forceinline__ Item item_of(const Params &prm, int w)
 {
     int qb, bh, sp = 0;
@@ -213,7 +213,7 @@ __device__ __forceinline__ Item item_of(const Params &prm, int w)
     it.bh = bh;
     it.b = bh / prm.H;
     it.h = bh % prm.H;
-    it.qrow0 = qb * 2 * BM;
+    it.qrow0 = qb * (ONE ? 1 : 2) * BM;
     it.n0 = CAUSAL ? min(prm.n_kv, 2 * qb + 1) : (SPLIT ? min(prm.n_kv - it.kv_lo, prm.kv_per) : prm.n_kv);
     it.n1 = CAUSAL ? min(prm.n_kv, 2 * qb + 2) : it.n0;
     return it;
@@ -262,8 +262,9 @@ __device__ __forceinline__ void store_o_row(void *o, int o_fp32, size_t row_elem
     }
 }
 
-// ONE: every item has a single query tile (at most 128 query rows per head,
-// unmasked).  The two softmax warpgroups then share that tile's key tiles,
+// ONE: every item has a single query tile (unmasked problems of at most 128
+// query rows per head, or with too few two-tile items to fill half of the
+// SMs; see one_tile_items).  The two softmax warpgroups then share that tile's key tiles,
 // even ones to warps 0-3 and odd ones to warps 4-7, each with its own running
 // maximum, sum and O accumulator in the tile slots of S, P and O; warps 0-3
 // merge the two partial results by the log-sum-exp rule before the epilogue.
@@ -338,7 +339,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             for (int it = 0; ok; ++it) {
                 const int w = item_index<PERSIST>(it);
                 if (w >= prm.n_items) break;
-                const Item wi = item_of<CAUSAL, SPLIT>(prm, w);
+                const Item wi = item_of<CAUSAL, SPLIT, ONE>(prm, w);
                 // stage s of the item = K_s (s < n1) and V_(s-1) (s >= 1), s = 0 .. n1
                 auto load_stage = [&](int s) -> bool {
                     const int slot = g % C::KVS;
@@ -469,7 +470,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             for (int it = 0; ok; ++it) {
                 const int w = item_index<PERSIST>(it);
                 if (w >= prm.n_items) break;
-                const Item wi = item_of<CAUSAL, SPLIT>(prm, w);
+                const Item wi = item_of<CAUSAL, SPLIT, ONE>(prm, w);
                 const int n0 = wi.n0, n1 = wi.n1;
                 // the first P_t V product of an item overwrites O_t: the previous
                 // item's epilogue must have read it
@@ -703,7 +704,7 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         for (int it = 0; ok; ++it) {
             const int w = item_index<PERSIST>(it);
             if (w >= prm.n_items) break;
-            const Item wi = item_of<CAUSAL, SPLIT>(prm, w);
+            const Item wi = item_of<CAUSAL, SPLIT, ONE>(prm, w);
             const int grow = wi.qrow0 + (ONE ? 0 : t * BM) + r;  // global query row of this thread
             // key tiles of this warpgroup (ONE: every other one, from key tile t)
             const int n_t = ONE ? (wi.n0 + 1 - t) >> 1 : (t == 0 ? wi.n0 : wi.n1);
@@ -1011,6 +1012,20 @@ SplitLayout split_layout(const Problem &p, int n_split)
     return L;
 }
 
+// Items of one query tile (ONE): unmasked problems of at most 128 query rows
+// per head, and unmasked problems whose two-tile items would fill at most half
+// of the SMs.  There twice as many CTAs, each with half the rows and its two
+// softmax warpgroups sharing the key tiles, halve the chain of every CTA.  With
+// the SMs full, two-tile items win: each K/V tile read from L2 serves 256 rows.
+bool one_tile_items(const Problem &p, int sms)
+{
+    if (p.causal) return false;
+    if (p.item_rows) return p.item_rows == BM;
+    if (p.N <= BM) return true;
+    const int64_t items2 = (p.N + 2 * BM - 1) / (2 * BM) * p.B * p.H;
+    return 2 * items2 <= sms;
+}
+
 template <int DK, int DV, bool CAUSAL>
 cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, const char **detail,
                          const TcSplit *split = nullptr, void *workspace = nullptr)
@@ -1034,7 +1049,12 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     prm.Nk = (int)Nk;
     prm.H = (int)p.H;
     prm.BH = (int)BH;
-    prm.n_qblocks = (int)((p.N + 2 * BM - 1) / (2 * BM));
+    cudaError_t e = cudaSuccess;
+    const int sms = sm_count(&e);
+    if (e != cudaSuccess) return e;
+    const bool one = one_tile_items(p, sms);
+    const int item_rows = one ? BM : 2 * BM;
+    prm.n_qblocks = (int)((p.N + item_rows - 1) / item_rows);
     prm.n_items = (int)(prm.n_qblocks * BH);
     {   // causal item order: as many heads per group as keep their K and V within
         // half of L2 (a head's K/V stays there while its query blocks run)
@@ -1083,13 +1103,8 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t stream, uint32_t flags, 
     // more of them than SMs, gain more from the overlap than they lose in
     // balance: at most 2048 key-tile columns (16 key tiles at d = 128, 32 at
     // d = 64) measured +4 to +31 % on 512-4096-key problems.
-    cudaError_t e = cudaSuccess;
-    const int sms = sm_count(&e);
-    if (e != cudaSuccess) return e;
     const bool persist = prm.n_split == 1 && (CAUSAL ? prm.n_items > sms && prm.n_kv * std::max(DK, DV) <= 2048
                                                      : prm.n_kv <= 64);
-    // at most 128 query rows, unmasked: items of a single query tile
-    const bool one = !CAUSAL && p.N <= BM;
     auto kern = prm.n_split > 1 ? (one ? fa_tc_kernel<DK, DV, CAUSAL, false, !CAUSAL, !CAUSAL>
                                        : fa_tc_kernel<DK, DV, CAUSAL, false, !CAUSAL, false>)
                 : persist       ? (one ? fa_tc_kernel<DK, DV, CAUSAL, true, false, !CAUSAL>
@@ -1151,6 +1166,13 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t stream, uint32_t flags, con
 // Flash-decoding style split for problems with few work items: unmasked, O
 // contiguous, at most one wave of (item, split) CTAs, two key tiles or more
 // per split, 16 splits at most (the combine kernel's limit).
+int tc_item_rows(const Problem &p)
+{
+    cudaError_t e = cudaSuccess;
+    const int sms = sm_count(&e);
+    return one_tile_items(p, e == cudaSuccess ? sms : 0) ? BM : 2 * BM;
+}
+
 TcSplit tc_split_plan(const Problem &p)
 {
     TcSplit sp{1, 0, 0};
@@ -1163,7 +1185,8 @@ TcSplit tc_split_plan(const Problem &p)
     cudaError_t e = cudaSuccess;
     const int sms = sm_count(&e);
     if (e != cudaSuccess) return sp;
-    const int64_t items = (p.N + 2 * BM - 1) / (2 * BM) * p.B * p.H;
+    const int64_t item_rows = one_tile_items(p, sms) ? BM : 2 * BM;
+    const int64_t items = (p.N + item_rows - 1) / item_rows * p.B * p.H;
     const int64_t n_kv = (keys_of(p) + BN - 1) / BN;
     if (2 * items > sms || n_kv < 4) return sp;
     int64_t n = std::min<int64_t>({16, sms / items, n_kv / 2});
