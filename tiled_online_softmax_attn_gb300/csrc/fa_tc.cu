@@ -708,6 +708,11 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const int grow = wi.qrow0 + (ONE ? 0 : t * BM) + r;  // global query row of this thread
             // key tiles of this warpgroup (ONE: every other one, from key tile t)
             const int n_t = ONE ? (wi.n0 + 1 - t) >> 1 : (t == 0 ? wi.n0 : wi.n1);
+            // every row of this warp is padding (short or ragged queries): the warp
+            // keeps its place in the barrier sequence -- the waits order its
+            // arrivals after the others' of the same tile -- but skips the scores,
+            // the weights and their tensor-memory traffic.  Its O rows are never stored.
+            const bool idle = grow - lane >= N;
             float m = -INFINITY;  // running maximum, log2 units
             float l = 0.f;        // running denominator (exact weights): LSE
             float dq = 0.f;       // bf16 rounding of each tile's largest weight: O / (l + dq)
@@ -717,6 +722,17 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     break;
                 }
                 ++sp;
+                if (idle) {
+                    if constexpr (C::SEP_P) mbar_arrive(smem_addr(&bars.s_read[t]));
+                    if (C::SEP_P && np > 0 && !wait_or_abort(smem_addr(&bars.p_free[t]), (np - 1) & 1u, limit, &abort_flag)) {
+                        fail();
+                        break;
+                    }
+                    ++np;
+#pragma unroll
+                    for (int h = 0; h < P_PARTS; ++h) mbar_arrive(smem_addr(&bars.p_part[t][h]));
+                    continue;
+                }
                 tc_fence_after();
                 float s[BN];
                 {
