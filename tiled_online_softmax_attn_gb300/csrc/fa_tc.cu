@@ -46,6 +46,12 @@
 // further split over key ranges (SPLIT): each writes unnormalised O, m, l and
 // the bf16 correction of its range, and a combine kernel merges them.
 //
+// Unmasked problems of at most 128 query rows, or with too few two-tile items
+// to fill half of the SMs, run items of a single query tile (ONE): Q1's shared
+// memory goes to a deeper K/V ring, the two softmax warpgroups take the even
+// and the odd key tiles into the S0/P0/O0 and S1/P1/O1 slots, and warps 0-3
+// merge the two partial results (m, l, O) before the epilogue.
+//
 // Every mbarrier wait is bounded (a caller-given limit in ns).  A wait that
 // gives up sets the device error word and a CTA-wide abort flag; every role
 // then leaves its loop, the MMA thread waits for its issued MMAs, the TMA
