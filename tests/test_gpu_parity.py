@@ -283,6 +283,30 @@ def test_host_buffer_entry_point_matches_device_path(B, H, N, d, dtype, causal):
     compare(oh.float().numpy(), lh.numpy(), o_ref, l_ref, dtype, dtype)
 
 
+def test_host_buffer_chunks_keep_the_whole_problems_item_shape():
+    """A problem whose two-tile items fill more than half of the SMs runs
+    two-tile items; the head chunks of fa_forward_host, each alone small enough
+    for single-tile items, still run the whole problem's item shape, so the
+    result is the device-buffer call's bit for bit."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, N, d = 1, 512, 64
+    H = sms // 2 + 8                        # 2 items per head: more than half of the SMs
+    assert "one query tile" not in fa.plan(B, H, N, d, torch.bfloat16, torch.bfloat16, False)[1]
+    assert "one query tile" in fa.plan(B, H // 4, N, d, torch.bfloat16, torch.bfloat16, False)[1]
+    w = synth.Workload("t", B, H, N, d, "bf16", False, seed=3200)
+    q, k, v = w.inputs()
+    qh, kh, vh = (torch.from_numpy(x).to(torch.bfloat16).pin_memory() for x in (q, k, v))
+    oh = torch.empty(w.shape, dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty(w.shape[:3], dtype=torch.float32).pin_memory()
+    ws = torch.empty(fa.host_workspace_size(B, H, N, d, torch.bfloat16, torch.bfloat16), dtype=torch.uint8, device="cuda")
+    fa.forward_host(qh, kh, vh, oh, lh, ws, scale=w.scale)
+    od, ld = fa.fa_forward(qh.cuda(), kh.cuda(), vh.cuda(), scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, od.cpu()) and torch.equal(lh, ld.cpu())
+    o_ref, l_ref = oracle.attention(q[:, :4], k[:, :4], v[:, :4], w.scale, False)  # the first 4 heads
+    compare(oh[:, :4].float().numpy(), lh[:, :4].numpy(), o_ref, l_ref, "bf16", "bf16")
+
+
 def test_host_buffer_entry_point_from_two_threads():
     """Two host threads call fa_forward_host at once on one device (the call
     releases the interpreter lock): the shared pipeline streams are taken in
