@@ -183,3 +183,25 @@ def test_single_query_tile_hot_key(d, hot):
     assert s_hot > 30.0                         # the hot key dominates the row
     compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "bf16", "bf16")
     assert np.abs(o_ref[:, :, :, :] - v[:, :, hot:hot + 1, :]).max() < 1e-6
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,dk,dv", [
+    (4, 64, 64, 1000, 64, 64),      # 256 items, 8 key tiles: CTAs with two items (d_v = 64)
+    (4, 64, 100, 700, 128, 128),    # the same at d_v = 128
+    (2, 96, 128, 300, 128, 64),     # 192 items, 3 key tiles: odd count per warpgroup pair
+    (8, 32, 77, 100, 64, 128),      # 256 items of one key tile: no odd tiles to merge
+])
+def test_single_query_tile_items_on_persistent_ctas(B, H, Nq, Nk, dk, dv):
+    """More single-tile items than SMs: persistent CTAs take two items each, so
+    the hand-over barriers (query tile, O columns, the merge's m/l/dq slots)
+    change phase between items.  Every head checked against the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert B * H > sms and -(-Nk // 128) <= 64
+    q, k, v = draw(7800 + Nq + Nk + dk, B, H, Nq, Nk, dk, dv, "bf16")
+    qd, kd, vd = (torch.from_numpy(x).to(torch.bfloat16).cuda() for x in (q, k, v))
+    scale = 1.0 / np.sqrt(dk)
+    o, lse = fa.fa_attention(qd, kd, vd, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.check_device_error() == fa.FA_OK, fa.last_error()
+    o_ref, l_ref = oracle.attention(q, k, v, scale, False)
+    compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "bf16", "bf16")
