@@ -337,7 +337,9 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             const uint64_t pol_q = policy_evict_first();
-            const uint64_t pol_kv = policy_evict_last();
+            // K/V: kept in L2 for the other query blocks of the head, or, with a
+            // single query block per head, read once
+            const uint64_t pol_kv = prm.n_qblocks > 1 ? policy_evict_last() : policy_evict_first();
             int g = 0;                     // stages issued over all items (ring position)
             int q_items = 0;               // items whose Q loads were issued
             int skipped = -1;              // ring position of the injected, never-filled stage
