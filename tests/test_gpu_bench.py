@@ -1,4 +1,4 @@
-"""The bench's JSON line on a small workload, run as the driver runs it.
+"""The bench's JSON line on a small workload, run with the flags of the benchmark contract.
 
 The tiny workload's inputs fit in L2, so the timed steps must be flushed
 (each bracketed by its own events); the line must count our launches and
