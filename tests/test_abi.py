@@ -154,3 +154,18 @@ def test_backward_plan_picks_the_path_by_head_width(lib, d, dtype, path):
     wider ones on the wide-head kernel, the rest on the CUDA cores."""
     n, desc = fa.backward_plan(1, 2, 300, d, dtype, True)
     assert desc == path and n >= 3
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,one", [
+    (1, 2, 100, 64, False, True), (1, 2, 128, 64, False, True), (1, 1, 1, 128, False, True),
+    (1, 2, 100, 64, True, False), (4, 32, 4096, 128, False, False)])
+def test_plan_reports_single_tile_items_for_short_queries(B, H, N, d, causal, one):
+    """Host-side choice of the forward's work items: unmasked problems of at
+    most 128 query rows run items of one query tile whatever the device; the
+    fill rule for longer queries needs the SM count, so without a GPU only the
+    short-query rule shows (the GPU test checks the fill rule)."""
+    import torch
+    n, desc = fa.plan(B, H, N, d, torch.bfloat16, torch.bfloat16, causal)
+    assert n == 1 and desc.startswith(f"tensor-core d={d}")
+    if not torch.cuda.is_available():
+        assert ("one query tile per item" in desc) == one, desc
