@@ -558,8 +558,8 @@ fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     // (S_t = Q K_s), and P_u V_(s-1) for u = 1 - t completes key tile
                     // s - 1.  S_t is issued first: slot t's previous P_t V product was
                     // issued a stage earlier, so it is ordered before the overwrite.
-                    // (the slot is passed as a literal at each call, so the per-slot
-                    // counters stay in registers)
+                    // (the tile slot t or u is passed as a literal at each call, so the
+                    // per-tile counters pp[] and ns[] stay in registers)
                     auto s_stage = [&](int t) -> bool {
                         if (C::SEP_P && !s_free(t)) return false;
                         tc_fence_after();
