@@ -122,6 +122,10 @@ size_t fa_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtyp
  * number of kernel launches one call enqueues (-1 for invalid sizes) and
  * writes a short description ("tensor-core d=128", "wide-head ...",
  * "general-d") into desc (may be NULL).  Pointer alignment is assumed.
+ * A tensor-core description ends in ", one query tile per item" when the
+ * kernel's work items are single 128-row query tiles rather than 256-row
+ * blocks: unmasked problems of at most 128 query rows, and unmasked problems
+ * whose 256-row blocks would occupy at most half of the device's SMs.
  */
 int fa_plan(int64_t B, int64_t H, int64_t N, int64_t d, int in_dtype, int o_dtype, int causal,
             size_t workspace_bytes, char *desc, size_t desc_len);
